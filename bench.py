@@ -1,0 +1,476 @@
+"""Benchmark of the paged KV write + PagedAttention decode step on GB300.
+
+One step = one pass of the whole hot path over one batch: the KV write of each
+sequence's newest token (reshape_and_cache, one token per sequence), then the
+decode of every sequence, split into 512-token partitions and merged when the
+device's work-unit count calls for it (the library's own choice).
+
+Default workload: the Llama-3-8B GQA decode (256 sequences, 32 query heads /
+8 KV heads, head size 128, block size 16, bf16 KV, context lengths
+log-uniform in [512, 4096], random block placement, seed 0x5EED0003).
+
+Metric: KV GB/s = (logical K/V bytes read + Q + out + KV-write bytes) / step
+time, on the device with inputs resident in HBM (1.8 GB of KV, far larger than
+the 129 MB L2, so no flush is needed between steps). Also reported: decode
+sequences per second per layer, the dominant kernel's roofline, an end-to-end
+figure through host buffers, the oracle timed on the host cores, and the SM
+clocks sampled during the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV GB/s (fraction of GB300 HBM peak); decode seqs/sec per layer"
+UNIT = "GB/s"
+DEFAULT_CONFIG = 3
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partitions_llama3_8b_traffic.txt")
+KERNEL_SOURCES = ["decode_simt.cuh", "device_common.cuh"]
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_141_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the partition kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    try:
+        fields = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------------------- workload
+
+class Step:
+    """Device-resident inputs of one decode step and the calls that run it."""
+
+    def __init__(self, case, device, partition_size=512):
+        import torch
+        from paged_kv_cache_141_gb300 import binding as pk
+        self.pk, self.torch, self.case, self.dev = pk, torch, case, device
+        c = case
+        self.P = partition_size
+
+        def t(a, dt):
+            a = np.ascontiguousarray(a)
+            if dt == "bf16":
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+            return torch.from_numpy(a).to(device)
+
+        self.q = t(c.query, c.q_dtype)
+        self.kc = t(c.k_cache, c.cache_dtype)
+        self.vc = t(c.v_cache, c.cache_dtype)
+        self.bt = t(c.block_tables, "i32")
+        self.cl = t(c.context_lens, "i32")
+        self.nk = t(c.new_key, c.kv_dtype)
+        self.nv = t(c.new_value, c.kv_dtype)
+        self.ns = t(c.new_slots, "i64")
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[c.q_dtype]
+        self.out = torch.empty(c.num_seqs, c.num_q_heads, c.head_size, dtype=odt, device=device)
+        if c.prefill_key is not None:
+            pk.reshape_and_cache(t(c.prefill_key, c.kv_dtype), t(c.prefill_value, c.kv_dtype),
+                                 self.kc, self.vc, t(c.prefill_slots, "i64"), c.k_scale,
+                                 c.v_scale, self.status)
+        self.split = pk.choose(c.num_seqs, c.num_q_heads, c.num_kv_heads, c.max_context_len,
+                               partition_size) == 1
+        self.ws = pk.alloc_workspace(c.num_seqs, c.num_q_heads, c.head_size, c.max_context_len,
+                                     partition_size, device)
+        self.views = pk.workspace_views(self.ws, c.num_seqs, c.num_q_heads, c.head_size,
+                                        c.max_context_len, partition_size)
+
+    @property
+    def launches_per_step(self) -> int:
+        return 3 if self.split else 2
+
+    def write(self, stream=None):
+        c = self.case
+        self.pk.reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.ns, c.k_scale,
+                                  c.v_scale, self.status, stream)
+
+    def decode_main(self, stream=None):
+        c = self.case
+        if self.split:
+            self.pk.decode_partitions(self.q, self.kc, self.vc, self.bt, self.cl,
+                                      c.max_context_len, c.scale, self.ws, self.P, c.k_scale,
+                                      c.v_scale, self.status, stream)
+        else:
+            self.pk.decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
+                           c.max_context_len, c.scale, c.k_scale, c.v_scale, self.status, stream)
+
+    def decode_merge(self, stream=None):
+        if self.split:
+            tmp, ml, es = self.views
+            self.pk.merge(self.out, tmp, ml, es, self.cl, self.P, self.status, stream)
+
+    def step(self, stream=None):
+        self.write(stream)
+        self.decode_main(stream)
+        self.decode_merge(stream)
+
+    def bytes_per_step(self) -> dict:
+        c = self.case
+        write = c.write_bytes()
+        decode = c.kv_bytes() + c.qo_bytes()
+        # the partition (or single-pass) kernel's algorithmic bytes: K/V read,
+        # Q read, and its output (partials with their (max, sum), or `out`)
+        if self.split:
+            n_parts = int(sum(-(-int(L) // self.P) for L in c.context_lens))
+            main_out = n_parts * c.num_q_heads * (c.head_size + 2) * 4
+        else:
+            main_out = c.num_seqs * c.num_q_heads * c.head_size * 2
+        main = c.kv_bytes() + c.qo_bytes() // 2 + main_out
+        return {"write": write, "decode": decode, "total": write + decode, "main_kernel": main}
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_141_gb300 import workloads as W
+    case = W.config_case(args.config)
+    st = Step(case, device, args.partition_size)
+    stream = torch.cuda.current_stream(device)
+
+    # correctness gate: one step, no device-side errors
+    st.step()
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise SystemExit(f"device status {int(st.status.item())} after the first step")
+
+    for _ in range(args.warmup):
+        st.step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(K):
+        e = ev[i]
+        e[0].record(stream)
+        st.write()
+        e[1].record(stream)
+        st.decode_main()
+        e[2].record(stream)
+        st.decode_merge()
+        e[3].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if sampler else None
+    total_ms = t_start.elapsed_time(t_end)
+    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    main_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    merge_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    by = st.bytes_per_step()
+    ms_per_step = total_ms / K
+    value = world * by["total"] / (ms_per_step * 1e-3) / 1e9
+    seqs_per_s = world * case.num_seqs / (ms_per_step * 1e-3)
+    peak, peak_kind = hbm_peak()
+    main_avg = sum(main_ms) / K
+    achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
+
+    e2e = run_e2e(st, max(20, min(200, K // 10)), device)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, st.P, budget_s=args.cpu_seconds)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": case.cache_dtype, "data": "synthetic",
+        "config": {"workload": f"{case.name} (configuration {args.config})",
+                   "num_seqs": case.num_seqs, "num_q_heads": case.num_q_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
+                   "block_size": case.block_size, "kv_dtype": case.cache_dtype,
+                   "context_lens": "log-uniform [512, 4096]" if args.config == 3 else "see workloads",
+                   "total_context_tokens": case.total_tokens, "partition_size": st.P,
+                   "decode_form": "partitioned+merge" if st.split else "single-pass",
+                   "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2); no flush"
+                         % (case.kv_bytes() / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "seqs_per_s_per_layer": round(seqs_per_s, 1),
+        "bytes_per_step": by,
+        "kernel_ms": {"reshape_and_cache": round(sum(write_ms) / K, 5),
+                      "decode_main": round(main_avg, 5),
+                      "merge": round(sum(merge_ms) / K, 5)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                     "kernel": "paged_decode_simt_kernel (partition kernel)" if st.split
+                     else "paged_decode_simt_kernel (single pass)",
+                     "peak_kind": f"{peak_kind} (HBM copy, MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": by["main_kernel"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * st.launches_per_step,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
+def run_e2e(st: Step, steps: int, device):
+    """The same step through the public API with host buffers: each step
+    copies its inputs from pinned host memory, runs the write and the decode,
+    and reads the output back."""
+    import torch
+    c = st.case
+    host = {}
+    for name in ("q", "bt", "cl", "nk", "nv", "ns"):
+        tdev = getattr(st, name)
+        host[name] = torch.empty(tdev.shape, dtype=tdev.dtype, pin_memory=True)
+        host[name].copy_(tdev.cpu())
+    out_host = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        for name, h in host.items():
+            getattr(st, name).copy_(h, non_blocking=True)
+        st.step()
+        out_host.copy_(st.out, non_blocking=True)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        for name, h in host.items():
+            getattr(st, name).copy_(h, non_blocking=True)
+        st.step()
+        out_host.copy_(st.out, non_blocking=True)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    by = st.bytes_per_step()["total"]
+    return {"value": round(by / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(case, partition_size, budget_s=12.0):
+    """The oracle, as it stands, on a bounded sample of the workload's
+    sequences (single-threaded C, fp64), timed on this host."""
+    import oracle
+    order = np.random.default_rng(1).permutation(case.num_seqs)
+    done, bytes_done, t0 = [], 0, time.perf_counter()
+    per_tok = 2 * case.num_kv_heads * case.head_size * {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[case.cache_dtype]
+    qo = 2 * case.num_q_heads * case.head_size * 2
+    kc, vc = case.k_cache, case.v_cache
+    if case.prefill_key is not None:
+        return None
+    elapsed = 0.0
+    for s in order:
+        sl = slice(int(s), int(s) + 1)
+        t = time.perf_counter()
+        oracle.decode(np.ascontiguousarray(case.query[sl]), case.q_dtype, kc, vc, case.cache_dtype,
+                      np.ascontiguousarray(case.block_tables[sl]),
+                      np.ascontiguousarray(case.context_lens[sl]), case.num_kv_heads,
+                      case.block_size, case.scale)
+        elapsed += time.perf_counter() - t
+        done.append(int(s))
+        bytes_done += int(case.context_lens[s]) * per_tok + qo
+        if elapsed >= budget_s:
+            break
+    return {"value": round(bytes_done / elapsed / 1e9, 4), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": f"{len(done)} of {case.num_seqs} sequences ({sum(int(case.context_lens[s]) for s in done)} "
+                      f"context tokens), single-threaded C oracle in fp64, {elapsed:.1f} s",
+            "seqs_per_s": round(len(done) / elapsed, 3)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm, on this host's cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_cache_141_gb300 import workloads as W
+    import oracle
+    case = W.config_case(args.config)
+    per_tok = 2 * case.num_kv_heads * case.head_size * 2
+    qo = 2 * case.num_q_heads * case.head_size * 2
+    order = np.random.default_rng(2).permutation(case.num_seqs)
+    K, Wm = args.steps, args.warmup
+    # each step decodes a slice of sequences sized so K + W steps take about
+    # args.reference_seconds in total
+    t = time.perf_counter()
+    oracle.decode(np.ascontiguousarray(case.query[:1]), case.q_dtype, case.k_cache, case.v_cache,
+                  case.cache_dtype, np.ascontiguousarray(case.block_tables[:1]),
+                  np.ascontiguousarray(case.context_lens[:1]), case.num_kv_heads,
+                  case.block_size, case.scale)
+    per_seq = max(1e-4, (time.perf_counter() - t) / max(1, int(case.context_lens[0])) *
+                  float(case.context_lens.mean()))
+    n = max(1, int(args.reference_seconds / (K + Wm) / per_seq))
+    n = min(n, case.num_seqs)
+    cursor = 0
+
+    def one_step():
+        nonlocal cursor
+        idx = np.array([order[(cursor + i) % case.num_seqs] for i in range(n)])
+        cursor += n
+        oracle.decode(np.ascontiguousarray(case.query[idx]), case.q_dtype, case.k_cache,
+                      case.v_cache, case.cache_dtype, np.ascontiguousarray(case.block_tables[idx]),
+                      np.ascontiguousarray(case.context_lens[idx]), case.num_kv_heads,
+                      case.block_size, case.scale)
+        return int(case.context_lens[idx].sum()) * per_tok + n * qo
+
+    for _ in range(Wm):
+        one_step()
+    total, t0 = 0, time.perf_counter()
+    for _ in range(K):
+        total += one_step()
+    el = time.perf_counter() - t0
+    value = total / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": world, "steps": K, "warmup": Wm, "ms_per_step": round(el / K * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": case.cache_dtype, "data": "synthetic",
+            "config": {"workload": f"{case.name} (configuration {args.config})",
+                       "num_seqs": case.num_seqs, "num_q_heads": case.num_q_heads,
+                       "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
+                       "block_size": case.block_size, "kv_dtype": case.cache_dtype},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{n} sequences per step of {case.num_seqs}, "
+                                       f"single-threaded C oracle in fp64"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--partition-size", type=int, default=512)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+/*
+ * pagedkv.h -- C ABI of the GB300 paged KV-cache library (libpagedkv.so).
+ *
+ * Two operations on a paged KV cache, as the pages describe them:
+ *
+ *  - the KV write ("reshape_and_cache"): each new token's key and value are
+ *    scattered into fixed-size physical blocks at the flat slot index the
+ *    scheduler assigned ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 4.1,
+ *    the write side "writes new key/value into the block cache by slots, with
+ *    FP8 KV-cache quantised writes");
+ *
+ *  - the decode step ("paged_attention"): for each sequence and query head,
+ *    walk the sequence's block table to gather K/V scattered across the block
+ *    pool, and compute softmax(scale * q K^T) V over the sequence's
+ *    context_len tokens ("Lecture 3: PagedAttention and vLLM", section "the
+ *    paged implementation of attention": logical block -> physical block, then
+ *    softmax and the weighted sum; TGI deep-dive sec. 4.3, block_tables passed
+ *    to the kernel). Long contexts are split into partitions (512 tokens on the
+ *    pages) computed in parallel and merged by a max / sum-exp reduction (TGI
+ *    deep-dive sec. 4.1, PagedAttention V2 and _PARTITION_SIZE 512).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Pointers.   Every tensor pointer is a DEVICE pointer owned by the caller.
+ *              The library allocates nothing and keeps no state between calls.
+ *  Streams.    `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *              Every call only enqueues work on it and returns; nothing
+ *              synchronises the host.
+ *  Errors.     Argument errors are found on the host before anything is
+ *              launched and returned as PA_ERR_INVALID_ARG or
+ *              PA_ERR_UNSUPPORTED; a failed launch returns PA_ERR_CUDA.
+ *              Errors found by a kernel in the data (a block id outside the
+ *              pool, a slot outside the pool, a bad context length) set bits
+ *              in *dev_status with an atomic OR; the kernel skips the bad
+ *              access and carries on, and the outputs that depended on it are
+ *              unspecified. dev_status is a device uint32 the caller zeroes
+ *              and reads back after synchronising; it may be NULL.
+ *              No kernel traps or asserts; every wait in a kernel is bounded
+ *              in time and reports PA_DEV_TIMEOUT when it runs out.
+ *  Types.      Element types are given by pa_dtype. The query and the output
+ *              share one type. A cache holds the query type, or OCP E4M3 codes
+ *              for a binary16 / bfloat16 query.
+ *
+ * Cache layout declared by this library
+ * -------------------------------------
+ *  k_cache and v_cache are separate tensors, each
+ *      [num_blocks][num_kv_heads][block_size][head_size]
+ *  contiguous, element = cache dtype. One (block, KV head) pair is a
+ *  contiguous slab of block_size * head_size elements, so a block's tokens for
+ *  one head are read in one bulk copy. (The pages show other layouts, e.g.
+ *  [num_blocks, num_heads, head_size, BLOCK_SIZE] in the TGI deep-dive
+ *  sec. 4.2; results do not depend on the layout.)
+ *
+ *  A token at logical position t of sequence s lives in physical block
+ *  block_tables[s * max_blocks_per_seq + t / block_size], slot t % block_size.
+ *  Its flat slot index is block * block_size + t % block_size.
+ *
+ * Decode arithmetic
+ * -----------------
+ *  G = num_q_heads / num_kv_heads (an integer); query head h reads KV head
+ *  h / G. For a sequence of length L the output of head h is
+ *      out = sum_i softmax_i(scale * <q_h, k_i>) v_i,  i < L,
+ *  accumulated in float32. An E4M3 cache is read as code_value * k_scale
+ *  (keys) and code_value * v_scale (values). A sequence with L == 0 gets a
+ *  zero output. The output is rounded to its type to nearest even.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* a NULL pointer, a negative size, inconsistent shapes */
+    PA_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement */
+    PA_ERR_WORKSPACE = 3,     /* the workspace is NULL, misaligned or too small */
+    PA_ERR_CUDA = 4           /* a CUDA call or launch failed */
+} pa_status;
+
+typedef enum pa_dtype {
+    PA_F32 = 0,               /* IEEE binary32 */
+    PA_F16 = 1,               /* IEEE binary16 */
+    PA_BF16 = 2,              /* bfloat16 */
+    PA_FP8_E4M3 = 3           /* OCP E4M3 (bias 7, max 448, no infinities) */
+} pa_dtype;
+
+/* Bits a kernel ORs into *dev_status. */
+#define PA_DEV_BAD_BLOCK_ID 1u  /* a block_tables entry it needed is outside [0, num_blocks) */
+#define PA_DEV_BAD_SLOT     2u  /* a slot_mapping entry is >= num_blocks * block_size */
+#define PA_DEV_BAD_LEN      4u  /* a context length is < 0, above max_context_len,
+                                   or needs more than max_blocks_per_seq blocks */
+#define PA_DEV_TIMEOUT      8u  /* a bounded wait inside a kernel ran out */
+
+/* Supported shapes: head_size in {64, 128, 256}; block_size in [1, 1024];
+ * partition_size a positive multiple of 32 (512 on the pages). */
+
+/*
+ * pa_reshape_and_cache -- the KV write (TGI deep-dive sec. 4.1, the write
+ * side; "vLLM Page Attention Continuous Batching" (lbrq.cn), "KV Block": a
+ * block holds block_size tokens of every head of a layer).
+ *
+ *  key, value     [num_tokens][num_kv_heads][head_size], type in_dtype.
+ *  k_cache,
+ *  v_cache        the block pool (layout above), type cache_dtype; written in
+ *                 place.
+ *  slot_mapping   [num_tokens] int64. slot >= 0: the token goes to block
+ *                 slot / block_size, position slot % block_size. slot < 0: a
+ *                 padding token, skipped. slot >= num_blocks * block_size:
+ *                 skipped and PA_DEV_BAD_SLOT is set.
+ *  cache_dtype == in_dtype: the element bits are copied.
+ *  cache_dtype == PA_FP8_E4M3 (in_dtype F32, F16 or BF16): each element x is
+ *                 stored as E4M3(x / scale), the quotient an IEEE binary32
+ *                 division, the conversion rounding to nearest even and
+ *                 saturating to +-448 (NaN stays NaN). k_scale applies to
+ *                 keys, v_scale to values; both must be finite and > 0.
+ *  Two tokens that name the same slot race; the result is one of them.
+ *  num_tokens == 0 launches nothing and returns PA_OK.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                               int head_size, int block_size, int64_t num_blocks,
+                               pa_dtype in_dtype, pa_dtype cache_dtype, float k_scale,
+                               float v_scale, uint32_t* dev_status, void* stream);
+
+/*
+ * pa_decode -- single-pass decode (PagedAttention "V1" on the pages: one
+ * pass per sequence, no reduction). One work unit per (sequence, KV head
+ * group); suits short contexts or many sequences.
+ *
+ *  out            [num_seqs][num_q_heads][head_size], type q_dtype.
+ *  query          [num_seqs][num_q_heads][head_size], type q_dtype.
+ *  k_cache,
+ *  v_cache        the block pool, type cache_dtype, num_blocks blocks.
+ *  block_tables   [num_seqs][max_blocks_per_seq] int32. Entries at or past
+ *                 ceil(context_lens[s] / block_size) are never read.
+ *  context_lens   [num_seqs] int32, 0 <= L <= max_context_len and
+ *                 ceil(L / block_size) <= max_blocks_per_seq.
+ *  max_context_len  an upper bound on context_lens the caller knows without
+ *                 reading the device (no device-to-host copy is made).
+ *  scale          the softmax scale (1/sqrt(head_size) is usual).
+ *  k_scale,
+ *  v_scale        E4M3 dequantisation scales (ignored for other caches).
+ *  num_seqs == 0 launches nothing.
+ */
+pa_status pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                    int head_size, int block_size, int64_t num_blocks, int max_context_len,
+                    float scale, pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                    float v_scale, uint32_t* dev_status, void* stream);
+
+/*
+ * Workspace of the partitioned decode (caller-allocated, 256-byte aligned):
+ *      tmp_out     float32 [num_seqs][num_q_heads][max_partitions][head_size]
+ *      max_logits  float32 [num_seqs][num_q_heads][max_partitions]
+ *      exp_sums    float32 [num_seqs][num_q_heads][max_partitions]
+ *  in that order, each region starting on a 256-byte boundary, with
+ *  max_partitions = ceil(max_context_len / partition_size) (at least 1).
+ *  For partition p of sequence s and head h (tokens [p*P, min((p+1)*P, L))):
+ *  max_logits = max_i scale*<q, k_i>, exp_sums = sum_i exp(s_i - max_logits),
+ *  tmp_out = sum_i exp(s_i - max_logits) v_i / exp_sums.
+ *  pa_decode_workspace_layout gives the three byte offsets and the total.
+ */
+size_t pa_decode_partitioned_workspace_bytes(int num_seqs, int num_q_heads, int head_size,
+                                             int max_context_len, int partition_size);
+pa_status pa_decode_workspace_layout(int num_seqs, int num_q_heads, int head_size,
+                                     int max_context_len, int partition_size,
+                                     size_t* tmp_out_offset, size_t* max_logits_offset,
+                                     size_t* exp_sums_offset, size_t* total_bytes);
+
+/*
+ * pa_decode_partitions -- the partition kernel of the split decode (the
+ * pages' "V2"): writes every partition's (tmp_out, max_logits, exp_sums) into
+ * the workspace and nothing else. Arguments as pa_decode, plus the partition
+ * size and the workspace. Partitions past a sequence's length are not
+ * written.
+ */
+pa_status pa_decode_partitions(const void* query, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_size, int block_size,
+                               int64_t num_blocks, int max_context_len, float scale,
+                               pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                               float v_scale, int partition_size, void* workspace,
+                               size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/*
+ * pa_merge -- the reduction of the split decode (TGI deep-dive sec. 4.1:
+ * partitions "computed in parallel, then merged"). For each (s, h) with
+ * n = ceil(context_lens[s] / partition_size) partitions:
+ *      M = max_p max_logits[p],  w_p = exp_sums[p] * exp(max_logits[p] - M),
+ *      out = sum_p w_p tmp_out[p] / sum_p w_p
+ *  (zero when n == 0). tmp_out, max_logits, exp_sums are the three workspace
+ *  regions (any float32 device arrays of those shapes); max_partitions is
+ *  their partition extent. out has type out_dtype (F32, F16 or BF16).
+ */
+pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, const float* exp_sums,
+                   const int32_t* context_lens, int num_seqs, int num_q_heads, int head_size,
+                   int partition_size, int max_partitions, pa_dtype out_dtype,
+                   uint32_t* dev_status, void* stream);
+
+/* pa_decode_partitioned -- pa_decode_partitions followed by pa_merge on the
+ * same stream. */
+pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                                int64_t num_blocks, int max_context_len, float scale,
+                                pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                                float v_scale, int partition_size, void* workspace,
+                                size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/*
+ * pa_decode_choose -- which decode to run: 0 = single pass (pa_decode),
+ * 1 = partitioned (pa_decode_partitioned). The pages' rule (TGI deep-dive
+ * sec. 4.1) picks V1 when there is one partition or when num_seqs x num_heads
+ * is large; this library decides from the current device's SM count and the
+ * number of work units each form would launch. Never fails; a non-positive
+ * argument gives 0.
+ */
+int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
+                     int partition_size);
+
+/* Human-readable name of a status code (a static string). */
+const char* pa_status_string(pa_status status);
+
+/* Library ABI version: 100 * major + minor. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,260 @@
+"""Python binding of libpagedkv.so (the C ABI in include/pagedkv.h).
+
+Argument marshalling only: every function passes tensor data pointers, sizes
+and the current CUDA stream to the library, and raises PagedKVError when the
+library returns a non-zero status. All computation happens in the library's
+CUDA kernels. If the library has not been built, loading fails with an error;
+there is no fallback path.
+
+Tensors are CUDA tensors, contiguous, in the library's layouts:
+  query/out        [num_seqs, num_q_heads, head_size]   float32/float16/bfloat16
+  key/value        [num_tokens, num_kv_heads, head_size]
+  k_cache/v_cache  [num_blocks, num_kv_heads, block_size, head_size]
+                   (E4M3 caches as torch.uint8 or torch.float8_e4m3fn)
+  block_tables     [num_seqs, max_blocks] int32
+  context_lens     [num_seqs] int32
+  slot_mapping     [num_tokens] int64
+  dev_status       [1] int32 (read as uint32 bits), zeroed by the caller
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv.so")
+_lock = threading.Lock()
+_lib = None
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
+DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
+
+DEFAULT_PARTITION_SIZE = 512
+
+_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16,
+           torch.uint8: PA_FP8_E4M3}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = PA_FP8_E4M3
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, what: str, status: int):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Load libpagedkv.so and declare its signatures (once)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it first "
+                "(python -m paged_kv_cache_141_gb300.build)")
+        L = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, F, S = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                           ctypes.c_size_t)
+        L.pa_reshape_and_cache.argtypes = [P, P, P, P, P, I64, I, I, I, I64, I, I, F, F, P, P]
+        L.pa_decode.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I, F, F, P, P]
+        L.pa_decode_partitioned_workspace_bytes.argtypes = [I, I, I, I, I]
+        L.pa_decode_partitioned_workspace_bytes.restype = S
+        L.pa_decode_workspace_layout.argtypes = [I, I, I, I, I, P, P, P, P]
+        L.pa_decode_partitions.argtypes = [P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I, F, F,
+                                           I, P, S, P, P]
+        L.pa_merge.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
+        L.pa_decode_partitioned.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I,
+                                            F, F, I, P, S, P, P]
+        L.pa_decode_choose.argtypes = [I, I, I, I, I]
+        L.pa_status_string.argtypes = [I]
+        L.pa_status_string.restype = ctypes.c_char_p
+        for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_layout",
+                     "pa_decode_partitions", "pa_merge", "pa_decode_partitioned",
+                     "pa_decode_choose", "pa_version"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedKVError(what, status)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported tensor dtype {t.dtype}") from None
+
+
+def _ptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, k_scale=1.0, v_scale=1.0,
+                      dev_status=None, stream=None) -> None:
+    """The KV write: scatter key/value [T, Hkv, d] into the caches at
+    slot_mapping (E4M3 caches quantise with k_scale / v_scale)."""
+    T, H, D = key.shape
+    nb, H2, B, D2 = k_cache.shape
+    if value.shape != key.shape or v_cache.shape != k_cache.shape or (H, D) != (H2, D2):
+        raise ValueError("inconsistent key/value/cache shapes")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
+        raise ValueError("slot_mapping must be int64 [num_tokens]")
+    _check(lib().pa_reshape_and_cache(
+        _ptr(key), _ptr(value), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, H, D, B, nb,
+        _dtype(key), _dtype(k_cache), float(k_scale), float(v_scale), _ptr(dev_status),
+        _stream(stream)), "pa_reshape_and_cache")
+
+
+def _decode_dims(query, k_cache, block_tables, context_lens):
+    S, Hq, D = query.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("query and cache head sizes differ")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.numel() != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks], context_lens [num_seqs]")
+    return S, Hq, D, nb, Hkv, B, block_tables.shape[1]
+
+
+def decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+           k_scale=1.0, v_scale=1.0, dev_status=None, stream=None) -> None:
+    """Single-pass paged decode into `out`."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _check(lib().pa_decode(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb,
+        _ptr(context_lens), S, Hq, Hkv, D, B, nb, int(max_context_len), float(scale),
+        _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), _ptr(dev_status),
+        _stream(stream)), "pa_decode")
+
+
+def workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len,
+                    partition_size=DEFAULT_PARTITION_SIZE) -> int:
+    return int(lib().pa_decode_partitioned_workspace_bytes(num_seqs, num_q_heads, head_size,
+                                                           int(max_context_len), partition_size))
+
+
+def max_partitions(max_context_len, partition_size=DEFAULT_PARTITION_SIZE) -> int:
+    return max(1, -(-int(max_context_len) // partition_size))
+
+
+def workspace_views(workspace, num_seqs, num_q_heads, head_size, max_context_len,
+                    partition_size=DEFAULT_PARTITION_SIZE):
+    """(tmp_out, max_logits, exp_sums) float32 views into a workspace tensor."""
+    offs = [ctypes.c_size_t() for _ in range(4)]
+    _check(lib().pa_decode_workspace_layout(num_seqs, num_q_heads, head_size,
+                                            int(max_context_len), partition_size,
+                                            *[ctypes.byref(o) for o in offs]),
+           "pa_decode_workspace_layout")
+    P = max_partitions(max_context_len, partition_size)
+    raw = workspace.view(torch.uint8)
+
+    def region(off, n, shape):
+        return raw[off:off + 4 * n].view(torch.float32).view(shape)
+
+    tmp = region(offs[0].value, num_seqs * num_q_heads * P * head_size,
+                 (num_seqs, num_q_heads, P, head_size))
+    ml = region(offs[1].value, num_seqs * num_q_heads * P, (num_seqs, num_q_heads, P))
+    es = region(offs[2].value, num_seqs * num_q_heads * P, (num_seqs, num_q_heads, P))
+    return tmp, ml, es
+
+
+def alloc_workspace(num_seqs, num_q_heads, head_size, max_context_len,
+                    partition_size=DEFAULT_PARTITION_SIZE, device=None) -> torch.Tensor:
+    n = workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len, partition_size)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_partitions(query, k_cache, v_cache, block_tables, context_lens, max_context_len,
+                      scale, workspace, partition_size=DEFAULT_PARTITION_SIZE, k_scale=1.0,
+                      v_scale=1.0, dev_status=None, stream=None) -> None:
+    """The partition kernel: per-partition partials into `workspace`."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _check(lib().pa_decode_partitions(
+        _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens),
+        S, Hq, Hkv, D, B, nb, int(max_context_len), float(scale), _dtype(query),
+        _dtype(k_cache), float(k_scale), float(v_scale), partition_size, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
+        "pa_decode_partitions")
+
+
+def merge(out, tmp_out, max_logits, exp_sums, context_lens, partition_size=DEFAULT_PARTITION_SIZE,
+          dev_status=None, stream=None) -> None:
+    """Merge partition partials [S, Hq, P, d] / [S, Hq, P] into `out`."""
+    S, Hq, P, D = tmp_out.shape
+    _check(lib().pa_merge(
+        _ptr(out), _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums), _ptr(context_lens), S, Hq, D,
+        partition_size, P, _dtype(out), _ptr(dev_status), _stream(stream)), "pa_merge")
+
+
+def decode_partitioned(out, query, k_cache, v_cache, block_tables, context_lens,
+                       max_context_len, scale, workspace, partition_size=DEFAULT_PARTITION_SIZE,
+                       k_scale=1.0, v_scale=1.0, dev_status=None, stream=None) -> None:
+    """Partition kernel then merge kernel."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _check(lib().pa_decode_partitioned(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb,
+        _ptr(context_lens), S, Hq, Hkv, D, B, nb, int(max_context_len), float(scale),
+        _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), partition_size,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
+        _stream(stream)), "pa_decode_partitioned")
+
+
+def choose(num_seqs, num_q_heads, num_kv_heads, max_context_len,
+           partition_size=DEFAULT_PARTITION_SIZE) -> int:
+    """0 = single pass, 1 = partitioned."""
+    return int(lib().pa_decode_choose(num_seqs, num_q_heads, num_kv_heads, int(max_context_len),
+                                      partition_size))
+
+
+def decode_auto(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+                workspace=None, partition_size=DEFAULT_PARTITION_SIZE, k_scale=1.0, v_scale=1.0,
+                dev_status=None, stream=None) -> int:
+    """Run the form `choose` picks; returns which (0 single pass, 1 split).
+    A partitioned run without a workspace allocates one with torch."""
+    S, Hq, D = query.shape
+    Hkv = k_cache.shape[1]
+    form = choose(S, Hq, Hkv, max_context_len, partition_size)
+    if form == 0:
+        decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context_len, scale,
+               k_scale, v_scale, dev_status, stream)
+    else:
+        if workspace is None:
+            workspace = alloc_workspace(S, Hq, D, max_context_len, partition_size, query.device)
+        decode_partitioned(out, query, k_cache, v_cache, block_tables, context_lens,
+                           max_context_len, scale, workspace, partition_size, k_scale, v_scale,
+                           dev_status, stream)
+    return form
+
+
+def version() -> int:
+    return int(lib().pa_version())

@@ -1,0 +1,311 @@
+// api.cu -- the C ABI (include/pagedkv.h): argument validation on the host,
+// then kernel launches on the caller's stream. Nothing here allocates memory
+// or synchronises.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "launch.h"
+#include "pagedkv.h"
+
+using namespace pagedkv;
+
+namespace {
+
+bool is_compute_type(pa_dtype t) { return t == PA_F32 || t == PA_F16 || t == PA_BF16; }
+
+bool supported_head_size(int d) { return d == 64 || d == 128 || d == 256; }
+
+// (query type, cache type) pairs the decode implements.
+bool supported_pair(pa_dtype q, pa_dtype c) {
+    if (q == c) return is_compute_type(q);
+    return c == PA_FP8_E4M3 && (q == PA_F16 || q == PA_BF16);
+}
+
+// Query heads per work unit: the largest of {8, 4, 2, 1} dividing the group
+// (at most 4 for head_size 256, to bound registers).
+int heads_per_unit(int group, int head_size) {
+    const int cap = head_size >= 256 ? 4 : 8;
+    for (int g = cap; g > 1; g >>= 1)
+        if (group % g == 0) return g;
+    return 1;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int max_partitions(int max_context_len, int partition_size) {
+    const int n = (max_context_len + partition_size - 1) / partition_size;
+    return n < 1 ? 1 : n;
+}
+
+struct Layout {
+    size_t tmp_out, max_logits, exp_sums, total;
+};
+
+Layout workspace_layout(int num_seqs, int num_q_heads, int head_size, int max_context_len,
+                        int partition_size) {
+    const size_t parts = (size_t)num_seqs * num_q_heads * max_partitions(max_context_len, partition_size);
+    Layout l;
+    l.tmp_out = 0;
+    l.max_logits = align256(parts * head_size * sizeof(float));
+    l.exp_sums = l.max_logits + align256(parts * sizeof(float));
+    l.total = l.exp_sums + align256(parts * sizeof(float));
+    return l;
+}
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+// Shared validation of the decode arguments. Fills `p` on success.
+pa_status check_decode(const void* query, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int num_seqs, int num_q_heads,
+                       int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                       int max_context_len, float scale, pa_dtype q_dtype, pa_dtype cache_dtype,
+                       float k_scale, float v_scale, uint32_t* dev_status, DecodeParams& p) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_size <= 0 ||
+        block_size <= 0 || num_blocks < 0 || max_blocks_per_seq < 0 || max_context_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (cache_dtype == PA_FP8_E4M3 &&
+        (!isfinite(k_scale) || !isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f))
+        return PA_ERR_INVALID_ARG;
+    if ((int)q_dtype < 0 || (int)q_dtype > 3 || (int)cache_dtype < 0 || (int)cache_dtype > 3)
+        return PA_ERR_INVALID_ARG;
+    if (!supported_pair(q_dtype, cache_dtype) || !supported_head_size(head_size) ||
+        block_size > 1024)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || (long long)num_kv_heads * (num_q_heads / num_kv_heads) > 65535)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 0 &&
+        (!query || !k_cache || !v_cache || !block_tables || !context_lens || max_blocks_per_seq == 0))
+        return PA_ERR_INVALID_ARG;
+    p = DecodeParams{};
+    p.query = query;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    p.status = dev_status;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.block_size = block_size;
+    p.max_context_len = max_context_len;
+    p.group = num_q_heads / num_kv_heads;
+    const int gs = heads_per_unit(p.group, head_size);
+    p.sub_groups = p.group / gs;
+    const bool fp8 = cache_dtype == PA_FP8_E4M3;
+    p.q_mul = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
+    p.v_mul = fp8 ? v_scale : 1.f;
+    return PA_OK;
+}
+
+cudaError_t run_decode_kernel(const DecodeParams& p, int head_size, pa_dtype q_dtype,
+                              pa_dtype cache_dtype, bool split, cudaStream_t stream) {
+    const int gs = p.group / p.sub_groups;
+    if (cache_dtype == PA_FP8_E4M3) {
+        if (q_dtype == PA_F16) return launch_decode_simt_f16_e4m3(p, head_size, gs, split, stream);
+        return launch_decode_simt_bf16_e4m3(p, head_size, gs, split, stream);
+    }
+    switch (q_dtype) {
+    case PA_F32: return launch_decode_simt_f32(p, head_size, gs, split, stream);
+    case PA_F16: return launch_decode_simt_f16(p, head_size, gs, split, stream);
+    default: return launch_decode_simt_bf16(p, head_size, gs, split, stream);
+    }
+}
+
+pa_status check_partition_size(int partition_size) {
+    if (partition_size <= 0 || partition_size % 32 != 0) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa_status bind_workspace(DecodeParams& p, int num_seqs, int num_q_heads, int head_size,
+                         int max_context_len, int partition_size, void* workspace,
+                         size_t workspace_bytes) {
+    const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) || workspace_bytes < l.total)
+        return PA_ERR_WORKSPACE;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    p.tmp_out = reinterpret_cast<float*>(w + l.tmp_out);
+    p.max_logits = reinterpret_cast<float*>(w + l.max_logits);
+    p.exp_sums = reinterpret_cast<float*>(w + l.exp_sums);
+    p.partition_size = partition_size;
+    p.max_parts = max_partitions(max_context_len, partition_size);
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int64_t num_tokens, int num_kv_heads,
+                               int head_size, int block_size, int64_t num_blocks,
+                               pa_dtype in_dtype, pa_dtype cache_dtype, float k_scale,
+                               float v_scale, uint32_t* dev_status, void* stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if ((int)in_dtype < 0 || (int)in_dtype > 3 || (int)cache_dtype < 0 || (int)cache_dtype > 3)
+        return PA_ERR_INVALID_ARG;
+    if (!is_compute_type(in_dtype)) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype != in_dtype && cache_dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (cache_dtype == PA_FP8_E4M3 &&
+        (!isfinite(k_scale) || !isfinite(v_scale) || k_scale <= 0.f || v_scale <= 0.f))
+        return PA_ERR_INVALID_ARG;
+    // rows move as 16-byte vectors
+    const int in_bytes = in_dtype == PA_F32 ? 4 : 2;
+    if ((head_size * in_bytes) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    return from_cuda(launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
+                                              num_kv_heads, head_size, block_size, num_blocks,
+                                              in_dtype, cache_dtype, k_scale, v_scale, dev_status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode(void* out, const void* query, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                    int head_size, int block_size, int64_t num_blocks, int max_context_len,
+                    float scale, pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                    float v_scale, uint32_t* dev_status, void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out) return PA_ERR_INVALID_ARG;
+    p.out = out;
+    return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, false,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+size_t pa_decode_partitioned_workspace_bytes(int num_seqs, int num_q_heads, int head_size,
+                                             int max_context_len, int partition_size) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len < 0 ||
+        partition_size <= 0)
+        return 0;
+    return workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size).total;
+}
+
+pa_status pa_decode_workspace_layout(int num_seqs, int num_q_heads, int head_size,
+                                     int max_context_len, int partition_size,
+                                     size_t* tmp_out_offset, size_t* max_logits_offset,
+                                     size_t* exp_sums_offset, size_t* total_bytes) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_context_len < 0 ||
+        partition_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
+    if (tmp_out_offset) *tmp_out_offset = l.tmp_out;
+    if (max_logits_offset) *max_logits_offset = l.max_logits;
+    if (exp_sums_offset) *exp_sums_offset = l.exp_sums;
+    if (total_bytes) *total_bytes = l.total;
+    return PA_OK;
+}
+
+pa_status pa_decode_partitions(const void* query, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_size, int block_size,
+                               int64_t num_blocks, int max_context_len, float scale,
+                               pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                               float v_scale, int partition_size, void* workspace,
+                               size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if ((st = check_partition_size(partition_size)) != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
+                             workspace, workspace_bytes)) != PA_OK)
+        return st;
+    return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, true,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, const float* exp_sums,
+                   const int32_t* context_lens, int num_seqs, int num_q_heads, int head_size,
+                   int partition_size, int max_partitions, pa_dtype out_dtype,
+                   uint32_t* dev_status, void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_partitions <= 0)
+        return PA_ERR_INVALID_ARG;
+    pa_status st = check_partition_size(partition_size);
+    if (st != PA_OK) return st;
+    if ((int)out_dtype < 0 || (int)out_dtype > 3) return PA_ERR_INVALID_ARG;
+    if (!is_compute_type(out_dtype) || head_size > 256) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
+    return from_cuda(launch_merge(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                  num_q_heads, head_size, partition_size, max_partitions,
+                                  out_dtype, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                                int64_t num_blocks, int max_context_len, float scale,
+                                pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                                float v_scale, int partition_size, void* workspace,
+                                size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+    if (num_seqs > 0 && !out) return PA_ERR_INVALID_ARG;
+    pa_status st = pa_decode_partitions(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                        context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                        head_size, block_size, num_blocks, max_context_len, scale,
+                                        q_dtype, cache_dtype, k_scale, v_scale, partition_size,
+                                        workspace, workspace_bytes, dev_status, stream);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
+    const uint8_t* w = static_cast<const uint8_t*>(workspace);
+    return pa_merge(out, reinterpret_cast<const float*>(w + l.tmp_out),
+                    reinterpret_cast<const float*>(w + l.max_logits),
+                    reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
+                    num_q_heads, head_size, partition_size,
+                    max_partitions(max_context_len, partition_size), q_dtype, dev_status, stream);
+}
+
+int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
+                     int partition_size) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_context_len <= 0 ||
+        partition_size <= 0)
+        return 0;
+    const int parts = max_partitions(max_context_len, partition_size);
+    if (parts <= 1) return 0;                    // one partition: the merge would only copy
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        sms = 148;
+    }
+    // Single pass launches one unit per (sequence, KV head); with ragged
+    // lengths the longest unit sets the finish time, so it only pays when
+    // the units fill many waves and no context spans many partitions.
+    const long long units = (long long)num_seqs * num_kv_heads;
+    const long long slots = (long long)sms * 3;
+    if (units >= 8 * slots && parts <= 2) return 0;
+    return 1;
+}
+
+const char* pa_status_string(pa_status status) {
+    switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case PA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+int pa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// launch.h -- host-side interface between the C ABI (api.cu) and the kernel
+// translation units. Arguments have been validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedkv.h"
+
+namespace pagedkv {
+
+struct DecodeParams {
+    void* out;                    // single pass: [S, Hq, D] of the query type
+    const void* query;            // [S, Hq, D]
+    const void* k_cache;          // [num_blocks, Hkv, B, D]
+    const void* v_cache;
+    const int32_t* block_tables;  // [S, max_blocks]
+    const int32_t* context_lens;  // [S]
+    float* tmp_out;               // split: [S, Hq, max_parts, D]
+    float* max_logits;            // split: [S, Hq, max_parts]
+    float* exp_sums;              // split: [S, Hq, max_parts]
+    uint32_t* status;             // may be null
+    int64_t num_blocks;
+    int max_blocks;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int max_context_len;
+    int partition_size;           // split only
+    int max_parts;                // split only
+    int group;                    // Hq / Hkv
+    int sub_groups;               // group / heads per work unit
+    float q_mul;                  // scale * log2(e) * (E4M3 cache ? k_scale : 1)
+    float v_mul;                  // E4M3 cache ? v_scale : 1
+};
+
+// Generic CUDA-core decode; one launcher per (query type, cache type).
+// head_size in {64, 128, 256}; heads_per_unit in {1, 2, 4, 8}.
+cudaError_t launch_decode_simt_f32(const DecodeParams& p, int head_size, int heads_per_unit,
+                                   bool split, cudaStream_t stream);
+cudaError_t launch_decode_simt_f16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                   bool split, cudaStream_t stream);
+cudaError_t launch_decode_simt_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                    bool split, cudaStream_t stream);
+cudaError_t launch_decode_simt_f16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                        bool split, cudaStream_t stream);
+cudaError_t launch_decode_simt_bf16_e4m3(const DecodeParams& p, int head_size,
+                                         int heads_per_unit, bool split, cudaStream_t stream);
+
+cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
+                         const float* exp_sums, const int32_t* context_lens, int num_seqs,
+                         int num_q_heads, int head_size, int partition_size, int max_parts,
+                         pa_dtype out_dtype, uint32_t* status, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
+                                     void* v_cache, const int64_t* slots, int64_t num_tokens,
+                                     int num_kv_heads, int head_size, int block_size,
+                                     int64_t num_blocks, pa_dtype in_dtype, pa_dtype cache_dtype,
+                                     float k_scale, float v_scale, uint32_t* status,
+                                     cudaStream_t stream);
+
+}  // namespace pagedkv

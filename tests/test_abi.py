@@ -1,0 +1,86 @@
+"""The C ABI without a GPU: the library builds, loads, and exports every
+entry point include/pagedkv.h declares; host-only calls behave."""
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_141_gb300 import build
+    build.build()
+    from paged_kv_cache_141_gb300 import binding
+    return binding.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pa_reshape_and_cache", "pa_decode", "pa_decode_partitions", "pa_merge",
+                 "pa_decode_partitioned", "pa_decode_partitioned_workspace_bytes",
+                 "pa_decode_choose", "pa_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from paged_kv_cache_141_gb300 import binding
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.library_path()],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (pa_[a-z_0-9]+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_host_only_calls(lib):
+    from paged_kv_cache_141_gb300 import binding as pk
+    assert pk.version() == 100
+    assert pk.status_string(pk.PA_ERR_WORKSPACE).startswith("workspace")
+    # workspace: three 256-byte aligned float32 regions
+    n = pk.workspace_bytes(256, 32, 128, 4096, 512)
+    parts = 256 * 32 * 8
+    assert n == parts * 128 * 4 + 2 * parts * 4
+    assert pk.workspace_bytes(3, 5, 64, 1, 512) % 256 == 0
+    assert pk.max_partitions(0) == 1 and pk.max_partitions(513) == 2
+    # one partition -> single pass, whatever the device
+    assert pk.choose(4, 4, 4, 64) == 0
+    assert pk.choose(0, 4, 4, 64) == 0
+
+
+def test_argument_errors_before_any_launch(lib):
+    import ctypes
+    from paged_kv_cache_141_gb300 import binding as pk
+    L = pk.lib()
+    # NULL pointers with work to do, negative sizes, non-integer GQA group
+    assert L.pa_decode(None, None, None, None, None, 4, None, 2, 8, 8, 128, 16, 10, 64, 0.1,
+                       pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_decode(None, None, None, None, None, 4, None, 2, 8, 3, 128, 16, 10, 64, 0.1,
+                       pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_reshape_and_cache(None, None, None, None, None, -1, 8, 128, 16, 10, pk.PA_BF16,
+                                  pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    # zero work is a no-op even with NULL data pointers
+    assert L.pa_reshape_and_cache(None, None, None, None, None, 0, 8, 128, 16, 10, pk.PA_BF16,
+                                  pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_OK
+    assert L.pa_decode(None, None, None, None, None, 0, None, 0, 8, 8, 128, 16, 10, 0, 0.1,
+                       pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_OK
+    # unsupported combinations
+    assert L.pa_decode(None, None, None, None, None, 4, None, 0, 8, 8, 96, 16, 10, 0, 0.1,
+                       pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_UNSUPPORTED
+    assert L.pa_reshape_and_cache(None, None, None, None, None, 1, 8, 128, 16, 10, pk.PA_BF16,
+                                  pk.PA_F16, 1.0, 1.0, None, None) == pk.PA_ERR_UNSUPPORTED
+    # workspace missing
+    assert L.pa_decode_partitions(ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+                                  ctypes.c_void_p(16), 4, ctypes.c_void_p(16), 2, 8, 8, 128, 16,
+                                  10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, 512, None, 0,
+                                  None, None) == pk.PA_ERR_WORKSPACE
