@@ -237,9 +237,8 @@ paged_decode_simt_kernel(const DecodeParams p) {
 
     for (int k = 0; k < n_st; ++k) {
         const int slot = k % NST;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+        // every lane acquires the stage itself: the bulk copies wrote it
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
         if (!ok) break;
 
         const CT* Ks = ring + (size_t)slot * (Shape::kStageBytes / TypeInfo<CT>::bytes);
@@ -327,13 +326,15 @@ paged_decode_simt_kernel(const DecodeParams p) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, cm[w * GS + h]);
+        // o of each warp is unnormalised (sum of 2^(s - m_w) v), so it is
+        // rescaled by 2^(m_w - M) alone; the sums l_w get the same factor.
         float W = 0.f, O = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
             const float mw = cm[w * GS + h];
-            const float ww = (mw == -INFINITY) ? 0.f : cl[w * GS + h] * fast_exp2(mw - M);
-            W += ww;
-            O = fmaf(ww, co[(w * GS + h) * D + e], O);
+            const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            W = fmaf(f, cl[w * GS + h], W);
+            O = fmaf(f, co[(w * GS + h) * D + e], O);
         }
         const float val = __fdiv_rn(O, W) * p.v_mul;
         const int hq = hq0 + h;
