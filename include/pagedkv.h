@@ -216,6 +216,40 @@ pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cach
                                 size_t workspace_bytes, uint32_t* dev_status, void* stream);
 
 /*
+ * pa_decode_partitioned_static -- pa_decode_partitioned for callers that
+ * cannot allocate device memory. The pages have no counterpart: this is a
+ * convenience of this library. A serving loop that has given all device memory
+ * to a fixed pool, or a plugin whose host program owns every allocation,
+ * cannot call cudaMalloc for the workspace (and cudaMalloc / cudaFree may
+ * synchronise the device). This call allocates nothing: it uses a fixed
+ * workspace of PA_STATIC_WORKSPACE_BYTES that lives in the library's own device
+ * memory, held by every GPU that loads the library until the process exits.
+ *
+ *  Arguments and results are those of pa_decode_partitioned without
+ *  `workspace` / `workspace_bytes`.
+ *  Size limit: a problem whose pa_decode_partitioned_workspace_bytes exceeds
+ *  PA_STATIC_WORKSPACE_BYTES is rejected with PA_ERR_WORKSPACE before any
+ *  launch (64 MiB holds, e.g., 256 sequences x 32 query heads x 8192-token
+ *  contexts at head size 128).
+ *  First call on a device: it looks up the device address of the array
+ *  (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *  first call before any stream capture. A failed lookup returns PA_ERR_CUDA.
+ *  Sharing: every call, on every stream, uses the same array, which keeps the
+ *  previous call's contents (nothing in it needs to start at zero). Calls whose
+ *  kernels overlap on the GPU race on it and give unspecified results:
+ *  serialise them, e.g. on one stream.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (64u * 1024u * 1024u)
+pa_status pa_decode_partitioned_static(void* out, const void* query, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_size, int block_size, int64_t num_blocks,
+                                       int max_context_len, float scale, pa_dtype q_dtype,
+                                       pa_dtype cache_dtype, float k_scale, float v_scale,
+                                       int partition_size, uint32_t* dev_status, void* stream);
+
+/*
  * pa_decode_choose -- which decode to run: 0 = single pass (pa_decode),
  * 1 = partitioned (pa_decode_partitioned). The pages' rule (TGI deep-dive
  * sec. 4.1) picks V1 when there is one partition or when num_seqs x num_heads

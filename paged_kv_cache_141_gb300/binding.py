@@ -73,11 +73,14 @@ def lib() -> ctypes.CDLL:
         L.pa_merge.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P]
         L.pa_decode_partitioned.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I,
                                             F, F, I, P, S, P, P]
+        L.pa_decode_partitioned_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, I,
+                                                   F, I, I, F, F, I, P, P]
         L.pa_decode_choose.argtypes = [I, I, I, I, I]
         L.pa_status_string.argtypes = [I]
         L.pa_status_string.restype = ctypes.c_char_p
         for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_layout",
                      "pa_decode_partitions", "pa_merge", "pa_decode_partitioned",
+                     "pa_decode_partitioned_static",
                      "pa_decode_choose", "pa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -227,6 +230,31 @@ def decode_partitioned(out, query, k_cache, v_cache, block_tables, context_lens,
         _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), partition_size,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)), "pa_decode_partitioned")
+
+
+STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024
+
+
+def decode_partitioned_static(out, query, k_cache, v_cache, block_tables, context_lens,
+                              max_context_len, scale, partition_size=DEFAULT_PARTITION_SIZE,
+                              k_scale=1.0, v_scale=1.0, dev_status=None, stream=None) -> None:
+    """The partitioned decode without a caller workspace, for callers that
+    cannot allocate device memory (a serving loop whose memory all sits in a
+    fixed pool, a plugin whose host program owns every allocation). The
+    library uses a fixed STATIC_WORKSPACE_BYTES array of its own, shared by
+    every call: calls that overlap on the GPU race. Nothing here allocates.
+    Problems needing a larger workspace raise PagedKVError (workspace)."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    need = workspace_bytes(S, Hq, D, max_context_len, partition_size)
+    status = lib().pa_decode_partitioned_static(
+        _ptr(out), _ptr(query), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb,
+        _ptr(context_lens), S, Hq, Hkv, D, B, nb, int(max_context_len), float(scale),
+        _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), partition_size,
+        _ptr(dev_status), _stream(stream))
+    if status == PA_ERR_WORKSPACE and need > STATIC_WORKSPACE_BYTES:
+        raise PagedKVError(f"pa_decode_partitioned_static: the problem needs {need} bytes of "
+                           f"workspace, above the fixed {STATIC_WORKSPACE_BYTES}", status)
+    _check(status, "pa_decode_partitioned_static")
 
 
 def choose(num_seqs, num_q_heads, num_kv_heads, max_context_len,
