@@ -22,10 +22,26 @@ bool supported_pair(pa_dtype q, pa_dtype c) {
     return c == PA_FP8_E4M3 && (q == PA_F16 || q == PA_BF16);
 }
 
-// Query heads per work unit: the largest of {8, 4, 2, 1} dividing the group
-// (at most 4 for head_size 256, to bound registers).
-int heads_per_unit(int group, int head_size) {
-    const int cap = head_size >= 256 ? 4 : 8;
+int elem_bytes(pa_dtype t) { return t == PA_F32 ? 4 : (t == PA_FP8_E4M3 ? 1 : 2); }
+
+// The tensor-TMA kernel takes rows of 128, 256 or 512 bytes (whole 128-byte
+// swizzle spans) and block sizes 8, 16 or a multiple of 32 (so every box lands
+// on a 1 KB-aligned row group), with row coordinates below 2^31.
+bool tma_eligible(int head_size, pa_dtype cache_dtype, int block_size, int64_t num_blocks,
+                  int num_kv_heads) {
+    const int row = head_size * elem_bytes(cache_dtype);
+    if (row != 128 && row != 256 && row != 512) return false;
+    if (!(block_size == 8 || block_size == 16 || (block_size >= 32 && block_size % 32 == 0)))
+        return false;
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    return rows > 0 && rows < (1ll << 31);
+}
+
+// Query heads per work unit: the largest power of two dividing the group, up
+// to a cap that bounds the per-lane accumulators.
+int heads_per_unit(int group, int head_size, bool tma) {
+    const int cap = tma ? (head_size <= 64 ? 16 : (head_size <= 128 ? 8 : 4))
+                        : (head_size >= 256 ? 4 : 8);
     for (int g = cap; g > 1; g >>= 1)
         if (group % g == 0) return g;
     return 1;
@@ -95,8 +111,8 @@ pa_status check_decode(const void* query, const void* k_cache, const void* v_cac
     p.block_size = block_size;
     p.max_context_len = max_context_len;
     p.group = num_q_heads / num_kv_heads;
-    const int gs = heads_per_unit(p.group, head_size);
-    p.sub_groups = p.group / gs;
+    const bool tma = tma_eligible(head_size, cache_dtype, block_size, num_blocks, num_kv_heads);
+    p.sub_groups = p.group / heads_per_unit(p.group, head_size, tma);
     const bool fp8 = cache_dtype == PA_FP8_E4M3;
     p.q_mul = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     p.v_mul = fp8 ? v_scale : 1.f;
@@ -106,6 +122,17 @@ pa_status check_decode(const void* query, const void* k_cache, const void* v_cac
 cudaError_t run_decode_kernel(const DecodeParams& p, int head_size, pa_dtype q_dtype,
                               pa_dtype cache_dtype, bool split, cudaStream_t stream) {
     const int gs = p.group / p.sub_groups;
+    if (tma_eligible(head_size, cache_dtype, p.block_size, p.num_blocks, p.num_kv_heads)) {
+        if (cache_dtype == PA_FP8_E4M3) {
+            if (q_dtype == PA_F16) return launch_decode_tma_f16_e4m3(p, head_size, gs, split, stream);
+            return launch_decode_tma_bf16_e4m3(p, head_size, gs, split, stream);
+        }
+        switch (q_dtype) {
+        case PA_F32: return launch_decode_tma_f32(p, head_size, gs, split, stream);
+        case PA_F16: return launch_decode_tma_f16(p, head_size, gs, split, stream);
+        default: return launch_decode_tma_bf16(p, head_size, gs, split, stream);
+        }
+    }
     if (cache_dtype == PA_FP8_E4M3) {
         if (q_dtype == PA_F16) return launch_decode_simt_f16_e4m3(p, head_size, gs, split, stream);
         return launch_decode_simt_bf16_e4m3(p, head_size, gs, split, stream);

@@ -1,0 +1,12 @@
+// decode_tma_f16.cu -- instantiates the tensor-TMA decode kernel for a
+// query of type __half and a cache of type __half.
+#include "decode_tma.cuh"
+
+namespace pagedkv {
+
+cudaError_t launch_decode_tma_f16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                bool split, cudaStream_t stream) {
+    return launch_tma<__half, __half>(p, head_size, heads_per_unit, split, stream);
+}
+
+}  // namespace pagedkv

@@ -48,6 +48,19 @@ cudaError_t launch_decode_simt_f16_e4m3(const DecodeParams& p, int head_size, in
 cudaError_t launch_decode_simt_bf16_e4m3(const DecodeParams& p, int head_size,
                                          int heads_per_unit, bool split, cudaStream_t stream);
 
+// Tensor-TMA decode (rows of 128/256/512 bytes, block size 8, 16 or a
+// multiple of 32); heads_per_unit <= 32 / (head_size / 32).
+cudaError_t launch_decode_tma_f32(const DecodeParams& p, int head_size, int heads_per_unit,
+                                  bool split, cudaStream_t stream);
+cudaError_t launch_decode_tma_f16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                  bool split, cudaStream_t stream);
+cudaError_t launch_decode_tma_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                   bool split, cudaStream_t stream);
+cudaError_t launch_decode_tma_f16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                       bool split, cudaStream_t stream);
+cudaError_t launch_decode_tma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                        bool split, cudaStream_t stream);
+
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int head_size, int partition_size, int max_parts,
