@@ -47,6 +47,16 @@ int heads_per_unit(int group, int head_size, bool tma) {
     return 1;
 }
 
+// The tensor-core decode: 16-bit query and cache of one type and an even
+// group (the MMA tile holds 8 heads; odd groups stay on the CUDA cores).
+bool mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int group) {
+    return q_dtype == cache_dtype && (q_dtype == PA_F16 || q_dtype == PA_BF16) && group % 2 == 0;
+}
+
+int mma_heads_per_unit(int group) {
+    return group % 8 == 0 ? 8 : (group % 4 == 0 ? 4 : 2);
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 int max_partitions(int max_context_len, int partition_size) {
@@ -112,7 +122,9 @@ pa_status check_decode(const void* query, const void* k_cache, const void* v_cac
     p.max_context_len = max_context_len;
     p.group = num_q_heads / num_kv_heads;
     const bool tma = tma_eligible(head_size, cache_dtype, block_size, num_blocks, num_kv_heads);
-    p.sub_groups = p.group / heads_per_unit(p.group, head_size, tma);
+    const bool mma = tma && mma_eligible(q_dtype, cache_dtype, p.group);
+    p.sub_groups = p.group / (mma ? mma_heads_per_unit(p.group)
+                                  : heads_per_unit(p.group, head_size, tma));
     const bool fp8 = cache_dtype == PA_FP8_E4M3;
     p.q_mul = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
     p.v_mul = fp8 ? v_scale : 1.f;
@@ -123,6 +135,10 @@ cudaError_t run_decode_kernel(const DecodeParams& p, int head_size, pa_dtype q_d
                               pa_dtype cache_dtype, bool split, cudaStream_t stream) {
     const int gs = p.group / p.sub_groups;
     if (tma_eligible(head_size, cache_dtype, p.block_size, p.num_blocks, p.num_kv_heads)) {
+        if (mma_eligible(q_dtype, cache_dtype, p.group)) {
+            if (q_dtype == PA_F16) return launch_decode_mma_f16(p, head_size, gs, split, stream);
+            return launch_decode_mma_bf16(p, head_size, gs, split, stream);
+        }
         if (cache_dtype == PA_FP8_E4M3) {
             if (q_dtype == PA_F16) return launch_decode_tma_f16_e4m3(p, head_size, gs, split, stream);
             return launch_decode_tma_bf16_e4m3(p, head_size, gs, split, stream);

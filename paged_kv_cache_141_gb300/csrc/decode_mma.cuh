@@ -1,0 +1,482 @@
+// decode_mma.cuh -- the paged decode for 16-bit caches with the GQA group's
+// two contractions on the tensor cores (warp-level mma m16n8k16).
+//
+// Work unit, producer and shared-memory layout are those of the tensor-TMA
+// kernel (decode_tma.cuh): a producer warp walks the block table ("Lecture 3:
+// PagedAttention and vLLM", "the paged implementation of attention") and
+// loads each 32-token stage of K and V with cp.async.bulk.tensor into the
+// 128-byte swizzled layout. Here each stage belongs to one consumer warp
+// (stage k -> warp k mod 4), which computes, per 16-token row tile:
+//   S (16 tokens x 8 heads) = K_tile (16 x d) . Q^T (d x 8), K fragments read
+//     with ldmatrix from the swizzled tile, Q^T fragments kept in registers;
+//   an online softmax over the tokens for each head (base 2, float32);
+//   O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads),
+//     V^T fragments read with ldmatrix.trans, P^T fragments made from the S
+//     accumulators with movmatrix. P is split into a 16-bit high part and a
+//     16-bit residual, two MMAs, so the weights keep ~16 significant bits.
+// Heads beyond the group (up to the MMA's 8 columns) carry zero queries and
+// are never written out. Rows of V past the context are zeroed before the
+// P.V product, since 0 x NaN would otherwise poison every output component.
+// At the end the four warps' (max, sum, output) are merged as in the other
+// kernels; the output is O / sum (the partition's normalised output).
+#pragma once
+
+#include "decode_tma.cuh"
+
+namespace pagedkv {
+
+template <typename CT> struct MmaOps;
+
+template <> struct MmaOps<__nv_bfloat16> {
+    __device__ __forceinline__ static void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    // (lo, hi) floats -> packed pair, round to nearest even; and the residuals
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+};
+
+template <> struct MmaOps<__half> {
+    __device__ __forceinline__ static void mma(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+    __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+    __device__ __forceinline__ static float2 unpack(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2*>(&w));
+    }
+};
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem_row)));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* smem_row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(smem_u32(smem_row)));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// Shared memory of the tensor-core decode: the stage ring (reused for the
+// final four-warp merge) and the stage barriers.
+// Stage k belongs to warp k mod 4 and sits in slot k mod NST; NST is a
+// multiple of the four consumer warps so that every slot has one owner and its
+// mbarrier phases advance one stage at a time (a parity wait cannot alias an
+// older phase).
+template <typename CT, int D>
+struct MmaSmem {
+    using S = TmaShape<CT, D>;
+    static constexpr int kNst0 = S::kNst / kTmaConsumerWarps * kTmaConsumerWarps;
+    static constexpr int kNst = kNst0 < kTmaConsumerWarps ? kTmaConsumerWarps : kNst0;
+    static constexpr int kRingBytes = kNst * S::kStageBytes;
+    static constexpr int kCombineBytes = kTmaConsumerWarps * 8 * (D + 2) * 4;
+    static constexpr int kBody = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
+    static constexpr int kBarOffset = (kBody + 127) / 128 * 128;
+    static constexpr int kBytes = kBarOffset + 2 * kNst * 8;
+    static constexpr int kAlloc = kBytes + 1024;                // room to align the ring to 1 KB
+};
+
+template <typename CT, int D, int GS, bool kSplit>
+__global__ void __launch_bounds__(kTmaThreads)
+paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
+    using S = TmaShape<CT, D>;
+    using Smem = MmaSmem<CT, D>;
+    using Ops = MmaOps<CT>;
+    constexpr int NST = Smem::kNst;
+    static_assert(NST % kTmaConsumerWarps == 0, "one owner per slot");
+    constexpr int KS = D / 16;                 // k-steps of the score product
+    static_assert(GS <= 8, "one MMA covers eight heads");
+    const DecodeParams& p = tp.p;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
+    uint64_t* empty = full + NST;
+
+    const int s = blockIdx.z;
+    const int kvh = blockIdx.y / p.sub_groups;
+    const int sub = blockIdx.y - kvh * p.sub_groups;
+    const int hq0 = kvh * p.group + sub * GS;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;                   // fragment row / B column
+    const int t4 = lane & 3;                   // fragment column pair
+
+    int L = p.context_lens[s];
+    {
+        int cap = p.max_context_len;
+        const long long tab = (long long)p.max_blocks * p.block_size;
+        if (tab < cap) cap = (int)tab;
+        if (L < 0 || L > cap) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && sub == 0 && p.status)
+                atomicOr(p.status, PA_DEV_BAD_LEN);
+            L = L < 0 ? 0 : cap;
+        }
+    }
+    int T0, Tend;
+    if constexpr (kSplit) {
+        T0 = blockIdx.x * p.partition_size;
+        if (T0 >= L) return;
+        Tend = min(T0 + p.partition_size, L);
+    } else {
+        T0 = 0;
+        Tend = L;
+        if (L == 0) {
+            CT* out = reinterpret_cast<CT*>(p.out);
+            for (int i = threadIdx.x; i < GS * D; i += blockDim.x)
+                out[((size_t)s * p.num_q_heads + hq0) * D + i] = from_float<CT>(0.f);
+            return;
+        }
+    }
+    const int n_st = (Tend - T0 + kTmaStageTokens - 1) / kTmaStageTokens;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kTmaConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        const int B = p.block_size;
+        const int rows = tp.box_rows;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+        if (lane == 0) {
+            tma_prefetch_map(&tp.k_map);
+            tma_prefetch_map(&tp.v_map);
+        }
+        int issued = 0;
+        for (int k = 0; k < n_st; ++k) {
+            const int slot = k % NST;
+            if (k >= NST) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int t_lo = T0 + k * kTmaStageTokens;
+            const int t_hi = min(t_lo + kTmaStageTokens, Tend);
+            const int j0 = t_lo / B;
+            const int nseg = (t_hi - 1) / B - j0 + 1;
+            uint32_t bytes = 0;
+            int y = 0, row0 = 0;
+            if (lane < nseg) {
+                const int j = j0 + lane;
+                const int pb = table[j];
+                if (pb < 0 || (int64_t)pb >= p.num_blocks) {
+                    if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+                } else {
+                    const int off = (B >= kTmaStageTokens) ? (t_lo - j * B) : 0;
+                    y = (pb * p.num_kv_heads + kvh) * B + off;
+                    row0 = (B >= kTmaStageTokens) ? 0 : j * B - t_lo;
+                    bytes = (uint32_t)(rows * S::kRowBytes);
+                }
+            }
+            uint32_t total = bytes;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * total);
+            __syncwarp();
+            if (bytes) {
+                uint8_t* st = ring + (size_t)slot * S::kStageBytes;
+#pragma unroll
+                for (int sp = 0; sp < S::kSpans; ++sp) {
+                    const int x = sp * (128 / S::kElem);
+                    uint8_t* kd = st + sp * S::kSpanTileBytes + row0 * 128;
+                    tma_load_2d(kd, &tp.k_map, x, y, &full[slot]);
+                    tma_load_2d(kd + S::kTileBytes, &tp.v_map, x, y, &full[slot]);
+                }
+            }
+            issued = k + 1;
+        }
+        if (lane == 0) {
+            for (int k = max(0, issued - NST); k < issued; ++k)
+                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Q^T fragments (B operand of S = K Q^T): column g = head g, rows = d.
+    uint32_t qb[KS][2];
+    {
+        const CT* qp = reinterpret_cast<const CT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (g < GS) {
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
+            } else {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            }
+        }
+    }
+    float acc[KS][4];                           // O^T fragments: rows d, columns heads
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};    // heads 2*t4 and 2*t4+1
+    float l_run[2] = {0.f, 0.f};                // this lane's share of the sums
+    const float qk_mul = p.q_mul;               // scale * log2(e)
+
+    // ldmatrix row addresses: lane -> (matrix mi, row r)
+    const int mi = lane >> 3, r8 = lane & 7;
+
+    for (int k = warp; k < n_st; k += kTmaConsumerWarps) {
+        const int slot = k % NST;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
+        if (!ok) break;
+        uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
+        uint8_t* Vst = Kst + S::kTileBytes;
+        const int nvalid = min(kTmaStageTokens, Tend - (T0 + k * kTmaStageTokens));
+        if (nvalid < kTmaStageTokens) {
+            // rows past the context: zero V so that 0-weights stay 0 in the MMA
+            const int n16 = (kTmaStageTokens - nvalid) * S::kRowBytes / 16;
+            for (int i = lane; i < n16; i += 32) {
+                const int row = nvalid + i / (S::kRowBytes / 16);
+                const int c = i % (S::kRowBytes / 16);
+                *reinterpret_cast<uint4*>(Vst + (c >> 3) * S::kSpanTileBytes + row * 128 + ((c & 7) << 4)) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // ---- S = K Q^T for both 16-token row tiles
+        float sc[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[mt][j] = 0.f;
+            const int row = 16 * mt + (mi & 1) * 8 + r8;
+            const uint8_t* rbase = Kst + row * 128;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int c = 2 * ks + (mi >> 1);
+                uint32_t a[4];
+                ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+                Ops::mma(sc[mt], a, qb[ks][0], qb[ks][1]);
+            }
+        }
+
+        // ---- online softmax per head (this lane: heads 2*t4, 2*t4+1; tokens g, g+8 of each tile)
+        float pv[2][4];
+        float alpha[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int tok = 16 * mt + g + 8 * hr;
+                    float v = sc[mt][2 * hr + j] * qk_mul;
+                    v = tok < nvalid ? v : -INFINITY;          // select, never multiply
+                    sc[mt][2 * hr + j] = v;
+                    mx = fmaxf(mx, v);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[j], mx);
+            alpha[j] = (m_new == -INFINITY) ? 1.f
+                     : ((m_run[j] == -INFINITY) ? 0.f : fast_exp2(m_run[j] - m_new));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float v = sc[mt][2 * hr + j];
+                    const float w = (v == -INFINITY) ? 0.f : fast_exp2(v - m_new);
+                    pv[mt][2 * hr + j] = w;
+                }
+            m_run[j] = m_new;
+            l_run[j] = l_run[j] * alpha[j];
+        }
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            acc[i][0] *= alpha[0];
+            acc[i][1] *= alpha[1];
+            acc[i][2] *= alpha[0];
+            acc[i][3] *= alpha[1];
+        }
+
+        // ---- P^T fragments: hi + residual, transposed from the S layout
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
+                const uint32_t hi = Ops::pack(w0, w1);
+                const float2 hf = Ops::unpack(hi);
+                const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
+                // the sums use exactly the weights the products use
+                const float2 lf = Ops::unpack(lo);
+                l_run[0] += hf.x + lf.x;
+                l_run[1] += hf.y + lf.y;
+                bh[mt][hr] = movmatrix_trans(hi);
+                bl[mt][hr] = movmatrix_trans(lo);
+            }
+        }
+
+        // ---- O^T += V^T P^T
+#pragma unroll
+        for (int md = 0; md < KS; ++md) {
+#pragma unroll
+            for (int kt = 0; kt < 2; ++kt) {
+                const int row = 16 * kt + (mi >> 1) * 8 + r8;      // token
+                const int c = 2 * md + (mi & 1);                    // 16-byte chunk of d
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
+                                         (((c & 7) ^ (row & 7)) << 4));
+                Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+            }
+        }
+        if (nvalid < kTmaStageTokens) {
+            // the generic-proxy zeroing must be ordered before the next bulk copy into this slot
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ------------------------------------------------- merge the four warps
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+    }
+    named_barrier(1, kTmaConsumerWarps * 32);    // ring is free: every stage was consumed
+    float* cm = reinterpret_cast<float*>(smem);                 // [4][8]
+    float* cl = cm + kTmaConsumerWarps * 8;                     // [4][8]
+    float* co = cl + kTmaConsumerWarps * 8;                     // [4][8][D]
+    if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            cm[warp * 8 + 2 * t4 + j] = m_run[j];
+            cl[warp * 8 + 2 * t4 + j] = l_run[j];
+        }
+    }
+#pragma unroll
+    for (int md = 0; md < KS; ++md) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int h = 2 * t4 + j;
+                if (h < GS) co[(warp * 8 + h) * D + 16 * md + g + 8 * hr] = acc[md][2 * hr + j];
+            }
+    }
+    named_barrier(1, kTmaConsumerWarps * 32);
+
+    for (int i = threadIdx.x; i < GS * D; i += kTmaConsumerWarps * 32) {
+        const int h = i / D;
+        const int e = i - h * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kTmaConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + h]);
+        float W = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < kTmaConsumerWarps; ++w) {
+            const float mw = cm[w * 8 + h];
+            const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            W = fmaf(f, cl[w * 8 + h], W);
+            O = fmaf(f, co[(w * 8 + h) * D + e], O);
+        }
+        const float val = __fdiv_rn(O, W);
+        const int hq = hq0 + h;
+        if constexpr (kSplit) {
+            const size_t row = ((size_t)s * p.num_q_heads + hq) * p.max_parts + blockIdx.x;
+            p.tmp_out[row * D + e] = val;
+            if (e == 0) {
+                p.max_logits[row] = M * kLn2;
+                p.exp_sums[row] = W;
+            }
+        } else {
+            CT* out = reinterpret_cast<CT*>(p.out);
+            out[((size_t)s * p.num_q_heads + hq) * D + e] = from_float<CT>(val);
+        }
+    }
+}
+
+template <typename CT, int D, int GS, bool kSplit>
+cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
+    using Smem = MmaSmem<CT, D>;
+    auto kern = paged_decode_mma_kernel<CT, D, GS, kSplit>;
+    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
+    if (e != cudaSuccess) return e;
+    const DecodeParams& p = tp.p;
+    dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups, p.num_seqs);
+    kern<<<grid, kTmaThreads, Smem::kAlloc, stream>>>(tp);
+    return cudaGetLastError();
+}
+
+template <typename CT, int D>
+cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStream_t stream) {
+#define PA_MMA_CASE(G)                                                        \
+    case G:                                                                   \
+        return split ? launch_mma_variant<CT, D, G, true>(tp, stream)         \
+                     : launch_mma_variant<CT, D, G, false>(tp, stream);
+    switch (gs) {
+        PA_MMA_CASE(2)
+        PA_MMA_CASE(4)
+        PA_MMA_CASE(8)
+    }
+#undef PA_MMA_CASE
+    return cudaErrorInvalidValue;
+}
+
+// 16-bit query and cache of the same type; head_size 64, 128 or 256;
+// heads_per_unit 2, 4 or 8.
+template <typename CT>
+cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
+                       cudaStream_t stream) {
+    TmaDecodeParams tp;
+    tp.p = p;
+    tp.box_rows = p.block_size < kTmaStageTokens ? p.block_size : kTmaStageTokens;
+    const unsigned long long rows =
+        (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    cudaError_t e = encode_cache_map(&tp.k_map, p.k_cache, 2, head_size, rows, tp.box_rows);
+    if (e == cudaSuccess) e = encode_cache_map(&tp.v_map, p.v_cache, 2, head_size, rows, tp.box_rows);
+    if (e != cudaSuccess) return e;
+    switch (head_size) {
+    case 64: return launch_mma_d<CT, 64>(tp, gs, split, stream);
+    case 128: return launch_mma_d<CT, 128>(tp, gs, split, stream);
+    case 256: return launch_mma_d<CT, 256>(tp, gs, split, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pagedkv

@@ -32,6 +32,11 @@
 
 namespace pagedkv {
 
+// Shared-memory ring per CTA (bytes); with 64 KB, three CTAs fit on an SM.
+#ifndef PA_TMA_RING_BYTES
+#define PA_TMA_RING_BYTES (64 * 1024)
+#endif
+
 constexpr int kTmaConsumerWarps = 4;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaStageTokens = 32;
@@ -44,25 +49,33 @@ struct TmaShape {
     static constexpr int kSpanTileBytes = kTmaStageTokens * 128;
     static constexpr int kTileBytes = kTmaStageTokens * kRowBytes;  // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kSlotsPerWarp = (kTmaConsumerWarps * kStageBytes <= 40 * 1024) ? 2 : 1;
-    static constexpr int kNst = kTmaConsumerWarps * kSlotsPerWarp;
+    static constexpr int kNst0 = PA_TMA_RING_BYTES / kStageBytes;
+    static constexpr int kNst = kNst0 < 2 ? 2 : (kNst0 > 8 ? 8 : kNst0);
     static constexpr int kRingBytes = kNst * kStageBytes;
     static constexpr int kChunks = kRowBytes / 16;              // 16-byte chunks per row
+    static constexpr int kChunksPerWarp = kChunks / kTmaConsumerWarps;
     static constexpr int kEpc = 16 / kElem;                     // elements per chunk
     static constexpr int kEpl = D / 32;                         // P.V components per lane
     static_assert(kRowBytes == 128 || kRowBytes == 256 || kRowBytes == 512, "row bytes");
+    static_assert(kChunksPerWarp >= 1, "chunks");
 };
+
+constexpr int kTmaTokensPerWarp = kTmaStageTokens / kTmaConsumerWarps;   // 8
 
 template <typename CT, int D, int GS>
 struct TmaSmem {
     using S = TmaShape<CT, D>;
-    static constexpr int kQBytes = D * GS * 4;                                  // q, float32
-    static constexpr int kPBytes = kTmaConsumerWarps * GS * kTmaStageTokens * 4;  // weights
+    static constexpr int kQBytes = D * GS * 4;                                      // q, float32
+    static constexpr int kPartBytes = 2 * kTmaConsumerWarps * kTmaStageTokens * GS * 4;  // partial scores
+    static constexpr int kPBytes = kTmaConsumerWarps * GS * kTmaTokensPerWarp * 4;      // weights
+    static constexpr int kABytes = kTmaConsumerWarps * GS * 4;                          // rescales
     static constexpr int kCombineBytes = kTmaConsumerWarps * GS * (D + 2) * 4;
     static constexpr int kBody = S::kRingBytes > kCombineBytes ? S::kRingBytes : kCombineBytes;
     static constexpr int kQOffset = (kBody + 127) / 128 * 128;
-    static constexpr int kPOffset = kQOffset + kQBytes;
-    static constexpr int kBarOffset = kPOffset + kPBytes;
+    static constexpr int kPartOffset = kQOffset + kQBytes;
+    static constexpr int kPOffset = kPartOffset + kPartBytes;
+    static constexpr int kAOffset = kPOffset + kPBytes;
+    static constexpr int kBarOffset = (kAOffset + kABytes + 7) / 8 * 8;
     static constexpr int kBytes = kBarOffset + 2 * S::kNst * 8;
     static constexpr int kAlloc = kBytes + 1024;                // room to align the ring to 1 KB
 };
@@ -158,8 +171,10 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     // the swizzle follows shared-memory address bits 4-9: align the ring to 1 KB
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* ring = smem;
-    float* qs = reinterpret_cast<float*>(smem + Smem::kQOffset);    // [chunk][GS][epc]
-    float* ps = reinterpret_cast<float*>(smem + Smem::kPOffset);    // [warp][GS][32]
+    float* qs = reinterpret_cast<float*>(smem + Smem::kQOffset);       // [chunk][GS][epc]
+    float* part = reinterpret_cast<float*>(smem + Smem::kPartOffset);  // [2][warp][GS][32]
+    float* ps = reinterpret_cast<float*>(smem + Smem::kPOffset);       // [warp][GS][8]
+    float* as = reinterpret_cast<float*>(smem + Smem::kAOffset);       // [warp][GS]
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
     uint64_t* empty = full + NST;
 
@@ -201,7 +216,7 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&empty[i], kTmaConsumerWarps);
         }
         fence_barrier_init();
     }
@@ -277,36 +292,54 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
 
     // ---------------------------------------------------------------- consumers
-    float m_run[GS], l_run[GS];
+    // Softmax / P.V lane layout: warp w owns tokens 8w..8w+7 of every stage;
+    // lane l holds VPL (token, head) values, value index l*VPL + i (mod NV).
+    constexpr int NV = kTmaTokensPerWarp * GS;
+    constexpr int VPL = NV >= 32 ? NV / 32 : 1;
+    constexpr int TOKMASK_LO = GS / VPL;          // lowest lane bit that changes the token
+    float m_run[VPL], l_run[VPL];
     float2 o2[GS][EPL];
 #pragma unroll
-    for (int h = 0; h < GS; ++h) {
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
+    for (int i = 0; i < VPL; ++i) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.f;
+    }
+#pragma unroll
+    for (int h = 0; h < GS; ++h)
 #pragma unroll
         for (int e = 0; e < EPL; ++e) o2[h][e] = make_float2(0.f, 0.f);
+    int my_t[VPL], my_h[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int idx = (lane * VPL + i) % NV;
+        my_t[i] = idx / GS;
+        my_h[i] = idx % GS;
     }
-    float* pw_buf = ps + warp * GS * kTmaStageTokens;            // [GS][32]
+    const bool canonical = lane * VPL < NV;       // lanes past NV repeat earlier values
+    float* pw_buf = ps + warp * GS * kTmaTokensPerWarp;          // [GS][8]
+    float* a_buf = as + warp * GS;                               // [GS]
     // this lane's P.V components: byte offset within a row, split into span / chunk
     const int vb = lane * EPL * S::kElem;
     const int v_span = vb >> 7, v_chunk = (vb & 127) >> 4, v_in = vb & 15;
+    const int c0 = warp * S::kChunksPerWarp;                     // this warp's score chunks
 
-    for (int k = warp; k < n_st; k += kTmaConsumerWarps) {
+    for (int k = 0; k < n_st; ++k) {
         const int slot = k % NST;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
-        if (!ok) break;
         const uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
         const uint8_t* Vst = Kst + S::kTileBytes;
         const int nvalid = min(kTmaStageTokens, Tend - (T0 + k * kTmaStageTokens));
 
-        // scores: lane owns token `lane`
+        // partial scores over this warp's quarter of the row: lane owns token `lane`
+        // (after a timed-out wait the values are garbage; the vote below ends the loop)
         float2 acc[GS];
 #pragma unroll
         for (int h = 0; h < GS; ++h) acc[h] = make_float2(0.f, 0.f);
         const uint8_t* krow = Kst + lane * 128;
         const int sw = lane & 7;
 #pragma unroll
-        for (int c = 0; c < S::kChunks; ++c) {
+        for (int cc = 0; cc < S::kChunksPerWarp; ++cc) {
+            const int c = c0 + cc;
             const uint4 kw = *reinterpret_cast<const uint4*>(
                 krow + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ sw) << 4));
             float2 kf[Widen16<CT>::kPairs];
@@ -322,46 +355,72 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                 }
             }
         }
-        const bool valid = lane < nvalid;
+        float* pbuf = part + (k & 1) * (kTmaConsumerWarps * GS * kTmaStageTokens);
 #pragma unroll
-        for (int h = 0; h < GS; ++h) {
-            const float sc = valid ? (acc[h].x + acc[h].y) : -INFINITY;   // select, never multiply
+        for (int h = 0; h < GS; ++h)
+            pbuf[(warp * GS + h) * kTmaStageTokens + lane] = acc[h].x + acc[h].y;
+        // all four warps' partials are in place; a timed-out wait anywhere ends
+        // the loop for every consumer warp at once
+        if (!named_barrier_and(1, kTmaConsumerWarps * 32, ok)) break;
+
+        // full scores of this warp's tokens, online softmax per head
+        float pw[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int tok = warp * kTmaTokensPerWarp + my_t[i];
+            float sc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kTmaConsumerWarps; ++w)
+                sc += pbuf[(w * GS + my_h[i]) * kTmaStageTokens + tok];
+            const bool valid = tok < nvalid;
+            sc = valid ? sc : -INFINITY;                              // select, never multiply
             float mx = sc;
 #pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-            const float m_new = fmaxf(m_run[h], mx);
-            const float alpha = (m_run[h] == -INFINITY) ? 0.f : fast_exp2(m_run[h] - m_new);
-            const float pw = valid ? fast_exp2(sc - m_new) : 0.f;
-            l_run[h] = l_run[h] * alpha + pw;
-            m_run[h] = m_new;
-            pw_buf[h * kTmaStageTokens + lane] = pw;
-            const float2 a2 = make_float2(alpha, alpha);
+            for (int m = TOKMASK_LO; m <= 16; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            const float m_new = fmaxf(m_run[i], mx);
+            const float alpha = (m_new == -INFINITY) ? 1.f
+                              : ((m_run[i] == -INFINITY) ? 0.f : fast_exp2(m_run[i] - m_new));
+            pw[i] = valid ? fast_exp2(sc - m_new) : 0.f;
+            l_run[i] = l_run[i] * alpha + (canonical ? pw[i] : 0.f);
+            m_run[i] = m_new;
+            pw_buf[my_h[i] * kTmaTokensPerWarp + my_t[i]] = pw[i];
+            if (my_t[i] == 0) a_buf[my_h[i]] = alpha;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < GS; ++h) {
+            const float a = a_buf[h];
+            const float2 a2 = make_float2(a, a);
 #pragma unroll
             for (int e = 0; e < EPL; ++e) o2[h][e] = __fmul2_rn(o2[h][e], a2);
         }
-        __syncwarp();
 
-        // P.V: lane owns EPL components; even/odd tokens in the two halves
+        // P.V over this warp's tokens: lane owns EPL components; even/odd tokens
+        // accumulate in the two halves of a packed pair
+        const int tw0 = warp * kTmaTokensPerWarp;
+        const int nv = min(kTmaTokensPerWarp, nvalid - tw0);          // may be <= 0
         const uint8_t* vbase = Vst + v_span * S::kSpanTileBytes + v_in;
         int t = 0;
-        for (; t + 1 < nvalid; t += 2) {
+        for (; t + 1 < nv; t += 2) {
+            const int ra = tw0 + t, rb = ra + 1;
             float va[EPL], vb2[EPL];
-            load_slice<CT, EPL>(vbase + t * 128 + ((v_chunk ^ (t & 7)) << 4), va);
-            load_slice<CT, EPL>(vbase + (t + 1) * 128 + ((v_chunk ^ ((t + 1) & 7)) << 4), vb2);
+            load_slice<CT, EPL>(vbase + ra * 128 + ((v_chunk ^ (ra & 7)) << 4), va);
+            load_slice<CT, EPL>(vbase + rb * 128 + ((v_chunk ^ (rb & 7)) << 4), vb2);
 #pragma unroll
             for (int h = 0; h < GS; ++h) {
-                const float2 pp = *reinterpret_cast<const float2*>(pw_buf + h * kTmaStageTokens + t);
+                const float2 pp = *reinterpret_cast<const float2*>(pw_buf + h * kTmaTokensPerWarp + t);
 #pragma unroll
                 for (int e = 0; e < EPL; ++e)
                     o2[h][e] = __ffma2_rn(make_float2(va[e], vb2[e]), pp, o2[h][e]);
             }
         }
-        if (t < nvalid) {
+        if (t < nv) {
+            const int ra = tw0 + t;
             float va[EPL];
-            load_slice<CT, EPL>(vbase + t * 128 + ((v_chunk ^ (t & 7)) << 4), va);
+            load_slice<CT, EPL>(vbase + ra * 128 + ((v_chunk ^ (ra & 7)) << 4), va);
 #pragma unroll
             for (int h = 0; h < GS; ++h) {
-                const float pt = pw_buf[h * kTmaStageTokens + t];
+                const float pt = pw_buf[h * kTmaTokensPerWarp + t];
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) o2[h][e].x = fmaf(va[e], pt, o2[h][e].x);
             }
@@ -372,19 +431,19 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 
     // ------------------------------------------------- merge the four warps
 #pragma unroll
-    for (int h = 0; h < GS; ++h) {
+    for (int i = 0; i < VPL; ++i) {
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], m);
+        for (int m = TOKMASK_LO; m <= 16; m <<= 1) l_run[i] += __shfl_xor_sync(0xffffffffu, l_run[i], m);
     }
     named_barrier(1, kTmaConsumerWarps * 32);    // ring is free: every stage was consumed
     float* cm = reinterpret_cast<float*>(smem);                 // [4][GS]
     float* cl = cm + kTmaConsumerWarps * GS;                    // [4][GS]
     float* co = cl + kTmaConsumerWarps * GS;                    // [4][GS][D]
-    if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < GS; ++h) {
-            cm[warp * GS + h] = m_run[h];
-            cl[warp * GS + h] = l_run[h];
+    for (int i = 0; i < VPL; ++i) {
+        if (canonical && my_t[i] == 0) {
+            cm[warp * GS + my_h[i]] = m_run[i];
+            cl[warp * GS + my_h[i]] = l_run[i];
         }
     }
 #pragma unroll

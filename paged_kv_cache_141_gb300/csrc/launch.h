@@ -61,6 +61,13 @@ cudaError_t launch_decode_tma_f16_e4m3(const DecodeParams& p, int head_size, int
 cudaError_t launch_decode_tma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
                                         bool split, cudaStream_t stream);
 
+// Tensor-core decode for 16-bit caches (query type = cache type), TMA-eligible
+// shapes, heads_per_unit in {2, 4, 8}.
+cudaError_t launch_decode_mma_f16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                  bool split, cudaStream_t stream);
+cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
+                                   bool split, cudaStream_t stream);
+
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int head_size, int partition_size, int max_parts,

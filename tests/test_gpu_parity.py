@@ -240,10 +240,12 @@ def test_shared_prefix_matches_copies():
 
 
 def test_block_size_does_not_change_result():
-    """The same logical K/V paged with block sizes 1, 16 and 256 gives
-    bit-identical outputs (the kernel's arithmetic follows token order)."""
+    """The same logical K/V paged with block sizes 8, 16 and 256 gives
+    bit-identical outputs (one kernel; its arithmetic follows token order, not
+    the placement); block size 1 runs the bulk-copy kernel and agrees within
+    tolerance."""
     outs = []
-    for B in (1, 16, 256):
+    for B in (8, 16, 256, 1):
         c = small_case("bf16", "bf16", 8, 2, 128, B, [300, 45, 1000], seed=21)
         # same logical values for every B: rebuild the pool from one logical draw
         rng = np.random.default_rng(4)
@@ -262,6 +264,8 @@ def test_block_size_does_not_change_result():
         d.write_step()
         outs.append(d.decode("split", 512).clone())
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    a, b = to_f64(outs[0]), to_f64(outs[3])
+    assert np.all(np.abs(a - b) <= 2e-3 + rounding_allowance(a, "bf16"))
 
 
 # --------------------------------------------------------------------- errors
