@@ -42,7 +42,7 @@ DEFAULT_CONFIG = 3
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partitions_llama3_8b_traffic.txt")
-KERNEL_SOURCES = ["decode_simt.cuh", "device_common.cuh"]
+KERNEL_SOURCES = ["decode_mma.cuh", "decode_tma.cuh", "device_common.cuh"]
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -124,6 +124,21 @@ class ClockSampler:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def decode_kernel_label(case) -> str:
+    """Which decode kernel the library runs for this workload (its dispatch
+    rule: 16-bit query and cache of one type with an even group -> tensor-core
+    kernel; other rows of 128/256/512 bytes with block size 8, 16 or a multiple
+    of 32 -> tensor-TMA CUDA-core kernel; anything else -> bulk-copy kernel)."""
+    eb = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[case.cache_dtype]
+    row = case.head_size * eb
+    B = case.block_size
+    tma = row in (128, 256, 512) and (B in (8, 16) or (B >= 32 and B % 32 == 0))
+    if tma and case.q_dtype == case.cache_dtype and case.q_dtype in ("f16", "bf16") \
+            and case.group % 2 == 0:
+        return "paged_decode_mma_kernel"
+    return "paged_decode_tma_kernel" if tma else "paged_decode_simt_kernel"
 
 
 def dist_env():
@@ -313,8 +328,8 @@ def run_ours(args):
                       "merge": round(sum(merge_ms) / K, 5)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
-                     "kernel": "paged_decode_simt_kernel (partition kernel)" if st.split
-                     else "paged_decode_simt_kernel (single pass)",
+                     "kernel": decode_kernel_label(case) + (" (partition kernel)" if st.split
+                                                             else " (single pass)"),
                      "peak_kind": f"{peak_kind} (HBM copy, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": by["main_kernel"]},
