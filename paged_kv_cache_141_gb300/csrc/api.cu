@@ -47,10 +47,12 @@ int heads_per_unit(int group, int head_size, bool tma) {
     return 1;
 }
 
-// The tensor-core decode: 16-bit query and cache of one type and an even
-// group (the MMA tile holds 8 heads; odd groups stay on the CUDA cores).
+// The tensor-core decode: a 16-bit query with a cache of the same type or of
+// E4M3 codes, and an even group (the MMA tile holds 8 heads; odd groups stay
+// on the CUDA cores).
 bool mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int group) {
-    return q_dtype == cache_dtype && (q_dtype == PA_F16 || q_dtype == PA_BF16) && group % 2 == 0;
+    if (group % 2 != 0 || !(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
+    return cache_dtype == q_dtype || cache_dtype == PA_FP8_E4M3;
 }
 
 int mma_heads_per_unit(int group) {
@@ -136,6 +138,10 @@ cudaError_t run_decode_kernel(const DecodeParams& p, int head_size, pa_dtype q_d
     const int gs = p.group / p.sub_groups;
     if (tma_eligible(head_size, cache_dtype, p.block_size, p.num_blocks, p.num_kv_heads)) {
         if (mma_eligible(q_dtype, cache_dtype, p.group)) {
+            if (cache_dtype == PA_FP8_E4M3) {
+                if (q_dtype == PA_F16) return launch_decode_mma_f16_e4m3(p, head_size, gs, split, stream);
+                return launch_decode_mma_bf16_e4m3(p, head_size, gs, split, stream);
+            }
             if (q_dtype == PA_F16) return launch_decode_mma_f16(p, head_size, gs, split, stream);
             return launch_decode_mma_bf16(p, head_size, gs, split, stream);
         }

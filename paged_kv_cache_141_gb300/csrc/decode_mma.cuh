@@ -101,12 +101,25 @@ struct MmaSmem {
     static constexpr int kAlloc = kBytes + 1024;                // room to align the ring to 1 KB
 };
 
-template <typename CT, int D, int GS, bool kSplit>
+// E4M3 caches run the MMAs in binary16 (every E4M3 value is exact in it):
+// K and V fragments are widened in registers, the query is rounded to f16.
+template <typename CT> struct MathType { using T = CT; };
+template <> struct MathType<e4m3_t> { using T = __half; };
+
+// Two E4M3 codes (low 16 bits of w) -> f16x2, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+template <typename QT, typename CT, int D, int GS, bool kSplit>
 __global__ void __launch_bounds__(kTmaThreads)
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
     using Smem = MmaSmem<CT, D>;
-    using Ops = MmaOps<CT>;
+    using MT = typename MathType<CT>::T;
+    using Ops = MmaOps<MT>;
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
     constexpr int NST = Smem::kNst;
     static_assert(NST % kTmaConsumerWarps == 0, "one owner per slot");
     constexpr int KS = D / 16;                 // k-steps of the score product
@@ -148,9 +161,9 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         T0 = 0;
         Tend = L;
         if (L == 0) {
-            CT* out = reinterpret_cast<CT*>(p.out);
+            QT* out = reinterpret_cast<QT*>(p.out);
             for (int i = threadIdx.x; i < GS * D; i += blockDim.x)
-                out[((size_t)s * p.num_q_heads + hq0) * D + i] = from_float<CT>(0.f);
+                out[((size_t)s * p.num_q_heads + hq0) * D + i] = from_float<QT>(0.f);
             return;
         }
     }
@@ -227,17 +240,24 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 
     // ---------------------------------------------------------------- consumers
     // Q^T fragments (B operand of S = K Q^T): column g = head g, rows = d.
+    // For E4M3 the k index of a 16-wide step maps to d as the widened ldmatrix
+    // bytes come: k = 2t+j <-> d = 4t+j and k = 2t+8+j <-> d = 4t+2+j (a
+    // permutation of the reduction, applied to K and Q alike).
     uint32_t qb[KS][2];
     {
-        const CT* qp = reinterpret_cast<const CT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
+        const QT* qp = reinterpret_cast<const QT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            if (g < GS) {
-                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
-                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
-            } else {
+            if (g >= GS) {
                 qb[ks][0] = 0u;
                 qb[ks][1] = 0u;
+            } else if constexpr (kFp8) {
+                const QT* q4 = qp + g * D + 16 * ks + 4 * t4;
+                qb[ks][0] = Ops::pack(to_float(q4[0]), to_float(q4[1]));
+                qb[ks][1] = Ops::pack(to_float(q4[2]), to_float(q4[3]));
+            } else {
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
             }
         }
     }
@@ -280,12 +300,29 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             for (int j = 0; j < 4; ++j) sc[mt][j] = 0.f;
             const int row = 16 * mt + (mi & 1) * 8 + r8;
             const uint8_t* rbase = Kst + row * 128;
+            if constexpr (kFp8) {
+                // one ldmatrix.x4 covers two 16-byte chunks (32 d) of 16 tokens
 #pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                const int c = 2 * ks + (mi >> 1);
-                uint32_t a[4];
-                ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
-                Ops::mma(sc[mt], a, qb[ks][0], qb[ks][1]);
+                for (int kp = 0; kp < KS / 2; ++kp) {
+                    const int c = 2 * kp + (mi >> 1);
+                    uint32_t x[4];
+                    ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t a[4] = {e4m3x2_to_f16x2(x[2 * h2]), e4m3x2_to_f16x2(x[2 * h2 + 1]),
+                                               e4m3x2_to_f16x2(x[2 * h2] >> 16),
+                                               e4m3x2_to_f16x2(x[2 * h2 + 1] >> 16)};
+                        Ops::mma(sc[mt], a, qb[2 * kp + h2][0], qb[2 * kp + h2][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int c = 2 * ks + (mi >> 1);
+                    uint32_t a[4];
+                    ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+                    Ops::mma(sc[mt], a, qb[ks][0], qb[ks][1]);
+                }
             }
         }
 
@@ -350,17 +387,40 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         }
 
         // ---- O^T += V^T P^T
+        if constexpr (kFp8) {
+            // one 16-byte chunk = 16 d of all 32 tokens: ldmatrix.trans on byte
+            // pairs gives lane (tokens 2t, 2t+1) x (d 2g, 2g+1); a byte permute
+            // regroups them by d. Fragment row g <-> d 2g, row g+8 <-> d 2g+1.
 #pragma unroll
-        for (int md = 0; md < KS; ++md) {
+            for (int md = 0; md < KS; ++md) {
+                const int row = 8 * mi + r8;                        // token
+                uint32_t y[4];
+                ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
+                                         (((md & 7) ^ (row & 7)) << 4));
 #pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int row = 16 * kt + (mi >> 1) * 8 + r8;      // token
-                const int c = 2 * md + (mi & 1);                    // 16-byte chunk of d
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
-                                         (((c & 7) ^ (row & 7)) << 4));
-                Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
-                Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
+                    const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0020)),
+                                           e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0031)),
+                                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020)),
+                                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031))};
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int row = 16 * kt + (mi >> 1) * 8 + r8;      // token
+                    const int c = 2 * md + (mi & 1);                    // 16-byte chunk of d
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
+                                             (((c & 7) ^ (row & 7)) << 4));
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                }
             }
         }
         if (nvalid < kTmaStageTokens) {
@@ -396,7 +456,8 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const int h = 2 * t4 + j;
-                if (h < GS) co[(warp * 8 + h) * D + 16 * md + g + 8 * hr] = acc[md][2 * hr + j];
+                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
+                if (h < GS) co[(warp * 8 + h) * D + d] = acc[md][2 * hr + j];
             }
     }
     named_barrier(1, kTmaConsumerWarps * 32);
@@ -415,7 +476,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             W = fmaf(f, cl[w * 8 + h], W);
             O = fmaf(f, co[(w * 8 + h) * D + e], O);
         }
-        const float val = __fdiv_rn(O, W);
+        const float val = __fdiv_rn(O, W) * p.v_mul;
         const int hq = hq0 + h;
         if constexpr (kSplit) {
             const size_t row = ((size_t)s * p.num_q_heads + hq) * p.max_parts + blockIdx.x;
@@ -425,16 +486,16 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                 p.exp_sums[row] = W;
             }
         } else {
-            CT* out = reinterpret_cast<CT*>(p.out);
-            out[((size_t)s * p.num_q_heads + hq) * D + e] = from_float<CT>(val);
+            QT* out = reinterpret_cast<QT*>(p.out);
+            out[((size_t)s * p.num_q_heads + hq) * D + e] = from_float<QT>(val);
         }
     }
 }
 
-template <typename CT, int D, int GS, bool kSplit>
+template <typename QT, typename CT, int D, int GS, bool kSplit>
 cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     using Smem = MmaSmem<CT, D>;
-    auto kern = paged_decode_mma_kernel<CT, D, GS, kSplit>;
+    auto kern = paged_decode_mma_kernel<QT, CT, D, GS, kSplit>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
     if (e != cudaSuccess) return e;
     const DecodeParams& p = tp.p;
@@ -443,12 +504,12 @@ cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-template <typename CT, int D>
+template <typename QT, typename CT, int D>
 cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStream_t stream) {
 #define PA_MMA_CASE(G)                                                        \
     case G:                                                                   \
-        return split ? launch_mma_variant<CT, D, G, true>(tp, stream)         \
-                     : launch_mma_variant<CT, D, G, false>(tp, stream);
+        return split ? launch_mma_variant<QT, CT, D, G, true>(tp, stream)     \
+                     : launch_mma_variant<QT, CT, D, G, false>(tp, stream);
     switch (gs) {
         PA_MMA_CASE(2)
         PA_MMA_CASE(4)
@@ -458,23 +519,31 @@ cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStre
     return cudaErrorInvalidValue;
 }
 
-// 16-bit query and cache of the same type; head_size 64, 128 or 256;
-// heads_per_unit 2, 4 or 8.
-template <typename CT>
+// Query type QT (16-bit); cache CT of the same type, or E4M3 codes; rows of
+// 128, 256 or 512 bytes; heads_per_unit 2, 4 or 8.
+template <typename QT, typename CT>
 cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
                        cudaStream_t stream) {
+    constexpr int eb = TypeInfo<CT>::bytes;
     TmaDecodeParams tp;
     tp.p = p;
     tp.box_rows = p.block_size < kTmaStageTokens ? p.block_size : kTmaStageTokens;
     const unsigned long long rows =
         (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
-    cudaError_t e = encode_cache_map(&tp.k_map, p.k_cache, 2, head_size, rows, tp.box_rows);
-    if (e == cudaSuccess) e = encode_cache_map(&tp.v_map, p.v_cache, 2, head_size, rows, tp.box_rows);
+    cudaError_t e = encode_cache_map(&tp.k_map, p.k_cache, eb, head_size, rows, tp.box_rows);
+    if (e == cudaSuccess) e = encode_cache_map(&tp.v_map, p.v_cache, eb, head_size, rows, tp.box_rows);
     if (e != cudaSuccess) return e;
-    switch (head_size) {
-    case 64: return launch_mma_d<CT, 64>(tp, gs, split, stream);
-    case 128: return launch_mma_d<CT, 128>(tp, gs, split, stream);
-    case 256: return launch_mma_d<CT, 256>(tp, gs, split, stream);
+    if constexpr (eb == 2) {
+        switch (head_size) {
+        case 64: return launch_mma_d<QT, CT, 64>(tp, gs, split, stream);
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
+        }
+    } else {
+        switch (head_size) {
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
+        }
     }
     return cudaErrorInvalidValue;
 }

@@ -1,0 +1,12 @@
+// decode_mma_f16_e4m3.cu -- instantiates the tensor-core decode kernel for a
+// query of type __half and a cache of type e4m3_t.
+#include "decode_mma.cuh"
+
+namespace pagedkv {
+
+cudaError_t launch_decode_mma_f16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                     bool split, cudaStream_t stream) {
+    return launch_mma<__half, e4m3_t>(p, head_size, heads_per_unit, split, stream);
+}
+
+}  // namespace pagedkv

@@ -67,6 +67,11 @@ cudaError_t launch_decode_mma_f16(const DecodeParams& p, int head_size, int head
                                   bool split, cudaStream_t stream);
 cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
                                    bool split, cudaStream_t stream);
+// E4M3 caches (rows of 128 or 256 bytes) with a 16-bit query, MMAs in f16.
+cudaError_t launch_decode_mma_f16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                       bool split, cudaStream_t stream);
+cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
+                                        bool split, cudaStream_t stream);
 
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,

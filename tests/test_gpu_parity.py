@@ -98,6 +98,8 @@ SWEEP = [
     ("e4m3", "bf16", 64, 8, 128, 16, [1, 20, 512, 777]),
     ("e4m3", "f16", 8, 2, 64, 16, [5, 48, 160]),
     ("e4m3", "bf16", 8, 8, 256, 8, [9, 130]),
+    ("e4m3", "bf16", 16, 4, 256, 16, [1, 33, 400]),
+    ("e4m3", "f16", 8, 4, 128, 32, [2, 64, 65, 513]),
     # shapes outside the tensor-TMA kernel (block sizes below 8, 64-byte E4M3
     # rows, 1 KB float32 rows) run the bulk-copy kernel
     ("bf16", "bf16", 32, 8, 128, 4, [1, 100, 511, 512, 513, 1200]),
