@@ -95,6 +95,8 @@ typedef enum pa_dtype {
 #define PA_DEV_BAD_LEN      4u  /* a context length is < 0, above max_context_len,
                                    or needs more than max_blocks_per_seq blocks */
 #define PA_DEV_TIMEOUT      8u  /* a bounded wait inside a kernel ran out */
+#define PA_DEV_SLOT_MISMATCH 16u /* a fused write's slot is not the newest position of its
+                                    sequence (the token is stored; the decode may miss it) */
 
 /* Supported shapes: head_size in {64, 128, 256}; block_size in [1, 1024];
  * partition_size a positive multiple of 32 (512 on the pages). */
@@ -214,6 +216,44 @@ pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cach
                                 pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
                                 float v_scale, int partition_size, void* workspace,
                                 size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/*
+ * pa_write_decode -- the KV write and the single-pass decode of one step in
+ * ONE launch (the TGI deep-dive, sec. 4.1, runs paged_reshape_and_cache and
+ * then paged_attention every decode step; here the write is folded into the
+ * decode kernel). Each sequence s brings one new token: key[s], value[s]
+ * ([num_seqs][num_kv_heads][head_size], of the query type) stored at
+ * slot_mapping[s] exactly as pa_reshape_and_cache stores it (bit copy, or E4M3
+ * with k_scale / v_scale), and that token is position context_lens[s] - 1 of
+ * the decode. The kernel that loads the stage holding that position stores the
+ * token first and then reads it back through its bulk copy, so the slot must be
+ * that position of the sequence's own block table (else PA_DEV_SLOT_MISMATCH;
+ * a token written elsewhere is not ordered with the reads of other sequences).
+ * A negative slot stores nothing (the decode still covers the context). A
+ * sequence with context_len 0 stores nothing and gets a zero output.
+ * Other arguments as pa_decode; k_cache / v_cache are written.
+ */
+pa_status pa_write_decode(void* out, const void* query, const void* key, const void* value,
+                          const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                          int max_context_len, float scale, pa_dtype q_dtype,
+                          pa_dtype cache_dtype, float k_scale, float v_scale,
+                          uint32_t* dev_status, void* stream);
+
+/* pa_write_decode_partitioned -- the same with the partitioned decode: the
+ * partition kernel (which also stores the new tokens) and the merge kernel. */
+pa_status pa_write_decode_partitioned(void* out, const void* query, const void* key,
+                                      const void* value, const int64_t* slot_mapping,
+                                      void* k_cache, void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size, int64_t num_blocks,
+                                      int max_context_len, float scale, pa_dtype q_dtype,
+                                      pa_dtype cache_dtype, float k_scale, float v_scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      uint32_t* dev_status, void* stream);
 
 /*
  * pa_decode_partitioned_static -- pa_decode_partitioned for callers that

@@ -30,7 +30,7 @@ _lib = None
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
-DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT, DEV_SLOT_MISMATCH = 1, 2, 4, 8, 16
 
 DEFAULT_PARTITION_SIZE = 512
 
@@ -75,12 +75,17 @@ def lib() -> ctypes.CDLL:
                                             F, F, I, P, S, P, P]
         L.pa_decode_partitioned_static.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I64, I,
                                                    F, I, I, F, F, I, P, P]
+        L.pa_write_decode.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I,
+                                      F, F, P, P]
+        L.pa_write_decode_partitioned.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I,
+                                                  I64, I, F, I, I, F, F, I, P, S, P, P]
         L.pa_decode_choose.argtypes = [I, I, I, I, I]
         L.pa_status_string.argtypes = [I]
         L.pa_status_string.restype = ctypes.c_char_p
         for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_layout",
                      "pa_decode_partitions", "pa_merge", "pa_decode_partitioned",
-                     "pa_decode_partitioned_static",
+                     "pa_decode_partitioned_static", "pa_write_decode",
+                     "pa_write_decode_partitioned",
                      "pa_decode_choose", "pa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -230,6 +235,45 @@ def decode_partitioned(out, query, k_cache, v_cache, block_tables, context_lens,
         _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), partition_size,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status),
         _stream(stream)), "pa_decode_partitioned")
+
+
+def _new_tokens(key, value, slot_mapping, query, k_cache):
+    S, Hkv, D = key.shape
+    if value.shape != key.shape or S != query.shape[0] or (Hkv, D) != (k_cache.shape[1], k_cache.shape[3]):
+        raise ValueError("key/value must be [num_seqs, num_kv_heads, head_size]")
+    if key.dtype != query.dtype or value.dtype != query.dtype:
+        raise ValueError("new key/value must have the query's dtype")
+    if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != S:
+        raise ValueError("slot_mapping must be int64 [num_seqs]")
+
+
+def write_decode(out, query, key, value, k_cache, v_cache, slot_mapping, block_tables,
+                 context_lens, max_context_len, scale, k_scale=1.0, v_scale=1.0, dev_status=None,
+                 stream=None) -> None:
+    """KV write of each sequence's newest token and single-pass decode, one launch."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _new_tokens(key, value, slot_mapping, query, k_cache)
+    _check(lib().pa_write_decode(
+        _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), S, Hq, Hkv, D, B, nb,
+        int(max_context_len), float(scale), _dtype(query), _dtype(k_cache), float(k_scale),
+        float(v_scale), _ptr(dev_status), _stream(stream)), "pa_write_decode")
+
+
+def write_decode_partitioned(out, query, key, value, k_cache, v_cache, slot_mapping,
+                             block_tables, context_lens, max_context_len, scale, workspace,
+                             partition_size=DEFAULT_PARTITION_SIZE, k_scale=1.0, v_scale=1.0,
+                             dev_status=None, stream=None) -> None:
+    """KV write fused into the partition kernel, then the merge."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _new_tokens(key, value, slot_mapping, query, k_cache)
+    _check(lib().pa_write_decode_partitioned(
+        _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), S, Hq, Hkv, D, B, nb,
+        int(max_context_len), float(scale), _dtype(query), _dtype(k_cache), float(k_scale),
+        float(v_scale), partition_size, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
+        "pa_write_decode_partitioned")
 
 
 STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024

@@ -186,6 +186,18 @@ pa_status bind_workspace(DecodeParams& p, int num_seqs, int num_q_heads, int hea
     return PA_OK;
 }
 
+void bind_fused_write(DecodeParams& p, const void* key, const void* value,
+                      const int64_t* slot_mapping, void* k_cache, void* v_cache, float k_scale,
+                      float v_scale) {
+    p.new_key = key;
+    p.new_value = value;
+    p.new_slots = slot_mapping;
+    p.wk_cache = k_cache;
+    p.wv_cache = v_cache;
+    p.k_scale_w = k_scale;
+    p.v_scale_w = v_scale;
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,6 +244,59 @@ pa_status pa_decode(void* out, const void* query, const void* k_cache, const voi
     p.out = out;
     return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, false,
                                        static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_write_decode(void* out, const void* query, const void* key, const void* value,
+                          const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* context_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_size, int block_size, int64_t num_blocks,
+                          int max_context_len, float scale, pa_dtype q_dtype,
+                          pa_dtype cache_dtype, float k_scale, float v_scale,
+                          uint32_t* dev_status, void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
+    p.out = out;
+    return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, false,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_write_decode_partitioned(void* out, const void* query, const void* key,
+                                      const void* value, const int64_t* slot_mapping,
+                                      void* k_cache, void* v_cache, const int32_t* block_tables,
+                                      int max_blocks_per_seq, const int32_t* context_lens,
+                                      int num_seqs, int num_q_heads, int num_kv_heads,
+                                      int head_size, int block_size, int64_t num_blocks,
+                                      int max_context_len, float scale, pa_dtype q_dtype,
+                                      pa_dtype cache_dtype, float k_scale, float v_scale,
+                                      int partition_size, void* workspace, size_t workspace_bytes,
+                                      uint32_t* dev_status, void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if ((st = check_partition_size(partition_size)) != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
+                             workspace, workspace_bytes)) != PA_OK)
+        return st;
+    bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    st = from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, true, cs));
+    if (st != PA_OK) return st;
+    return from_cuda(launch_merge(out, p.tmp_out, p.max_logits, p.exp_sums, context_lens, num_seqs,
+                                  num_q_heads, head_size, partition_size, p.max_parts, q_dtype,
+                                  dev_status, cs));
 }
 
 size_t pa_decode_partitioned_workspace_bytes(int num_seqs, int num_q_heads, int head_size,
@@ -289,7 +354,7 @@ pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, con
     pa_status st = check_partition_size(partition_size);
     if (st != PA_OK) return st;
     if ((int)out_dtype < 0 || (int)out_dtype > 3) return PA_ERR_INVALID_ARG;
-    if (!is_compute_type(out_dtype) || head_size > 256) return PA_ERR_UNSUPPORTED;
+    if (!is_compute_type(out_dtype) || !supported_head_size(head_size)) return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;

@@ -29,6 +29,7 @@
 #pragma once
 
 #include "device_common.cuh"
+#include "kv_store.cuh"
 #include "launch.h"
 
 namespace pagedkv {
@@ -172,6 +173,8 @@ paged_decode_simt_kernel(const DecodeParams p) {
             }
             const int t_lo = T0 + k * kStageTokens;
             const int t_hi = min(t_lo + kStageTokens, Tend);
+            if (p.new_key && L - 1 >= t_lo && L - 1 < t_hi)
+                fused_write_token<QT, CT, D>(p, s, kvh, L, lane);
             const int j0 = t_lo / B;
             const int nseg = (t_hi - 1) / B - j0 + 1;             // <= 32
             uint32_t bytes = 0;

@@ -28,6 +28,7 @@
 #include <cuda.h>
 
 #include "device_common.cuh"
+#include "kv_store.cuh"
 #include "launch.h"
 
 namespace pagedkv {
@@ -251,6 +252,8 @@ paged_decode_tma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             }
             const int t_lo = T0 + k * kTmaStageTokens;
             const int t_hi = min(t_lo + kTmaStageTokens, Tend);
+            if (p.new_key && L - 1 >= t_lo && L - 1 < t_hi)
+                fused_write_token<QT, CT, D>(p, s, kvh, L, lane);
             const int j0 = t_lo / B;
             const int nseg = (t_hi - 1) / B - j0 + 1;           // 1 when B >= 32
             uint32_t bytes = 0;

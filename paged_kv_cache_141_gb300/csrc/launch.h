@@ -33,6 +33,15 @@ struct DecodeParams {
     int sub_groups;               // group / heads per work unit
     float q_mul;                  // scale * log2(e) * (E4M3 cache ? k_scale : 1)
     float v_mul;                  // E4M3 cache ? v_scale : 1
+    // fused KV write (all null for a plain decode): each sequence's newest
+    // key/value [S, Hkv, D] of the query type, stored at new_slots[s]
+    const void* new_key;
+    const void* new_value;
+    const int64_t* new_slots;
+    void* wk_cache;               // the caches, writable (same addresses as k_cache / v_cache)
+    void* wv_cache;
+    float k_scale_w;              // E4M3 quantisation scales of the write
+    float v_scale_w;
 };
 
 // Generic CUDA-core decode; one launcher per (query type, cache type).

@@ -2,47 +2,37 @@
 // deep-dive" (lpnh.cn) sec. 4.1: long sequences are cut into partitions that
 // are computed in parallel and then merged). For each (sequence, query head):
 //   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p.
-// One CTA per (head, sequence); 128 threads stride over the head components.
-// Partition weights are staged through shared memory in chunks, so any number
-// of partitions fits.
+// One warp per (sequence, head), eight per CTA: the lanes take partitions for
+// the maximum and the weights (warp shuffles, no block barriers), then every
+// lane accumulates head_size/32 components of each partition's output, the
+// weight broadcast by shuffle, reading each partition's row as coalesced
+// vectors. One partition is copied; none gives zeros.
 #include "device_common.cuh"
 #include "launch.h"
 
 namespace pagedkv {
 
-constexpr int kMergeThreads = 128;
-constexpr int kMergeChunk = 1024;
+constexpr int kMergeWarps = 8;
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    float r = red[0];
-#pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w) r = fmaxf(r, red[w]);
-    return r;
-}
-
-template <typename OT>
-__global__ void __launch_bounds__(kMergeThreads)
+template <int D, typename OT>
+__global__ void __launch_bounds__(kMergeWarps * 32)
 paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
                    const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
-                   const int32_t* __restrict__ context_lens, int num_q_heads, int D,
+                   const int32_t* __restrict__ context_lens, int num_seqs, int num_q_heads,
                    int partition_size, int max_parts, uint32_t* status) {
-    __shared__ float w_s[kMergeChunk];
-    __shared__ float red[kMergeThreads / 32];
-    const int h = blockIdx.x;
-    const int s = blockIdx.y;
+    constexpr int EPL = D / 32;                // components per lane
+    const int lane = threadIdx.x & 31;
+    const long long item = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+    if (item >= (long long)num_seqs * num_q_heads) return;
+    const int s = (int)(item / num_q_heads);
+    const int h = (int)(item - (long long)s * num_q_heads);
     const size_t row = (size_t)s * num_q_heads + h;
     OT* o = out + row * D;
 
     int L = context_lens[s];
     const long long cap = (long long)max_parts * partition_size;
     if (L < 0 || L > cap) {
-        if (threadIdx.x == 0 && h == 0 && status) atomicOr(status, PA_DEV_BAD_LEN);
+        if (lane == 0 && h == 0 && status) atomicOr(status, PA_DEV_BAD_LEN);
         L = L < 0 ? 0 : (int)cap;
     }
     const int n = (L + partition_size - 1) / partition_size;
@@ -50,65 +40,107 @@ paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
     const float* es = exp_sums + row * max_parts;
     const float* to = tmp_out + row * max_parts * D;
 
-    if (n == 0) {
-        for (int e = threadIdx.x; e < D; e += kMergeThreads) o[e] = from_float<OT>(0.f);
-        return;
-    }
-    if (n == 1) {  // one partition: its normalised output is the answer
-        for (int e = threadIdx.x; e < D; e += kMergeThreads) o[e] = from_float<OT>(to[e]);
+    float acc[EPL];
+    if (n <= 1) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = n == 1 ? to[lane * EPL + e] : 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[lane * EPL + e] = from_float<OT>(acc[e]);
         return;
     }
 
     float M = -INFINITY;
-    for (int i = threadIdx.x; i < n; i += kMergeThreads) M = fmaxf(M, ml[i]);
-    M = block_max(M, red);
+    for (int i = lane; i < n; i += 32) M = fmaxf(M, ml[i]);
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
 
-    // each thread keeps up to two components (head_size <= 256)
-    float acc0 = 0.f, acc1 = 0.f, wsum = 0.f;
-    const int e0 = threadIdx.x, e1 = threadIdx.x + kMergeThreads;
-    for (int c0 = 0; c0 < n; c0 += kMergeChunk) {
-        const int cn = min(kMergeChunk, n - c0);
-        __syncthreads();
-        for (int i = threadIdx.x; i < cn; i += kMergeThreads)
-            w_s[i] = es[c0 + i] * fast_exp2((ml[c0 + i] - M) * kLog2e);
-        __syncthreads();
-        for (int i = 0; i < cn; ++i) {
-            const float w = w_s[i];
-            wsum += w;
-            const float* tp = to + (size_t)(c0 + i) * D;
-            if (e0 < D) acc0 = fmaf(w, tp[e0], acc0);
-            if (e1 < D) acc1 = fmaf(w, tp[e1], acc1);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    float wsum = 0.f;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int i = c0 + lane;
+        const float w = i < n ? es[i] * fast_exp2((ml[i] - M) * kLog2e) : 0.f;
+        wsum += w;
+        const int cn = min(32, n - c0);
+#pragma unroll 4
+        for (int j = 0; j < cn; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            const float* tp = to + (size_t)(c0 + j) * D + lane * EPL;
+            if constexpr (EPL == 2) {
+                const float2 v = *reinterpret_cast<const float2*>(tp);
+                acc[0] = fmaf(wj, v.x, acc[0]);
+                acc[1] = fmaf(wj, v.y, acc[1]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < EPL; e += 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(tp + e);
+                    acc[e] = fmaf(wj, v.x, acc[e]);
+                    acc[e + 1] = fmaf(wj, v.y, acc[e + 1]);
+                    acc[e + 2] = fmaf(wj, v.z, acc[e + 2]);
+                    acc[e + 3] = fmaf(wj, v.w, acc[e + 3]);
+                }
+            }
         }
     }
-    if (e0 < D) o[e0] = from_float<OT>(__fdiv_rn(acc0, wsum));
-    if (e1 < D) o[e1] = from_float<OT>(__fdiv_rn(acc1, wsum));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, m);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[lane * EPL + e] = from_float<OT>(__fdiv_rn(acc[e], wsum));
+}
+
+template <int D, typename OT>
+static cudaError_t launch_merge_t(OT* out, const float* tmp_out, const float* max_logits,
+                                  const float* exp_sums, const int32_t* context_lens, int num_seqs,
+                                  int num_q_heads, int partition_size, int max_parts,
+                                  uint32_t* status, cudaStream_t stream) {
+    const long long items = (long long)num_seqs * num_q_heads;
+    const unsigned grid = (unsigned)((items + kMergeWarps - 1) / kMergeWarps);
+    paged_merge_kernel<D, OT><<<grid, kMergeWarps * 32, 0, stream>>>(
+        out, tmp_out, max_logits, exp_sums, context_lens, num_seqs, num_q_heads, partition_size,
+        max_parts, status);
+    return cudaGetLastError();
+}
+
+template <typename OT>
+static cudaError_t launch_merge_o(void* out, const float* tmp_out, const float* max_logits,
+                                  const float* exp_sums, const int32_t* context_lens, int num_seqs,
+                                  int num_q_heads, int head_size, int partition_size, int max_parts,
+                                  uint32_t* status, cudaStream_t stream) {
+    OT* o = static_cast<OT*>(out);
+    switch (head_size) {
+    case 64:
+        return launch_merge_t<64>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                  num_q_heads, partition_size, max_parts, status, stream);
+    case 128:
+        return launch_merge_t<128>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                   num_q_heads, partition_size, max_parts, status, stream);
+    case 256:
+        return launch_merge_t<256>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                   num_q_heads, partition_size, max_parts, status, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int head_size, int partition_size, int max_parts,
                          pa_dtype out_dtype, uint32_t* status, cudaStream_t stream) {
-    dim3 grid(num_q_heads, num_seqs);
     switch (out_dtype) {
     case PA_F32:
-        paged_merge_kernel<float><<<grid, kMergeThreads, 0, stream>>>(
-            static_cast<float*>(out), tmp_out, max_logits, exp_sums, context_lens, num_q_heads,
-            head_size, partition_size, max_parts, status);
-        break;
+        return launch_merge_o<float>(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                     num_q_heads, head_size, partition_size, max_parts, status,
+                                     stream);
     case PA_F16:
-        paged_merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(
-            static_cast<__half*>(out), tmp_out, max_logits, exp_sums, context_lens, num_q_heads,
-            head_size, partition_size, max_parts, status);
-        break;
+        return launch_merge_o<__half>(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                      num_q_heads, head_size, partition_size, max_parts, status,
+                                      stream);
     case PA_BF16:
-        paged_merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(
-            static_cast<__nv_bfloat16*>(out), tmp_out, max_logits, exp_sums, context_lens,
-            num_q_heads, head_size, partition_size, max_parts, status);
-        break;
+        return launch_merge_o<__nv_bfloat16>(out, tmp_out, max_logits, exp_sums, context_lens,
+                                             num_seqs, num_q_heads, head_size, partition_size,
+                                             max_parts, status, stream);
     default:
         return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace pagedkv

@@ -9,54 +9,12 @@
 // round-to-nearest-even and saturation to +-448 (CUDA's E4M3 converter).
 // A grid-stride loop keeps the grid at a multiple of the SM count.
 #include "device_common.cuh"
+#include "kv_store.cuh"
 #include "launch.h"
 
 namespace pagedkv {
 
 constexpr int kWriteThreads = 256;
-
-template <typename TI>
-struct Vec16 {
-    static constexpr int n = 16 / (int)sizeof(TI);
-};
-
-
-template <typename TI>
-__device__ __forceinline__ void widen16(const uint4& w, float (&x)[Vec16<TI>::n]) {
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-    if constexpr (std::is_same<TI, float>::value) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[i] = __uint_as_float(ws[i]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 f;
-            if constexpr (std::is_same<TI, __half>::value)
-                f = __half22float2(*reinterpret_cast<const __half2*>(&ws[i]));
-            else
-                f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ws[i]));
-            x[2 * i] = f.x;
-            x[2 * i + 1] = f.y;
-        }
-    }
-}
-
-template <typename TI>
-__device__ __forceinline__ void store_e4m3(uint8_t* dst, const uint4& w, float scale) {
-    constexpr int N = Vec16<TI>::n;   // 4 (binary32) or 8 (16-bit types)
-    float x[N];
-    widen16<TI>(w, x);
-    uint32_t packed[N / 4];
-#pragma unroll
-    for (int i = 0; i < N; i += 2) {
-        const float2 q = make_float2(__fdiv_rn(x[i], scale), __fdiv_rn(x[i + 1], scale));
-        const uint32_t two = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
-        if ((i & 2) == 0) packed[i / 4] = two;
-        else packed[i / 4] |= two << 16;
-    }
-    if constexpr (N == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-    else *reinterpret_cast<uint32_t*>(dst) = packed[0];
-}
 
 template <typename TI, bool kE4M3>
 __global__ void __launch_bounds__(kWriteThreads)
