@@ -151,12 +151,18 @@ def dist_env():
 # ----------------------------------------------------------------------------- workload
 
 class Step:
-    """Device-resident inputs of one decode step and the calls that run it."""
+    """Device-resident inputs of one decode step and the calls that run it.
 
-    def __init__(self, case, device, partition_size=512):
+    form "fused":    pa_write_decode_partitions (the KV write folded into the
+                     partition kernel) then pa_merge; or pa_write_decode.
+    form "separate": pa_reshape_and_cache, pa_decode_partitions, pa_merge; or
+                     pa_reshape_and_cache, pa_decode.
+    """
+
+    def __init__(self, case, device, partition_size=512, form="fused"):
         import torch
         from paged_kv_cache_141_gb300 import binding as pk
-        self.pk, self.torch, self.case, self.dev = pk, torch, case, device
+        self.pk, self.torch, self.case, self.dev, self.form = pk, torch, case, device, form
         c = case
         self.P = partition_size
 
@@ -183,52 +189,75 @@ class Step:
                                  c.v_scale, self.status)
         self.split = pk.choose(c.num_seqs, c.num_q_heads, c.num_kv_heads, c.max_context_len,
                                partition_size) == 1
+        if form == "fused" and c.kv_dtype != c.q_dtype:
+            self.form = form = "separate"     # the fused write takes tokens of the query type
         self.ws = pk.alloc_workspace(c.num_seqs, c.num_q_heads, c.head_size, c.max_context_len,
                                      partition_size, device)
         self.views = pk.workspace_views(self.ws, c.num_seqs, c.num_q_heads, c.head_size,
                                         c.max_context_len, partition_size)
+        self.calls = self._calls()
+
+    def _calls(self):
+        pk, c = self.pk, self.case
+        common = (self.bt, self.cl, c.max_context_len, c.scale)
+
+        def write(stream=None):
+            pk.reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.ns, c.k_scale,
+                                 c.v_scale, self.status, stream)
+
+        def write_decode(stream=None):
+            pk.write_decode(self.out, self.q, self.nk, self.nv, self.kc, self.vc, self.ns,
+                            *common, c.k_scale, c.v_scale, self.status, stream)
+
+        def write_partitions(stream=None):
+            pk.write_decode_partitions(self.q, self.nk, self.nv, self.kc, self.vc, self.ns,
+                                       *common, self.ws, self.P, c.k_scale, c.v_scale,
+                                       self.status, stream)
+
+        def decode(stream=None):
+            pk.decode(self.out, self.q, self.kc, self.vc, *common, c.k_scale, c.v_scale,
+                      self.status, stream)
+
+        def partitions(stream=None):
+            pk.decode_partitions(self.q, self.kc, self.vc, *common, self.ws, self.P, c.k_scale,
+                                 c.v_scale, self.status, stream)
+
+        def merge(stream=None):
+            tmp, ml, es = self.views
+            pk.merge(self.out, tmp, ml, es, self.cl, self.P, self.status, stream)
+
+        if self.form == "fused":
+            if self.split:
+                return [("write+decode", write_partitions), ("merge", merge)]
+            return [("write+decode", write_decode)]
+        if self.split:
+            return [("reshape_and_cache", write), ("decode", partitions), ("merge", merge)]
+        return [("reshape_and_cache", write), ("decode", decode)]
 
     @property
     def launches_per_step(self) -> int:
-        return 3 if self.split else 2
-
-    def write(self, stream=None):
-        c = self.case
-        self.pk.reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.ns, c.k_scale,
-                                  c.v_scale, self.status, stream)
-
-    def decode_main(self, stream=None):
-        c = self.case
-        if self.split:
-            self.pk.decode_partitions(self.q, self.kc, self.vc, self.bt, self.cl,
-                                      c.max_context_len, c.scale, self.ws, self.P, c.k_scale,
-                                      c.v_scale, self.status, stream)
-        else:
-            self.pk.decode(self.out, self.q, self.kc, self.vc, self.bt, self.cl,
-                           c.max_context_len, c.scale, c.k_scale, c.v_scale, self.status, stream)
-
-    def decode_merge(self, stream=None):
-        if self.split:
-            tmp, ml, es = self.views
-            self.pk.merge(self.out, tmp, ml, es, self.cl, self.P, self.status, stream)
+        return len(self.calls)
 
     def step(self, stream=None):
-        self.write(stream)
-        self.decode_main(stream)
-        self.decode_merge(stream)
+        for _, f in self.calls:
+            f(stream)
 
     def bytes_per_step(self) -> dict:
+        """Algorithmic bytes. The step: K/V read, Q read, out written, and the
+        new tokens' K/V read and stored with their slots. The decode kernel
+        (partition or single pass): K/V and Q read, and its output -- every
+        partition's partials, or `out` -- plus, in the fused form, the new
+        tokens' write."""
         c = self.case
         write = c.write_bytes()
         decode = c.kv_bytes() + c.qo_bytes()
-        # the partition (or single-pass) kernel's algorithmic bytes: K/V read,
-        # Q read, and its output (partials with their (max, sum), or `out`)
+        q_bytes = c.qo_bytes() // 2
         if self.split:
-            n_parts = int(sum(-(-int(L) // self.P) for L in c.context_lens))
-            main_out = n_parts * c.num_q_heads * (c.head_size + 2) * 4
+            parts = sum(-(-int(L) // self.P) for L in c.context_lens)
+            produced = parts * c.num_q_heads * (c.head_size + 2) * 4
         else:
-            main_out = c.num_seqs * c.num_q_heads * c.head_size * 2
-        main = c.kv_bytes() + c.qo_bytes() // 2 + main_out
+            produced = q_bytes
+        main = c.kv_bytes() + q_bytes + produced + (write if self.form == "fused" else 0)
         return {"write": write, "decode": decode, "total": write + decode, "main_kernel": main}
 
 
@@ -246,7 +275,10 @@ def run_ours(args):
     torch.cuda.set_device(device)
     from paged_kv_cache_141_gb300 import workloads as W
     case = W.config_case(args.config)
-    st = Step(case, device, args.partition_size)
+    from paged_kv_cache_141_gb300 import binding as pk
+    P = (pk.partition_size(case.num_seqs, case.num_kv_heads, case.max_context_len)
+         if args.partition_size == "auto" else int(args.partition_size))
+    st = Step(case, device, P, args.form)
     stream = torch.cuda.current_stream(device)
 
     # correctness gate: one step, no device-side errors
@@ -260,7 +292,8 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    ncall = st.launches_per_step
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(ncall + 1)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -272,21 +305,17 @@ def run_ours(args):
     for i in range(K):
         e = ev[i]
         e[0].record(stream)
-        st.write()
-        e[1].record(stream)
-        st.decode_main()
-        e[2].record(stream)
-        st.decode_merge()
-        e[3].record(stream)
+        for j, (_, f) in enumerate(st.calls):
+            f()
+            e[j + 1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if sampler else None
     total_ms = t_start.elapsed_time(t_end)
-    write_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    main_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    merge_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    call_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
+               for j, (name, _) in enumerate(st.calls)}
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=device)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -297,7 +326,8 @@ def run_ours(args):
     value = world * by["total"] / (ms_per_step * 1e-3) / 1e9
     seqs_per_s = world * case.num_seqs / (ms_per_step * 1e-3)
     peak, peak_kind = hbm_peak()
-    main_avg = sum(main_ms) / K
+    main_name = "write+decode" if "write+decode" in call_ms else "decode"
+    main_avg = call_ms[main_name]
     achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
 
     e2e = run_e2e(st, max(20, min(200, K // 10)), device)
@@ -316,20 +346,20 @@ def run_ours(args):
                    "block_size": case.block_size, "kv_dtype": case.cache_dtype,
                    "context_lens": "log-uniform [512, 4096]" if args.config == 3 else "see workloads",
                    "total_context_tokens": case.total_tokens, "partition_size": st.P,
-                   "decode_form": "partitioned+merge" if st.split else "single-pass",
+                   "decode_form": ("partitioned" if st.split else "single-pass") + ", " + st.form,
                    "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2); no flush"
                          % (case.kv_bytes() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "frac_of_hbm_peak": round(value / peak, 4),
         "seqs_per_s_per_layer": round(seqs_per_s, 1),
         "bytes_per_step": by,
-        "kernel_ms": {"reshape_and_cache": round(sum(write_ms) / K, 5),
-                      "decode_main": round(main_avg, 5),
-                      "merge": round(sum(merge_ms) / K, 5)},
+        "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
-                     "kernel": decode_kernel_label(case) + (" (partition kernel)" if st.split
-                                                             else " (single pass)"),
+                     "kernel": decode_kernel_label(case) + (
+                         (" (partition kernel" if st.split else " (single pass")
+                         + (", KV write fused)" if st.form == "fused" else ")")),
+                     "timed_call": main_name,
                      "peak_kind": f"{peak_kind} (HBM copy, MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": by["main_kernel"]},
@@ -474,7 +504,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
-    ap.add_argument("--partition-size", type=int, default=512)
+    ap.add_argument("--partition-size", default="auto",
+                    help="tokens per partition, or 'auto' (the library's choice)")
+    ap.add_argument("--form", choices=["fused", "separate"], default="fused",
+                    help="how the step is launched (see Step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -207,7 +207,7 @@ pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, con
                    uint32_t* dev_status, void* stream);
 
 /* pa_decode_partitioned -- pa_decode_partitions followed by pa_merge on the
- * same stream. */
+ * same stream (two kernels). */
 pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cache,
                                 const void* v_cache, const int32_t* block_tables,
                                 int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
@@ -242,8 +242,21 @@ pa_status pa_write_decode(void* out, const void* query, const void* key, const v
                           pa_dtype cache_dtype, float k_scale, float v_scale,
                           uint32_t* dev_status, void* stream);
 
-/* pa_write_decode_partitioned -- the same with the partitioned decode: the
- * partition kernel (which also stores the new tokens) and the merge kernel. */
+/* pa_write_decode_partitions -- the partition kernel of the split decode
+ * with the new tokens' write folded in (pa_decode_partitions + the write):
+ * stores the tokens and every partition's partials in the workspace. */
+pa_status pa_write_decode_partitions(const void* query, const void* key, const void* value,
+                                     const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_size, int block_size,
+                                     int64_t num_blocks, int max_context_len, float scale,
+                                     pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                                     float v_scale, int partition_size, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/* pa_write_decode_partitioned -- pa_write_decode_partitions, then pa_merge on
+ * the same stream: two launches for the whole step instead of three. */
 pa_status pa_write_decode_partitioned(void* out, const void* query, const void* key,
                                       const void* value, const int64_t* slot_mapping,
                                       void* k_cache, void* v_cache, const int32_t* block_tables,
@@ -299,6 +312,15 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  */
 int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,
                      int partition_size);
+
+/*
+ * pa_decode_partition_size -- a partition size for this device: 512 (the
+ * pages' _PARTITION_SIZE) doubled (up to 2048) while the longest context
+ * still spans three or more partitions and the launch keeps about four waves of
+ * work units. Longer partitions mean fewer CTA start-ups and fewer partials to
+ * merge. Never fails.
+ */
+int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len);
 
 /* Human-readable name of a status code (a static string). */
 const char* pa_status_string(pa_status status);

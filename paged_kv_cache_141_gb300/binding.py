@@ -79,14 +79,17 @@ def lib() -> ctypes.CDLL:
                                       F, F, P, P]
         L.pa_write_decode_partitioned.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I,
                                                   I64, I, F, I, I, F, F, I, P, S, P, P]
+        L.pa_write_decode_partitions.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64,
+                                                 I, F, I, I, F, F, I, P, S, P, P]
         L.pa_decode_choose.argtypes = [I, I, I, I, I]
+        L.pa_decode_partition_size.argtypes = [I, I, I]
         L.pa_status_string.argtypes = [I]
         L.pa_status_string.restype = ctypes.c_char_p
         for name in ("pa_reshape_and_cache", "pa_decode", "pa_decode_workspace_layout",
                      "pa_decode_partitions", "pa_merge", "pa_decode_partitioned",
                      "pa_decode_partitioned_static", "pa_write_decode",
-                     "pa_write_decode_partitioned",
-                     "pa_decode_choose", "pa_version"):
+                     "pa_write_decode_partitioned", "pa_write_decode_partitions",
+                     "pa_decode_choose", "pa_decode_partition_size", "pa_version"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return _lib
@@ -260,11 +263,26 @@ def write_decode(out, query, key, value, k_cache, v_cache, slot_mapping, block_t
         float(v_scale), _ptr(dev_status), _stream(stream)), "pa_write_decode")
 
 
+def write_decode_partitions(query, key, value, k_cache, v_cache, slot_mapping, block_tables,
+                            context_lens, max_context_len, scale, workspace,
+                            partition_size=DEFAULT_PARTITION_SIZE, k_scale=1.0, v_scale=1.0,
+                            dev_status=None, stream=None) -> None:
+    """The partition kernel with the new tokens' KV write folded in (partials only)."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    _new_tokens(key, value, slot_mapping, query, k_cache)
+    _check(lib().pa_write_decode_partitions(
+        _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), mb, _ptr(context_lens), S, Hq, Hkv, D, B, nb, int(max_context_len),
+        float(scale), _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale),
+        partition_size, _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(dev_status), _stream(stream)), "pa_write_decode_partitions")
+
+
 def write_decode_partitioned(out, query, key, value, k_cache, v_cache, slot_mapping,
                              block_tables, context_lens, max_context_len, scale, workspace,
                              partition_size=DEFAULT_PARTITION_SIZE, k_scale=1.0, v_scale=1.0,
                              dev_status=None, stream=None) -> None:
-    """KV write fused into the partition kernel, then the merge."""
+    """KV write fused into the partition kernel, then the merge kernel."""
     S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
     _new_tokens(key, value, slot_mapping, query, k_cache)
     _check(lib().pa_write_decode_partitioned(
@@ -299,6 +317,11 @@ def decode_partitioned_static(out, query, k_cache, v_cache, block_tables, contex
         raise PagedKVError(f"pa_decode_partitioned_static: the problem needs {need} bytes of "
                            f"workspace, above the fixed {STATIC_WORKSPACE_BYTES}", status)
     _check(status, "pa_decode_partitioned_static")
+
+
+def partition_size(num_seqs, num_kv_heads, max_context_len) -> int:
+    """The library's partition size for this device (512, 1024 or 2048)."""
+    return int(lib().pa_decode_partition_size(num_seqs, num_kv_heads, int(max_context_len)))
 
 
 def choose(num_seqs, num_q_heads, num_kv_heads, max_context_len,

@@ -268,6 +268,32 @@ pa_status pa_write_decode(void* out, const void* query, const void* key, const v
                                        static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_write_decode_partitions(const void* query, const void* key, const void* value,
+                                     const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                     const int32_t* block_tables, int max_blocks_per_seq,
+                                     const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                     int num_kv_heads, int head_size, int block_size,
+                                     int64_t num_blocks, int max_context_len, float scale,
+                                     pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale,
+                                     float v_scale, int partition_size, void* workspace,
+                                     size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if ((st = check_partition_size(partition_size)) != PA_OK) return st;
+    if (num_seqs == 0) return PA_OK;
+    if (!key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
+                             workspace, workspace_bytes)) != PA_OK)
+        return st;
+    bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
+    return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, true,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_write_decode_partitioned(void* out, const void* query, const void* key,
                                       const void* value, const int64_t* slot_mapping,
                                       void* k_cache, void* v_cache, const int32_t* block_tables,
@@ -278,25 +304,22 @@ pa_status pa_write_decode_partitioned(void* out, const void* query, const void* 
                                       pa_dtype cache_dtype, float k_scale, float v_scale,
                                       int partition_size, void* workspace, size_t workspace_bytes,
                                       uint32_t* dev_status, void* stream) {
-    DecodeParams p;
-    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
-                                block_size, num_blocks, max_context_len, scale, q_dtype,
-                                cache_dtype, k_scale, v_scale, dev_status, p);
-    if (st != PA_OK) return st;
-    if ((st = check_partition_size(partition_size)) != PA_OK) return st;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
-    if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
-                             workspace, workspace_bytes)) != PA_OK)
-        return st;
-    bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    st = from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, true, cs));
-    if (st != PA_OK) return st;
-    return from_cuda(launch_merge(out, p.tmp_out, p.max_logits, p.exp_sums, context_lens, num_seqs,
-                                  num_q_heads, head_size, partition_size, p.max_parts, q_dtype,
-                                  dev_status, cs));
+    if (num_seqs > 0 && !out) return PA_ERR_INVALID_ARG;
+    pa_status st = pa_write_decode_partitions(query, key, value, slot_mapping, k_cache, v_cache,
+                                              block_tables, max_blocks_per_seq, context_lens,
+                                              num_seqs, num_q_heads, num_kv_heads, head_size,
+                                              block_size, num_blocks, max_context_len, scale,
+                                              q_dtype, cache_dtype, k_scale, v_scale,
+                                              partition_size, workspace, workspace_bytes,
+                                              dev_status, stream);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
+    const uint8_t* w = static_cast<const uint8_t*>(workspace);
+    return pa_merge(out, reinterpret_cast<const float*>(w + l.tmp_out),
+                    reinterpret_cast<const float*>(w + l.max_logits),
+                    reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
+                    num_q_heads, head_size, partition_size,
+                    max_partitions(max_context_len, partition_size), q_dtype, dev_status, stream);
 }
 
 size_t pa_decode_partitioned_workspace_bytes(int num_seqs, int num_q_heads, int head_size,
@@ -385,6 +408,30 @@ pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cach
                     reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
                     num_q_heads, head_size, partition_size,
                     max_partitions(max_context_len, partition_size), q_dtype, dev_status, stream);
+}
+
+int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len) {
+    if (num_seqs <= 0 || num_kv_heads <= 0 || max_context_len <= 0) return 512;
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        sms = 148;
+    }
+    // Longer partitions mean fewer CTA start-ups and fewer partials, while the
+    // longest context still spans three or more of them (balance) and the launch
+    // keeps about four waves of work units (3 CTAs per SM), estimating a
+    // context's length at half the maximum.
+    const long long want = 4ll * 3 * sms;
+    int P = 512;
+    while (P < 2048) {
+        const int next = 2 * P;
+        const long long units = (long long)num_seqs * num_kv_heads *
+                                ((max_context_len / 2 + next - 1) / next);
+        if (max_context_len < 3 * next || units < want) break;
+        P = next;
+    }
+    return P;
 }
 
 int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_context_len,

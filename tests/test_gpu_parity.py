@@ -322,3 +322,4 @@ def test_host_argument_errors():
         kc8 = torch.zeros(4, 2, 16, 128, dtype=torch.uint8, device="cuda")
         pk.decode(q, q, kc8, kc8, d.block_tables, d.context_lens, 10, 0.1)
     assert e.value.status == pk.PA_ERR_UNSUPPORTED
+
