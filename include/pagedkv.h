@@ -79,7 +79,8 @@ typedef enum pa_status {
     PA_ERR_INVALID_ARG = 1,   /* a NULL pointer, a negative size, inconsistent shapes */
     PA_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement */
     PA_ERR_WORKSPACE = 3,     /* the workspace is NULL, misaligned or too small */
-    PA_ERR_CUDA = 4           /* a CUDA call or launch failed */
+    PA_ERR_CUDA = 4,          /* a CUDA call or launch failed */
+    PA_ERR_NO_BLOCKS = 5      /* the block allocator has too few free blocks */
 } pa_status;
 
 typedef enum pa_dtype {
@@ -301,6 +302,61 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
                                        int max_context_len, float scale, pa_dtype q_dtype,
                                        pa_dtype cache_dtype, float k_scale, float v_scale,
                                        int partition_size, uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Block management: the host-side allocator and the copy-on-write copy.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * pa_copy_blocks -- copy whole physical blocks (every KV head of K and of V)
+ * for each (src, dst) pair of block_pairs ([num_pairs][2] int64, device), the
+ * copy of copy-on-write ("vLLM Page Attention Continuous Batching" (lbrq.cn),
+ * "Sharing KV Cache-COW"). A pair naming a block outside [0, num_blocks) is
+ * skipped and sets PA_DEV_BAD_BLOCK_ID. Pairs must not write the same dst, or
+ * read a block another pair writes, in one call (they run concurrently).
+ */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs,
+                         int64_t num_pairs, int num_kv_heads, int head_size, int block_size,
+                         int64_t num_blocks, pa_dtype cache_dtype, uint32_t* dev_status,
+                         void* stream);
+
+/*
+ * pa_block_allocator -- host-side free list of physical block ids with
+ * reference counts (TGI deep-dive sec. 4.3 SimpleAllocator: div_ceil(tokens,
+ * block_size) blocks taken from the end of the free list, block 0 reserved;
+ * "Continuous Batching and PagedAttention" sec. 3.2: fork shares blocks by
+ * reference, free returns a block when its count reaches zero). Host memory
+ * only; every call validates first and changes nothing when it fails; calls
+ * are serialised by an internal mutex.
+ *
+ *  create      num_blocks ids, block 0 kept out of the free list if
+ *              reserve_block0 (NULL on bad arguments or no memory).
+ *  allocate    ceil(num_tokens / block_size) blocks into blocks[], reference
+ *              count 1; PA_ERR_NO_BLOCKS (nothing taken) when short.
+ *  fork        one more reference to each listed block (all must be held).
+ *  free        one reference less for each listed entry; a block returns to
+ *              the free list at zero. Listing a block more often than it is
+ *              referenced is PA_ERR_INVALID_ARG.
+ *  append_slot the slot of a sequence's token at `position` given its block
+ *              table (table_len entries, room for capacity): a token starting
+ *              a new block gets a fresh block appended; a token in a block
+ *              referenced by others (count > 1) triggers copy-on-write: a fresh
+ *              block replaces it in the table, the old one loses a reference,
+ *              and (*copy_src, *copy_dst) name the copy the caller must make
+ *              (pa_copy_blocks) before writing; otherwise both are -1.
+ */
+typedef struct pa_block_allocator pa_block_allocator;
+pa_block_allocator* pa_allocator_create(int64_t num_blocks, int block_size, int reserve_block0);
+void pa_allocator_destroy(pa_block_allocator* allocator);
+int64_t pa_allocator_num_free(pa_block_allocator* allocator);
+int32_t pa_allocator_refcount(pa_block_allocator* allocator, int32_t block);
+pa_status pa_allocator_allocate(pa_block_allocator* allocator, int64_t num_tokens, int32_t* blocks,
+                                int64_t capacity, int64_t* num_allocated);
+pa_status pa_allocator_fork(pa_block_allocator* allocator, const int32_t* blocks, int64_t n);
+pa_status pa_allocator_free(pa_block_allocator* allocator, const int32_t* blocks, int64_t n);
+pa_status pa_allocator_append_slot(pa_block_allocator* allocator, int32_t* table,
+                                   int64_t* table_len, int64_t capacity, int64_t position,
+                                   int64_t* slot, int32_t* copy_src, int32_t* copy_dst);
 
 /*
  * pa_decode_choose -- which decode to run: 0 = single pass (pa_decode),

@@ -71,6 +71,8 @@ def _bind(path: str):
     lib.or_decode_partitioned.argtypes = [P, P, P, P, P, I, P, P, I, P, P, I, P, I, I, I,
                                           I, I, I64, D, D, D, I, I]
     lib.or_decode_partitioned.restype = I
+    lib.or_copy_blocks.argtypes = [P, P, P, I64, I64, I64, I]
+    lib.or_copy_blocks.restype = I
     lib.or_blocks_needed.argtypes = [I64, I]
     lib.or_blocks_needed.restype = I64
     return lib
@@ -249,3 +251,12 @@ def merge(part_o, part_m, part_l, context_lens, partition_size: int) -> np.ndarr
 
 def blocks_needed(tokens: int, block_size: int) -> int:
     return _load().or_blocks_needed(tokens, block_size)
+
+
+def copy_blocks(k_cache, v_cache, pairs) -> int:
+    """Copy whole blocks (in place) for each (src, dst) row of pairs."""
+    pairs = np.ascontiguousarray(pairs, dtype=np.int64).reshape(-1, 2)
+    nb = k_cache.shape[0]
+    per = int(np.prod(k_cache.shape[1:]))
+    return _load().or_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], nb,
+                                  per, k_cache.dtype.itemsize)

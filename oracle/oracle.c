@@ -486,6 +486,28 @@ done:
     return rc;
 }
 
+/* The copy of copy-on-write ("vLLM Page Attention Continuous Batching"
+ * (lbrq.cn), "Sharing KV Cache-COW"): for each (src, dst) pair, every element
+ * of block src of both caches is copied to block dst. block_elems =
+ * Hkv * B * d elements of elem_bytes each, blocks contiguous. Pairs are applied
+ * in order. Returns OR_BAD_BLOCK (and stops) on an id outside the pool. */
+int or_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int64_t num_pairs,
+                   int64_t num_blocks, int64_t block_elems, int elem_bytes)
+{
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        int64_t src = pairs[2 * i], dst = pairs[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+            return OR_BAD_BLOCK;
+        for (int64_t e = 0; e < block_elems * elem_bytes; ++e) {
+            ((char*)k_cache)[dst * block_elems * elem_bytes + e] =
+                ((const char*)k_cache)[src * block_elems * elem_bytes + e];
+            ((char*)v_cache)[dst * block_elems * elem_bytes + e] =
+                ((const char*)v_cache)[src * block_elems * elem_bytes + e];
+        }
+    }
+    return OR_OK;
+}
+
 /* ceil(tokens / block_size): the number of blocks a sequence of `tokens`
  * tokens occupies ([TGI] sec. 4.3 div_ceil; [CB] sec. 3.2). */
 int64_t or_blocks_needed(int64_t tokens, int block_size)

@@ -28,7 +28,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedkv
 _lock = threading.Lock()
 _lib = None
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_NO_BLOCKS = range(6)
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
 DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT, DEV_SLOT_MISMATCH = 1, 2, 4, 8, 16
 
@@ -81,6 +81,19 @@ def lib() -> ctypes.CDLL:
                                                   I64, I, F, I, I, F, F, I, P, S, P, P]
         L.pa_write_decode_partitions.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64,
                                                  I, F, I, I, F, F, I, P, S, P, P]
+        L.pa_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I64, I, P, P]
+        L.pa_allocator_create.argtypes = [I64, I, I]
+        L.pa_allocator_create.restype = P
+        L.pa_allocator_destroy.argtypes = [P]
+        L.pa_allocator_destroy.restype = None
+        L.pa_allocator_num_free.argtypes = [P]
+        L.pa_allocator_num_free.restype = I64
+        L.pa_allocator_refcount.argtypes = [P, ctypes.c_int32]
+        L.pa_allocator_refcount.restype = ctypes.c_int32
+        L.pa_allocator_allocate.argtypes = [P, I64, P, I64, P]
+        L.pa_allocator_fork.argtypes = [P, P, I64]
+        L.pa_allocator_free.argtypes = [P, P, I64]
+        L.pa_allocator_append_slot.argtypes = [P, P, P, I64, I64, P, P, P]
         L.pa_decode_choose.argtypes = [I, I, I, I, I]
         L.pa_decode_partition_size.argtypes = [I, I, I]
         L.pa_status_string.argtypes = [I]
@@ -89,7 +102,9 @@ def lib() -> ctypes.CDLL:
                      "pa_decode_partitions", "pa_merge", "pa_decode_partitioned",
                      "pa_decode_partitioned_static", "pa_write_decode",
                      "pa_write_decode_partitioned", "pa_write_decode_partitions",
-                     "pa_decode_choose", "pa_decode_partition_size", "pa_version"):
+                     "pa_decode_choose", "pa_decode_partition_size", "pa_version",
+                     "pa_copy_blocks", "pa_allocator_allocate", "pa_allocator_fork",
+                     "pa_allocator_free", "pa_allocator_append_slot"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
         return _lib
@@ -353,3 +368,86 @@ def decode_auto(out, query, k_cache, v_cache, block_tables, context_lens, max_co
 
 def version() -> int:
     return int(lib().pa_version())
+
+
+# ----------------------------------------------------------------------------- block management
+
+def copy_blocks(k_cache, v_cache, block_pairs, dev_status=None, stream=None) -> None:
+    """Copy whole blocks for each (src, dst) row of block_pairs ([n, 2] int64,
+    on the device): the copy of copy-on-write."""
+    nb, H, B, D = k_cache.shape
+    if block_pairs.dtype != torch.int64 or block_pairs.dim() != 2 or block_pairs.shape[1] != 2:
+        raise ValueError("block_pairs must be int64 [n, 2]")
+    _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
+                                block_pairs.shape[0], H, D, B, nb, _dtype(k_cache),
+                                _ptr(dev_status), _stream(stream)), "pa_copy_blocks")
+
+
+class BlockAllocator:
+    """The library's host-side block allocator (free list + reference
+    counts). Block ids are plain Python ints / int32 numpy arrays."""
+
+    def __init__(self, num_blocks: int, block_size: int, reserve_block0: bool = True):
+        self._lib = lib()
+        self._h = self._lib.pa_allocator_create(num_blocks, block_size, int(reserve_block0))
+        if not self._h:
+            raise ValueError("invalid allocator arguments")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pa_allocator_num_free(self._h))
+
+    def refcount(self, block: int) -> int:
+        return int(self._lib.pa_allocator_refcount(self._h, block))
+
+    def allocate(self, num_tokens: int):
+        """ceil(num_tokens / block_size) blocks (int32 array)."""
+        import numpy as np
+        n = -(-num_tokens // self.block_size)
+        out = np.zeros(max(1, n), dtype=np.int32)
+        got = ctypes.c_int64(0)
+        _check(self._lib.pa_allocator_allocate(self._h, num_tokens, out.ctypes.data, out.size,
+                                               ctypes.byref(got)), "pa_allocator_allocate")
+        return out[:got.value].copy()
+
+    def fork(self, blocks) -> None:
+        import numpy as np
+        b = np.ascontiguousarray(blocks, dtype=np.int32)
+        _check(self._lib.pa_allocator_fork(self._h, b.ctypes.data, b.size), "pa_allocator_fork")
+
+    def free(self, blocks) -> None:
+        import numpy as np
+        b = np.ascontiguousarray(blocks, dtype=np.int32)
+        _check(self._lib.pa_allocator_free(self._h, b.ctypes.data, b.size), "pa_allocator_free")
+
+    def append_slot(self, table, position: int):
+        """Slot of the token at `position` for a sequence whose block table is
+        `table` (an int32 numpy array of capacity entries, updated in place)
+        holding `len` blocks: returns (slot, new_len, copy) with copy =
+        (src, dst) when copy-on-write replaced a shared block, else None.
+        Pass the table as (array, length)."""
+        import numpy as np
+        arr, length = table
+        assert arr.dtype == np.int32 and arr.flags["C_CONTIGUOUS"]
+        n = ctypes.c_int64(length)
+        slot = ctypes.c_int64(0)
+        src = ctypes.c_int32(0)
+        dst = ctypes.c_int32(0)
+        _check(self._lib.pa_allocator_append_slot(self._h, arr.ctypes.data, ctypes.byref(n),
+                                                  arr.size, position, ctypes.byref(slot),
+                                                  ctypes.byref(src), ctypes.byref(dst)),
+               "pa_allocator_append_slot")
+        copy = (int(src.value), int(dst.value)) if src.value >= 0 else None
+        return int(slot.value), int(n.value), copy

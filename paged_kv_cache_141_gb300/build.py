@@ -35,7 +35,7 @@ def nvcc() -> str:
 
 
 def sources() -> list[str]:
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
 
 
 def _headers() -> list[str]:
@@ -56,7 +56,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     headers = _headers()
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         if force or _stale(obj, [src] + headers):
             jobs.append((src, obj))
 
@@ -75,7 +75,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
             for log in ex.map(compile_one, jobs):
                 if verbose and log:
                     print(log)
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in sources()]
+    objs = [os.path.join(BUILD, os.path.splitext(os.path.basename(s))[0] + ".o") for s in sources()]
     if force or jobs or _stale(LIB, objs):
         cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", LIB] + objs
         subprocess.run(cmd, check=True)

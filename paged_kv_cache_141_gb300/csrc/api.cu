@@ -456,6 +456,21 @@ int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_co
     return 1;
 }
 
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs,
+                         int64_t num_pairs, int num_kv_heads, int head_size, int block_size,
+                         int64_t num_blocks, pa_dtype cache_dtype, uint32_t* dev_status,
+                         void* stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_size <= 0 || block_size <= 0 || num_blocks < 0)
+        return PA_ERR_INVALID_ARG;
+    if ((int)cache_dtype < 0 || (int)cache_dtype > 3) return PA_ERR_INVALID_ARG;
+    const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_size * elem_bytes(cache_dtype);
+    if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PA_OK;
+    if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
+    return from_cuda(launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, num_blocks,
+                                        block_bytes, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 const char* pa_status_string(pa_status status) {
     switch (status) {
     case PA_OK: return "ok";
@@ -463,6 +478,7 @@ const char* pa_status_string(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "unsupported configuration";
     case PA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_NO_BLOCKS: return "not enough free blocks";
     }
     return "unknown status";
 }

@@ -87,6 +87,10 @@ cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logit
                          int num_q_heads, int head_size, int partition_size, int max_parts,
                          pa_dtype out_dtype, uint32_t* status, cudaStream_t stream);
 
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs,
+                               int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
+                               uint32_t* status, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
                                      void* v_cache, const int64_t* slots, int64_t num_tokens,
                                      int num_kv_heads, int head_size, int block_size,

@@ -528,3 +528,18 @@ ALL = [
     check_token_permutation_and_v_shift, check_merge_identity, check_merge_closed_form,
     check_write_scatter, check_write_e4m3,
 ]
+
+
+def check_copy_blocks():
+    """The block copy: block dst equals block src afterwards, others untouched."""
+    rng = np.random.default_rng(12)
+    kc = rng.integers(0, 255, (6, 2, 4, 8), dtype=np.uint8)
+    vc = rng.integers(0, 255, (6, 2, 4, 8), dtype=np.uint8)
+    k0, v0 = kc.copy(), vc.copy()
+    assert oracle.copy_blocks(kc, vc, [[1, 4], [2, 5]]) == 0
+    assert np.array_equal(kc[4], k0[1]) and np.array_equal(vc[5], v0[2])
+    assert np.array_equal(kc[:4], k0[:4]) and np.array_equal(vc[:4], v0[:4])
+    assert oracle.copy_blocks(kc, vc, [[1, 6]]) == oracle.BAD_BLOCK
+
+
+ALL.append(check_copy_blocks)

@@ -24,6 +24,7 @@ MUTANTS = {
                            "if (a >= 480.0)\n        return (uint8_t)(sign | 0x7f);"),
     "write_offset": ("int64_t off = slot % block_size;", "int64_t off = (slot + 1) % block_size;"),
     "write_no_scale": ("float qk = xk / k_scale;", "float qk = xk;"),
+    "copy_wrong_target": ("((char*)k_cache)[dst * block_elems", "((char*)k_cache)[src * block_elems"),
     "fp8_dequant_no_scale": ("double ks = cache_dtype == OR_E4M3 ? k_scale : 1.0;", "double ks = 1.0;"),
     "bf16_exponent": ("v = ldexp((double)(128 + m), e - 134);", "v = ldexp((double)(128 + m), e - 133);"),
     "f16_subnormal": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -23);"),
