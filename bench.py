@@ -141,6 +141,25 @@ def decode_kernel_label(case) -> str:
     return "paged_decode_tma_kernel" if tma else "paged_decode_simt_kernel"
 
 
+def max_over_ranks(value_ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: an all-reduce MAX over the default process
+    group (identity for one rank)."""
+    if world <= 1:
+        return value_ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value_ms], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload, so the
+    job moves world x the bytes in the slowest rank's time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -316,14 +335,11 @@ def run_ours(args):
     total_ms = t_start.elapsed_time(t_end)
     call_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) / K
                for j, (name, _) in enumerate(st.calls)}
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, device)
 
     by = st.bytes_per_step()
     ms_per_step = total_ms / K
-    value = world * by["total"] / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(by["total"], world, ms_per_step)
     seqs_per_s = world * case.num_seqs / (ms_per_step * 1e-3)
     peak, peak_kind = hbm_peak()
     main_name = "write+decode" if "write+decode" in call_ms else "decode"
