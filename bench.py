@@ -42,7 +42,7 @@ DEFAULT_CONFIG = 3
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_partitions_llama3_8b_traffic.txt")
-KERNEL_SOURCES = ["decode_mma.cuh", "decode_tma.cuh", "device_common.cuh"]
+KERNEL_SOURCES = ["decode_mma.cuh", "decode_tma.cuh", "device_common.cuh", "kv_store.cuh"]
 
 
 # ----------------------------------------------------------------------------- helpers
