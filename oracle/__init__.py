@@ -71,6 +71,8 @@ def _bind(path: str):
     lib.or_decode_partitioned.argtypes = [P, P, P, P, P, I, P, P, I, P, P, I, P, I, I, I,
                                           I, I, I64, D, D, D, I, I]
     lib.or_decode_partitioned.restype = I
+    lib.or_paged_prefill.argtypes = [P, P, I, P, P, P, I, P, P, I, P, I, I, I, I, I, I64, D, D, D]
+    lib.or_paged_prefill.restype = I
     lib.or_copy_blocks.argtypes = [P, P, P, I64, I64, I64, I]
     lib.or_copy_blocks.restype = I
     lib.or_blocks_needed.argtypes = [I64, I]
@@ -260,3 +262,25 @@ def copy_blocks(k_cache, v_cache, pairs) -> int:
     per = int(np.prod(k_cache.shape[1:]))
     return _load().or_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(pairs), pairs.shape[0], nb,
                                   per, k_cache.dtype.itemsize)
+
+
+def paged_prefill(query, q_dtype: str, query_start, k_cache, v_cache, cache_dtype: str,
+                  block_tables, context_lens, num_kv_heads: int, block_size: int, scale: float,
+                  k_scale=1.0, v_scale=1.0, strides=None) -> np.ndarray:
+    """Multi-query paged attention; query [T, Hq, d] -> out [T, Hq, d] float64."""
+    T, Hq, d = query.shape
+    if strides is None:
+        strides = declared_strides(num_kv_heads, block_size, d)
+    strides = np.ascontiguousarray(strides, dtype=np.int64)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.zeros((T, Hq, d), dtype=np.float64)
+    rc = _load().or_paged_prefill(_ptr(out), _ptr(np.ascontiguousarray(query)), code(q_dtype),
+                                  _ptr(qs), _ptr(k_cache), _ptr(v_cache), code(cache_dtype),
+                                  _ptr(strides), _ptr(bt), bt.shape[1], _ptr(cl), cl.size, Hq,
+                                  num_kv_heads, d, block_size, k_cache.shape[0], float(scale),
+                                  float(k_scale), float(v_scale))
+    if rc != OK:
+        raise RuntimeError(f"oracle paged prefill failed with code {rc}")
+    return out

@@ -486,6 +486,64 @@ done:
     return rc;
 }
 
+/*
+ * Multi-query paged attention (chunked prefill, speculative verification):
+ * sequence s brings Q_s = query_start[s+1] - query_start[s] query tokens, the
+ * last Q_s positions of its context of L_s tokens; query i sits at position
+ * p = L_s - Q_s + i and attends to the keys at positions 0..p (causal), through
+ * the block table exactly as the decode does ("Lecture 3: PagedAttention and
+ * vLLM", "the paged implementation of attention", whose listing already takes
+ * queries [num_queries, num_heads, head_dim]). query and out are
+ * [total_queries, Hq, d]. Q_s > L_s is an error. With Q_s = 1 this is the
+ * decode.
+ */
+int or_paged_prefill(double* out, const void* query, int q_dtype, const int32_t* query_start,
+                     const void* k_cache, const void* v_cache, int cache_dtype,
+                     const int64_t* cache_strides, const int32_t* block_tables, int max_blocks,
+                     const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_size, int block_size, int64_t num_blocks, double scale,
+                     double k_scale, double v_scale)
+{
+    if (!or_check_shape(num_q_heads, num_kv_heads, head_size, block_size))
+        return OR_BAD_ARG;
+    int G = num_q_heads / num_kv_heads;
+    for (int s = 0; s < num_seqs; ++s) {
+        int L = context_lens[s];
+        int q0 = query_start[s], Q = query_start[s + 1] - q0;
+        if (L < 0 || Q < 0 || Q > L || L > (int64_t)max_blocks * block_size)
+            return OR_BAD_ARG;
+        if (Q == 0)
+            continue;
+        size_t n = (size_t)L * num_kv_heads * head_size;
+        double* K = malloc(n * sizeof(double));
+        double* V = malloc(n * sizeof(double));
+        double* sc = malloc((size_t)L * sizeof(double));
+        double* q = malloc((size_t)head_size * sizeof(double));
+        if (!K || !V || !sc || !q) {
+            free(K); free(V); free(sc); free(q);
+            return OR_NOMEM;
+        }
+        int rc = or_gather_sequence(K, V, k_cache, v_cache, cache_dtype, cache_strides,
+                                    block_tables + (int64_t)s * max_blocks, L, num_kv_heads,
+                                    head_size, block_size, num_blocks, k_scale, v_scale);
+        for (int i = 0; i < Q && rc == OR_OK; ++i) {
+            int pos = L - Q + i;
+            for (int h = 0; h < num_q_heads; ++h) {
+                int64_t row = ((int64_t)(q0 + i) * num_q_heads + h) * head_size;
+                for (int e = 0; e < head_size; ++e)
+                    q[e] = or_read(query, q_dtype, row + e);
+                double m, l;
+                or_attend_range(out + row, &m, &l, q, K, V, 0, pos + 1, h / G, num_kv_heads,
+                                head_size, scale, sc);
+            }
+        }
+        free(K); free(V); free(sc); free(q);
+        if (rc != OR_OK)
+            return rc;
+    }
+    return OR_OK;
+}
+
 /* The copy of copy-on-write ("vLLM Page Attention Continuous Batching"
  * (lbrq.cn), "Sharing KV Cache-COW"): for each (src, dst) pair, every element
  * of block src of both caches is copied to block dst. block_elems =

@@ -543,3 +543,39 @@ def check_copy_blocks():
 
 
 ALL.append(check_copy_blocks)
+
+
+def check_prefill_reduces_to_decode_and_dense(seed=13):
+    """Multi-query paged attention: one query per sequence is the decode; and
+    every query equals a dense causal attention (torch SDPA with an explicit
+    mask) on the unpaged sequence."""
+    rng = np.random.default_rng(seed)
+    S, Hq, Hkv, d, B = 3, 8, 2, 16, 8
+    lens = [5, 40, 19]
+    q_counts = [5, 7, 1]
+    ks = [random_values(rng, (L, Hkv, d), "bf16") for L in lens]
+    vs = [random_values(rng, (L, Hkv, d), "bf16") for L in lens]
+    kc, vc, tables, cl, st = page(ks, vs, B, rng, "bf16", Hkv, d)
+    qstart = np.concatenate([[0], np.cumsum(q_counts)]).astype(np.int32)
+    q = random_values(rng, (int(qstart[-1]), Hq, d), "bf16")
+    got = oracle.paged_prefill(q, "bf16", qstart, kc, vc, "bf16", tables, cl, Hkv, B, 0.3)
+    # single query per sequence: the decode of the last position
+    last = qstart[1:] - 1
+    dec = oracle.decode(np.ascontiguousarray(q[last]), "bf16", kc, vc, "bf16", tables, cl, Hkv, B, 0.3)
+    assert np.abs(got[last] - dec).max() <= 1e-12
+    # dense causal reference per sequence
+    qf = storage_to_f64(q, "bf16")
+    G = Hq // Hkv
+    for s in range(S):
+        L, Q = lens[s], q_counts[s]
+        K = torch.from_numpy(np.repeat(storage_to_f64(ks[s], "bf16"), G, axis=1).transpose(1, 0, 2)[None].copy())
+        V = torch.from_numpy(np.repeat(storage_to_f64(vs[s], "bf16"), G, axis=1).transpose(1, 0, 2)[None].copy())
+        Qs = torch.from_numpy(qf[qstart[s]:qstart[s + 1]].transpose(1, 0, 2)[None].copy())
+        pos = torch.arange(L - Q, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos                        # [Q, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(Qs, K, V, attn_mask=mask, scale=0.3)
+        want = ref[0].permute(1, 0, 2).numpy()
+        assert np.abs(got[qstart[s]:qstart[s + 1]] - want).max() <= 1e-12
+
+
+ALL.append(check_prefill_reduces_to_decode_and_dense)

@@ -24,6 +24,8 @@ MUTANTS = {
                            "if (a >= 480.0)\n        return (uint8_t)(sign | 0x7f);"),
     "write_offset": ("int64_t off = slot % block_size;", "int64_t off = (slot + 1) % block_size;"),
     "write_no_scale": ("float qk = xk / k_scale;", "float qk = xk;"),
+    "prefill_causal_off_by_one": ("0, pos + 1, h / G, num_kv_heads", "0, pos, h / G, num_kv_heads"),
+    "prefill_wrong_position": ("int pos = L - Q + i;", "int pos = L - 1 - i;"),
     "copy_wrong_target": ("((char*)k_cache)[dst * block_elems", "((char*)k_cache)[src * block_elems"),
     "fp8_dequant_no_scale": ("double ks = cache_dtype == OR_E4M3 ? k_scale : 1.0;", "double ks = 1.0;"),
     "bf16_exponent": ("v = ldexp((double)(128 + m), e - 134);", "v = ldexp((double)(128 + m), e - 133);"),
