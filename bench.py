@@ -387,6 +387,116 @@ def run_ours(args):
     print(json.dumps(line))
 
 
+PREFILL_METRIC = {
+    "chunk512": "multi-query paged attention TFLOP/s (causal, algorithmic), 512-token prefill chunks",
+    "spec8": "multi-query paged attention KV GB/s, 8-token speculative verification",
+}
+
+
+def prefill_queries(case, kind):
+    """The query law of a multi-query workload: a 512-token chunk at the end
+    of every context (capped at L_s), or 8 draft tokens per sequence."""
+    if kind == "chunk512":
+        return ("fixed", np.minimum(512, case.context_lens))
+    return ("fixed", np.minimum(8, case.context_lens))
+
+
+def prefill_work(case, qs: np.ndarray):
+    """Algorithmic work of one multi-query step: FLOPs (QK^T and PV over each
+    query token's causal prefix, 4 d per (query head, key)) and bytes (the
+    K/V of every context once, Q read, out written)."""
+    counts = np.diff(qs).astype(np.int64)
+    L = case.context_lens.astype(np.int64)
+    # keys seen by the Q_s tokens: sum_{i<Q} (L - Q + i + 1)
+    keys = (counts * (L - counts) + counts * (counts + 1) // 2).sum()
+    flops = 4 * case.head_size * case.num_q_heads * int(keys)
+    eb = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+    qo = 2 * int(counts.sum()) * case.num_q_heads * case.head_size * eb[case.q_dtype]
+    return flops, case.kv_bytes() + qo
+
+
+def run_prefill(args):
+    """Multi-query paged attention (pa_paged_prefill) on the Llama-3-8B GQA
+    pool: the kernel alone, K timed launches, CUDA events, clocks sampled."""
+    import torch
+    from paged_kv_cache_141_gb300 import binding as pk
+    from paged_kv_cache_141_gb300 import workloads as W
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    case = W.config_case(args.config)
+    q = W.make_queries(case, prefill_queries(case, args.prefill))
+    st = Step(case, device, 512, "separate")
+    st.calls[0][1]()                       # the step's KV write: every context token stored
+    query = torch.from_numpy(np.ascontiguousarray(q.query).view(np.int16)).view(
+        torch.bfloat16).to(device) if case.q_dtype == "bf16" else torch.from_numpy(q.query).to(device)
+    qstart = torch.from_numpy(q.query_start).to(device)
+    out = torch.empty_like(query)
+
+    def launch():
+        pk.paged_prefill(out, query, qstart, st.kc, st.vc, st.bt, st.cl, q.max_queries,
+                         case.max_context_len, case.scale, case.k_scale, case.v_scale, st.status)
+
+    launch()
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise SystemExit(f"device status {int(st.status.item())} after the first launch")
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    K = args.steps
+    stream = torch.cuda.current_stream(device)
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.25)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        launch()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = a.elapsed_time(b) / K
+    flops, nbytes = prefill_work(case, q.query_start)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak_hbm, hk = hbm_peak()
+    try:
+        with open(PEAKS_FILE) as f:
+            peak_tc, tk = float(json.load(f)["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        peak_tc, tk = 1700.0, "fallback"
+    tensor = args.prefill == "chunk512"
+    value, unit = (tflops, "TFLOP/s") if tensor else (gbs, "GB/s")
+    line = {
+        "metric": PREFILL_METRIC[args.prefill], "value": round(value, 2), "unit": unit,
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": case.cache_dtype, "data": "synthetic",
+        "config": {"workload": f"{case.name} pool, {args.prefill} queries",
+                   "num_seqs": case.num_seqs, "num_q_heads": case.num_q_heads,
+                   "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
+                   "block_size": case.block_size, "query_tokens": int(q.query_start[-1]),
+                   "max_queries_per_seq": q.max_queries, "total_context_tokens": case.total_tokens,
+                   "l2": "KV pool %.2f GB vs 129 MB L2; no flush" % (case.kv_bytes() / 1e9)},
+        "tflops": round(tflops, 2), "kv_q_o_gbs": round(gbs, 2),
+        "flops_per_step": flops, "bytes_per_step": nbytes,
+        "roofline": ({"bound": "tensor", "achieved": round(tflops, 2), "peak": peak_tc,
+                      "unit": "TFLOP/s", "frac": round(tflops / peak_tc, 4), "traffic": None,
+                      "peak_kind": f"{tk} bf16 sustained"}
+                     if tensor else
+                     {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                      "frac": round(gbs / peak_hbm, 4), "traffic": None,
+                      "peak_kind": f"{hk} HBM copy"}),
+        "kernel": "paged_prefill_tc_kernel",
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+
+
 def run_e2e(st: Step, steps: int, device):
     """The same step through the public API with host buffers: each step
     copies its inputs from pinned host memory, runs the write and the decode,
@@ -527,11 +637,15 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", choices=["chunk512", "spec8"], default=None,
+                    help="time multi-query paged attention on the configuration's pool instead")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill:
+        run_prefill(args)
     else:
         run_ours(args)
 

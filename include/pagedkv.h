@@ -303,6 +303,43 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
                                        pa_dtype cache_dtype, float k_scale, float v_scale,
                                        int partition_size, uint32_t* dev_status, void* stream);
 
+/*
+ * pa_paged_prefill -- multi-query paged attention: several query tokens per
+ * sequence against the paged cache, for a prefill chunk (TGI deep-dive sec.
+ * 6.2, PREFILL_CHUNKING: a long prefill is cut into chunks) or the draft
+ * tokens of a speculative-decoding verification ("vLLM Page Attention
+ * Continuous Batching" (lbrq.cn), "vLLM 主要能力"). The paged attention of
+ * "Lecture 3: PagedAttention and vLLM" ("the paged implementation of
+ * attention") already takes queries [num_queries, num_heads, head_dim]; the
+ * pages give no mask, and this call reads it causally: the Q_s query tokens
+ * of sequence s are the last Q_s of its L_s = context_lens[s] tokens (their
+ * K/V already written), and query token i (0-based within s) attends to keys
+ * 0 .. L_s - Q_s + i. With Q_s = 1 this is the decode.
+ *
+ *  out, query     [num_queries][num_q_heads][head_size], type q_dtype; the
+ *                 tokens of sequence s are rows query_start[s] ..
+ *                 query_start[s+1] - 1. 16-byte aligned.
+ *  query_start    [num_seqs + 1] int32, device, non-decreasing,
+ *                 query_start[0] = 0, query_start[num_seqs] = num_queries.
+ *  max_queries_per_seq  an upper bound on Q_s known on the host (sizes the
+ *                 grid); 0 <= Q_s <= max_queries_per_seq and Q_s <= L_s.
+ *  Other arguments as pa_decode; scale must be > 0.
+ *  A 16-bit query with a cache of the same type, head_size 64/128/256, a
+ *  block_size that is a power of two in [8, 256] and a group of at most 128
+ *  heads runs on the tensor cores (tcgen05); other supported combinations run
+ *  one query token per work unit on the CUDA cores. A sequence whose lengths
+ *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
+ *  num_queries == 0 launches nothing.
+ */
+pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_start,
+                           int num_queries, int max_queries_per_seq, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                           int64_t num_blocks, int max_context_len, float scale,
+                           pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
+                           uint32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------
  * Block management: the host-side allocator and the copy-on-write copy.
  * ------------------------------------------------------------------------ */

@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
                                                   I64, I, F, I, I, F, F, I, P, S, P, P]
         L.pa_write_decode_partitions.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64,
                                                  I, F, I, I, F, F, I, P, S, P, P]
+        L.pa_paged_prefill.argtypes = [P, P, P, I, I, P, P, P, I, P, I, I, I, I, I, I64, I, F, I,
+                                       I, F, F, P, P]
         L.pa_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I64, I, P, P]
         L.pa_allocator_create.argtypes = [I64, I, I]
         L.pa_allocator_create.restype = P
@@ -181,6 +183,30 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context
         _ptr(context_lens), S, Hq, Hkv, D, B, nb, int(max_context_len), float(scale),
         _dtype(query), _dtype(k_cache), float(k_scale), float(v_scale), _ptr(dev_status),
         _stream(stream)), "pa_decode")
+
+
+def paged_prefill(out, query, query_start, k_cache, v_cache, block_tables, context_lens,
+                  max_queries_per_seq, max_context_len, scale, k_scale=1.0, v_scale=1.0,
+                  dev_status=None, stream=None) -> None:
+    """Causal multi-query paged attention into `out` ([T, Hq, D] like `query`);
+    the tokens of sequence s are rows query_start[s]..query_start[s+1]-1 and
+    are the last Q_s positions of its context_lens[s] tokens."""
+    T, Hq, D = query.shape
+    nb, Hkv, B, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("query and cache head sizes differ")
+    S = context_lens.numel()
+    if query_start.dtype != torch.int32 or query_start.numel() != S + 1:
+        raise ValueError("query_start must be int32 [num_seqs + 1]")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block_tables and context_lens must be int32")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    _check(lib().pa_paged_prefill(
+        _ptr(out), _ptr(query), _ptr(query_start), T, int(max_queries_per_seq), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, Hq, Hkv,
+        D, B, nb, int(max_context_len), float(scale), _dtype(query), _dtype(k_cache),
+        float(k_scale), float(v_scale), _ptr(dev_status), _stream(stream)), "pa_paged_prefill")
 
 
 def workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len,

@@ -166,6 +166,22 @@ cudaError_t run_decode_kernel(const DecodeParams& p, int head_size, pa_dtype q_d
     }
 }
 
+// The CUDA-core decode alone (the multi-query fallback).
+cudaError_t run_simt_decode_kernel(DecodeParams p, int head_size, pa_dtype q_dtype,
+                                   pa_dtype cache_dtype, cudaStream_t stream) {
+    p.sub_groups = p.group / heads_per_unit(p.group, head_size, false);
+    const int gs = p.group / p.sub_groups;
+    if (cache_dtype == PA_FP8_E4M3) {
+        if (q_dtype == PA_F16) return launch_decode_simt_f16_e4m3(p, head_size, gs, false, stream);
+        return launch_decode_simt_bf16_e4m3(p, head_size, gs, false, stream);
+    }
+    switch (q_dtype) {
+    case PA_F32: return launch_decode_simt_f32(p, head_size, gs, false, stream);
+    case PA_F16: return launch_decode_simt_f16(p, head_size, gs, false, stream);
+    default: return launch_decode_simt_bf16(p, head_size, gs, false, stream);
+    }
+}
+
 pa_status check_partition_size(int partition_size) {
     if (partition_size <= 0 || partition_size % 32 != 0) return PA_ERR_INVALID_ARG;
     return PA_OK;
@@ -196,6 +212,24 @@ void bind_fused_write(DecodeParams& p, const void* key, const void* value,
     p.wv_cache = v_cache;
     p.k_scale_w = k_scale;
     p.v_scale_w = v_scale;
+}
+
+// The tcgen05 multi-query kernel: 16-bit query and cache of one type, whole
+// 128-byte column spans, block sizes that are powers of two in [8, 256] (every
+// TMA box then starts on a swizzle-atom boundary), groups that fit the
+// 128-row tile, 16-byte-aligned rows, row coordinates below 2^31.
+bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, int block_size,
+                         int group, int64_t num_blocks, int num_kv_heads, const void* out,
+                         const void* query, const void* k_cache, const void* v_cache) {
+    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16) || cache_dtype != q_dtype) return false;
+    if (!supported_head_size(head_size)) return false;
+    if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0) return false;
+    if (group < 1 || group > 128) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(query) |
+                        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
+    if (a & 15) return false;
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    return rows > 0 && rows < (1ll << 31);
 }
 
 }  // namespace
@@ -454,6 +488,61 @@ int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_co
     const long long slots = (long long)sms * 3;
     if (units >= 8 * slots && parts <= 2) return 0;
     return 1;
+}
+
+pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_start,
+                           int num_queries, int max_queries_per_seq, const void* k_cache,
+                           const void* v_cache, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_size, int block_size,
+                           int64_t num_blocks, int max_context_len, float scale,
+                           pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
+                           uint32_t* dev_status, void* stream) {
+    if (num_queries < 0 || max_queries_per_seq < 0 || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    // with no query tokens the data pointers may be null: validate the shape only
+    const int seqs_with_work = num_queries == 0 ? 0 : num_seqs;
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, seqs_with_work, num_q_heads, num_kv_heads,
+                                head_size, block_size, num_blocks, max_context_len, scale,
+                                q_dtype, cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if (num_queries == 0) return PA_OK;
+    if (num_seqs == 0) return PA_ERR_INVALID_ARG;        // query tokens need a sequence
+    if (!out || !query_start || max_queries_per_seq == 0) return PA_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, p.group, num_blocks,
+                            num_kv_heads, out, query, k_cache, v_cache)) {
+        PrefillParams pp{};
+        pp.out = out;
+        pp.query = query;
+        pp.query_start = query_start;
+        pp.k_cache = k_cache;
+        pp.v_cache = v_cache;
+        pp.block_tables = block_tables;
+        pp.context_lens = context_lens;
+        pp.status = dev_status;
+        pp.num_blocks = num_blocks;
+        pp.max_blocks = max_blocks_per_seq;
+        pp.num_seqs = num_seqs;
+        pp.num_q_heads = num_q_heads;
+        pp.num_kv_heads = num_kv_heads;
+        pp.block_size = block_size;
+        pp.group = p.group;
+        pp.max_context_len = max_context_len;
+        pp.max_queries = max_queries_per_seq;
+        pp.tokens_per_tile = 128 / p.group;
+        pp.q_tiles = (max_queries_per_seq + pp.tokens_per_tile - 1) / pp.tokens_per_tile;
+        pp.q_mul = scale * 1.4426950408889634f;
+        return from_cuda(q_dtype == PA_F16 ? launch_prefill_tc_f16(pp, head_size, s)
+                                           : launch_prefill_tc_bf16(pp, head_size, s));
+    }
+    // CUDA cores: one query token per work unit, the decode kernel over the
+    // token's causal prefix
+    p.out = out;
+    p.query_start = query_start;
+    p.num_queries = num_queries;
+    return from_cuda(run_simt_decode_kernel(p, head_size, q_dtype, cache_dtype, s));
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs,

@@ -111,7 +111,8 @@ paged_decode_simt_kernel(const DecodeParams p) {
     uint64_t* empty = full + NST;
     SimtScratch<GS>& scr = *reinterpret_cast<SimtScratch<GS>*>(smem + Smem::kScratchOffset);
 
-    const int s = blockIdx.z;
+    int s = blockIdx.z;
+    size_t qrow = (size_t)s;                                      // row of query / out
     const int kvh = blockIdx.y / p.sub_groups;
     const int sub = blockIdx.y - kvh * p.sub_groups;
     const int hq0 = kvh * p.group + sub * GS;
@@ -119,11 +120,36 @@ paged_decode_simt_kernel(const DecodeParams p) {
     const int lane = threadIdx.x & 31;
 
     // context length, clamped to what the table and the grid can cover
-    int L = p.context_lens[s];
+    int L;
+    int cap = p.max_context_len;
     {
-        int cap = p.max_context_len;
         const long long tab = (long long)p.max_blocks * p.block_size;
         if (tab < cap) cap = (int)tab;
+    }
+    if constexpr (!kSplit) {
+        if (p.query_start) {
+            // multi-query: blockIdx.x is a query token; its sequence is the
+            // last s with query_start[s] <= token
+            const int t = blockIdx.x;
+            qrow = (size_t)t;
+            int lo = 0, hi = p.num_seqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (p.query_start[mid] <= t) lo = mid;
+                else hi = mid - 1;
+            }
+            s = lo;
+            const int qs0 = p.query_start[s], qs1 = p.query_start[s + 1];
+            const int Ls = p.context_lens[s];
+            if (t < qs0 || t >= qs1 || Ls > cap || qs1 - qs0 > Ls) {
+                if (threadIdx.x == 0 && sub == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_LEN);
+                return;
+            }
+            L = Ls - (qs1 - qs0) + (t - qs0) + 1;
+        }
+    }
+    if (kSplit || !p.query_start) {
+        L = p.context_lens[s];
         if (L < 0 || L > cap) {
             if (threadIdx.x == 0 && blockIdx.x == 0 && sub == 0 && p.status)
                 atomicOr(p.status, PA_DEV_BAD_LEN);
@@ -141,7 +167,7 @@ paged_decode_simt_kernel(const DecodeParams p) {
         if (L == 0) {                                             // empty context: zeros
             QT* out = reinterpret_cast<QT*>(p.out);
             for (int i = threadIdx.x; i < GS * D; i += blockDim.x)
-                out[((size_t)s * p.num_q_heads + hq0) * D + i] = from_float<QT>(0.f);
+                out[(qrow * p.num_q_heads + hq0) * D + i] = from_float<QT>(0.f);
             return;
         }
     }
@@ -216,7 +242,7 @@ paged_decode_simt_kernel(const DecodeParams p) {
     // ---------------------------------------------------------------- consumers
     float q[GS][EPL];
     {
-        const QT* qp = reinterpret_cast<const QT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
+        const QT* qp = reinterpret_cast<const QT*>(p.query) + (qrow * p.num_q_heads + hq0) * D;
 #pragma unroll
         for (int h = 0; h < GS; ++h) {
             float x[EPL];
@@ -350,7 +376,7 @@ paged_decode_simt_kernel(const DecodeParams p) {
             }
         } else {
             QT* out = reinterpret_cast<QT*>(p.out);
-            out[((size_t)s * p.num_q_heads + hq) * D + e] = from_float<QT>(val);
+            out[(qrow * p.num_q_heads + hq) * D + e] = from_float<QT>(val);
         }
     }
 }
@@ -361,7 +387,8 @@ cudaError_t launch_simt_variant(const DecodeParams& p, cudaStream_t stream) {
     auto kern = paged_decode_simt_kernel<QT, CT, D, GS, kSplit>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups, p.num_seqs);
+    dim3 grid(p.query_start ? p.num_queries : (kSplit ? p.max_parts : 1),
+              p.num_kv_heads * p.sub_groups, p.query_start ? 1 : p.num_seqs);
     kern<<<grid, kSimtThreads, Smem::kBytes, stream>>>(p);
     return cudaGetLastError();
 }

@@ -42,6 +42,12 @@ struct DecodeParams {
     void* wv_cache;
     float k_scale_w;              // E4M3 quantisation scales of the write
     float v_scale_w;
+    // multi-query attention on the CUDA cores (null for the decode): the
+    // rows of query/out are query tokens; token t of sequence s (query_start[s]
+    // <= t < query_start[s+1]) attends to the first L_s - Q_s + (t -
+    // query_start[s]) + 1 keys. Single pass only, no fused write.
+    const int32_t* query_start;   // [S + 1]
+    int num_queries;              // rows of query / out
 };
 
 // Generic CUDA-core decode; one launcher per (query type, cache type).
@@ -81,6 +87,35 @@ cudaError_t launch_decode_mma_f16_e4m3(const DecodeParams& p, int head_size, int
                                        bool split, cudaStream_t stream);
 cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
                                         bool split, cudaStream_t stream);
+
+// Multi-query paged attention on the tensor cores (tcgen05): 16-bit query and
+// cache of the same type, head_size in {64, 128, 256}, block size a power of
+// two in [8, 256], group <= 128.
+struct PrefillParams {
+    void* out;                    // [T, Hq, D], query type
+    const void* query;            // [T, Hq, D]
+    const int32_t* query_start;   // [S + 1]
+    const void* k_cache;          // [num_blocks, Hkv, B, D]
+    const void* v_cache;
+    const int32_t* block_tables;  // [S, max_blocks]
+    const int32_t* context_lens;  // [S]
+    uint32_t* status;             // may be null
+    int64_t num_blocks;
+    int max_blocks;
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int block_size;
+    int group;                    // Hq / Hkv
+    int max_context_len;
+    int max_queries;              // max over s of Q_s (sizes the grid)
+    int tokens_per_tile;          // floor(128 / G)
+    int q_tiles;                  // ceil(max_queries / tokens_per_tile)
+    float q_mul;                  // scale * log2(e)
+};
+
+cudaError_t launch_prefill_tc_f16(const PrefillParams& p, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_tc_bf16(const PrefillParams& p, int head_size, cudaStream_t stream);
 
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,

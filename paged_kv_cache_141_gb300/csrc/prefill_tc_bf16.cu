@@ -1,0 +1,11 @@
+// prefill_tc_bf16.cu -- instantiation of the tcgen05 multi-query kernel for
+// bf16 queries and caches.
+#include "prefill_tc.cuh"
+
+namespace pagedkv {
+
+cudaError_t launch_prefill_tc_bf16(const PrefillParams& p, int head_size, cudaStream_t stream) {
+    return launch_prefill_tc<__nv_bfloat16>(p, head_size, stream);
+}
+
+}  // namespace pagedkv

@@ -44,6 +44,7 @@ _BITS = {"f32": np.uint32, "f16": np.uint16, "bf16": np.uint16, "e4m3": np.uint8
 
 _CHUNK = 1 << 22
 _STREAM_Q, _STREAM_K, _STREAM_V, _STREAM_NEWK, _STREAM_NEWV = 1, 2, 3, 4, 5
+_STREAM_MQ, _STREAM_QCOUNT = 6, 7
 
 
 def _threads() -> int:
@@ -278,6 +279,48 @@ def make_case(*, name="case", num_seqs, num_q_heads, num_kv_heads, head_size, bl
         case.v_scale = _amax_scale(case.prefill_value, new_value, kv_dtype)
     case.meta = {"owned_blocks": int(owned.sum()), "prefix_tokens": prefix_tokens}
     return case
+
+
+@dataclass
+class Queries:
+    """Query tokens of a multi-query attention step over a Case's sequences."""
+    query: np.ndarray          # [T, Hq, d], the Case's query type
+    query_start: np.ndarray    # [S + 1] int32; sequence s owns rows query_start[s]..[s+1]-1
+    max_queries: int           # max over s of Q_s
+
+    @property
+    def counts(self) -> np.ndarray:
+        return np.diff(self.query_start)
+
+
+def make_queries(case: Case, law, seed: int | None = None) -> Queries:
+    """Q_s query tokens per sequence, the last Q_s positions of its context.
+
+    law: ("uniform", lo, hi) draws Q_s, clipped to [min(1, L_s), L_s];
+    ("fixed", [Q...]) gives them, clipped to [0, L_s]; ("all",) takes
+    Q_s = L_s (a whole prefill).
+    Query values are N(0,1) in the Case's query type, on their own stream.
+    """
+    seed = case.seed if seed is None else seed
+    S = case.num_seqs
+    L = case.context_lens.astype(np.int64)
+    if law[0] == "all":
+        q = L.copy()
+    elif law[0] == "fixed":
+        q = np.asarray(law[1], dtype=np.int64).reshape(S)
+    elif law[0] == "uniform":
+        rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _STREAM_QCOUNT])))
+        q = rng.integers(law[1], law[2] + 1, size=S).astype(np.int64)
+    else:
+        raise ValueError(law)
+    q = np.minimum(np.maximum(q, 0 if law[0] == "fixed" else np.minimum(1, L)), L)
+    start = np.zeros(S + 1, dtype=np.int64)
+    np.cumsum(q, out=start[1:])
+    assert start[-1] < 2 ** 31
+    T = int(start[-1])
+    query = normal(seed, _STREAM_MQ, (T, case.num_q_heads, case.head_size), case.q_dtype)
+    return Queries(query=query, query_start=start.astype(np.int32),
+                   max_queries=int(q.max(initial=0)))
 
 
 def _amax_scale(a: np.ndarray, b: np.ndarray, dtype: str) -> float:

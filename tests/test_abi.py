@@ -86,3 +86,27 @@ def test_argument_errors_before_any_launch(lib):
                                   ctypes.c_void_p(16), 4, ctypes.c_void_p(16), 2, 8, 8, 128, 16,
                                   10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, 512, None, 0,
                                   None, None) == pk.PA_ERR_WORKSPACE
+
+
+def test_paged_prefill_argument_errors(lib):
+    import ctypes
+    from paged_kv_cache_141_gb300 import binding as pk
+    L = pk.lib()
+    v = ctypes.c_void_p(256)
+    # (out, query, query_start, T, maxQ, k, v, tables, max_blocks, lens, S, Hq, Hkv, d, B,
+    #  num_blocks, max_len, scale, q_dtype, cache_dtype, k_scale, v_scale, status, stream)
+    def call(T=4, maxq=2, S=2, scale=0.1, d=128, q=pk.PA_BF16, c=pk.PA_BF16, out=v, qs=v):
+        return L.pa_paged_prefill(out, v, qs, T, maxq, v, v, v, 4, v, S, 8, 2, d, 16, 10, 64,
+                                  scale, q, c, 1.0, 1.0, None, None)
+    assert call(scale=0.0) == pk.PA_ERR_INVALID_ARG          # scale must be > 0
+    assert call(scale=-1.0) == pk.PA_ERR_INVALID_ARG
+    assert call(T=-1) == pk.PA_ERR_INVALID_ARG
+    assert call(maxq=0) == pk.PA_ERR_INVALID_ARG             # queries but no per-sequence bound
+    assert call(out=None) == pk.PA_ERR_INVALID_ARG
+    assert call(qs=None) == pk.PA_ERR_INVALID_ARG
+    assert call(d=96) == pk.PA_ERR_UNSUPPORTED
+    assert call(q=pk.PA_BF16, c=pk.PA_F16) == pk.PA_ERR_UNSUPPORTED
+    # nothing to do: no launch
+    assert call(T=0, out=None, qs=None) == pk.PA_OK
+    assert call(S=0, T=0) == pk.PA_OK
+    assert call(S=0, T=3) == pk.PA_ERR_INVALID_ARG           # tokens without sequences

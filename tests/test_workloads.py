@@ -78,3 +78,19 @@ def test_loguniform_lengths():
     assert L.min() >= 512 and L.max() <= 4096
     # log-uniform: log-lengths have mean near (ln 512 + ln 4096) / 2
     assert abs(np.log(L).mean() - (np.log(512) + np.log(4096)) / 2) < 0.05
+
+
+def test_make_queries_counts_and_determinism():
+    from paged_kv_cache_141_gb300.workloads import make_case, make_queries
+    c = make_case(num_seqs=6, num_q_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                  q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", [0, 1, 5, 40, 17, 3]),
+                  seed=3)
+    a = make_queries(c, ("uniform", 2, 9))
+    b = make_queries(c, ("uniform", 2, 9))
+    assert np.array_equal(a.query, b.query) and np.array_equal(a.query_start, b.query_start)
+    q = a.counts
+    assert q[0] == 0 and q[1] == 1 and np.all(q <= c.context_lens) and np.all(q[2:] >= 2)
+    assert a.query.shape == (int(a.query_start[-1]), 4, 64)
+    assert a.max_queries == int(q.max())
+    full = make_queries(c, ("all",))
+    assert np.array_equal(full.counts, c.context_lens)
