@@ -10,29 +10,40 @@
 // KV head read each key once. Query token i of s sits at position
 // L - Q + i and sees keys 0..position.
 //
-// Data movement. Warp 4 (one lane) walks the block table and loads each
-// 128-key (64 for head size 256) tile of K and V with tensor TMA copies into
-// 128-byte-swizzled shared memory, one box per block segment and 64-element
-// column span, on rings of KS (K) and VS (V) stages.
+// Data movement. Warp 8 walks the block table and loads each 128-key (64 for
+// head size 256) tile of K with tensor TMA copies into 128-byte-swizzled
+// shared memory, one box per block segment and 64-element column span, lane i
+// taking box i; warp 10 does the same for V. K and V have rings of their own
+// (three stages each at head size 128), so a K tile is fetched as soon as the
+// S = Q.K^T of the tile three stages back has consumed its slot, whatever P.V
+// is doing.
 //
-// Tensor cores. Warp 5 (one lane) issues tcgen05.mma: S = Q.K^T for tile j
-// into one of two TMEM score buffers (A = Q and B = K both K-major), then
-// O += P.V for tile j-1 (A = P K-major, B = V with the head dimension
-// contiguous, i.e. MN-major). Commits on mbarriers hand S to the softmax, free
-// K and V stages, and report each P.V done.
+// Tensor cores. Warp 9 (one lane) issues tcgen05.mma in the order S_0, S_1,
+// PV_0, S_2, PV_1, ...: S_j = Q.K_j^T into TMEM score buffer j mod 2 (A = Q
+// and B = K, both K-major in shared memory), then O += P_j.V_j with P_j read
+// from TMEM and V_j (head dimension contiguous, i.e. MN-major) from shared
+// memory. The tensor pipe runs one CTA's MMAs in issue order, so S_{j+2}
+// overwriting P_j's buffer after PV_j needs no extra wait. Commits on
+// mbarriers hand S to the softmax, free K and V slots and report each P.V.
 //
-// Softmax. Warps 0-3: thread t owns TMEM lane t, i.e. row t. It loads its row
-// of S, applies the causal mask, keeps the running max m and sum l in base 2,
-// writes the weights P into shared memory (swizzled, K-major) and rescales its
-// row of O in TMEM when the max has grown by more than 2^8 since the last
-// rescale (weights up to 2^8 cannot overflow). At the end it divides by l and
-// stores its output row.
+// Softmax. Warps 0-7: a TMEM lane (row) is readable by warps w and w + 4, so
+// thread t takes row t mod 128 and half t / 128 of the tile's key columns;
+// two warps per SM sub-partition hide each other's latencies. Both halves
+// load the whole row of S, apply the causal mask and take its max, so they
+// keep the same running max m (base 2) and make the same rescale decisions;
+// each exponentiates its own columns, keeps their running sum, and stores
+// their weights P over the same TMEM buffer. O is rescaled in TMEM (each half its
+// half of the columns) only when the max has grown by more than 2^8 since the
+// last rescale (weights up to 2^8 cannot overflow; the rescale waits for the
+// previous P.V). At the end the two halves' sums are added through shared
+// memory and each half divides and stores its half of the output row.
 //
 // Precision. A weight rounded to bf16 carries a relative error up to 2^-8,
 // which on a row with few keys moves the output by up to ~2^-8 |v - out|,
 // beyond a 2e-3 bound. So P goes to the tensor cores as two 16-bit terms,
-// P_hi = round(p) and P_lo = round(p - P_hi) (relative error ~2^-16), and O
-// accumulates P_hi.V + P_lo.V: three MMAs per key tile instead of two.
+// P_hi = round(p) and P_lo = round(p - P_hi) (relative error ~2^-16), packed
+// side by side in the score buffer, and O accumulates P_hi.V + P_lo.V: three
+// MMAs per key tile instead of two.
 //
 // Every wait is bounded; a wait that runs out raises PA_DEV_TIMEOUT and a
 // shared abort flag that ends every role's loop, and the CTA drains its copies
@@ -48,37 +59,44 @@
 namespace pagedkv {
 
 constexpr int kTcRows = 128;                  // MMA M: rows of a query tile
-constexpr int kTcThreads = 6 * 32;            // 4 softmax warps, producer, MMA
-constexpr int kTcProducerWarp = 4;
-constexpr int kTcMmaWarp = 5;
+constexpr int kTcSoftmaxThreads = 256;       // 8 softmax warps: two per row quarter
+constexpr int kTcThreads = 11 * 32;           // softmax, K loads, MMA, V loads
+constexpr int kTcKWarp = 8;
+constexpr int kTcMmaWarp = 9;
+constexpr int kTcVWarp = 10;
 constexpr float kTcRescaleLog2 = 8.0f;        // lazy rescale threshold (base 2)
+constexpr int kTcSmemLimit = 227 * 1024;
 
 template <int D>
 struct TcShape {
     static constexpr int N = D == 256 ? 64 : 128;            // keys per tile
-    static constexpr int KS = 2;                             // K stages
-    static constexpr int VS = 2;                             // V stages
     static constexpr int kSpans = D / 64;                    // 128-byte column spans per row
     static constexpr int kQBytes = kTcRows * D * 2;
     static constexpr int kKvBytes = N * D * 2;               // one stage of K (or V)
-    static constexpr int kPBytes = kTcRows * N * 2;          // one of P_hi, P_lo
+    static constexpr int kFixed = kQBytes + 1024 + 256 + 1024;  // Q, slack, barriers, sums
+    static constexpr int kStages0 = (kTcSmemLimit - kFixed) / (2 * kKvBytes);
+    static constexpr int NS = kStages0 > 4 ? 4 : kStages0;   // K stages = V stages
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
-    static constexpr int kVOff = kKOff + KS * kKvBytes;
-    static constexpr int kPOff = kVOff + VS * kKvBytes;
-    static constexpr int kBarOff = kPOff + 2 * kPBytes;
-    // barriers: k_full[KS] k_empty[KS] v_full[VS] v_empty[VS] s_full[2] s_free[2] p_full pv_done drain
-    static constexpr int kNumBars = 2 * KS + 2 * VS + 7;
+    static constexpr int kVOff = kKOff + NS * kKvBytes;
+    static constexpr int kBarOff = kVOff + NS * kKvBytes;
+    // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
+    static constexpr int kNumBars = 4 * NS + 5;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
-    static constexpr int kBytes = kMiscOff + 16;
-    // one CTA per SM: the CTA allocates all 512 TMEM columns
-    static constexpr int kAlloc0 = kBytes + 1024;
-    static constexpr int kAlloc = kAlloc0 < 120 * 1024 ? 120 * 1024 : kAlloc0;
+    static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
+    static constexpr int kBytes = kLsumOff + kTcSoftmaxThreads * 4;
+    static constexpr int kAlloc = kBytes + 1024;
+    // TMEM: two score buffers of N columns (S as f32, then P_hi | P_lo as
+    // packed 16-bit pairs, N/2 columns each) and O (D columns). The CTA takes
+    // all 512 columns, so one CTA runs per SM; the shared memory it asks for
+    // keeps a second one off the SM.
     static constexpr int kTmemCols = 512;
-    static constexpr int kSCol = 0;                          // score buffers at 0 and N
+    static constexpr int kSCol = 0;
     static constexpr int kOCol = 2 * N;
+    static_assert(NS >= 2, "stages");
     static_assert(2 * N + D <= kTmemCols, "TMEM columns");
-    static_assert(kAlloc <= 227 * 1024, "shared memory");
+    static_assert(kAlloc <= kTcSmemLimit, "shared memory");
+    static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
 
 struct TcPrefillParams {
@@ -112,6 +130,16 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
+// Same, with A read from TMEM (a_tmem: lane = row, 16-bit pairs per column).
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
 
@@ -154,6 +182,29 @@ __device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32])
           "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
           "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// NC consecutive columns (16 or a multiple of 32) from r[0..NC).
+template <int NC>
+__device__ __forceinline__ void tc_st_n(uint32_t taddr, const uint32_t* r) {
+    static_assert(NC == 16 || NC % 32 == 0, "columns");
+    if constexpr (NC == 16) {
+        tc_st16(taddr, r);
+    } else {
+#pragma unroll
+        for (int c = 0; c < NC; c += 32)
+            tc_st32(taddr + c, *reinterpret_cast<const uint32_t(*)[32]>(r + c));
+    }
 }
 
 __device__ __forceinline__ void tc_wait_ld() {
@@ -211,25 +262,87 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 
 // ---------------------------------------------------------------- the kernel
 
+// One role's loads, by a whole warp: K (or V) tiles of the unit into the
+// ring `ring` of NS slots, each slot freed by a commit on `empty`, filled on
+// `full`. Lane i owns box i of a tile (keys i*box_rows ..): it reads that
+// box's block-table entry and issues the box's copies. The entries of the
+// next kAhead tiles are in flight while a tile is issued, so the table's
+// latency is paid once per unit, not once per tile.
+template <int D>
+__device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CUtensorMap* map,
+                                             uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                             int s, int hk, int ntiles, int kend, int lane,
+                                             volatile int* abort_flag) {
+    using Sh = TcShape<D>;
+    constexpr int N = Sh::N;
+    constexpr int NS = Sh::NS;
+    constexpr int64_t kNone = -1;
+    const PrefillParams& p = tp.p;
+    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+    const int rows = tp.box_rows;                            // >= 8, so <= 16 boxes per tile
+    const int B = p.block_size;
+    const int r0 = lane * rows;
+    auto fetch = [&](int j) -> int64_t {
+        const int key = j * N + r0;
+        if (r0 < N && key < kend) return (int64_t)table[key / B];
+        return kNone;
+    };
+    constexpr int kAhead = 4;
+    int64_t ahead[kAhead];                                   // entries of tiles j .. j+3
+#pragma unroll
+    for (int k = 0; k < kAhead; ++k) ahead[k] = k < ntiles ? fetch(k) : kNone;
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+        const int64_t blk = ahead[0];
+#pragma unroll
+        for (int k = 0; k + 1 < kAhead; ++k) ahead[k] = ahead[k + 1];
+        ahead[kAhead - 1] = j + kAhead < ntiles ? fetch(j + kAhead) : kNone;
+        const int st = j % NS;
+        if (j >= NS) {
+            bool ok = true;
+            if (lane == 0) ok = tc_wait(&empty[st], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        const bool has = blk != kNone;
+        const bool valid = has && blk >= 0 && blk < p.num_blocks;
+        if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+        // the barrier must expect exactly the bytes that land
+        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes * (uint32_t)rows * 128u * Sh::kSpans);
+        __syncwarp();
+        if (valid) {
+            const int key = j * N + r0;
+            const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
+            uint8_t* dst = ring + st * Sh::kKvBytes + r0 * 128;
+#pragma unroll
+            for (int h = 0; h < Sh::kSpans; ++h)
+                tma_load_2d(dst + h * (N * 128), map, h * 64, y, &full[st]);
+        }
+        issued = j + 1;
+    }
+    // copies still in flight (only after an abort) land before the CTA ends
+    if (lane == 0)
+        for (int j = issued - 1; j >= 0 && j >= issued - NS; --j)
+            mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     using Sh = TcShape<D>;
     constexpr int N = Sh::N;
-    constexpr int KS = Sh::KS;
-    constexpr int VS = Sh::VS;
+    constexpr int NS = Sh::NS;
     const PrefillParams& p = tp.p;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::kBarOff);
     uint64_t* k_full = bars;
-    uint64_t* k_empty = k_full + KS;
-    uint64_t* v_full = k_empty + KS;
-    uint64_t* v_empty = v_full + VS;
-    uint64_t* s_full = v_empty + VS;
-    uint64_t* s_free = s_full + 2;
-    uint64_t* p_full = s_free + 2;
+    uint64_t* k_empty = k_full + NS;
+    uint64_t* v_full = k_empty + NS;
+    uint64_t* v_empty = v_full + NS;
+    uint64_t* s_full = v_empty + NS;
+    uint64_t* p_full = s_full + 2;
     uint64_t* pv_done = p_full + 1;
     uint64_t* drain = pv_done + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
@@ -265,11 +378,16 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int ntiles = (kend + N - 1) / N;
 
     // ---- setup: barriers, TMEM, the query tile
-    if (tid == kTcProducerWarp * 32) {
-        for (int i = 0; i < KS; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1); }
-        for (int i = 0; i < VS; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_free[i], 128); }
-        mbar_init(p_full, 128);
+    if (tid == kTcKWarp * 32) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(p_full, kTcSoftmaxThreads);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -283,19 +401,29 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     const int G = p.group;
-    if (warp < 4) {
-        // rows (token, head) of the tile; padding rows are zero
+    if (tid < kTcSoftmaxThreads) {
+        // rows (token, head) of the tile; padding rows are zero. All of a
+        // thread's loads are in flight before the first store.
         const T* qbase = reinterpret_cast<const T*>(p.query);
         constexpr int CPR = D / 8;                           // 16-byte chunks per row
-        for (int idx = tid; idx < kTcRows * CPR; idx += 128) {
+        constexpr int PER = kTcRows * CPR / kTcSoftmaxThreads;  // chunks per thread
+        uint4 v[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = tid + k * kTcSoftmaxThreads;
             const int r = idx / CPR, c = idx - r * CPR;
             const int i = r / G, g = r - i * G;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
             if (i < ntok) {
                 const size_t row = (size_t)(q0 + tok0 + i) * p.num_q_heads + (size_t)hk * G + g;
-                v = *reinterpret_cast<const uint4*>(qbase + row * D + c * 8);
+                v[k] = __ldg(reinterpret_cast<const uint4*>(qbase + row * D + c * 8));
             }
-            *reinterpret_cast<uint4*>(sm + Sh::kQOff + sw128_chunk<kTcRows>(r, c)) = v;
+        }
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = tid + k * kTcSoftmaxThreads;
+            const int r = idx / CPR, c = idx - r * CPR;
+            *reinterpret_cast<uint4*>(sm + Sh::kQOff + sw128_chunk<kTcRows>(r, c)) = v[k];
         }
         fence_async_smem();
     }
@@ -304,225 +432,210 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kTcProducerWarp) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-            const int rows = tp.box_rows;
-            const int B = p.block_size;
-            int issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const int ks = j % KS, vs = j % VS;
-                if (j >= KS && !tc_wait(&k_empty[ks], (uint32_t)((j / KS - 1) & 1), p.status, abort_flag)) break;
-                if (j >= VS && !tc_wait(&v_empty[vs], (uint32_t)((j / VS - 1) & 1), p.status, abort_flag)) break;
-                const int key0 = j * N;
-                const int nvalid = min(N, kend - key0);
-                // count the boxes first: the barrier must expect exactly what lands
-                uint32_t boxes = 0;
-                for (int r0 = 0; r0 < nvalid; r0 += rows) {
-                    const int key = key0 + r0;
-                    const int32_t blk = table[key / B];
-                    if (blk >= 0 && blk < p.num_blocks) ++boxes;
-                }
-                const uint32_t bytes = boxes * (uint32_t)rows * 128u * Sh::kSpans;
-                mbar_arrive_expect_tx(&k_full[ks], bytes);
-                mbar_arrive_expect_tx(&v_full[vs], bytes);
-                uint8_t* kd = sm + Sh::kKOff + ks * Sh::kKvBytes;
-                uint8_t* vd = sm + Sh::kVOff + vs * Sh::kKvBytes;
-                for (int r0 = 0; r0 < nvalid; r0 += rows) {
-                    const int key = key0 + r0;
-                    const int32_t blk = table[key / B];
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
-                        continue;
-                    }
-                    const int y = (int)(((int64_t)blk * p.num_kv_heads + hk) * B + key % B);
-#pragma unroll
-                    for (int h = 0; h < Sh::kSpans; ++h) {
-                        tma_load_2d(kd + h * (N * 128) + r0 * 128, &tp.k_map, h * 64, y, &k_full[ks]);
-                        tma_load_2d(vd + h * (N * 128) + r0 * 128, &tp.v_map, h * 64, y, &v_full[vs]);
-                    }
-                }
-                issued = j + 1;
-            }
-            // copies still in flight (only after an abort) land before the CTA ends
-            for (int j = issued - 1; j >= 0 && j >= issued - KS; --j)
-                mbar_wait_bounded(&k_full[j % KS], (uint32_t)((j / KS) & 1), p.status);
-            for (int j = issued - 1; j >= 0 && j >= issued - VS; --j)
-                mbar_wait_bounded(&v_full[j % VS], (uint32_t)((j / VS) & 1), p.status);
-        }
+    if (warp == kTcKWarp) {
+        // ------------------------------------------------------------ K loads
+        tc_load_ring<D>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend, lane,
+                        abort_flag);
+    } else if (warp == kTcVWarp) {
+        // ------------------------------------------------------------ V loads
+        tc_load_ring<D>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend, lane,
+                        abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = tc_idesc<T>(kTcRows, N, 0);
             constexpr uint32_t idO = tc_idesc<T>(kTcRows, D, 1);
             const uint32_t qa = smem_u32(sm + Sh::kQOff);
-            const uint32_t pa = smem_u32(sm + Sh::kPOff);
-            auto pv = [&](int j) -> bool {
-                const int vs = j % VS;
-                if (!tc_wait(p_full, (uint32_t)(j & 1), p.status, abort_flag)) return false;
-                if (!tc_wait(&v_full[vs], (uint32_t)((j / VS) & 1), p.status, abort_flag)) return false;
+            auto qk = [&](int j) -> bool {
+                const int st = j % NS;
+                if (!tc_wait(&k_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t va = smem_u32(sm + Sh::kVOff + vs * Sh::kKvBytes);
+                const uint32_t ka = smem_u32(sm + Sh::kKOff + st * Sh::kKvBytes);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk & 3) * 32u;
+                    const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
+                    const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
+                    tc_mma(tmem + Sh::kSCol + (j & 1) * N, a, b, idS, kk > 0);
+                }
+                tc_commit(&k_empty[st]);
+                tc_commit(&s_full[j & 1]);
+                return true;
+            };
+            auto pv = [&](int j) -> bool {
+                const int st = j % NS;
+                if (!tc_wait(p_full, (uint32_t)(j & 1), p.status, abort_flag)) return false;
+                if (!tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kKvBytes);
+                const uint32_t pt = tmem + Sh::kSCol + (j & 1) * N;   // P_hi | P_lo
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t a = tc_desc(pa + (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
-                    tc_mma(tmem + Sh::kOCol, a, b, idO, j > 0 || kk > 0);
+                    tc_mma_ts(tmem + Sh::kOCol, pt + kk * 8, b, idO, j > 0 || kk > 0);
                 }
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t a = tc_desc(pa + Sh::kPBytes + (kk >> 2) * (kTcRows * 128) + (kk & 3) * 32,
-                                               16, 1024);
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
-                    tc_mma(tmem + Sh::kOCol, a, b, idO, true);
+                    tc_mma_ts(tmem + Sh::kOCol, pt + N / 2 + kk * 8, b, idO, true);
                 }
-                tc_commit(&v_empty[vs]);
+                tc_commit(&v_empty[st]);
                 tc_commit(pv_done);
                 return true;
             };
-            bool ok = true;
+            bool ok = qk(0);
             for (int j = 0; j < ntiles && ok; ++j) {
-                const int ks = j % KS, b = j & 1;
-                ok = tc_wait(&k_full[ks], (uint32_t)((j / KS) & 1), p.status, abort_flag);
-                if (ok && j >= 2)
-                    ok = tc_wait(&s_free[b], (uint32_t)((j / 2 - 1) & 1), p.status, abort_flag);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t ka = smem_u32(sm + Sh::kKOff + ks * Sh::kKvBytes);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
-                    const uint64_t bd = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
-                    tc_mma(tmem + Sh::kSCol + b * N, a, bd, idS, kk > 0);
-                }
-                tc_commit(&k_empty[ks]);
-                tc_commit(&s_full[b]);
-                if (j >= 1) ok = pv(j - 1);
+                if (j + 1 < ntiles) ok = qk(j + 1);
+                if (ok) ok = pv(j);
             }
-            if (ok) pv(ntiles - 1);
-            // everything issued has finished before TMEM is freed
+            // everything issued has finished before the epilogue reads O and
+            // before TMEM is freed
             tc_commit(drain);
             mbar_wait_bounded(drain, 0, p.status);
         }
     } else {
         // ------------------------------------------------------------ softmax (rows)
-        const int r = tid;                                   // TMEM lane = row
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // Thread t: row r = t mod 128 (its warp's TMEM lane quarter), half
+        // hf = t / 128 of the key columns. Both halves read the whole row to
+        // take the same max, so they make the same rescale decision; each
+        // exponentiates, sums and stores only its own columns.
+        constexpr int NH = N / 2;
+        const int r = tid & (kTcRows - 1);
+        const int hf = tid / kTcRows;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int i = r / G;
         const bool row_valid = i < ntok && r < Tq * G;
         const int pos = first_pos + (row_valid ? i : ntok - 1);
         const float qm = p.q_mul;
+        const float2 qm2 = make_float2(qm, qm);
         float m = -INFINITY;                                 // running max (base 2, scaled)
-        float l = 0.f;
+        float l = 0.f;                                       // this half's running sum
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;
+            const uint32_t sbuf = lane_base + Sh::kSCol + b * N;
             ok = tc_wait(&s_full[b], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            // the whole row in flight at once, one wait
+            uint32_t xr[N];
+#pragma unroll
+            for (int c = 0; c < N; c += 32)
+                tc_ld32(sbuf + c, *reinterpret_cast<uint32_t(*)[32]>(xr + c));
+            tc_wait_ld();
             float x[N];
 #pragma unroll
-            for (int c = 0; c < N; c += 32) {
-                uint32_t rr[32];
-                tc_ld32(lane_base + Sh::kSCol + b * N + c, rr);
-                tc_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(rr[e]);
-            }
-            tc_fence_before();
-            mbar_arrive(&s_free[b]);
+            for (int c = 0; c < N; ++c) x[c] = __uint_as_float(xr[c]);
             const int key0 = j * N;
             if (key0 + N - 1 > pos) {                        // the causal edge crosses this tile
 #pragma unroll
                 for (int c = 0; c < N; ++c)
                     if (key0 + c > pos) x[c] = -INFINITY;
             }
-            float mx = x[0];
+            // the max as 8 independent chains
+            constexpr int R = 8;
+            float mr[R];
 #pragma unroll
-            for (int c = 1; c < N; ++c) mx = fmaxf(mx, x[c]);
-            const float m_cand = fmaxf(m, mx * qm);
+            for (int k = 0; k < R; ++k) mr[k] = x[k];
+#pragma unroll
+            for (int c = R; c < N; ++c) mr[c % R] = fmaxf(mr[c % R], x[c]);
+#pragma unroll
+            for (int w = R / 2; w >= 1; w /= 2)
+#pragma unroll
+                for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
+            const float m_cand = fmaxf(m, mr[0] * qm);
             const bool rescale = m_cand > m + kTcRescaleLog2;
             const float m_use = rescale ? m_cand : m;
             const float alpha = fast_exp2(m - m_use);        // 0 on the first tile, 1 if kept
-            float sum = 0.f;
-            uint32_t phi[N / 2], plo[N / 2];
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            // this half's weights: 2^(x qm - m), as hi + lo 16-bit pairs
+            uint32_t phi[NH / 2], plo[NH / 2];
+            float2 sr[R / 2];
 #pragma unroll
-            for (int c = 0; c < N; c += 2) {
-                const float e0 = fast_exp2(fmaf(x[c], qm, -m_use));
-                const float e1 = fast_exp2(fmaf(x[c + 1], qm, -m_use));
-                sum += e0 + e1;
-                phi[c / 2] = pack2<T>(e0, e1);
-                const float2 h = unpack2<T>(phi[c / 2]);
-                plo[c / 2] = pack2<T>(e0 - h.x, e1 - h.y);
-            }
-            l = fmaf(l, alpha, sum);
+            for (int k = 0; k < R / 2; ++k) sr[k] = make_float2(0.f, 0.f);
+            auto weights = [&](auto off) {
+                constexpr int c0 = decltype(off)::value;
+#pragma unroll
+                for (int c = 0; c < NH; c += 2) {
+                    const float2 t = __ffma2_rn(make_float2(x[c0 + c], x[c0 + c + 1]), qm2, nm2);
+                    const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+                    sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
+                    phi[c / 2] = pack2<T>(e.x, e.y);
+                    const float2 lo = __ffma2_rn(unpack2<T>(phi[c / 2]), make_float2(-1.f, -1.f), e);
+                    plo[c / 2] = pack2<T>(lo.x, lo.y);
+                }
+            };
+            if (hf == 0) weights(std::integral_constant<int, 0>{});
+            else weights(std::integral_constant<int, NH>{});
+#pragma unroll
+            for (int w = R / 4; w >= 1; w /= 2)
+#pragma unroll
+                for (int k = 0; k < w; ++k) sr[k] = __fadd2_rn(sr[k], sr[k + w]);
+            l = fmaf(l, alpha, sr[0].x + sr[0].y);
             m = m_use;
-            // the previous P.V must be done: P's buffer is reused and O is read
-            if (j > 0) {
+            // P over S in the same buffer: P_hi pairs in columns [0, N/2), P_lo
+            // in [N/2, N); this half's keys are a quarter of the buffer each
+            tc_st_n<NH / 2>(sbuf + hf * (NH / 2), phi);
+            tc_st_n<NH / 2>(sbuf + N / 2 + hf * (NH / 2), plo);
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // O holds tiles < j once the previous P.V is done; each half
+                // rescales its half of the columns
                 ok = tc_wait(pv_done, (uint32_t)((j - 1) & 1), p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t o[32];
-                        tc_ld32(lane_base + Sh::kOCol + c, o);
-                        tc_wait_ld();
+                for (int c = 0; c < D / 2; c += 32) {
+                    const uint32_t oa = lane_base + Sh::kOCol + hf * (D / 2) + c;
+                    uint32_t o[32];
+                    tc_ld32(oa, o);
+                    tc_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e)
-                            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tc_st32(lane_base + Sh::kOCol + c, o);
-                    }
-                    tc_wait_st();
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc_st32(oa, o);
                 }
             }
-            // P row, 16-byte chunks into the swizzled K-major tiles
-#pragma unroll
-            for (int c = 0; c < N / 8; ++c) {
-                const uint32_t off = Sh::kPOff + sw128_chunk<kTcRows>(r, c);
-                *reinterpret_cast<uint4*>(sm + off) =
-                    make_uint4(phi[4 * c], phi[4 * c + 1], phi[4 * c + 2], phi[4 * c + 3]);
-                *reinterpret_cast<uint4*>(sm + off + Sh::kPBytes) =
-                    make_uint4(plo[4 * c], plo[4 * c + 1], plo[4 * c + 2], plo[4 * c + 3]);
-            }
+            tc_wait_st();
             if (key0 + N > kend) {
                 // last tile: V rows at or past kend hold stale data or cache
                 // poison; zero them so that 0-weights stay 0 in the MMA
-                const int vs = j % VS;
-                ok = tc_wait(&v_full[vs], (uint32_t)((j / VS) & 1), p.status, abort_flag);
+                const int st = j % NS;
+                ok = tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const int first = kend - key0;
                 constexpr int CPR = D / 8;
-                uint8_t* vd = sm + Sh::kVOff + vs * Sh::kKvBytes;
-                for (int idx = tid; idx < (N - first) * CPR; idx += 128) {
+                uint8_t* vd = sm + Sh::kVOff + st * Sh::kKvBytes;
+                for (int idx = tid; idx < (N - first) * CPR; idx += kTcSoftmaxThreads) {
                     const int rr = first + idx / CPR, c = idx % CPR;
                     *reinterpret_cast<uint4*>(vd + sw128_chunk<N>(rr, c)) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_async_smem();
             }
-            fence_async_smem();
             tc_fence_before();
             mbar_arrive(p_full);
         }
-        // ---- epilogue: O / l to the output row
+        // ---- epilogue: O / l to the output row, once every MMA has finished
+        // (the MMA issuer's final commit; pv_done could alias two phases here)
+        float* lsum = reinterpret_cast<float*>(sm + Sh::kLsumOff);
+        lsum[tid] = l;
+        named_barrier(1, kTcSoftmaxThreads);
+        const float inv = 1.f / (lsum[r] + lsum[r + kTcRows]);
         if (ok) {
-            ok = tc_wait(pv_done, (uint32_t)((ntiles - 1) & 1), p.status, abort_flag);
+            ok = tc_wait(drain, 0u, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             tc_fence_after();
-            const float inv = 1.f / l;
             T* orow = reinterpret_cast<T*>(p.out) +
                       ((size_t)(q0 + tok0 + (row_valid ? i : 0)) * p.num_q_heads + (size_t)hk * G +
-                       (r - i * G)) * D;
+                       (r - i * G)) * D + hf * (D / 2);
 #pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
+            for (int c = 0; c < D / 2; c += 32) {
                 uint32_t o[32];
-                tc_ld32(lane_base + Sh::kOCol + c, o);
+                tc_ld32(lane_base + Sh::kOCol + hf * (D / 2) + c, o);
                 tc_wait_ld();
                 if (row_valid) {
 #pragma unroll
