@@ -396,6 +396,46 @@ pa_status pa_allocator_append_slot(pa_block_allocator* allocator, int32_t* table
                                    int64_t* slot, int32_t* copy_src, int32_t* copy_dst);
 
 /*
+ * pa_radix_allocator -- prefix caching: a radix trie from token sequences to
+ * the physical blocks holding their K/V, so that requests sharing a prompt
+ * prefix share its blocks (TGI deep-dive sec. 5.2-5.3, RadixAllocator). Host
+ * memory only; calls are serialised by an internal mutex; each validates
+ * first and changes nothing when it fails.
+ *
+ *  create      num_blocks ids, block 0 kept out if reserve_block0 (NULL on
+ *              bad arguments or no memory).
+ *  allocate    blocks for a request whose prompt is tokens[0, num_tokens) and
+ *              which may grow to total_tokens (>= num_tokens): the longest
+ *              cached block-aligned prefix of the prompt (*prefix_len tokens,
+ *              a multiple of block_size) is shared -- its blocks come first in
+ *              blocks[] -- and ceil(total_tokens / block_size) blocks are
+ *              returned in all (*num_allocated <= capacity). Missing blocks
+ *              come from the free list, evicting cached sequences nobody uses,
+ *              least recently used first. PA_ERR_NO_BLOCKS (nothing changed)
+ *              when even eviction cannot supply them. *allocation_id names the
+ *              request for pa_radix_free.
+ *  free        ends a request. tokens[0, num_tokens) are the tokens its blocks
+ *              now hold (prompt and generated tokens; they must start with the
+ *              shared prefix): their whole blocks are inserted into the trie
+ *              for later requests, a node that only partly matches is split,
+ *              and blocks the trie does not take return to the free list.
+ *  num_free    blocks on the free list; num_cached: blocks held by the trie;
+ *              num_evictable: blocks of trie leaves no request uses.
+ */
+typedef struct pa_radix_allocator pa_radix_allocator;
+pa_radix_allocator* pa_radix_create(int64_t num_blocks, int block_size, int reserve_block0);
+void pa_radix_destroy(pa_radix_allocator* allocator);
+pa_status pa_radix_allocate(pa_radix_allocator* allocator, const int32_t* tokens,
+                            int64_t num_tokens, int64_t total_tokens, int32_t* blocks,
+                            int64_t capacity, int64_t* num_allocated, int64_t* prefix_len,
+                            int64_t* allocation_id);
+pa_status pa_radix_free(pa_radix_allocator* allocator, int64_t allocation_id,
+                        const int32_t* tokens, int64_t num_tokens);
+int64_t pa_radix_num_free(pa_radix_allocator* allocator);
+int64_t pa_radix_num_cached(pa_radix_allocator* allocator);
+int64_t pa_radix_num_evictable(pa_radix_allocator* allocator);
+
+/*
  * pa_decode_choose -- which decode to run: 0 = single pass (pa_decode),
  * 1 = partitioned (pa_decode_partitioned). The pages' rule (TGI deep-dive
  * sec. 4.1) picks V1 when there is one partition or when num_seqs x num_heads

@@ -96,6 +96,15 @@ def lib() -> ctypes.CDLL:
         L.pa_allocator_fork.argtypes = [P, P, I64]
         L.pa_allocator_free.argtypes = [P, P, I64]
         L.pa_allocator_append_slot.argtypes = [P, P, P, I64, I64, P, P, P]
+        L.pa_radix_create.argtypes = [I64, I, I]
+        L.pa_radix_create.restype = P
+        L.pa_radix_destroy.argtypes = [P]
+        L.pa_radix_destroy.restype = None
+        L.pa_radix_allocate.argtypes = [P, P, I64, I64, P, I64, P, P, P]
+        L.pa_radix_free.argtypes = [P, I64, P, I64]
+        for f in ("pa_radix_num_free", "pa_radix_num_cached", "pa_radix_num_evictable"):
+            getattr(L, f).argtypes = [P]
+            getattr(L, f).restype = I64
         L.pa_decode_choose.argtypes = [I, I, I, I, I]
         L.pa_decode_partition_size.argtypes = [I, I, I]
         L.pa_status_string.argtypes = [I]
@@ -477,3 +486,59 @@ class BlockAllocator:
                "pa_allocator_append_slot")
         copy = (int(src.value), int(dst.value)) if src.value >= 0 else None
         return int(slot.value), int(n.value), copy
+
+
+class RadixAllocator:
+    """The library's prefix-caching block allocator (a radix trie from token
+    sequences to blocks, LRU eviction of unused cached sequences)."""
+
+    def __init__(self, num_blocks: int, block_size: int, reserve_block0: bool = True):
+        self._lib = lib()
+        self._h = self._lib.pa_radix_create(num_blocks, block_size, int(reserve_block0))
+        if not self._h:
+            raise ValueError("invalid allocator arguments")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def close(self):
+        if self._h:
+            self._lib.pa_radix_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pa_radix_num_free(self._h))
+
+    @property
+    def num_cached(self) -> int:
+        return int(self._lib.pa_radix_num_cached(self._h))
+
+    @property
+    def num_evictable(self) -> int:
+        return int(self._lib.pa_radix_num_evictable(self._h))
+
+    def allocate(self, prompt, total_tokens: int | None = None):
+        """Blocks for a request with this prompt (int32 tokens) that may grow
+        to total_tokens: returns (blocks, prefix_len, allocation_id)."""
+        import numpy as np
+        t = np.ascontiguousarray(prompt, dtype=np.int32)
+        total = t.size if total_tokens is None else int(total_tokens)
+        n = -(-total // self.block_size)
+        out = np.zeros(max(1, n), dtype=np.int32)
+        got, plen, aid = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(self._lib.pa_radix_allocate(self._h, t.ctypes.data, t.size, total, out.ctypes.data,
+                                           out.size, ctypes.byref(got), ctypes.byref(plen),
+                                           ctypes.byref(aid)), "pa_radix_allocate")
+        return out[:got.value].copy(), int(plen.value), int(aid.value)
+
+    def free(self, allocation_id: int, tokens) -> None:
+        """End a request; `tokens` are those its blocks now hold."""
+        import numpy as np
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(self._lib.pa_radix_free(self._h, int(allocation_id), t.ctypes.data, t.size),
+               "pa_radix_free")
