@@ -426,7 +426,8 @@ def run_prefill(args):
         raise SystemExit("bench.py needs a CUDA device")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
-    case = W.config_case(args.config)
+    case = (W.config_case(args.config, num_seqs=args.num_seqs) if args.num_seqs
+            else W.config_case(args.config))
     q = W.make_queries(case, prefill_queries(case, args.prefill))
     st = Step(case, device, 512, "separate")
     st.calls[0][1]()                       # the step's KV write: every context token stored
@@ -639,6 +640,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", choices=["chunk512", "spec8"], default=None,
                     help="time multi-query paged attention on the configuration's pool instead")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="with --prefill: fewer sequences of the same shape (small ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

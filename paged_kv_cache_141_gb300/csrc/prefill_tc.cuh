@@ -80,8 +80,8 @@ struct TcShape {
     static constexpr int kKOff = kQOff + kQBytes;
     static constexpr int kVOff = kKOff + NS * kKvBytes;
     static constexpr int kBarOff = kVOff + NS * kKvBytes;
-    // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
-    static constexpr int kNumBars = 4 * NS + 5;
+    // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain q_ready
+    static constexpr int kNumBars = 4 * NS + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
     static constexpr int kBytes = kLsumOff + kTcSoftmaxThreads * 4;
@@ -345,6 +345,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* p_full = s_full + 2;
     uint64_t* pv_done = p_full + 1;
     uint64_t* drain = pv_done + 1;
+    uint64_t* q_ready = drain + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -377,7 +378,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int kend = first_pos + ntok;                       // keys [0, kend)
     const int ntiles = (kend + N - 1) / N;
 
-    // ---- setup: barriers, TMEM, the query tile
+    // ---- setup: barriers and TMEM; the K/V producers start at once, while
+    // the softmax warps load the query tile (the MMA issuer waits for it)
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&k_full[i], 1);
@@ -390,6 +392,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         mbar_init(p_full, kTcSoftmaxThreads);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
+        mbar_init(q_ready, kTcSoftmaxThreads);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_map(&tp.k_map);
@@ -400,6 +403,10 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                      ::"r"(smem_u32(tmem_slot)), "r"(Sh::kTmemCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     const int G = p.group;
     if (tid < kTcSoftmaxThreads) {
         // rows (token, head) of the tile; padding rows are zero. All of a
@@ -426,11 +433,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             *reinterpret_cast<uint4*>(sm + Sh::kQOff + sw128_chunk<kTcRows>(r, c)) = v[k];
         }
         fence_async_smem();
+        mbar_arrive(q_ready);
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+
 
     if (warp == kTcKWarp) {
         // ------------------------------------------------------------ K loads
@@ -483,7 +488,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 tc_commit(pv_done);
                 return true;
             };
-            bool ok = qk(0);
+            bool ok = tc_wait(q_ready, 0u, p.status, abort_flag);
+            tc_fence_after();
+            if (ok) ok = qk(0);
             for (int j = 0; j < ntiles && ok; ++j) {
                 if (j + 1 < ntiles) ok = qk(j + 1);
                 if (ok) ok = pv(j);
