@@ -237,6 +237,42 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
     return __half22float2(*reinterpret_cast<__half2*>(&w));
 }
 
+// Multicast of one box to both CTAs of the pair (same shared-memory offset,
+// completing on the same-offset barrier in each).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
+                                                 uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+        "r"(smem_u32(bar)), "h"((uint16_t)0x3)
+        : "memory");
+}
+
+// Free a ring slot once the MMAs issued so far are done: this CTA's barrier,
+// or both CTAs' barriers for a pair (each slot is filled in both).
+template <bool kPair>
+__device__ __forceinline__ void release_slot(uint64_t* bar) {
+    if constexpr (kPair) {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster"
+            ".multicast::cluster.b64 [%0], %1;"
+            ::"r"(smem_u32(bar)), "h"((uint16_t)0x3)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+            ::"r"(smem_u32(bar))
+            : "memory");
+    }
+}
+
+// Every thread of both CTAs of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
 // Bounded mbarrier wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
                                         volatile int* abort_flag) {
@@ -266,13 +302,13 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 // ring `ring` of NS slots, each slot freed by a commit on `empty`, filled on
 // `full`. Lane i owns box i of a tile (keys i*box_rows ..): it reads that
 // box's block-table entry and issues the box's copies. The entries of the
-// next kAhead tiles are in flight while a tile is issued, so the table's
-// latency is paid once per unit, not once per tile.
-template <int D>
+// next kAhead tiles are in flight while the current ones are issued, so the
+// table's latency is not paid per tile.
+template <int D, bool kPair>
 __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CUtensorMap* map,
                                              uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              int s, int hk, int ntiles, int kend, int lane,
-                                             volatile int* abort_flag) {
+                                             int rank, volatile int* abort_flag) {
     using Sh = TcShape<D>;
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
@@ -287,38 +323,57 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
         if (r0 < N && key < kend) return (int64_t)table[key / B];
         return kNone;
     };
+    // Entries for groups of kAhead tiles: the next group's loads are issued
+    // when a group starts and read when it ends, so no register copy waits on
+    // a load still in flight.
     constexpr int kAhead = 4;
-    int64_t ahead[kAhead];                                   // entries of tiles j .. j+3
+    int64_t cur[kAhead], nxt[kAhead];
 #pragma unroll
-    for (int k = 0; k < kAhead; ++k) ahead[k] = k < ntiles ? fetch(k) : kNone;
+    for (int k = 0; k < kAhead; ++k) cur[k] = k < ntiles ? fetch(k) : kNone;
     int issued = 0;
-    for (int j = 0; j < ntiles; ++j) {
-        const int64_t blk = ahead[0];
+    bool live = true;
+    for (int j0 = 0; j0 < ntiles && live; j0 += kAhead) {
 #pragma unroll
-        for (int k = 0; k + 1 < kAhead; ++k) ahead[k] = ahead[k + 1];
-        ahead[kAhead - 1] = j + kAhead < ntiles ? fetch(j + kAhead) : kNone;
-        const int st = j % NS;
-        if (j >= NS) {
-            bool ok = true;
-            if (lane == 0) ok = tc_wait(&empty[st], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        }
-        const bool has = blk != kNone;
-        const bool valid = has && blk >= 0 && blk < p.num_blocks;
-        if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
-        // the barrier must expect exactly the bytes that land
-        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes * (uint32_t)rows * 128u * Sh::kSpans);
-        __syncwarp();
-        if (valid) {
-            const int key = j * N + r0;
-            const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
-            uint8_t* dst = ring + st * Sh::kKvBytes + r0 * 128;
+        for (int k = 0; k < kAhead; ++k) nxt[k] = j0 + kAhead + k < ntiles ? fetch(j0 + kAhead + k) : kNone;
 #pragma unroll
-            for (int h = 0; h < Sh::kSpans; ++h)
-                tma_load_2d(dst + h * (N * 128), map, h * 64, y, &full[st]);
+        for (int k = 0; k < kAhead; ++k) {
+            const int j = j0 + k;
+            if (j >= ntiles || !live) break;
+            const int64_t blk = cur[k];
+            const int st = j % NS;
+            if (j >= NS) {
+                bool ok = true;
+                if (lane == 0) ok = tc_wait(&empty[st], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    live = false;
+                    break;
+                }
+            }
+            const bool has = blk != kNone;
+            const bool valid = has && blk >= 0 && blk < p.num_blocks;
+            if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+            // the barrier must expect exactly the bytes that land
+            const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes * (uint32_t)rows * 128u * Sh::kSpans);
+            __syncwarp();
+            // a CTA pair splits the boxes (even lanes: rank 0) and multicasts
+            // each to both CTAs' rings
+            if (valid && (!kPair || (lane & 1) == rank)) {
+                const int key = j * N + r0;
+                const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
+                uint8_t* dst = ring + st * Sh::kKvBytes + r0 * 128;
+#pragma unroll
+                for (int h = 0; h < Sh::kSpans; ++h) {
+                    if constexpr (kPair)
+                        tma_load_2d_pair(dst + h * (N * 128), map, h * 64, y, &full[st]);
+                    else
+                        tma_load_2d(dst + h * (N * 128), map, h * 64, y, &full[st]);
+                }
+            }
+            issued = j + 1;
         }
-        issued = j + 1;
+#pragma unroll
+        for (int k = 0; k < kAhead; ++k) cur[k] = nxt[k];
     }
     // copies still in flight (only after an abort) land before the CTA ends
     if (lane == 0)
@@ -326,7 +381,7 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kPair>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     using Sh = TcShape<D>;
@@ -353,9 +408,14 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- the work unit
-    const int tile = blockIdx.x % p.q_tiles;
-    const int rest = blockIdx.x / p.q_tiles;
+    // ---- the work unit. A CTA pair (a 2-CTA cluster) takes query tiles 2t
+    // and 2t+1 of one (sequence, KV head) and shares their K/V tiles.
+    const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
+    const int groups = kPair ? (p.q_tiles + 1) / 2 : p.q_tiles;
+    const int gidx = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int tile0 = (gidx % groups) * (kPair ? 2 : 1);    // first tile of the group
+    const int tile = tile0 + rank;
+    const int rest = gidx / groups;
     const int hk = rest % p.num_kv_heads;
     const int s = rest / p.num_kv_heads;
     const int q0 = p.query_start[s];
@@ -367,15 +427,18 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         if (tab < cap) cap = (int)tab;
         if (Q < 0 || Q > p.max_queries || L < Q || L > cap) {
             if (tid == 0 && tile == 0 && hk == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_LEN);
-            return;
+            return;                                          // (both CTAs of a pair)
         }
     }
     const int Tq = p.tokens_per_tile;
+    if (tile0 * Tq >= Q) return;                             // no such tile (group)
+    // this CTA's rows; the second CTA of a pair may have none (it still
+    // loads its half of the shared tiles and runs on padding rows)
     const int tok0 = tile * Tq;
-    if (tok0 >= Q) return;                                   // no such tile
-    const int ntok = min(Tq, Q - tok0);
+    const int ntok = max(0, min(Tq, Q - tok0));
     const int first_pos = L - Q + tok0;
-    const int kend = first_pos + ntok;                       // keys [0, kend)
+    // keys [0, kend) cover every row of the group
+    const int kend = L - Q + min(Q, (tile0 + (kPair ? 2 : 1)) * Tq);
     const int ntiles = (kend + N - 1) / N;
 
     // ---- setup: barriers and TMEM; the K/V producers start at once, while
@@ -383,9 +446,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], 1);
+            mbar_init(&k_empty[i], kPair ? 2 : 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], kPair ? 2 : 1);
         }
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
@@ -405,6 +468,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();                     // the peer's barriers exist
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int G = p.group;
@@ -439,12 +503,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
     if (warp == kTcKWarp) {
         // ------------------------------------------------------------ K loads
-        tc_load_ring<D>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend, lane,
-                        abort_flag);
+        tc_load_ring<D, kPair>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
+                               kend, lane, rank, abort_flag);
     } else if (warp == kTcVWarp) {
         // ------------------------------------------------------------ V loads
-        tc_load_ring<D>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend, lane,
-                        abort_flag);
+        tc_load_ring<D, kPair>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
+                               kend, lane, rank, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -463,7 +527,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
                     tc_mma(tmem + Sh::kSCol + (j & 1) * N, a, b, idS, kk > 0);
                 }
-                tc_commit(&k_empty[st]);
+                release_slot<kPair>(&k_empty[st]);
                 tc_commit(&s_full[j & 1]);
                 return true;
             };
@@ -484,7 +548,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
                     tc_mma_ts(tmem + Sh::kOCol, pt + N / 2 + kk * 8, b, idO, true);
                 }
-                tc_commit(&v_empty[st]);
+                release_slot<kPair>(&v_empty[st]);
                 tc_commit(pv_done);
                 return true;
             };
@@ -531,6 +595,11 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             for (int c = 0; c < N; c += 32)
                 tc_ld32(sbuf + c, *reinterpret_cast<uint32_t(*)[32]>(xr + c));
             tc_wait_ld();
+            // the other half of this row must have read S before either half
+            // writes its weights over it
+            tc_fence_before();
+            named_barrier(2, kTcSoftmaxThreads);
+            tc_fence_after();
             float x[N];
 #pragma unroll
             for (int c = 0; c < N; ++c) x[c] = __uint_as_float(xr[c]);
@@ -659,10 +728,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
     }
 
-    // ---- teardown: all TMEM traffic has completed
+    // ---- teardown: all TMEM traffic has completed; a pair also waits for
+    // its peer, whose copies and commits target this CTA's shared memory
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    if constexpr (kPair) cluster_sync();
     if (warp == kTcMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -676,15 +747,30 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 template <typename T, int D>
 cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) {
     using Sh = TcShape<D>;
-    auto kern = paged_prefill_tc_kernel<T, D>;
+    const PrefillParams& p = tp.p;
+    // query tiles pair up in 2-CTA clusters whenever a sequence can have two
+    const bool pair = p.q_tiles >= 2;
+    const long long groups = (long long)p.num_seqs * p.num_kv_heads *
+                             (pair ? (p.q_tiles + 1) / 2 : p.q_tiles);
+    if (groups <= 0) return cudaSuccess;
+    const long long ctas = groups * (pair ? 2 : 1);
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
+    auto kern = pair ? paged_prefill_tc_kernel<T, D, true> : paged_prefill_tc_kernel<T, D, false>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
     if (e != cudaSuccess) return e;
-    const PrefillParams& p = tp.p;
-    const long long units = (long long)p.num_seqs * p.num_kv_heads * p.q_tiles;
-    if (units <= 0) return cudaSuccess;
-    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kern<<<(unsigned)units, kTcThreads, Sh::kAlloc, stream>>>(tp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = Sh::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tp);
 }
 
 template <typename T>

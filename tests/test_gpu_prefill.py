@@ -247,3 +247,16 @@ def test_full_size_llama3_8b_sampled(law):
     rows = np.array(sorted(rows))
     want = p.oracle_rows(rows)
     assert_decode_close(got[rows], want, c, "full size")
+
+
+@pytest.mark.parametrize("law", [("uniform", 1, 8), ("uniform", 200, 600)], ids=["spec", "chunk"])
+def test_repeated_launches_are_bit_identical(law):
+    """The same launch three times gives the same bits (no race between the
+    warps that share a row, the producers and the MMA issuer)."""
+    c = config_case(3, num_seqs=64)
+    p = Prefill(c, law)
+    first = p.run().clone()
+    assert p.dc.status_bits() == 0
+    for _ in range(2):
+        p.out.fill_(float("nan"))
+        assert torch.equal(p.run(), first)
