@@ -237,42 +237,6 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
     return __half22float2(*reinterpret_cast<__half2*>(&w));
 }
 
-// Multicast of one box to both CTAs of the pair (same shared-memory offset,
-// completing on the same-offset barrier in each).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int x, int y,
-                                                 uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
-        "r"(smem_u32(bar)), "h"((uint16_t)0x3)
-        : "memory");
-}
-
-// Free a ring slot once the MMAs issued so far are done: this CTA's barrier,
-// or both CTAs' barriers for a pair (each slot is filled in both).
-template <bool kPair>
-__device__ __forceinline__ void release_slot(uint64_t* bar) {
-    if constexpr (kPair) {
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster"
-            ".multicast::cluster.b64 [%0], %1;"
-            ::"r"(smem_u32(bar)), "h"((uint16_t)0x3)
-            : "memory");
-    } else {
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-            ::"r"(smem_u32(bar))
-            : "memory");
-    }
-}
-
-// Every thread of both CTAs of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
-}
-
 // Bounded mbarrier wait that also gives up once another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
                                         volatile int* abort_flag) {
@@ -304,12 +268,11 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 // box's block-table entry and issues the box's copies. The entries of the
 // next kAhead tiles are in flight while the current ones are issued, so the
 // table's latency is not paid per tile.
-template <int D, bool kPair>
+template <typename Sh>
 __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CUtensorMap* map,
                                              uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              int s, int hk, int ntiles, int kend, int lane,
-                                             int rank, volatile int* abort_flag) {
-    using Sh = TcShape<D>;
+                                             volatile int* abort_flag) {
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
     constexpr int64_t kNone = -1;
@@ -356,19 +319,13 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
             if (lane == 0) mbar_arrive_expect_tx(&full[st], boxes * (uint32_t)rows * 128u * Sh::kSpans);
             __syncwarp();
-            // a CTA pair splits the boxes (even lanes: rank 0) and multicasts
-            // each to both CTAs' rings
-            if (valid && (!kPair || (lane & 1) == rank)) {
+            if (valid) {
                 const int key = j * N + r0;
                 const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
                 uint8_t* dst = ring + st * Sh::kKvBytes + r0 * 128;
 #pragma unroll
-                for (int h = 0; h < Sh::kSpans; ++h) {
-                    if constexpr (kPair)
-                        tma_load_2d_pair(dst + h * (N * 128), map, h * 64, y, &full[st]);
-                    else
-                        tma_load_2d(dst + h * (N * 128), map, h * 64, y, &full[st]);
-                }
+                for (int h = 0; h < Sh::kSpans; ++h)
+                    tma_load_2d(dst + h * (N * 128), map, h * 64, y, &full[st]);
             }
             issued = j + 1;
         }
@@ -381,7 +338,7 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
 }
 
-template <typename T, int D, bool kPair>
+template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     using Sh = TcShape<D>;
@@ -408,14 +365,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // ---- the work unit. A CTA pair (a 2-CTA cluster) takes query tiles 2t
-    // and 2t+1 of one (sequence, KV head) and shares their K/V tiles.
-    const int rank = kPair ? (int)(blockIdx.x & 1) : 0;
-    const int groups = kPair ? (p.q_tiles + 1) / 2 : p.q_tiles;
-    const int gidx = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-    const int tile0 = (gidx % groups) * (kPair ? 2 : 1);    // first tile of the group
-    const int tile = tile0 + rank;
-    const int rest = gidx / groups;
+    // ---- the work unit
+    const int tile = blockIdx.x % p.q_tiles;
+    const int rest = blockIdx.x / p.q_tiles;
     const int hk = rest % p.num_kv_heads;
     const int s = rest / p.num_kv_heads;
     const int q0 = p.query_start[s];
@@ -427,18 +379,15 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         if (tab < cap) cap = (int)tab;
         if (Q < 0 || Q > p.max_queries || L < Q || L > cap) {
             if (tid == 0 && tile == 0 && hk == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_LEN);
-            return;                                          // (both CTAs of a pair)
+            return;
         }
     }
     const int Tq = p.tokens_per_tile;
-    if (tile0 * Tq >= Q) return;                             // no such tile (group)
-    // this CTA's rows; the second CTA of a pair may have none (it still
-    // loads its half of the shared tiles and runs on padding rows)
     const int tok0 = tile * Tq;
-    const int ntok = max(0, min(Tq, Q - tok0));
+    if (tok0 >= Q) return;                                   // no such tile
+    const int ntok = min(Tq, Q - tok0);
     const int first_pos = L - Q + tok0;
-    // keys [0, kend) cover every row of the group
-    const int kend = L - Q + min(Q, (tile0 + (kPair ? 2 : 1)) * Tq);
+    const int kend = first_pos + ntok;                       // keys [0, kend)
     const int ntiles = (kend + N - 1) / N;
 
     // ---- setup: barriers and TMEM; the K/V producers start at once, while
@@ -446,9 +395,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(&k_full[i], 1);
-            mbar_init(&k_empty[i], kPair ? 2 : 1);
+            mbar_init(&k_empty[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&v_empty[i], kPair ? 2 : 1);
+            mbar_init(&v_empty[i], 1);
         }
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
@@ -468,7 +417,6 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (kPair) cluster_sync();                     // the peer's barriers exist
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int G = p.group;
@@ -503,12 +451,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
     if (warp == kTcKWarp) {
         // ------------------------------------------------------------ K loads
-        tc_load_ring<D, kPair>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
-                               kend, lane, rank, abort_flag);
+        tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
+                        lane, abort_flag);
     } else if (warp == kTcVWarp) {
         // ------------------------------------------------------------ V loads
-        tc_load_ring<D, kPair>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
-                               kend, lane, rank, abort_flag);
+        tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
+                        lane, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -527,7 +475,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
                     tc_mma(tmem + Sh::kSCol + (j & 1) * N, a, b, idS, kk > 0);
                 }
-                release_slot<kPair>(&k_empty[st]);
+                tc_commit(&k_empty[st]);
                 tc_commit(&s_full[j & 1]);
                 return true;
             };
@@ -548,7 +496,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
                     tc_mma_ts(tmem + Sh::kOCol, pt + N / 2 + kk * 8, b, idO, true);
                 }
-                release_slot<kPair>(&v_empty[st]);
+                tc_commit(&v_empty[st]);
                 tc_commit(pv_done);
                 return true;
             };
@@ -728,12 +676,389 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
     }
 
-    // ---- teardown: all TMEM traffic has completed; a pair also waits for
-    // its peer, whose copies and commits target this CTA's shared memory
+    // ---- teardown: all TMEM traffic has completed
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if constexpr (kPair) cluster_sync();
+    if (warp == kTcMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tmem), "r"(Sh::kTmemCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- two query tiles per CTA
+
+// Shapes of the two-tile kernel (head size 64 or 128): two 128-row query
+// tiles share every K/V tile, so each loaded tile feeds twice the rows.
+template <int D>
+struct TcShape2 {
+    static constexpr int N = 128;                            // keys per tile
+    static constexpr int kSpans = D / 64;
+    static constexpr int kQBytes = kTcRows * D * 2;          // one query tile
+    static constexpr int kKvBytes = N * D * 2;
+    static constexpr int kFixed = 2 * kQBytes + 1024 + 256;  // Q0, Q1, slack, barriers
+    static constexpr int kStages0 = (kTcSmemLimit - kFixed) / (2 * kKvBytes);
+    static constexpr int NS = kStages0 > 4 ? 4 : kStages0;
+    static constexpr int kQOff = 0;                          // Q0, then Q1
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + NS * kKvBytes;
+    static constexpr int kBarOff = kVOff + NS * kKvBytes;
+    // k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full[2] drain q_ready
+    static constexpr int kNumBars = 4 * NS + 6;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    // TMEM: per query tile t, S_t (N columns; S as f32, then P_hi | P_lo)
+    // and O_t (D columns)
+    static constexpr int kTmemCols = 512;
+    static constexpr int kTileCols = N + D;
+    static_assert(D == 64 || D == 128, "head size");
+    static_assert(NS >= 2, "stages");
+    static_assert(2 * kTileCols <= kTmemCols, "TMEM columns");
+    static_assert(kAlloc <= kTcSmemLimit, "shared memory");
+    static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
+};
+
+// Two query tiles per CTA: warps 0-3 run the softmax of tile 0, warps 4-7 of
+// tile 1, each thread a whole row of 128 keys. The MMA issuer interleaves the
+// tiles -- S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... -- so one tile's
+// softmax runs while the tensor cores work for the other. S_t_{j+1} is issued
+// after PV_t_j, so a softmax that sees S_t_j also sees O_t final for the
+// earlier key tiles and can rescale it at once. A K slot is freed after the
+// second tile's S, a V slot after its P.V. Without a second tile (the last
+// group of a sequence with an odd tile count) warps 4-7 idle and the tile-1
+// MMAs are skipped.
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
+    using Sh = TcShape2<D>;
+    constexpr int N = Sh::N;
+    constexpr int NS = Sh::NS;
+    const PrefillParams& p = tp.p;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::kBarOff);
+    uint64_t* k_full = bars;
+    uint64_t* k_empty = k_full + NS;
+    uint64_t* v_full = k_empty + NS;
+    uint64_t* v_empty = v_full + NS;
+    uint64_t* s_full = v_empty + NS;                         // [2], per query tile
+    uint64_t* p_full = s_full + 2;                           // [2]
+    uint64_t* drain = p_full + 2;
+    uint64_t* q_ready = drain + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // ---- the work unit: query tiles 2g and 2g+1 of (sequence s, KV head hk)
+    const int groups = (p.q_tiles + 1) / 2;
+    const int g = blockIdx.x % groups;
+    const int rest = blockIdx.x / groups;
+    const int hk = rest % p.num_kv_heads;
+    const int s = rest / p.num_kv_heads;
+    const int q0 = p.query_start[s];
+    const int Q = p.query_start[s + 1] - q0;
+    const int L = p.context_lens[s];
+    {
+        int cap = p.max_context_len;
+        const long long tab = (long long)p.max_blocks * p.block_size;
+        if (tab < cap) cap = (int)tab;
+        if (Q < 0 || Q > p.max_queries || L < Q || L > cap) {
+            if (tid == 0 && g == 0 && hk == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_LEN);
+            return;
+        }
+    }
+    const int Tq = p.tokens_per_tile;
+    const int tok0 = 2 * g * Tq;
+    if (tok0 >= Q) return;                                   // no such group
+    const int ntok0 = min(Tq, Q - tok0);
+    const int ntok1 = max(0, min(Tq, Q - tok0 - Tq));
+    const bool two = ntok1 > 0;
+    const int kend = L - Q + tok0 + ntok0 + ntok1;           // keys [0, kend)
+    const int ntiles = (kend + N - 1) / N;
+
+    if (tid == kTcKWarp * 32) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&s_full[t], 1);
+            mbar_init(&p_full[t], kTcRows);
+        }
+        mbar_init(drain, 1);
+        mbar_init(q_ready, kTcSoftmaxThreads);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_map(&tp.k_map);
+        tma_prefetch_map(&tp.v_map);
+    }
+    if (warp == kTcMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tmem_slot)), "r"(Sh::kTmemCols) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int G = p.group;
+    const int qt = tid / kTcRows;                            // softmax threads: query tile
+    if (tid < kTcSoftmaxThreads) {
+        // tile qt's rows (token, head); padding rows are zero
+        const int r = tid & (kTcRows - 1);
+        (void)r;
+        const T* qbase = reinterpret_cast<const T*>(p.query);
+        const int tt0 = tok0 + qt * Tq;
+        const int nt = qt == 0 ? ntok0 : ntok1;
+        constexpr int CPR = D / 8;
+        constexpr int PER = CPR;                             // 128 rows x CPR chunks / 128 threads
+        uint4 v[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = (tid & (kTcRows - 1)) + k * kTcRows;
+            const int rr = idx / CPR, c = idx - rr * CPR;
+            const int i = rr / G, gg = rr - i * G;
+            v[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (i < nt) {
+                const size_t row = (size_t)(q0 + tt0 + i) * p.num_q_heads + (size_t)hk * G + gg;
+                v[k] = __ldg(reinterpret_cast<const uint4*>(qbase + row * D + c * 8));
+            }
+        }
+        uint8_t* qd = sm + Sh::kQOff + qt * Sh::kQBytes;
+#pragma unroll
+        for (int k = 0; k < PER; ++k) {
+            const int idx = (tid & (kTcRows - 1)) + k * kTcRows;
+            const int rr = idx / CPR, c = idx - rr * CPR;
+            *reinterpret_cast<uint4*>(qd + sw128_chunk<kTcRows>(rr, c)) = v[k];
+        }
+        fence_async_smem();
+        mbar_arrive(q_ready);
+    }
+
+    if (warp == kTcKWarp) {
+        tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
+                        lane, abort_flag);
+    } else if (warp == kTcVWarp) {
+        tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
+                        lane, abort_flag);
+    } else if (warp == kTcMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = tc_idesc<T>(kTcRows, N, 0);
+            constexpr uint32_t idO = tc_idesc<T>(kTcRows, D, 1);
+            const int last_t = two ? 1 : 0;
+            auto qk = [&](int t, int j) -> bool {
+                const int st = j % NS;
+                if (t == 0) {
+                    if (!tc_wait(&k_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag))
+                        return false;
+                    tc_fence_after();
+                }
+                const uint32_t qa = smem_u32(sm + Sh::kQOff + t * Sh::kQBytes);
+                const uint32_t ka = smem_u32(sm + Sh::kKOff + st * Sh::kKvBytes);
+                const uint32_t sc = tmem + t * Sh::kTileCols;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (uint32_t)(kk & 3) * 32u;
+                    const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
+                    const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
+                    tc_mma(sc, a, b, idS, kk > 0);
+                }
+                if (t == last_t) tc_commit(&k_empty[st]);
+                tc_commit(&s_full[t]);
+                return true;
+            };
+            auto pv = [&](int t, int j) -> bool {
+                const int st = j % NS;
+                if (!tc_wait(&p_full[t], (uint32_t)(j & 1), p.status, abort_flag)) return false;
+                if (t == 0 &&
+                    !tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kKvBytes);
+                const uint32_t pt = tmem + t * Sh::kTileCols;          // P_hi | P_lo
+                const uint32_t oc = pt + N;
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                    const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
+                    tc_mma_ts(oc, pt + kk * 8, b, idO, j > 0 || kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                    const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
+                    tc_mma_ts(oc, pt + N / 2 + kk * 8, b, idO, true);
+                }
+                if (t == last_t) tc_commit(&v_empty[st]);
+                return true;
+            };
+            bool ok = tc_wait(q_ready, 0u, p.status, abort_flag);
+            tc_fence_after();
+            if (ok) ok = qk(0, 0);
+            if (ok && two) ok = qk(1, 0);
+            for (int j = 0; j < ntiles && ok; ++j) {
+                ok = pv(0, j);
+                if (ok && j + 1 < ntiles) ok = qk(0, j + 1);
+                if (ok && two) {
+                    ok = pv(1, j);
+                    if (ok && j + 1 < ntiles) ok = qk(1, j + 1);
+                }
+            }
+            // everything issued has finished before the epilogue reads O and
+            // before TMEM is freed
+            tc_commit(drain);
+            mbar_wait_bounded(drain, 0, p.status);
+        }
+    } else if (qt == 0 || two) {
+        // ------------------------------------------------------------ softmax (tile qt)
+        const int r = tid & (kTcRows - 1);
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t sbuf = lane_base + qt * Sh::kTileCols;
+        const uint32_t obuf = sbuf + N;
+        const int i = r / G;
+        const int nt = qt == 0 ? ntok0 : ntok1;
+        const bool row_valid = i < nt && r < Tq * G;
+        const int pos = L - Q + tok0 + qt * Tq + (row_valid ? i : nt - 1);
+        const float qm = p.q_mul;
+        const float2 qm2 = make_float2(qm, qm);
+        float m = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            ok = tc_wait(&s_full[qt], (uint32_t)(j & 1), p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t xr[N];
+#pragma unroll
+            for (int c = 0; c < N; c += 32)
+                tc_ld32(sbuf + c, *reinterpret_cast<uint32_t(*)[32]>(xr + c));
+            tc_wait_ld();
+            float x[N];
+#pragma unroll
+            for (int c = 0; c < N; ++c) x[c] = __uint_as_float(xr[c]);
+            const int key0 = j * N;
+            if (key0 + N - 1 > pos) {
+#pragma unroll
+                for (int c = 0; c < N; ++c)
+                    if (key0 + c > pos) x[c] = -INFINITY;
+            }
+            constexpr int R = 8;
+            float mr[R];
+#pragma unroll
+            for (int k = 0; k < R; ++k) mr[k] = x[k];
+#pragma unroll
+            for (int c = R; c < N; ++c) mr[c % R] = fmaxf(mr[c % R], x[c]);
+#pragma unroll
+            for (int w = R / 2; w >= 1; w /= 2)
+#pragma unroll
+                for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
+            const float m_cand = fmaxf(m, mr[0] * qm);
+            const bool rescale = m_cand > m + kTcRescaleLog2;
+            const float m_use = rescale ? m_cand : m;
+            const float alpha = fast_exp2(m - m_use);
+            const float2 nm2 = make_float2(-m_use, -m_use);
+            float2 sr[R / 2];
+#pragma unroll
+            for (int k = 0; k < R / 2; ++k) sr[k] = make_float2(0.f, 0.f);
+            // weights in two halves of 64 keys: each half's P_hi and P_lo go
+            // to TMEM before the next is formed (S is all in registers already)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t phi[N / 4], plo[N / 4];
+#pragma unroll
+                for (int c = 0; c < N / 2; c += 2) {
+                    const int cc = h * (N / 2) + c;
+                    const float2 t2 = __ffma2_rn(make_float2(x[cc], x[cc + 1]), qm2, nm2);
+                    const float2 e = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
+                    sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
+                    phi[c / 2] = pack2<T>(e.x, e.y);
+                    const float2 lo = __ffma2_rn(unpack2<T>(phi[c / 2]), make_float2(-1.f, -1.f), e);
+                    plo[c / 2] = pack2<T>(lo.x, lo.y);
+                }
+                tc_st_n<N / 4>(sbuf + h * (N / 4), phi);
+                tc_st_n<N / 4>(sbuf + N / 2 + h * (N / 4), plo);
+            }
+#pragma unroll
+            for (int w = R / 4; w >= 1; w /= 2)
+#pragma unroll
+                for (int k = 0; k < w; ++k) sr[k] = __fadd2_rn(sr[k], sr[k + w]);
+            l = fmaf(l, alpha, sr[0].x + sr[0].y);
+            m = m_use;
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // O_t already holds key tiles < j (S_t_j came after PV_t_{j-1})
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t o[32];
+                    tc_ld32(obuf + c, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tc_st32(obuf + c, o);
+                }
+            }
+            tc_wait_st();
+            if (qt == 0 && key0 + N > kend) {
+                // last tile: V rows at or past kend hold stale data or cache
+                // poison; zero them before either tile's P.V reads the slot
+                const int st = j % NS;
+                ok = tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const int first = kend - key0;
+                constexpr int CPR = D / 8;
+                uint8_t* vd = sm + Sh::kVOff + st * Sh::kKvBytes;
+                for (int idx = r; idx < (N - first) * CPR; idx += kTcRows) {
+                    const int rr = first + idx / CPR, c = idx % CPR;
+                    *reinterpret_cast<uint4*>(vd + sw128_chunk<N>(rr, c)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_async_smem();
+            }
+            tc_fence_before();
+            mbar_arrive(&p_full[qt]);
+        }
+        if (ok) {
+            ok = tc_wait(drain, 0u, p.status, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            T* orow = reinterpret_cast<T*>(p.out) +
+                      ((size_t)(q0 + tok0 + qt * Tq + (row_valid ? i : 0)) * p.num_q_heads +
+                       (size_t)hk * G + (r - i * G)) * D;
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                uint32_t o[32];
+                tc_ld32(obuf + c, o);
+                tc_wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 8) {
+                        uint4 v;
+                        v.x = pack2<T>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        *reinterpret_cast<uint4*>(orow + c + e) = v;
+                    }
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
     if (warp == kTcMmaWarp) {
         __syncwarp();
         tc_fence_after();
@@ -746,31 +1071,30 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
 template <typename T, int D>
 cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) {
-    using Sh = TcShape<D>;
     const PrefillParams& p = tp.p;
-    // query tiles pair up in 2-CTA clusters whenever a sequence can have two
-    const bool pair = p.q_tiles >= 2;
-    const long long groups = (long long)p.num_seqs * p.num_kv_heads *
-                             (pair ? (p.q_tiles + 1) / 2 : p.q_tiles);
-    if (groups <= 0) return cudaSuccess;
-    const long long ctas = groups * (pair ? 2 : 1);
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;
-    auto kern = pair ? paged_prefill_tc_kernel<T, D, true> : paged_prefill_tc_kernel<T, D, false>;
+    // two query tiles per CTA when sequences have at least two (head size
+    // <= 128); otherwise one tile with double-buffered scores
+    if constexpr (D <= 128) {
+        if (p.q_tiles >= 2) {
+            using Sh = TcShape2<D>;
+            auto kern = paged_prefill_tc2_kernel<T, D>;
+            cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
+            if (e != cudaSuccess) return e;
+            const long long units = (long long)p.num_seqs * p.num_kv_heads * ((p.q_tiles + 1) / 2);
+            if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+            kern<<<(unsigned)units, kTcThreads, Sh::kAlloc, stream>>>(tp);
+            return cudaGetLastError();
+        }
+    }
+    using Sh = TcShape<D>;
+    auto kern = paged_prefill_tc_kernel<T, D>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)ctas);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = Sh::kAlloc;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = pair ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, tp);
+    const long long units = (long long)p.num_seqs * p.num_kv_heads * p.q_tiles;
+    if (units <= 0) return cudaSuccess;
+    if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+    kern<<<(unsigned)units, kTcThreads, Sh::kAlloc, stream>>>(tp);
+    return cudaGetLastError();
 }
 
 template <typename T>
