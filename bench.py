@@ -491,7 +491,9 @@ def run_prefill(args):
                      {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                       "frac": round(gbs / peak_hbm, 4), "traffic": None,
                       "peak_kind": f"{hk} HBM copy"}),
-        "kernel": "paged_prefill_tc_kernel",
+        "kernel": ("paged_prefill_tc2_kernel (two query tiles per CTA)"
+                   if case.head_size <= 128 and q.max_queries > 128 // case.group
+                   else "paged_prefill_tc_kernel"),
         "gpu_launches": K,
         "clocks": clocks,
     }
