@@ -218,7 +218,9 @@ class Step:
 
     def _calls(self):
         pk, c = self.pk, self.case
-        common = (self.bt, self.cl, c.max_context_len, c.scale)
+
+        def common():          # read at call time: the end-to-end loop swaps buffers
+            return (self.bt, self.cl, c.max_context_len, c.scale)
 
         def write(stream=None):
             pk.reshape_and_cache(self.nk, self.nv, self.kc, self.vc, self.ns, c.k_scale,
@@ -226,19 +228,19 @@ class Step:
 
         def write_decode(stream=None):
             pk.write_decode(self.out, self.q, self.nk, self.nv, self.kc, self.vc, self.ns,
-                            *common, c.k_scale, c.v_scale, self.status, stream)
+                            *common(), c.k_scale, c.v_scale, self.status, stream)
 
         def write_partitions(stream=None):
             pk.write_decode_partitions(self.q, self.nk, self.nv, self.kc, self.vc, self.ns,
-                                       *common, self.ws, self.P, c.k_scale, c.v_scale,
+                                       *common(), self.ws, self.P, c.k_scale, c.v_scale,
                                        self.status, stream)
 
         def decode(stream=None):
-            pk.decode(self.out, self.q, self.kc, self.vc, *common, c.k_scale, c.v_scale,
+            pk.decode(self.out, self.q, self.kc, self.vc, *common(), c.k_scale, c.v_scale,
                       self.status, stream)
 
         def partitions(stream=None):
-            pk.decode_partitions(self.q, self.kc, self.vc, *common, self.ws, self.P, c.k_scale,
+            pk.decode_partitions(self.q, self.kc, self.vc, *common(), self.ws, self.P, c.k_scale,
                                  c.v_scale, self.status, stream)
 
         def merge(stream=None):
@@ -501,40 +503,72 @@ def run_prefill(args):
 
 
 def run_e2e(st: Step, steps: int, device):
-    """The same step through the public API with host buffers: each step
+    """The same step through the public API with host buffers: every step
     copies its inputs from pinned host memory, runs the write and the decode,
-    and reads the output back."""
+    and reads its output back, as a serving loop would -- pipelined: two sets
+    of device inputs/outputs alternate, host-to-device copies run on one
+    stream, the step on the compute stream and the device-to-host read on a
+    third, so step i+1's inputs arrive and step i-1's output leaves while step
+    i computes (events order every reuse of a buffer)."""
     import torch
-    c = st.case
+    names = ("q", "bt", "cl", "nk", "nv", "ns")
     host = {}
-    for name in ("q", "bt", "cl", "nk", "nv", "ns"):
+    for name in names:
         tdev = getattr(st, name)
         host[name] = torch.empty(tdev.shape, dtype=tdev.dtype, pin_memory=True)
         host[name].copy_(tdev.cpu())
-    out_host = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    dev_in = [{n: getattr(st, n) for n in names}, {n: torch.empty_like(getattr(st, n)) for n in names}]
+    dev_out = [st.out, torch.empty_like(st.out)]
+    host_out = [torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_host.numel() * out_host.element_size()
-    stream = torch.cuda.current_stream(device)
-    for _ in range(3):
-        for name, h in host.items():
-            getattr(st, name).copy_(h, non_blocking=True)
-        st.step()
-        out_host.copy_(st.out, non_blocking=True)
+    d2h = host_out[0].numel() * host_out[0].element_size()
+    comp = torch.cuda.current_stream(device)
+    s_in = torch.cuda.Stream(device)
+    s_out = torch.cuda.Stream(device)
+    ev = lambda: [torch.cuda.Event() for _ in range(2)]
+    in_ready, done, out_read = ev(), ev(), ev()
+    saved = {n: getattr(st, n) for n in names + ("out",)}
+
+    def run(count):
+        for i in range(count):
+            k = i % 2
+            if i >= 2:
+                s_in.wait_event(done[k])                 # step i-2 has used buffer k
+            with torch.cuda.stream(s_in):
+                for n in names:
+                    dev_in[k][n].copy_(host[n], non_blocking=True)
+            in_ready[k].record(s_in)
+            comp.wait_event(in_ready[k])
+            if i >= 2:
+                comp.wait_event(out_read[k])             # step i-2's output has left
+            for n in names:
+                setattr(st, n, dev_in[k][n])
+            st.out = dev_out[k]
+            st.step(comp)
+            done[k].record(comp)
+            s_out.wait_event(done[k])
+            with torch.cuda.stream(s_out):
+                host_out[k].copy_(dev_out[k], non_blocking=True)
+            out_read[k].record(s_out)
+
+    run(4)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        for name, h in host.items():
-            getattr(st, name).copy_(h, non_blocking=True)
-        st.step()
-        out_host.copy_(st.out, non_blocking=True)
-    b.record(stream)
+    a.record(s_in)
+    comp.wait_event(a)
+    run(steps)
+    s_out.wait_event(done[(steps - 1) % 2])
+    b.record(s_out)
     torch.cuda.synchronize()
+    for n, t in saved.items():
+        setattr(st, n, t)
     ms = a.elapsed_time(b) / steps
     by = st.bytes_per_step()["total"]
     return {"value": round(by / (ms * 1e-3) / 1e9, 2), "unit": UNIT, "ms_per_step": round(ms, 5),
-            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "pipelined": "inputs of step i+1 copied in and output of step i-1 copied out "
+                         "while step i runs (two buffer sets, three streams)"}
 
 
 def cpu_baseline(case, partition_size, budget_s=12.0):
