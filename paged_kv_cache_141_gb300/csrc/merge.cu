@@ -12,8 +12,10 @@ namespace pagedkv {
 
 constexpr int kMergeWarps = 8;
 
+// Four CTAs (32 warps) per SM at least: the merge is a latency-bound pass
+// over L2-resident partials, so occupancy is what hides its loads.
 template <int D, typename OT>
-__global__ void __launch_bounds__(kMergeWarps * 32)
+__global__ void __launch_bounds__(kMergeWarps * 32, 4)
 paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
                    const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
                    const int32_t* __restrict__ context_lens, int num_seqs, int num_q_heads,
