@@ -218,6 +218,13 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// max(a, b, c) in one instruction (three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // Two floats to a packed pair of 16-bit values (low half = first), RNE.
 template <typename T> __device__ __forceinline__ uint32_t pack2(float a, float b);
 template <> __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
@@ -563,7 +570,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
             for (int k = 0; k < R; ++k) mr[k] = x[k];
 #pragma unroll
-            for (int c = R; c < N; ++c) mr[c % R] = fmaxf(mr[c % R], x[c]);
+            for (int c = R; c + 1 < N; c += 2) mr[(c / 2) % R] = fmax3(mr[(c / 2) % R], x[c], x[c + 1]);
 #pragma unroll
             for (int w = R / 2; w >= 1; w /= 2)
 #pragma unroll
@@ -956,7 +963,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
             for (int k = 0; k < R; ++k) mr[k] = x[k];
 #pragma unroll
-            for (int c = R; c < N; ++c) mr[c % R] = fmaxf(mr[c % R], x[c]);
+            for (int c = R; c + 1 < N; c += 2) mr[(c / 2) % R] = fmax3(mr[(c / 2) % R], x[c], x[c + 1]);
 #pragma unroll
             for (int w = R / 2; w >= 1; w /= 2)
 #pragma unroll
