@@ -91,7 +91,12 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 template <typename CT, int D>
 struct MmaSmem {
     using S = TmaShape<CT, D>;
-    static constexpr int kNst0 = S::kNst / kTmaConsumerWarps * kTmaConsumerWarps;
+    // E4M3 stages are half the bytes: four stages (one per consumer warp)
+    // keep the ring at 32 KB, so that the register file, not shared memory,
+    // limits the CTAs per SM (4 instead of 3) for these latency-bound tiles
+    static constexpr int kNstCap = std::is_same<CT, e4m3_t>::value ? kTmaConsumerWarps : 1 << 30;
+    static constexpr int kNstT = S::kNst < kNstCap ? S::kNst : kNstCap;
+    static constexpr int kNst0 = kNstT / kTmaConsumerWarps * kTmaConsumerWarps;
     static constexpr int kNst = kNst0 < kTmaConsumerWarps ? kTmaConsumerWarps : kNst0;
     static constexpr int kRingBytes = kNst * S::kStageBytes;
     static constexpr int kCombineBytes = kTmaConsumerWarps * 8 * (D + 2) * 4;
@@ -113,7 +118,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
 }
 
 template <typename QT, typename CT, int D, int GS, bool kSplit>
-__global__ void __launch_bounds__(kTmaThreads)
+__global__ void __launch_bounds__(kTmaThreads, (std::is_same<CT, e4m3_t>::value && D <= 128) ? 5 : 1)
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
     using Smem = MmaSmem<CT, D>;
