@@ -117,8 +117,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// CTAs per SM the registers must allow: 4 at head size <= 128 (shared memory
+// allows 3 for 16-bit caches), 5 for E4M3 caches whose 32 KB ring allows more;
+// 2 at head size 256.
+template <typename CT, int D>
+constexpr int mma_min_blocks() {
+    return D <= 128 ? (std::is_same<CT, e4m3_t>::value ? 5 : 4) : 2;
+}
+
 template <typename QT, typename CT, int D, int GS, bool kSplit>
-__global__ void __launch_bounds__(kTmaThreads, (std::is_same<CT, e4m3_t>::value && D <= 128) ? 5 : 1)
+__global__ void __launch_bounds__(kTmaThreads, mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
     using Smem = MmaSmem<CT, D>;
