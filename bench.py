@@ -128,7 +128,7 @@ class ClockSampler:
 
 def decode_kernel_label(case) -> str:
     """Which decode kernel the library runs for this workload (its dispatch
-    rule: 16-bit query, cache of that type or E4M3, even group -> tensor-core
+    rule: 16-bit query, cache of that type or E4M3, even group or none -> tensor-core
     kernel; other rows of 128/256/512 bytes with block size 8, 16 or a multiple
     of 32 -> tensor-TMA CUDA-core kernel; anything else -> bulk-copy kernel)."""
     eb = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[case.cache_dtype]
@@ -136,7 +136,7 @@ def decode_kernel_label(case) -> str:
     B = case.block_size
     tma = row in (128, 256, 512) and (B in (8, 16) or (B >= 32 and B % 32 == 0))
     if tma and case.q_dtype in ("f16", "bf16") and case.cache_dtype in (case.q_dtype, "e4m3") \
-            and case.group % 2 == 0:
+            and (case.group % 2 == 0 or case.group == 1):
         return "paged_decode_mma_kernel"
     return "paged_decode_tma_kernel" if tma else "paged_decode_simt_kernel"
 

@@ -48,15 +48,15 @@ int heads_per_unit(int group, int head_size, bool tma) {
 }
 
 // The tensor-core decode: a 16-bit query with a cache of the same type or of
-// E4M3 codes, and an even group (the MMA tile holds 8 heads; odd groups stay
-// on the CUDA cores).
+// E4M3 codes, and an even group or none (multi-head attention, one head per
+// unit in the MMA tile's 8 columns); other odd groups stay on the CUDA cores.
 bool mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int group) {
-    if (group % 2 != 0 || !(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
+    if ((group % 2 != 0 && group != 1) || !(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
     return cache_dtype == q_dtype || cache_dtype == PA_FP8_E4M3;
 }
 
 int mma_heads_per_unit(int group) {
-    return group % 8 == 0 ? 8 : (group % 4 == 0 ? 4 : 2);
+    return group % 8 == 0 ? 8 : (group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

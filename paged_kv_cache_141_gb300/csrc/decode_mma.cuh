@@ -526,6 +526,7 @@ cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStre
         return split ? launch_mma_variant<QT, CT, D, G, true>(tp, stream)     \
                      : launch_mma_variant<QT, CT, D, G, false>(tp, stream);
     switch (gs) {
+        PA_MMA_CASE(1)
         PA_MMA_CASE(2)
         PA_MMA_CASE(4)
         PA_MMA_CASE(8)
@@ -535,7 +536,7 @@ cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStre
 }
 
 // Query type QT (16-bit); cache CT of the same type, or E4M3 codes; rows of
-// 128, 256 or 512 bytes; heads_per_unit 2, 4 or 8.
+// 128, 256 or 512 bytes; heads_per_unit 1, 2, 4 or 8.
 template <typename QT, typename CT>
 cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
                        cudaStream_t stream) {

@@ -77,7 +77,7 @@ cudaError_t launch_decode_tma_bf16_e4m3(const DecodeParams& p, int head_size, in
                                         bool split, cudaStream_t stream);
 
 // Tensor-core decode for 16-bit caches (query type = cache type), TMA-eligible
-// shapes, heads_per_unit in {2, 4, 8}.
+// shapes, heads_per_unit in {1, 2, 4, 8}.
 cudaError_t launch_decode_mma_f16(const DecodeParams& p, int head_size, int heads_per_unit,
                                   bool split, cudaStream_t stream);
 cudaError_t launch_decode_mma_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
