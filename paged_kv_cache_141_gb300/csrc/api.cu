@@ -214,15 +214,19 @@ void bind_fused_write(DecodeParams& p, const void* key, const void* value,
     p.v_scale_w = v_scale;
 }
 
-// The tcgen05 multi-query kernel: 16-bit query and cache of one type, whole
-// 128-byte column spans, block sizes that are powers of two in [8, 256] (every
+// The tcgen05 multi-query kernel: 16-bit query and a cache of the same type
+// or of E4M3 codes (head size 64 or 128), whole 128-byte column spans, block sizes that are powers of two in [8, 256] (every
 // TMA box then starts on a swizzle-atom boundary), groups that fit the
 // 128-row tile, 16-byte-aligned rows, row coordinates below 2^31.
 bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, int block_size,
                          int group, int64_t num_blocks, int num_kv_heads, const void* out,
                          const void* query, const void* k_cache, const void* v_cache) {
-    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16) || cache_dtype != q_dtype) return false;
-    if (!supported_head_size(head_size)) return false;
+    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
+    if (cache_dtype == PA_FP8_E4M3) {
+        if (head_size != 64 && head_size != 128) return false;      // E4M3 staging fits
+    } else if (cache_dtype != q_dtype || !supported_head_size(head_size)) {
+        return false;
+    }
     if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0) return false;
     if (group < 1 || group > 128) return false;
     const uintptr_t a = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(query) |
@@ -533,7 +537,12 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
         pp.max_queries = max_queries_per_seq;
         pp.tokens_per_tile = 128 / p.group;
         pp.q_tiles = (max_queries_per_seq + pp.tokens_per_tile - 1) / pp.tokens_per_tile;
-        pp.q_mul = scale * 1.4426950408889634f;
+        const bool fp8 = cache_dtype == PA_FP8_E4M3;
+        pp.q_mul = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
+        pp.v_mul = fp8 ? v_scale : 1.f;
+        if (fp8)
+            return from_cuda(q_dtype == PA_F16 ? launch_prefill_tc_f16_e4m3(pp, head_size, s)
+                                               : launch_prefill_tc_bf16_e4m3(pp, head_size, s));
         return from_cuda(q_dtype == PA_F16 ? launch_prefill_tc_f16(pp, head_size, s)
                                            : launch_prefill_tc_bf16(pp, head_size, s));
     }

@@ -89,8 +89,8 @@ cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, in
                                         bool split, cudaStream_t stream);
 
 // Multi-query paged attention on the tensor cores (tcgen05): 16-bit query and
-// cache of the same type, head_size in {64, 128, 256}, block size a power of
-// two in [8, 256], group <= 128.
+// cache of the same type (head_size in {64, 128, 256}) or E4M3 (64, 128),
+// block size a power of two in [8, 256], group <= 128.
 struct PrefillParams {
     void* out;                    // [T, Hq, D], query type
     const void* query;            // [T, Hq, D]
@@ -111,11 +111,15 @@ struct PrefillParams {
     int max_queries;              // max over s of Q_s (sizes the grid)
     int tokens_per_tile;          // floor(128 / G)
     int q_tiles;                  // ceil(max_queries / tokens_per_tile)
-    float q_mul;                  // scale * log2(e)
+    float q_mul;                  // scale * log2(e) * (E4M3 cache ? k_scale : 1)
+    float v_mul;                  // E4M3 cache ? v_scale : 1
 };
 
 cudaError_t launch_prefill_tc_f16(const PrefillParams& p, int head_size, cudaStream_t stream);
 cudaError_t launch_prefill_tc_bf16(const PrefillParams& p, int head_size, cudaStream_t stream);
+// E4M3 caches with a 16-bit query, head_size 64 or 128 (MMAs in binary16).
+cudaError_t launch_prefill_tc_f16_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_tc_bf16_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream);
 
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,

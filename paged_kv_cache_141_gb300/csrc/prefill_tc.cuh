@@ -67,21 +67,28 @@ constexpr int kTcVWarp = 10;
 constexpr float kTcRescaleLog2 = 8.0f;        // lazy rescale threshold (base 2)
 constexpr int kTcSmemLimit = 227 * 1024;
 
-template <int D>
+// kFp8: E4M3 caches. Their tiles land row-major (D bytes per key) in two
+// staging slots per K and V, and the producer warp widens them to binary16
+// in the 16-bit rings the MMAs read.
+template <int D, bool kFp8 = false>
 struct TcShape {
     static constexpr int N = D == 256 ? 64 : 128;            // keys per tile
     static constexpr int kSpans = D / 64;                    // 128-byte column spans per row
     static constexpr int kQBytes = kTcRows * D * 2;
     static constexpr int kKvBytes = N * D * 2;               // one stage of K (or V)
-    static constexpr int kFixed = kQBytes + 1024 + 256 + 1024;  // Q, slack, barriers, sums
+    static constexpr int kStage8Bytes = kFp8 ? N * D : 0;    // one E4M3 staging slot
+    static constexpr int kFixed = kQBytes + 1024 + 256 + 1024 + 4 * kStage8Bytes;
     static constexpr int kStages0 = (kTcSmemLimit - kFixed) / (2 * kKvBytes);
     static constexpr int NS = kStages0 > 4 ? 4 : kStages0;   // K stages = V stages
     static constexpr int kQOff = 0;
     static constexpr int kKOff = kQOff + kQBytes;
     static constexpr int kVOff = kKOff + NS * kKvBytes;
-    static constexpr int kBarOff = kVOff + NS * kKvBytes;
-    // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain q_ready
-    static constexpr int kNumBars = 4 * NS + 6;
+    static constexpr int kK8Off = kVOff + NS * kKvBytes;     // E4M3 staging: K[2], V[2]
+    static constexpr int kV8Off = kK8Off + 2 * kStage8Bytes;
+    static constexpr int kBarOff = kV8Off + 2 * kStage8Bytes;
+    // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
+    // q_ready, then (E4M3) k_staged[2] v_staged[2]
+    static constexpr int kNumBars = 4 * NS + 6 + (kFp8 ? 4 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
     static constexpr int kBytes = kLsumOff + kTcSoftmaxThreads * 4;
@@ -97,7 +104,13 @@ struct TcShape {
     static_assert(2 * N + D <= kTmemCols, "TMEM columns");
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
+    static_assert(!kFp8 || D <= 128, "E4M3 staging fits at head size <= 128");
 };
+
+// The MMAs' operand type: the query's for 16-bit caches; binary16 for E4M3
+// caches (every E4M3 value is exact in it; the query is rounded to it).
+template <typename QT, typename CT> struct TcMath { using T = QT; };
+template <typename QT> struct TcMath<QT, e4m3_t> { using T = __half; };
 
 struct TcPrefillParams {
     PrefillParams p;
@@ -216,6 +229,12 @@ __device__ __forceinline__ void tc_wait_st() {
 
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Two E4M3 codes (low 16 bits) -> two binary16 values, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_bits_to_f16x2(uint32_t w) {
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
 // max(a, b, c) in one instruction (three-input max.f32).
@@ -345,10 +364,105 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
 }
 
-template <typename T, int D>
+// E4M3 K (or V) tiles, by a whole warp: each tile lands row-major in one of
+// two staging slots (one plain TMA box per block segment), then the warp
+// widens it to binary16 into the ring slot the MMAs read -- 16 codes per
+// lane and step, the 128-byte swizzled K-major layout -- orders its writes
+// for the tensor cores (fence.proxy.async) and arrives on the slot's `full`
+// barrier. A slot is refilled once `empty` says its MMAs are done; staging
+// slot j % 2 is reloaded (tile j + 2) as soon as tile j is widened, with
+// that tile's block-table entries read one tile earlier.
+template <typename Sh>
+__device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const CUtensorMap* map,
+                                              uint8_t* staging, uint8_t* ring, uint64_t* staged,
+                                              uint64_t* full, uint64_t* empty, int s, int hk,
+                                              int ntiles, int kend, int lane,
+                                              volatile int* abort_flag) {
+    constexpr int N = Sh::N;
+    constexpr int NS = Sh::NS;
+    constexpr int D = Sh::kKvBytes / (2 * N);                // head size
+    constexpr int kRow8 = D;                                 // bytes of an E4M3 row
+    constexpr int kChunks = N * kRow8 / 16;                  // 16-code chunks per tile
+    constexpr int64_t kNone = -1;
+    const PrefillParams& p = tp.p;
+    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+    const int rows = tp.box_rows;
+    const int B = p.block_size;
+    const int r0 = lane * rows;
+    auto fetch = [&](int j) -> int64_t {
+        const int key = j * N + r0;
+        if (j < ntiles && r0 < N && key < kend) return (int64_t)table[key / B];
+        return kNone;
+    };
+    auto issue = [&](int j, int64_t blk) {
+        const bool has = blk != kNone;
+        const bool valid = has && blk >= 0 && blk < p.num_blocks;
+        if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
+        if (lane == 0) mbar_arrive_expect_tx(&staged[j & 1], boxes * (uint32_t)rows * kRow8);
+        __syncwarp();
+        if (valid) {
+            const int key = j * N + r0;
+            const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
+            tma_load_2d(staging + (j & 1) * Sh::kStage8Bytes + r0 * kRow8, map, 0, y, &staged[j & 1]);
+        }
+    };
+    issue(0, fetch(0));
+    int64_t next = fetch(1);
+    if (ntiles > 1) issue(1, next);
+    next = fetch(2);
+    int issued = ntiles > 1 ? 2 : 1;
+    bool live = true;
+    for (int j = 0; j < ntiles && live; ++j) {
+        const int64_t after = fetch(j + 3);                  // in flight while tile j is widened
+        bool ok = true;
+        if (lane == 0) {
+            ok = tc_wait(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
+            if (ok && j >= NS)
+                ok = tc_wait(&empty[j % NS], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            live = false;
+            break;
+        }
+        const uint8_t* src = staging + (j & 1) * Sh::kStage8Bytes;
+        uint8_t* dst = ring + (j % NS) * Sh::kKvBytes;
+#pragma unroll 4
+        for (int k = 0; k < kChunks / 32; ++k) {
+            const int q = lane + 32 * k;
+            const int r = q / (kRow8 / 16), c = q - r * (kRow8 / 16);
+            const uint4 w = *reinterpret_cast<const uint4*>(src + r * kRow8 + c * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_bits_to_f16x2(ws[e] & 0xffffu);
+                h[2 * e + 1] = e4m3x2_bits_to_f16x2(ws[e] >> 16);
+            }
+            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[j % NS]);
+        if (j + 2 < ntiles) {
+            issue(j + 2, next);                              // staging slot j % 2 is free again
+            issued = j + 3;
+        }
+        next = after;
+    }
+    // copies still in flight (only after an abort) land before the CTA ends
+    if (lane == 0)
+        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+            mbar_wait_bounded(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
+}
+
+template <typename QT, typename CT, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
-    using Sh = TcShape<D>;
+    using MT = typename TcMath<QT, CT>::T;                  // MMA operand type
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    using Sh = TcShape<D, kFp8>;
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
     const PrefillParams& p = tp.p;
@@ -365,6 +479,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* pv_done = p_full + 1;
     uint64_t* drain = pv_done + 1;
     uint64_t* q_ready = drain + 1;
+    uint64_t* k_staged = q_ready + 1;                        // E4M3: [2]
+    uint64_t* v_staged = k_staged + 2;                       // E4M3: [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -412,6 +528,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
+        if constexpr (kFp8) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(&k_staged[i], 1);
+                mbar_init(&v_staged[i], 1);
+            }
+        }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_map(&tp.k_map);
@@ -430,7 +552,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     if (tid < kTcSoftmaxThreads) {
         // rows (token, head) of the tile; padding rows are zero. All of a
         // thread's loads are in flight before the first store.
-        const T* qbase = reinterpret_cast<const T*>(p.query);
+        const QT* qbase = reinterpret_cast<const QT*>(p.query);
         constexpr int CPR = D / 8;                           // 16-byte chunks per row
         constexpr int PER = kTcRows * CPR / kTcSoftmaxThreads;  // chunks per thread
         uint4 v[PER];
@@ -449,7 +571,19 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         for (int k = 0; k < PER; ++k) {
             const int idx = tid + k * kTcSoftmaxThreads;
             const int r = idx / CPR, c = idx - r * CPR;
-            *reinterpret_cast<uint4*>(sm + Sh::kQOff + sw128_chunk<kTcRows>(r, c)) = v[k];
+            uint4 w = v[k];
+            if constexpr (!std::is_same<QT, MT>::value) {
+                // E4M3 caches: the query in the MMAs' binary16
+                const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack2<QT>(in[e]);
+                    o4[e] = pack2<MT>(f.x, f.y);
+                }
+                w = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+            *reinterpret_cast<uint4*>(sm + Sh::kQOff + sw128_chunk<kTcRows>(r, c)) = w;
         }
         fence_async_smem();
         mbar_arrive(q_ready);
@@ -458,17 +592,25 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
     if (warp == kTcKWarp) {
         // ------------------------------------------------------------ K loads
-        tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                        lane, abort_flag);
+        if constexpr (kFp8)
+            tc_load_widen<Sh>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_full,
+                              k_empty, s, hk, ntiles, kend, lane, abort_flag);
+        else
+            tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
+                             lane, abort_flag);
     } else if (warp == kTcVWarp) {
         // ------------------------------------------------------------ V loads
-        tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                        lane, abort_flag);
+        if constexpr (kFp8)
+            tc_load_widen<Sh>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_full,
+                              v_empty, s, hk, ntiles, kend, lane, abort_flag);
+        else
+            tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
+                             lane, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = tc_idesc<T>(kTcRows, N, 0);
-            constexpr uint32_t idO = tc_idesc<T>(kTcRows, D, 1);
+            constexpr uint32_t idS = tc_idesc<MT>(kTcRows, N, 0);
+            constexpr uint32_t idO = tc_idesc<MT>(kTcRows, D, 1);
             const uint32_t qa = smem_u32(sm + Sh::kQOff);
             auto qk = [&](int j) -> bool {
                 const int st = j % NS;
@@ -592,9 +734,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const float2 t = __ffma2_rn(make_float2(x[c0 + c], x[c0 + c + 1]), qm2, nm2);
                     const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
                     sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
-                    phi[c / 2] = pack2<T>(e.x, e.y);
-                    const float2 lo = __ffma2_rn(unpack2<T>(phi[c / 2]), make_float2(-1.f, -1.f), e);
-                    plo[c / 2] = pack2<T>(lo.x, lo.y);
+                    phi[c / 2] = pack2<MT>(e.x, e.y);
+                    const float2 lo = __ffma2_rn(unpack2<MT>(phi[c / 2]), make_float2(-1.f, -1.f), e);
+                    plo[c / 2] = pack2<MT>(lo.x, lo.y);
                 }
             };
             if (hf == 0) weights(std::integral_constant<int, 0>{});
@@ -653,14 +795,15 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         float* lsum = reinterpret_cast<float*>(sm + Sh::kLsumOff);
         lsum[tid] = l;
         named_barrier(1, kTcSoftmaxThreads);
-        const float inv = 1.f / (lsum[r] + lsum[r + kTcRows]);
+        // E4M3: the values were widened without their scale; it comes in here
+        const float inv = p.v_mul / (lsum[r] + lsum[r + kTcRows]);
         if (ok) {
             ok = tc_wait(drain, 0u, p.status, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok) {
             tc_fence_after();
-            T* orow = reinterpret_cast<T*>(p.out) +
+            QT* orow = reinterpret_cast<QT*>(p.out) +
                       ((size_t)(q0 + tok0 + (row_valid ? i : 0)) * p.num_q_heads + (size_t)hk * G +
                        (r - i * G)) * D + hf * (D / 2);
 #pragma unroll 1
@@ -672,10 +815,10 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 v;
-                        v.x = pack2<T>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        v.x = pack2<QT>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack2<QT>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack2<QT>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack2<QT>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
                         *reinterpret_cast<uint4*>(orow + c + e) = v;
                     }
                 }
@@ -1076,6 +1219,39 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 
 // ---------------------------------------------------------------- host side
 
+// Host: a [rows][head_size] byte tensor (E4M3 cache) with unswizzled boxes
+// [head_size bytes][box_rows].
+inline cudaError_t encode_plain_map(CUtensorMap* map, const void* base, int head_size,
+                                    unsigned long long rows, int box_rows) {
+    using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static std::atomic<EncodeFn> fn{nullptr};
+    EncodeFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr)
+            return e != cudaSuccess ? e : cudaErrorNotSupported;
+        f = reinterpret_cast<EncodeFn>(ptr);
+        fn.store(f, std::memory_order_release);
+    }
+    const cuuint64_t dims[2] = {(cuuint64_t)head_size, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)head_size};
+    const cuuint32_t box[2] = {(cuuint32_t)head_size, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+
+
 template <typename T, int D>
 cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) {
     const PrefillParams& p = tp.p;
@@ -1094,7 +1270,7 @@ cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) 
         }
     }
     using Sh = TcShape<D>;
-    auto kern = paged_prefill_tc_kernel<T, D>;
+    auto kern = paged_prefill_tc_kernel<T, T, D>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
     if (e != cudaSuccess) return e;
     const long long units = (long long)p.num_seqs * p.num_kv_heads * p.q_tiles;
@@ -1119,6 +1295,40 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
     case 64: return launch_prefill_tc_d<T, 64>(tp, stream);
     case 128: return launch_prefill_tc_d<T, 128>(tp, stream);
     case 256: return launch_prefill_tc_d<T, 256>(tp, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+// E4M3 caches: the one-tile kernel with widened K/V (head size 64 or 128).
+// The tensor maps view each cache as [num_blocks*Hkv*B rows][D bytes] with
+// plain (unswizzled) boxes of one block segment.
+template <typename QT>
+cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
+    TcPrefillParams tp;
+    tp.p = p;
+    constexpr int n = TcShape<128, true>::N;
+    static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
+    tp.box_rows = p.block_size < n ? p.block_size : n;
+    const unsigned long long rows =
+        (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    cudaError_t e = encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
+    if (e == cudaSuccess) e = encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
+    if (e != cudaSuccess) return e;
+    auto go = [&](auto dtag) -> cudaError_t {
+        constexpr int D = decltype(dtag)::value;
+        using Sh = TcShape<D, true>;
+        auto kern = paged_prefill_tc_kernel<QT, e4m3_t, D>;
+        cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
+        if (e2 != cudaSuccess) return e2;
+        const long long units = (long long)p.num_seqs * p.num_kv_heads * p.q_tiles;
+        if (units <= 0) return cudaSuccess;
+        if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+        kern<<<(unsigned)units, kTcThreads, Sh::kAlloc, stream>>>(tp);
+        return cudaGetLastError();
+    };
+    switch (head_size) {
+    case 64: return go(std::integral_constant<int, 64>{});
+    case 128: return go(std::integral_constant<int, 128>{});
     }
     return cudaErrorInvalidValue;
 }

@@ -101,13 +101,30 @@ def test_prefill_tensor_core_sweep(i):
     check(c, ql, f"tc sweep {i}")
 
 
-# CUDA-core shapes: binary32, block size 1, E4M3 caches, odd groups
+# CUDA-core shapes: binary32, block size 1 (16-bit and E4M3), E4M3 at head
+# size 256
 SIMT_SWEEP = [
     (4, 4, 4, 64, 16, "f32", "f32", ("uniform", 1, 64), ("uniform", 1, 20)),
     (3, 8, 2, 128, 1, "bf16", "bf16", ("uniform", 5, 90), ("uniform", 1, 12)),
-    (3, 8, 1, 128, 16, "bf16", "e4m3", ("uniform", 20, 200), ("uniform", 1, 9)),
-    (2, 6, 2, 64, 32, "f16", "e4m3", ("uniform", 40, 120), ("all",)),
+    (2, 8, 2, 128, 1, "bf16", "e4m3", ("uniform", 20, 150), ("uniform", 1, 9)),
+    (2, 8, 2, 256, 16, "f16", "e4m3", ("uniform", 20, 150), ("uniform", 1, 9)),
 ]
+
+# E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory)
+E4M3_TC_SWEEP = [
+    (3, 8, 1, 128, 16, "bf16", ("uniform", 20, 300), ("uniform", 1, 40)),
+    (2, 6, 2, 64, 32, "f16", ("uniform", 40, 200), ("all",)),
+    (4, 32, 8, 128, 16, "bf16", ("uniform", 100, 700), ("uniform", 100, 300)),
+    (3, 16, 2, 128, 256, "f16", ("uniform", 200, 600), ("uniform", 1, 12)),
+]
+
+
+@pytest.mark.parametrize("i", range(len(E4M3_TC_SWEEP)))
+def test_prefill_e4m3_tensor_core_sweep(i):
+    S, Hq, Hkv, d, B, qt, lens, ql = E4M3_TC_SWEEP[i]
+    c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
+                  q_dtype=qt, cache_dtype="e4m3", kv_dtype=qt, lengths=lens, seed=960 + i)
+    check(c, ql, f"e4m3 tc sweep {i}")
 
 
 @pytest.mark.parametrize("i", range(len(SIMT_SWEEP)))
