@@ -507,7 +507,9 @@ def run_prefill(args):
                       "peak_kind": f"{hk} HBM copy"}),
         "kernel": ("paged_prefill_tc2_kernel (two query tiles per CTA)"
                    if case.head_size <= 128 and q.max_queries > 128 // case.group
-                   else "paged_prefill_tc_kernel"),
+                   and case.cache_dtype != "e4m3"
+                   else "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)"
+                                                     if case.cache_dtype == "e4m3" else "")),
         "gpu_launches": K,
         "clocks": clocks,
     }
