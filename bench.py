@@ -357,6 +357,7 @@ def run_ours(args):
     achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
 
     graph = run_graph(st, max(20, min(1000, K)), device)
+    write_bulk = run_write_bulk(st, device)
     e2e = run_e2e(st, max(20, min(200, K // 10)), device)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -395,6 +396,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "graph": graph,
+        "write_bulk": write_bulk,
         "gpu_launches": K * st.launches_per_step,
         "clocks": clocks,
     }
@@ -514,6 +516,41 @@ def run_prefill(args):
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def run_write_bulk(st: Step, device, tokens: int = 65536, steps: int = 50):
+    """The KV write alone in its bandwidth-bound regime: a prefill-sized batch
+    of new tokens (default 65,536, the configuration's head shape) scattered
+    to seeded random slots of the pool -- write tokens/s and bytes/s (input
+    read + cache written + slots). Runs last: it overwrites pool slots."""
+    import torch
+    c, pk = st.case, st.pk
+    slots_total = c.num_blocks * c.block_size
+    tokens = min(tokens, slots_total - c.block_size)
+    g = torch.Generator(device="cpu").manual_seed(0x5EED)
+    slots = (torch.randperm(slots_total - c.block_size, generator=g)[:tokens] + c.block_size)
+    slots = slots.to(torch.int64).to(device)                 # block 0 stays reserved
+    dt = st.nk.dtype
+    key = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=g).to(dt).to(device)
+    value = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=g).to(dt).to(device)
+    for _ in range(3):
+        pk.reshape_and_cache(key, value, st.kc, st.vc, slots, c.k_scale, c.v_scale, st.status)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        pk.reshape_and_cache(key, value, st.kc, st.vc, slots, c.k_scale, c.v_scale, st.status)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nbytes = c.write_bytes(tokens)
+    peak, _ = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"tokens": tokens, "ms": round(ms, 5), "tokens_per_s": round(tokens / (ms * 1e-3), 1),
+            "gbs": round(gbs, 1), "frac_of_hbm_peak": round(gbs / peak, 4),
+            "bytes": nbytes, "kernel": "reshape_and_cache_kernel"}
 
 
 def run_graph(st: Step, steps: int, device):
