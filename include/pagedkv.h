@@ -23,6 +23,10 @@
  * ---------------------------------------
  *  Pointers.   Every tensor pointer is a DEVICE pointer owned by the caller.
  *              The library allocates nothing and keeps no state between calls.
+ *              Data arrays (query, out, key, value, the caches, the
+ *              workspace) must be 16-byte aligned, index arrays (block
+ *              tables, lengths, query starts: 4 bytes; slots, block pairs:
+ *              8 bytes) naturally aligned; otherwise PA_ERR_INVALID_ARG.
  *  Streams.    `stream` is a cudaStream_t (NULL = the legacy default stream).
  *              Every call only enqueues work on it and returns; nothing
  *              synchronises the host.

@@ -61,6 +61,16 @@ int mma_heads_per_unit(int group) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Data arrays move as 16-byte vectors and bulk copies: their addresses must
+// be 16-byte aligned; index arrays need their element's alignment.
+bool aligned(const void* p, uintptr_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) & (bytes - 1)) == 0;
+}
+bool aligned16(const void* a, const void* b = nullptr, const void* c = nullptr,
+               const void* d = nullptr) {
+    return aligned(a, 16) && aligned(b, 16) && aligned(c, 16) && aligned(d, 16);
+}
+
 int max_partitions(int max_context_len, int partition_size) {
     const int n = (max_context_len + partition_size - 1) / partition_size;
     return n < 1 ? 1 : n;
@@ -107,6 +117,8 @@ pa_status check_decode(const void* query, const void* k_cache, const void* v_cac
         return PA_ERR_UNSUPPORTED;
     if (num_seqs > 0 &&
         (!query || !k_cache || !v_cache || !block_tables || !context_lens || max_blocks_per_seq == 0))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(query, k_cache, v_cache) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return PA_ERR_INVALID_ARG;
     p = DecodeParams{};
     p.query = query;
@@ -259,6 +271,8 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
     if ((head_size * in_bytes) % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key, value, k_cache, v_cache) || !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID_ARG;
     return from_cuda(launch_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, num_tokens,
                                               num_kv_heads, head_size, block_size, num_blocks,
                                               in_dtype, cache_dtype, k_scale, v_scale, dev_status,
@@ -278,7 +292,7 @@ pa_status pa_decode(void* out, const void* query, const void* k_cache, const voi
                                 cache_dtype, k_scale, v_scale, dev_status, p);
     if (st != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
-    if (!out) return PA_ERR_INVALID_ARG;
+    if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
     p.out = out;
     return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, false,
                                        static_cast<cudaStream_t>(stream)));
@@ -300,6 +314,7 @@ pa_status pa_write_decode(void* out, const void* query, const void* key, const v
     if (st != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
     if (!out || !key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out, key, value) || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
     bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
     p.out = out;
     return from_cuda(run_decode_kernel(p, head_size, q_dtype, cache_dtype, false,
@@ -324,6 +339,7 @@ pa_status pa_write_decode_partitions(const void* query, const void* key, const v
     if ((st = check_partition_size(partition_size)) != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
     if (!key || !value || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(key, value) || !aligned(slot_mapping, 8)) return PA_ERR_INVALID_ARG;
     if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
                              workspace, workspace_bytes)) != PA_OK)
         return st;
@@ -419,6 +435,9 @@ pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, con
     if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out, tmp_out) || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
+        !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
     return from_cuda(launch_merge(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
                                   num_q_heads, head_size, partition_size, max_partitions,
                                   out_dtype, dev_status, static_cast<cudaStream_t>(stream)));
@@ -514,6 +533,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     if (num_queries == 0) return PA_OK;
     if (num_seqs == 0) return PA_ERR_INVALID_ARG;        // query tokens need a sequence
     if (!out || !query_start || max_queries_per_seq == 0) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned(query_start, 4)) return PA_ERR_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, p.group, num_blocks,
                             num_kv_heads, out, query, k_cache, v_cache)) {
@@ -565,6 +585,7 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pair
     if (block_bytes % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache, v_cache) || !aligned(block_pairs, 8)) return PA_ERR_INVALID_ARG;
     return from_cuda(launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, num_blocks,
                                         block_bytes, dev_status, static_cast<cudaStream_t>(stream)));
 }

@@ -110,3 +110,35 @@ def test_paged_prefill_argument_errors(lib):
     assert call(T=0, out=None, qs=None) == pk.PA_OK
     assert call(S=0, T=0) == pk.PA_OK
     assert call(S=0, T=3) == pk.PA_ERR_INVALID_ARG           # tokens without sequences
+
+
+def test_misaligned_pointers_are_rejected_before_any_launch(lib):
+    import ctypes
+    from paged_kv_cache_141_gb300 import binding as pk
+    L = pk.lib()
+    ok, odd = ctypes.c_void_p(256), ctypes.c_void_p(264)      # 8-byte but not 16-byte aligned
+    # decode: query, caches 16-byte aligned
+    assert L.pa_decode(ok, odd, ok, ok, ok, 4, ok, 2, 8, 8, 128, 16, 10, 64, 0.1, pk.PA_BF16,
+                       pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_decode(ok, ok, odd, ok, ok, 4, ok, 2, 8, 8, 128, 16, 10, 64, 0.1, pk.PA_BF16,
+                       pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    # ... and int32 tables at 4 bytes
+    assert L.pa_decode(ok, ok, ok, ok, ctypes.c_void_p(258), 4, ok, 2, 8, 8, 128, 16, 10, 64, 0.1,
+                       pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    # the write: key/value 16 bytes, slots 8 bytes
+    assert L.pa_reshape_and_cache(odd, ok, ok, ok, ok, 4, 8, 128, 16, 10, pk.PA_BF16, pk.PA_BF16,
+                                  1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_reshape_and_cache(ok, ok, ok, ok, ctypes.c_void_p(260), 4, 8, 128, 16, 10,
+                                  pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    # copy-on-write copies
+    assert L.pa_copy_blocks(odd, ok, ok, 2, 8, 128, 16, 10, pk.PA_BF16, None,
+                            None) == pk.PA_ERR_INVALID_ARG
+    # merge: out and partials
+    assert L.pa_merge(odd, ok, ok, ok, ok, 2, 8, 128, 512, 4, pk.PA_BF16, None,
+                      None) == pk.PA_ERR_INVALID_ARG
+    # multi-query: out 16 bytes, query_start 4 bytes
+    assert L.pa_paged_prefill(odd, ok, ok, 4, 2, ok, ok, ok, 4, ok, 2, 8, 2, 128, 16, 10, 64, 0.1,
+                              pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_paged_prefill(ok, ok, ctypes.c_void_p(258), 4, 2, ok, ok, ok, 4, ok, 2, 8, 2, 128,
+                              16, 10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None,
+                              None) == pk.PA_ERR_INVALID_ARG
