@@ -90,6 +90,13 @@ TC_SWEEP = [
     (6, 8, 4, 128, 64, "f16", ("fixed", [1, 2, 127, 128, 129, 300]), ("all",)),
     (2, 128, 1, 64, 16, "bf16", ("uniform", 10, 300), ("uniform", 1, 5)),
     (8, 32, 8, 128, 16, "bf16", ("loguniform", 64, 2048), ("uniform", 1, 8)),
+    # one query tile per sequence (the compact 64-key kernel): a full
+    # 128-row tile at G=1, block sizes below, at and above 64 keys, a group
+    # that does not divide 128, lengths around the key tile
+    (5, 4, 4, 64, 8, "f16", ("uniform", 1, 500), ("uniform", 1, 128)),
+    (4, 6, 2, 128, 256, "bf16", ("fixed", [63, 64, 65, 700]), ("uniform", 1, 14)),
+    (4, 16, 2, 64, 64, "bf16", ("uniform", 1, 300), ("uniform", 1, 16)),
+    (3, 8, 8, 128, 32, "f16", ("fixed", [1, 128, 129]), ("all",)),
 ]
 
 
@@ -147,7 +154,12 @@ def test_one_query_per_sequence_is_the_decode():
               c.max_context_len, c.scale, 1.0, 1.0, dc.status)
     got = to_f64(p.run())
     assert dc.status_bits() == 0
-    assert np.abs(got - to_f64(out_d)).max() <= 1e-3
+    dec = to_f64(out_d)
+    # both paths round an fp32 result to bf16: where the two fp32 values lie
+    # on either side of a rounding boundary they differ by one bf16 ulp
+    mag = np.maximum(np.abs(dec), 2.0 ** -126)
+    ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+    assert np.all(np.abs(got - dec) <= np.maximum(1e-3, ulp))
     rows, want = p.oracle()
     assert_decode_close(got[rows], want, c, "one query")
 
@@ -277,3 +289,18 @@ def test_repeated_launches_are_bit_identical(law):
     for _ in range(2):
         p.out.fill_(float("nan"))
         assert torch.equal(p.run(), first)
+
+
+def test_full_size_shared_prefix_e4m3_sampled():
+    """The shared-prefix E4M3 pool (128 sequences, 64 query heads / 8 KV
+    heads, a 1024-token prefix shared by 32 sequences each): a 256-token chunk
+    per sequence on the tensor cores, sampled rows against the oracle."""
+    c = config_case(5)
+    p = Prefill(c, ("fixed", np.minimum(256, c.context_lens)))
+    got = to_f64(p.run())
+    assert p.dc.status_bits() == 0
+    rng = np.random.default_rng(12)
+    qs = p.q.query_start
+    rows = np.array(sorted(set(int(r) for r in rng.integers(0, int(qs[-1]), size=48))))
+    want = p.oracle_rows(rows)
+    assert_decode_close(got[rows], want, c, "shared-prefix e4m3")
