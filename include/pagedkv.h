@@ -459,6 +459,20 @@ int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_co
  */
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len);
 
+/*
+ * pa_selftest_wait -- a device check of the kernels' bounded waits (see
+ * "Errors" above). Launches one CTA in which two threads wait on mbarriers
+ * expecting one arrival each, one through the wait of the TMA pipelines and
+ * one through the wait of the tensor-core pipelines. arrive = 1: the
+ * arrivals are made first; both waits return at once and nothing is set.
+ * arrive = 0: nothing arrives; each wait runs out after its limit (about a
+ * second of SM clocks), sets PA_DEV_TIMEOUT in *dev_status and returns, and
+ * the kernel ends, the context still usable. A wait that returned without an
+ * arrival sets PA_DEV_BAD_LEN. dev_status (device, 4-byte aligned) is
+ * required; arrive must be 0 or 1 (else PA_ERR_INVALID_ARG).
+ */
+pa_status pa_selftest_wait(int arrive, uint32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (a static string). */
 const char* pa_status_string(pa_status status);
 

@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
         L.pa_paged_prefill.argtypes = [P, P, P, I, I, P, P, P, I, P, I, I, I, I, I, I64, I, F, I,
                                        I, F, F, P, P]
         L.pa_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I64, I, P, P]
+        L.pa_selftest_wait.argtypes = [I, P, P]
         L.pa_allocator_create.argtypes = [I64, I, I]
         L.pa_allocator_create.restype = P
         L.pa_allocator_destroy.argtypes = [P]
@@ -114,7 +115,7 @@ def lib() -> ctypes.CDLL:
                      "pa_decode_partitioned_static", "pa_write_decode",
                      "pa_write_decode_partitioned", "pa_write_decode_partitions",
                      "pa_decode_choose", "pa_decode_partition_size", "pa_version",
-                     "pa_copy_blocks", "pa_allocator_allocate", "pa_allocator_fork",
+                     "pa_copy_blocks", "pa_selftest_wait", "pa_allocator_allocate", "pa_allocator_fork",
                      "pa_allocator_free", "pa_allocator_append_slot"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -416,6 +417,14 @@ def copy_blocks(k_cache, v_cache, block_pairs, dev_status=None, stream=None) -> 
     _check(lib().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs),
                                 block_pairs.shape[0], H, D, B, nb, _dtype(k_cache),
                                 _ptr(dev_status), _stream(stream)), "pa_copy_blocks")
+
+
+def selftest_wait(arrive: bool, dev_status, stream=None) -> None:
+    """Launch the device check of the kernels' bounded waits: with arrive
+    False both waits run out (about a second each, concurrently) and set
+    DEV_TIMEOUT in dev_status; with arrive True nothing is set."""
+    _check(lib().pa_selftest_wait(int(bool(arrive)), _ptr(dev_status), _stream(stream)),
+           "pa_selftest_wait")
 
 
 class BlockAllocator:

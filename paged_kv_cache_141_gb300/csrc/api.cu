@@ -590,6 +590,12 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pair
                                         block_bytes, dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_selftest_wait(int arrive, uint32_t* dev_status, void* stream) {
+    if (!dev_status || (arrive != 0 && arrive != 1)) return PA_ERR_INVALID_ARG;
+    if (!aligned(dev_status, 4)) return PA_ERR_INVALID_ARG;
+    return from_cuda(launch_wait_selftest(arrive, dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 const char* pa_status_string(pa_status status) {
     switch (status) {
     case PA_OK: return "ok";

@@ -130,6 +130,8 @@ cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pair
                                int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,
                                uint32_t* status, cudaStream_t stream);
 
+cudaError_t launch_wait_selftest(int arrive, uint32_t* status, cudaStream_t stream);
+
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* k_cache,
                                      void* v_cache, const int64_t* slots, int64_t num_tokens,
                                      int num_kv_heads, int head_size, int block_size,

@@ -142,3 +142,12 @@ def test_misaligned_pointers_are_rejected_before_any_launch(lib):
     assert L.pa_paged_prefill(ok, ok, ctypes.c_void_p(258), 4, 2, ok, ok, ok, 4, ok, 2, 8, 2, 128,
                               16, 10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None,
                               None) == pk.PA_ERR_INVALID_ARG
+
+
+def test_wait_selftest_argument_errors(lib):
+    import ctypes
+    from paged_kv_cache_141_gb300 import binding as pk
+    L = pk.lib()
+    assert L.pa_selftest_wait(0, None, None) == pk.PA_ERR_INVALID_ARG       # status required
+    assert L.pa_selftest_wait(2, ctypes.c_void_p(256), None) == pk.PA_ERR_INVALID_ARG
+    assert L.pa_selftest_wait(1, ctypes.c_void_p(258), None) == pk.PA_ERR_INVALID_ARG
