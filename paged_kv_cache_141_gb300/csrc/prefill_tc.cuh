@@ -43,7 +43,9 @@
 // beyond a 2e-3 bound. So P goes to the tensor cores as two 16-bit terms,
 // P_hi = round(p) and P_lo = round(p - P_hi) (relative error ~2^-16), packed
 // side by side in the score buffer, and O accumulates P_hi.V + P_lo.V: three
-// MMAs per key tile instead of two.
+// MMAs per key tile instead of two. Binary16 operands (f16 caches, and E4M3
+// caches widened to binary16) keep 11 significant bits, a relative error of
+// at most 2^-12 per weight: P goes as one term and the P_lo product is skipped.
 //
 // Every wait is bounded; a wait that runs out raises PA_DEV_TIMEOUT and a
 // shared abort flag that ends every role's loop, and the CTA drains its copies
@@ -110,6 +112,8 @@ struct TcShape {
 // The MMAs' operand type: the query's for 16-bit caches; binary16 for E4M3
 // caches (every E4M3 value is exact in it; the query is rounded to it).
 template <typename QT, typename CT> struct TcMath { using T = QT; };
+// whether weights in this MMA type need the P_lo correction term
+template <typename T> constexpr bool kTcPLo = std::is_same<T, __nv_bfloat16>::value;
 template <typename QT> struct TcMath<QT, e4m3_t> { using T = __half; };
 
 struct TcPrefillParams {
@@ -640,10 +644,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
                     tc_mma_ts(tmem + Sh::kOCol, pt + kk * 8, b, idO, j > 0 || kk > 0);
                 }
+                if constexpr (kTcPLo<MT>) {
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
-                    tc_mma_ts(tmem + Sh::kOCol, pt + N / 2 + kk * 8, b, idO, true);
+                    for (int kk = 0; kk < N / 16; ++kk) {
+                        const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
+                        tc_mma_ts(tmem + Sh::kOCol, pt + N / 2 + kk * 8, b, idO, true);
+                    }
                 }
                 tc_commit(&v_empty[st]);
                 tc_commit(pv_done);
@@ -735,8 +741,10 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const float2 e = make_float2(fast_exp2(t.x), fast_exp2(t.y));
                     sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
                     phi[c / 2] = pack2<MT>(e.x, e.y);
-                    const float2 lo = __ffma2_rn(unpack2<MT>(phi[c / 2]), make_float2(-1.f, -1.f), e);
-                    plo[c / 2] = pack2<MT>(lo.x, lo.y);
+                    if constexpr (kTcPLo<MT>) {
+                        const float2 lo = __ffma2_rn(unpack2<MT>(phi[c / 2]), make_float2(-1.f, -1.f), e);
+                        plo[c / 2] = pack2<MT>(lo.x, lo.y);
+                    }
                 }
             };
             if (hf == 0) weights(std::integral_constant<int, 0>{});
@@ -750,7 +758,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             // P over S in the same buffer: P_hi pairs in columns [0, N/2), P_lo
             // in [N/2, N); this half's keys are a quarter of the buffer each
             tc_st_n<NH / 2>(sbuf + hf * (NH / 2), phi);
-            tc_st_n<NH / 2>(sbuf + N / 2 + hf * (NH / 2), plo);
+            if constexpr (kTcPLo<MT>) tc_st_n<NH / 2>(sbuf + N / 2 + hf * (NH / 2), plo);
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 // O holds tiles < j once the previous P.V is done; each half
                 // rescales its half of the columns
@@ -1042,10 +1050,12 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
                     tc_mma_ts(oc, pt + kk * 8, b, idO, j > 0 || kk > 0);
                 }
+                if constexpr (kTcPLo<T>) {
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
-                    tc_mma_ts(oc, pt + N / 2 + kk * 8, b, idO, true);
+                    for (int kk = 0; kk < N / 16; ++kk) {
+                        const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
+                        tc_mma_ts(oc, pt + N / 2 + kk * 8, b, idO, true);
+                    }
                 }
                 if (t == last_t) tc_commit(&v_empty[st]);
                 return true;
@@ -1131,11 +1141,13 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                     const float2 e = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
                     sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
                     phi[c / 2] = pack2<T>(e.x, e.y);
-                    const float2 lo = __ffma2_rn(unpack2<T>(phi[c / 2]), make_float2(-1.f, -1.f), e);
-                    plo[c / 2] = pack2<T>(lo.x, lo.y);
+                    if constexpr (kTcPLo<T>) {
+                        const float2 lo = __ffma2_rn(unpack2<T>(phi[c / 2]), make_float2(-1.f, -1.f), e);
+                        plo[c / 2] = pack2<T>(lo.x, lo.y);
+                    }
                 }
                 tc_st_n<N / 4>(sbuf + h * (N / 4), phi);
-                tc_st_n<N / 4>(sbuf + N / 2 + h * (N / 4), plo);
+                if constexpr (kTcPLo<T>) tc_st_n<N / 4>(sbuf + N / 2 + h * (N / 4), plo);
             }
 #pragma unroll
             for (int w = R / 4; w >= 1; w /= 2)
