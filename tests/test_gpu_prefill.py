@@ -97,6 +97,10 @@ TC_SWEEP = [
     (4, 6, 2, 128, 256, "bf16", ("fixed", [63, 64, 65, 700]), ("uniform", 1, 14)),
     (4, 16, 2, 64, 64, "bf16", ("uniform", 1, 300), ("uniform", 1, 16)),
     (3, 8, 8, 128, 32, "f16", ("fixed", [1, 128, 129]), ("all",)),
+    # binary16 weights as one term: every row of a short causal prefix sees
+    # 1..24 keys, where single weights dominate the output
+    (48, 8, 2, 128, 16, "f16", ("uniform", 2, 24), ("all",)),
+    (32, 4, 4, 64, 8, "f16", ("uniform", 1, 12), ("all",)),
 ]
 
 
