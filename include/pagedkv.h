@@ -81,7 +81,7 @@ extern "C" {
 typedef enum pa_status {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,   /* a NULL pointer, a negative size, inconsistent shapes */
-    PA_ERR_UNSUPPORTED = 2,   /* a valid request this build does not implement */
+    PA_ERR_UNSUPPORTED = 2,   /* a valid request this library does not implement */
     PA_ERR_WORKSPACE = 3,     /* the workspace is NULL, misaligned or too small */
     PA_ERR_CUDA = 4,          /* a CUDA call or launch failed */
     PA_ERR_NO_BLOCKS = 5      /* the block allocator has too few free blocks */
