@@ -308,6 +308,10 @@ def run_ours(args):
     if int(st.status.item()) != 0:
         raise SystemExit(f"device status {int(st.status.item())} after the first step")
 
+    # the clock sampler starts (and settles) before the warm-up, so that the
+    # GPU goes from the warm-up straight into the timed region at full clocks
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.25 if sampler else 0)
     for _ in range(args.warmup):
         st.step()
     torch.cuda.synchronize()
@@ -322,8 +326,6 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    time.sleep(0.25 if sampler else 0)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -460,13 +462,14 @@ def run_prefill(args):
     torch.cuda.synchronize()
     if int(st.status.item()) != 0:
         raise SystemExit(f"device status {int(st.status.item())} after the first launch")
+    K = args.steps
+    stream = torch.cuda.current_stream(device)
+    # sampler first, then the warm-up: no idle gap before the timed region
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.25)
     for _ in range(args.warmup):
         launch()
     torch.cuda.synchronize()
-    K = args.steps
-    stream = torch.cuda.current_stream(device)
-    sampler = ClockSampler(torch.cuda.current_device())
-    time.sleep(0.25)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
