@@ -298,10 +298,33 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 // box's block-table entry and issues the box's copies. The entries of the
 // next kAhead tiles are in flight while the current ones are issued, so the
 // table's latency is not paid per tile.
+constexpr int kTcAhead = 4;                   // key tiles whose table entries load together
+
+// The block-table entries of a unit's first kTcAhead key tiles for this
+// lane's box, read before the sequence's lengths are known: every unit's keys
+// start at 0, so they depend on the sequence alone (entries past the context
+// are dropped once kend is known, and none past max_blocks is read). The
+// table read then overlaps the length reads and the CTA's setup instead of
+// following them.
+template <typename Sh>
+__device__ __forceinline__ void tc_ring_first(const TcPrefillParams& tp, int s, int lane,
+                                              int64_t (&first)[kTcAhead]) {
+    constexpr int N = Sh::N;
+    const PrefillParams& p = tp.p;
+    const int r0 = lane * tp.box_rows;
+    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+#pragma unroll
+    for (int k = 0; k < kTcAhead; ++k) {
+        const int e = (k * N + r0) / p.block_size;
+        first[k] = (r0 < N && e < p.max_blocks) ? (int64_t)__ldg(table + e) : -1;
+    }
+}
+
 template <typename Sh>
 __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CUtensorMap* map,
                                              uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              int s, int hk, int ntiles, int kend, int lane,
+                                             const int64_t (&first)[kTcAhead],
                                              volatile int* abort_flag) {
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
@@ -318,11 +341,12 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
     };
     // Entries for groups of kAhead tiles: the next group's loads are issued
     // when a group starts and read when it ends, so no register copy waits on
-    // a load still in flight.
-    constexpr int kAhead = 4;
+    // a load still in flight. The first group's were read at kernel entry.
+    constexpr int kAhead = kTcAhead;
     int64_t cur[kAhead], nxt[kAhead];
 #pragma unroll
-    for (int k = 0; k < kAhead; ++k) cur[k] = k < ntiles ? fetch(k) : kNone;
+    for (int k = 0; k < kAhead; ++k)
+        cur[k] = (k < ntiles && r0 < N && k * N + r0 < kend) ? first[k] : kNone;
     int issued = 0;
     bool live = true;
     for (int j0 = 0; j0 < ntiles && live; j0 += kAhead) {
@@ -497,6 +521,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int rest = blockIdx.x / p.q_tiles;
     const int hk = rest % p.num_kv_heads;
     const int s = rest / p.num_kv_heads;
+    int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
+    if constexpr (!kFp8)
+        if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
     const int L = p.context_lens[s];
@@ -601,7 +628,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                               k_empty, s, hk, ntiles, kend, lane, abort_flag);
         else
             tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                             lane, abort_flag);
+                             lane, first, abort_flag);
     } else if (warp == kTcVWarp) {
         // ------------------------------------------------------------ V loads
         if constexpr (kFp8)
@@ -609,7 +636,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                               v_empty, s, hk, ntiles, kend, lane, abort_flag);
         else
             tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                             lane, abort_flag);
+                             lane, first, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -920,6 +947,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int rest = blockIdx.x / groups;
     const int hk = rest % p.num_kv_heads;
     const int s = rest / p.num_kv_heads;
+    int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
+    if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
     const int L = p.context_lens[s];
@@ -1004,10 +1033,10 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 
     if (warp == kTcKWarp) {
         tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                        lane, abort_flag);
+                        lane, first, abort_flag);
     } else if (warp == kTcVWarp) {
         tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                        lane, abort_flag);
+                        lane, first, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
