@@ -13,7 +13,9 @@
 //   O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads),
 //     V^T fragments read with ldmatrix.trans, P^T fragments made from the S
 //     accumulators with movmatrix. P is split into a 16-bit high part and a
-//     16-bit residual, two MMAs, so the weights keep ~16 significant bits.
+//     16-bit residual, two MMAs, so the weights keep ~16 significant bits
+//     (E4M3 caches: binary16 weights as one term, 11 bits, far below the
+//     codes' own error).
 // Heads beyond the group (up to the MMA's 8 columns) carry zero queries and
 // are never written out. Rows of V past the context are zeroed before the
 // P.V product, since 0 x NaN would otherwise poison every output component.
@@ -391,13 +393,20 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                 const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
                 const uint32_t hi = Ops::pack(w0, w1);
                 const float2 hf = Ops::unpack(hi);
-                const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
                 // the sums use exactly the weights the products use
-                const float2 lf = Ops::unpack(lo);
-                l_run[0] += hf.x + lf.x;
-                l_run[1] += hf.y + lf.y;
+                if constexpr (kFp8) {
+                    // binary16 weights as one term: relative error at most
+                    // 2^-11, far inside the E4M3 codes' own 2^-4
+                    l_run[0] += hf.x;
+                    l_run[1] += hf.y;
+                } else {
+                    const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
+                    const float2 lf = Ops::unpack(lo);
+                    l_run[0] += hf.x + lf.x;
+                    l_run[1] += hf.y + lf.y;
+                    bl[mt][hr] = movmatrix_trans(lo);
+                }
                 bh[mt][hr] = movmatrix_trans(hi);
-                bl[mt][hr] = movmatrix_trans(lo);
             }
         }
 
@@ -420,7 +429,6 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                                            e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020)),
                                            e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031))};
                     Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
-                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
                 }
             }
         } else {
