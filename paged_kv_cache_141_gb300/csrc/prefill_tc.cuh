@@ -320,14 +320,14 @@ __device__ __forceinline__ void tc_ring_first(const TcPrefillParams& tp, int s, 
     }
 }
 
-template <typename Sh>
+template <typename Sh, int NS>
 __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CUtensorMap* map,
                                              uint8_t* ring, uint64_t* full, uint64_t* empty,
                                              int s, int hk, int ntiles, int kend, int lane,
                                              const int64_t (&first)[kTcAhead],
                                              volatile int* abort_flag) {
     constexpr int N = Sh::N;
-    constexpr int NS = Sh::NS;
+    static_assert(NS >= 2, "ring stages");
     constexpr int64_t kNone = -1;
     const PrefillParams& p = tp.p;
     const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
@@ -627,16 +627,16 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             tc_load_widen<Sh>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_full,
                               k_empty, s, hk, ntiles, kend, lane, abort_flag);
         else
-            tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                             lane, first, abort_flag);
+            tc_load_ring<Sh, NS>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
+                                 kend, lane, first, abort_flag);
     } else if (warp == kTcVWarp) {
         // ------------------------------------------------------------ V loads
         if constexpr (kFp8)
             tc_load_widen<Sh>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_full,
                               v_empty, s, hk, ntiles, kend, lane, abort_flag);
         else
-            tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                             lane, first, abort_flag);
+            tc_load_ring<Sh, NS>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
+                                 kend, lane, first, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -877,7 +877,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
 // Shapes of the two-tile kernel (head size 64 or 128): two 128-row query
 // tiles share every K/V tile, so each loaded tile feeds twice the rows.
-template <int D>
+template <int D, bool kPLo>
 struct TcShape2 {
     static constexpr int N = 128;                            // keys per tile
     static constexpr int kSpans = D / 64;
@@ -885,13 +885,21 @@ struct TcShape2 {
     static constexpr int kKvBytes = N * D * 2;
     static constexpr int kFixed = 2 * kQBytes + 1024 + 256;  // Q0, Q1, slack, barriers
     static constexpr int kStages0 = (kTcSmemLimit - kFixed) / (2 * kKvBytes);
-    static constexpr int NS = kStages0 > 4 ? 4 : kStages0;
+    // K and V rings of their own depths: a K slot is free once both tiles'
+    // S products have read it, a V slot only after both P.V products, so V
+    // takes the stage that is left over (head size 128: 2 K, 3 V stages).
+    // With the P_lo term (bf16) the softmax's registers are at their limit
+    // and the deeper V ring measured slower: K and V get equal depths.
+    static constexpr int NSK = kStages0 > 4 ? 4 : kStages0;
+    static constexpr int kStagesV0 = (kTcSmemLimit - kFixed - NSK * kKvBytes) / kKvBytes;
+    static constexpr int kStagesV1 = kPLo ? NSK : kStagesV0;
+    static constexpr int NSV = kStagesV1 > 4 ? 4 : kStagesV1;
     static constexpr int kQOff = 0;                          // Q0, then Q1
     static constexpr int kKOff = 2 * kQBytes;
-    static constexpr int kVOff = kKOff + NS * kKvBytes;
-    static constexpr int kBarOff = kVOff + NS * kKvBytes;
-    // k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full[2] drain q_ready
-    static constexpr int kNumBars = 4 * NS + 6;
+    static constexpr int kVOff = kKOff + NSK * kKvBytes;
+    static constexpr int kBarOff = kVOff + NSV * kKvBytes;
+    // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
+    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -900,7 +908,7 @@ struct TcShape2 {
     static constexpr int kTmemCols = 512;
     static constexpr int kTileCols = N + D;
     static_assert(D == 64 || D == 128, "head size");
-    static_assert(NS >= 2, "stages");
+    static_assert(NSK >= 2 && NSV >= 2, "stages");
     static_assert(2 * kTileCols <= kTmemCols, "TMEM columns");
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
@@ -918,19 +926,20 @@ struct TcShape2 {
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
-    using Sh = TcShape2<D>;
+    using Sh = TcShape2<D, kTcPLo<T>>;
     constexpr int N = Sh::N;
-    constexpr int NS = Sh::NS;
+    constexpr int NSK = Sh::NSK;                             // K ring stages
+    constexpr int NSV = Sh::NSV;                             // V ring stages
     const PrefillParams& p = tp.p;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Sh::kBarOff);
     uint64_t* k_full = bars;
-    uint64_t* k_empty = k_full + NS;
-    uint64_t* v_full = k_empty + NS;
-    uint64_t* v_empty = v_full + NS;
-    uint64_t* s_full = v_empty + NS;                         // [2], per query tile
+    uint64_t* k_empty = k_full + NSK;
+    uint64_t* v_full = k_empty + NSK;
+    uint64_t* v_empty = v_full + NSV;
+    uint64_t* s_full = v_empty + NSV;                        // [2], per query tile
     uint64_t* p_full = s_full + 2;                           // [2]
     uint64_t* drain = p_full + 2;
     uint64_t* q_ready = drain + 1;
@@ -971,9 +980,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int ntiles = (kend + N - 1) / N;
 
     if (tid == kTcKWarp * 32) {
-        for (int i = 0; i < NS; ++i) {
+        for (int i = 0; i < NSK; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < NSV; ++i) {
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
         }
@@ -1032,11 +1043,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     }
 
     if (warp == kTcKWarp) {
-        tc_load_ring<Sh>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                        lane, first, abort_flag);
+        tc_load_ring<Sh, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
+                              lane, first, abort_flag);
     } else if (warp == kTcVWarp) {
-        tc_load_ring<Sh>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                        lane, first, abort_flag);
+        tc_load_ring<Sh, NSV>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
+                              lane, first, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -1044,9 +1055,9 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             constexpr uint32_t idO = tc_idesc<T>(kTcRows, D, 1);
             const int last_t = two ? 1 : 0;
             auto qk = [&](int t, int j) -> bool {
-                const int st = j % NS;
+                const int st = j % NSK;
                 if (t == 0) {
-                    if (!tc_wait(&k_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag))
+                    if (!tc_wait(&k_full[st], (uint32_t)((j / NSK) & 1), p.status, abort_flag))
                         return false;
                     tc_fence_after();
                 }
@@ -1065,10 +1076,10 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 return true;
             };
             auto pv = [&](int t, int j) -> bool {
-                const int st = j % NS;
+                const int st = j % NSV;
                 if (!tc_wait(&p_full[t], (uint32_t)(j & 1), p.status, abort_flag)) return false;
                 if (t == 0 &&
-                    !tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag))
+                    !tc_wait(&v_full[st], (uint32_t)((j / NSV) & 1), p.status, abort_flag))
                     return false;
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kKvBytes);
@@ -1201,8 +1212,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             if (qt == 0 && key0 + N > kend) {
                 // last tile: V rows at or past kend hold stale data or cache
                 // poison; zero them before either tile's P.V reads the slot
-                const int st = j % NS;
-                ok = tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag);
+                const int st = j % NSV;
+                ok = tc_wait(&v_full[st], (uint32_t)((j / NSV) & 1), p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const int first = kend - key0;
@@ -1300,7 +1311,7 @@ cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) 
     // <= 128); otherwise one tile with double-buffered scores
     if constexpr (D <= 128) {
         if (p.q_tiles >= 2) {
-            using Sh = TcShape2<D>;
+            using Sh = TcShape2<D, kTcPLo<T>>;
             auto kern = paged_prefill_tc2_kernel<T, D>;
             cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
             if (e != cudaSuccess) return e;
