@@ -4,7 +4,8 @@
 // PagedAttention and vLLM", "the paged implementation of attention": logical
 // block -> physical block; the queries there already carry a num_queries axis).
 //
-// Work unit. One CTA takes one (sequence s, KV head, query tile). The tile's
+// Work unit. One CTA takes one (sequence s, KV head, query tile) (the
+// two-tile kernel further down takes two query tiles). The tile's
 // 128 rows are (query token, head in the group) pairs, token-major: row r is
 // token r / G and query head hk*G + r % G, so the G query heads that share the
 // KV head read each key once. Query token i of s sits at position
@@ -16,7 +17,8 @@
 // taking box i; warp 10 does the same for V. K and V have rings of their own
 // (three stages each at head size 128), so a K tile is fetched as soon as the
 // S = Q.K^T of the tile three stages back has consumed its slot, whatever P.V
-// is doing.
+// is doing. The block-table entries of a unit's first four key tiles are read
+// at kernel entry, alongside the sequence's lengths.
 //
 // Tensor cores. Warp 9 (one lane) issues tcgen05.mma in the order S_0, S_1,
 // PV_0, S_2, PV_1, ...: S_j = Q.K_j^T into TMEM score buffer j mod 2 (A = Q
@@ -45,7 +47,7 @@
 // side by side in the score buffer, and O accumulates P_hi.V + P_lo.V: three
 // MMAs per key tile instead of two. Binary16 operands (f16 caches, and E4M3
 // caches widened to binary16) keep 11 significant bits, a relative error of
-// at most 2^-12 per weight: P goes as one term and the P_lo product is skipped.
+// at most 2^-11 per weight: P goes as one term and the P_lo product is skipped.
 //
 // Every wait is bounded; a wait that runs out raises PA_DEV_TIMEOUT and a
 // shared abort flag that ends every role's loop, and the CTA drains its copies
