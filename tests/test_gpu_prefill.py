@@ -308,3 +308,22 @@ def test_full_size_shared_prefix_e4m3_sampled():
     rows = np.array(sorted(set(int(r) for r in rng.integers(0, int(qs[-1]), size=48))))
     want = p.oracle_rows(rows)
     assert_decode_close(got[rows], want, c, "shared-prefix e4m3")
+
+
+def test_full_size_llama7b_mha_f16_sampled():
+    """The LLaMA-7B fp16 MHA pool (64 sequences, 32 heads, contexts up to
+    2016): a 512-token chunk per sequence on the two-tile kernel with single
+    binary16 weights and its deeper V ring, sampled rows against the oracle."""
+    c = config_case(2)
+    p = Prefill(c, ("fixed", np.minimum(512, c.context_lens)))
+    got = to_f64(p.run())
+    assert p.dc.status_bits() == 0
+    rng = np.random.default_rng(21)
+    qs = p.q.query_start
+    rows = set(int(r) for r in rng.integers(0, int(qs[-1]), size=40))
+    L = c.context_lens
+    for s in {int(np.argmin(L)), int(np.argmax(L))}:
+        rows.update({int(qs[s]), int(qs[s + 1]) - 1})          # first and last token
+    rows = np.array(sorted(rows))
+    want = p.oracle_rows(rows)
+    assert_decode_close(got[rows], want, c, "llama-7b mha f16 chunk")
