@@ -63,17 +63,22 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
+def recorded_traffic(config: int, partition_size: int, form: str, split: bool):
     """DRAM bytes per launch of the partition kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+    summary, if it was taken on the current kernel source and on this
+    workload (configuration, partition size, fused or separate write)."""
     try:
         fields = {}
         with open(TRAFFIC_FILE) as f:
             for line in f:
-                if ":" in line:
+                if ":" in line and not line.startswith("#"):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
         if fields.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        if (fields.get("workload") != f"configuration {config}"
+                or int(fields.get("partition_size", -1)) != partition_size
+                or fields.get("form") != form or not split):
             return None
         return float(fields["dram_bytes_per_launch"])
     except Exception:
@@ -357,6 +362,16 @@ def run_ours(args):
     main_name = "write+decode" if "write+decode" in call_ms else "decode"
     main_avg = call_ms[main_name]
     achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
+    # shared blocks (read by several sequences, served from L2 after the
+    # first) counted once: the rate on the bytes that exist in the pool
+    unique_kv = case.unique_kv_bytes()
+    unique = None
+    if unique_kv < case.kv_bytes():
+        ub = by["total"] - case.kv_bytes() + unique_kv
+        ug = whole_job_gbs(ub, world, ms_per_step)
+        unique = {"kv_bytes": unique_kv, "bytes_per_step": ub, "gbs": round(ug, 2),
+                  "frac_of_hbm_peak": round(ug / peak, 4),
+                  "note": "each distinct cached token's K/V once (shared prefix blocks count once)"}
 
     graph = run_graph(st, max(20, min(1000, K)), device)
     write_bulk = run_write_bulk(st, device)
@@ -381,11 +396,13 @@ def run_ours(args):
                          % (case.kv_bytes() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "frac_of_hbm_peak": round(value / peak, 4),
+        **({"unique_bytes": unique} if unique else {}),
         "seqs_per_s_per_layer": round(seqs_per_s, 1),
         "bytes_per_step": by,
         "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(args.config, st.P, st.form, st.split),
                      "kernel": decode_kernel_label(case) + (
                          (" (partition kernel" if st.split else " (single pass")
                          + (", KV write fused)" if st.form == "fused" else ")")),
@@ -521,21 +538,23 @@ def run_prefill(args):
     print(json.dumps(line))
 
 
-def run_write_bulk(st: Step, device, tokens: int = 65536, steps: int = 50):
-    """The KV write alone in its bandwidth-bound regime: a prefill-sized batch
-    of new tokens (default 65,536, the configuration's head shape) scattered
-    to seeded random slots of the pool -- write tokens/s and bytes/s (input
-    read + cache written + slots). Runs last: it overwrites pool slots."""
+def run_write_bulk(st: Step, device, tokens: int | None = None, steps: int = 50):
+    """The KV write alone in its bandwidth-bound regime: as many new tokens
+    as the configuration's contexts hold (default; capped by the pool's free
+    slots), of its head shape, scattered to seeded random distinct slots of
+    the pool -- write tokens/s and bytes/s (input read + cache written +
+    slots). Runs last: it overwrites pool slots."""
     import torch
     c, pk = st.case, st.pk
     slots_total = c.num_blocks * c.block_size
-    tokens = min(tokens, slots_total - c.block_size)
+    tokens = min(c.total_tokens if tokens is None else tokens, slots_total - c.block_size)
     g = torch.Generator(device="cpu").manual_seed(0x5EED)
     slots = (torch.randperm(slots_total - c.block_size, generator=g)[:tokens] + c.block_size)
     slots = slots.to(torch.int64).to(device)                 # block 0 stays reserved
     dt = st.nk.dtype
-    key = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=g).to(dt).to(device)
-    value = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=g).to(dt).to(device)
+    gd = torch.Generator(device=device).manual_seed(0x5EED)
+    key = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=gd, device=device).to(dt)
+    value = torch.randn(tokens, c.num_kv_heads, c.head_size, generator=gd, device=device).to(dt)
     for _ in range(3):
         pk.reshape_and_cache(key, value, st.kc, st.vc, slots, c.k_scale, c.v_scale, st.status)
     torch.cuda.synchronize()
@@ -654,17 +673,56 @@ def run_e2e(st: Step, steps: int, device):
                          "while step i runs (two buffer sets, three streams)"}
 
 
+def host_cpu() -> dict:
+    """This host's CPU model (x86 'model name'; Arm implementer/part codes)
+    and hardware thread count, for the CPU-baseline record."""
+    import platform
+    model, impl, part = None, None, None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k = k.strip().lower()
+                if k == "model name" and model is None:
+                    model = v.strip()
+                elif k == "cpu implementer" and impl is None:
+                    impl = v.strip()
+                elif k == "cpu part" and part is None:
+                    part = v.strip()
+    except OSError:
+        pass
+    if model is None and impl is not None:
+        model = f"Arm implementer {impl} part {part}"
+    return {"cpu_model": model or platform.machine(), "host_threads": os.cpu_count()}
+
+
+def oracle_inputs(case):
+    """The pool as the oracle sees it (E4M3 pools: the context tokens written
+    through the oracle's own encoder) and the logical bytes per context token
+    and per sequence's query + output."""
+    import oracle
+    kc, vc = case.k_cache, case.v_cache
+    if case.prefill_key is not None:
+        kc, vc = kc.copy(), vc.copy()
+        rc = oracle.reshape_and_cache(case.prefill_key, case.prefill_value, kc, vc,
+                                      case.prefill_slots, case.num_kv_heads, case.head_size,
+                                      case.block_size, case.kv_dtype, case.cache_dtype,
+                                      case.k_scale, case.v_scale)
+        if rc != 0:
+            raise SystemExit(f"oracle write of the prefill tokens failed ({rc})")
+    eb = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
+    per_tok = 2 * case.num_kv_heads * case.head_size * eb[case.cache_dtype]
+    qo = 2 * case.num_q_heads * case.head_size * eb[case.q_dtype]
+    return kc, vc, per_tok, qo
+
+
 def cpu_baseline(case, partition_size, budget_s=12.0):
     """The oracle, as it stands, on a bounded sample of the workload's
     sequences (single-threaded C, fp64), timed on this host."""
     import oracle
     order = np.random.default_rng(1).permutation(case.num_seqs)
-    done, bytes_done, t0 = [], 0, time.perf_counter()
-    per_tok = 2 * case.num_kv_heads * case.head_size * {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}[case.cache_dtype]
-    qo = 2 * case.num_q_heads * case.head_size * 2
-    kc, vc = case.k_cache, case.v_cache
-    if case.prefill_key is not None:
-        return None
+    done, bytes_done = [], 0
+    kc, vc, per_tok, qo = oracle_inputs(case)
     elapsed = 0.0
     for s in order:
         sl = slice(int(s), int(s) + 1)
@@ -672,14 +730,14 @@ def cpu_baseline(case, partition_size, budget_s=12.0):
         oracle.decode(np.ascontiguousarray(case.query[sl]), case.q_dtype, kc, vc, case.cache_dtype,
                       np.ascontiguousarray(case.block_tables[sl]),
                       np.ascontiguousarray(case.context_lens[sl]), case.num_kv_heads,
-                      case.block_size, case.scale)
+                      case.block_size, case.scale, case.k_scale, case.v_scale)
         elapsed += time.perf_counter() - t
         done.append(int(s))
         bytes_done += int(case.context_lens[s]) * per_tok + qo
         if elapsed >= budget_s:
             break
     return {"value": round(bytes_done / elapsed / 1e9, 4), "unit": UNIT, "cores": 1,
-            "kind": "oracle",
+            "kind": "oracle", **host_cpu(),
             "sample": f"{len(done)} of {case.num_seqs} sequences ({sum(int(case.context_lens[s]) for s in done)} "
                       f"context tokens), single-threaded C oracle in fp64, {elapsed:.1f} s",
             "seqs_per_s": round(len(done) / elapsed, 3)}
@@ -693,17 +751,16 @@ def run_reference(args):
     from paged_kv_cache_141_gb300 import workloads as W
     import oracle
     case = W.config_case(args.config)
-    per_tok = 2 * case.num_kv_heads * case.head_size * 2
-    qo = 2 * case.num_q_heads * case.head_size * 2
+    kc, vc, per_tok, qo = oracle_inputs(case)
     order = np.random.default_rng(2).permutation(case.num_seqs)
     K, Wm = args.steps, args.warmup
     # each step decodes a slice of sequences sized so K + W steps take about
     # args.reference_seconds in total
     t = time.perf_counter()
-    oracle.decode(np.ascontiguousarray(case.query[:1]), case.q_dtype, case.k_cache, case.v_cache,
+    oracle.decode(np.ascontiguousarray(case.query[:1]), case.q_dtype, kc, vc,
                   case.cache_dtype, np.ascontiguousarray(case.block_tables[:1]),
                   np.ascontiguousarray(case.context_lens[:1]), case.num_kv_heads,
-                  case.block_size, case.scale)
+                  case.block_size, case.scale, case.k_scale, case.v_scale)
     per_seq = max(1e-4, (time.perf_counter() - t) / max(1, int(case.context_lens[0])) *
                   float(case.context_lens.mean()))
     n = max(1, int(args.reference_seconds / (K + Wm) / per_seq))
@@ -714,10 +771,10 @@ def run_reference(args):
         nonlocal cursor
         idx = np.array([order[(cursor + i) % case.num_seqs] for i in range(n)])
         cursor += n
-        oracle.decode(np.ascontiguousarray(case.query[idx]), case.q_dtype, case.k_cache,
-                      case.v_cache, case.cache_dtype, np.ascontiguousarray(case.block_tables[idx]),
+        oracle.decode(np.ascontiguousarray(case.query[idx]), case.q_dtype, kc, vc,
+                      case.cache_dtype, np.ascontiguousarray(case.block_tables[idx]),
                       np.ascontiguousarray(case.context_lens[idx]), case.num_kv_heads,
-                      case.block_size, case.scale)
+                      case.block_size, case.scale, case.k_scale, case.v_scale)
         return int(case.context_lens[idx].sum()) * per_tok + n * qo
 
     for _ in range(Wm):
@@ -737,7 +794,7 @@ def run_reference(args):
                        "block_size": case.block_size, "kv_dtype": case.cache_dtype},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{n} sequences per step of {case.num_seqs}, "
-                                       f"single-threaded C oracle in fp64"},
+                                       f"single-threaded C oracle in fp64", **host_cpu()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))

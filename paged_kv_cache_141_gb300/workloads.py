@@ -145,6 +145,16 @@ class Case:
         return (2 * self.total_tokens * self.num_kv_heads * self.head_size
                 * ELEM_BYTES[self.cache_dtype])
 
+    def unique_kv_bytes(self) -> int:
+        """K+V bytes of the distinct cache slots the decode reads: a block
+        shared by several sequences' tables counts once (equals kv_bytes()
+        when no block is shared)."""
+        B = self.block_size
+        slots = [self.block_tables[s, np.arange(L) // B].astype(np.int64) * B + np.arange(L) % B
+                 for s, L in enumerate(self.context_lens.astype(np.int64)) if L > 0]
+        n = int(np.unique(np.concatenate(slots)).size) if slots else 0
+        return 2 * n * self.num_kv_heads * self.head_size * ELEM_BYTES[self.cache_dtype]
+
     def qo_bytes(self) -> int:
         return 2 * self.num_seqs * self.num_q_heads * self.head_size * ELEM_BYTES[self.q_dtype]
 

@@ -94,3 +94,20 @@ def test_make_queries_counts_and_determinism():
     assert a.max_queries == int(q.max())
     full = make_queries(c, ("all",))
     assert np.array_equal(full.counts, c.context_lens)
+
+
+def test_unique_kv_bytes_counts_shared_prefix_blocks_once():
+    from paged_kv_cache_141_gb300.workloads import ELEM_BYTES, make_case
+    # no sharing: every context slot is distinct
+    c = make_case(num_seqs=5, num_q_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                  q_dtype="bf16", cache_dtype="bf16", lengths=("uniform", 1, 300), seed=3)
+    assert c.unique_kv_bytes() == c.kv_bytes()
+    # 2 groups of 3 sequences sharing 4 blocks (64 tokens): the prefix counts
+    # once per group, each private suffix once
+    c = make_case(num_seqs=6, num_q_heads=8, num_kv_heads=2, head_size=64, block_size=16,
+                  q_dtype="bf16", cache_dtype="e4m3", lengths=("uniform", 1, 40), seed=4,
+                  shared_prefix=(2, 4))
+    prefix = c.meta["prefix_tokens"]
+    tokens = 2 * prefix + int((c.context_lens.astype(np.int64) - prefix).sum())
+    assert c.unique_kv_bytes() == 2 * tokens * 2 * 64 * ELEM_BYTES["e4m3"]
+    assert c.unique_kv_bytes() < c.kv_bytes()
