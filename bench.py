@@ -374,6 +374,7 @@ def run_ours(args):
                   "note": "each distinct cached token's K/V once (shared prefix blocks count once)"}
 
     graph = run_graph(st, max(20, min(1000, K)), device)
+    write_step = run_write_step(st, device)
     write_bulk = run_write_bulk(st, device)
     e2e = run_e2e(st, max(20, min(200, K // 10)), device)
     cpu = None
@@ -415,6 +416,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "graph": graph,
+        "write_step": write_step,
         "write_bulk": write_bulk,
         "gpu_launches": K * st.launches_per_step,
         "clocks": clocks,
@@ -536,6 +538,47 @@ def run_prefill(args):
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def run_write_step(st: Step, device, per_graph: int = 20, replays: int = 20):
+    """The decode step's own KV write alone (one new token per sequence to
+    its slot, as pa_reshape_and_cache in the separate form): device time per
+    launch, from a CUDA graph of back-to-back launches (a launch from Python
+    costs more host time than this write takes on the GPU), and tokens/s.
+    Rewrites the same tokens, so the pool is unchanged."""
+    import torch
+    c, pk = st.case, st.pk
+
+    def write(stream=None):
+        pk.reshape_and_cache(st.nk, st.nv, st.kc, st.vc, st.ns, c.k_scale, c.v_scale,
+                             st.status, stream)
+
+    write()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per_graph):
+                write(s)
+    torch.cuda.current_stream(device).wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(replays):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (replays * per_graph)
+    return {"tokens": c.num_seqs, "us_per_launch": round(ms * 1e3, 2),
+            "tokens_per_s": round(c.num_seqs / (ms * 1e-3), 1), "bytes": c.write_bytes(),
+            "kernel": "reshape_and_cache_kernel",
+            "timing": f"CUDA graph of {per_graph} launches, replayed {replays} times"}
 
 
 def run_write_bulk(st: Step, device, tokens: int | None = None, steps: int = 50):
