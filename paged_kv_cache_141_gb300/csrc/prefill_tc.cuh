@@ -1171,14 +1171,15 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             float2 sr[R / 2];
 #pragma unroll
             for (int k = 0; k < R / 2; ++k) sr[k] = make_float2(0.f, 0.f);
-            // weights in two halves of 64 keys: each half's P_hi and P_lo go
-            // to TMEM before the next is formed (S is all in registers already)
+            // weights in four quarters of 32 keys: each quarter's P_hi and
+            // P_lo go to TMEM before the next is formed, so few packed words
+            // are live next to the scores not yet used
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t phi[N / 4], plo[N / 4];
+            for (int h = 0; h < 4; ++h) {
+                uint32_t phi[N / 8], plo[N / 8];
 #pragma unroll
-                for (int c = 0; c < N / 2; c += 2) {
-                    const int cc = h * (N / 2) + c;
+                for (int c = 0; c < N / 4; c += 2) {
+                    const int cc = h * (N / 4) + c;
                     const float2 t2 = __ffma2_rn(make_float2(x[cc], x[cc + 1]), qm2, nm2);
                     const float2 e = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
                     sr[(c / 2) % (R / 2)] = __fadd2_rn(sr[(c / 2) % (R / 2)], e);
@@ -1188,8 +1189,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                         plo[c / 2] = pack2<T>(lo.x, lo.y);
                     }
                 }
-                tc_st_n<N / 4>(sbuf + h * (N / 4), phi);
-                if constexpr (kTcPLo<T>) tc_st_n<N / 4>(sbuf + N / 2 + h * (N / 4), plo);
+                tc_st_n<N / 8>(sbuf + h * (N / 8), phi);
+                if constexpr (kTcPLo<T>) tc_st_n<N / 8>(sbuf + N / 2 + h * (N / 8), plo);
             }
 #pragma unroll
             for (int w = R / 4; w >= 1; w /= 2)
