@@ -438,18 +438,59 @@ def prefill_queries(case, kind):
     return ("fixed", np.minimum(8, case.context_lens))
 
 
-def prefill_work(case, qs: np.ndarray):
-    """Algorithmic work of one multi-query step: FLOPs (QK^T and PV over each
-    query token's causal prefix, 4 d per (query head, key)) and bytes (the
-    K/V of every context once, Q read, out written)."""
+def prefill_work(case, qs: np.ndarray, seqs=None):
+    """Algorithmic work of one multi-query step (or of the sequences `seqs`):
+    FLOPs (QK^T and PV over each query token's causal prefix, 4 d per (query
+    head, key)) and bytes (the K/V of every context once, Q read, out
+    written)."""
     counts = np.diff(qs).astype(np.int64)
     L = case.context_lens.astype(np.int64)
+    if seqs is not None:
+        counts, L = counts[seqs], L[seqs]
     # keys seen by the Q_s tokens: sum_{i<Q} (L - Q + i + 1)
     keys = (counts * (L - counts) + counts * (counts + 1) // 2).sum()
     flops = 4 * case.head_size * case.num_q_heads * int(keys)
     eb = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
     qo = 2 * int(counts.sum()) * case.num_q_heads * case.head_size * eb[case.q_dtype]
-    return flops, case.kv_bytes() + qo
+    kv = 2 * int(L.sum()) * case.num_kv_heads * case.head_size * eb[case.cache_dtype]
+    return flops, kv + qo
+
+
+def prefill_cpu_baseline(case, q, tensor: bool, budget_s: float = 12.0):
+    """The oracle's multi-query attention, as it stands, on this host: one
+    sequence at a time in a seeded order until the budget is spent; the rate
+    in the line's unit over the work done."""
+    import oracle
+    kc, vc, _, _ = oracle_inputs(case)
+    qs = q.query_start
+    # a FLOP rate hardly depends on the context length: the shortest contexts
+    # first keep one sequence's oracle time inside the budget; a byte rate
+    # takes a seeded random order
+    order = (np.argsort(case.context_lens, kind="stable") if tensor
+             else np.random.default_rng(3).permutation(case.num_seqs))
+    done, elapsed = [], 0.0
+    for s_ in order:
+        s_ = int(s_)
+        rows = slice(int(qs[s_]), int(qs[s_ + 1]))
+        t = time.perf_counter()
+        oracle.paged_prefill(np.ascontiguousarray(q.query[rows]), case.q_dtype,
+                             np.array([0, int(qs[s_ + 1] - qs[s_])], dtype=np.int32), kc, vc,
+                             case.cache_dtype, np.ascontiguousarray(case.block_tables[s_:s_ + 1]),
+                             np.ascontiguousarray(case.context_lens[s_:s_ + 1]),
+                             case.num_kv_heads, case.block_size, case.scale, case.k_scale,
+                             case.v_scale)
+        elapsed += time.perf_counter() - t
+        done.append(s_)
+        if elapsed >= budget_s:
+            break
+    flops, nbytes = prefill_work(case, qs, np.array(done))
+    value = flops / elapsed / 1e12 if tensor else nbytes / elapsed / 1e9
+    return {"value": round(value, 6), "unit": "TFLOP/s" if tensor else "GB/s", "cores": 1,
+            "kind": "oracle", **host_cpu(),
+            "sample": f"{len(done)} of {case.num_seqs} sequences "
+                      f"({'shortest contexts first, ' if tensor else ''}"
+                      f"{int(np.diff(qs)[done].sum())} query tokens), single-threaded C oracle "
+                      f"in fp64, {elapsed:.1f} s"}
 
 
 def run_prefill(args):
@@ -498,6 +539,37 @@ def run_prefill(args):
     torch.cuda.synchronize()
     clocks = sampler.stop()
     ms = a.elapsed_time(b) / K
+    # end to end through the binding with host buffers: each step copies its
+    # query tokens and lengths in from pinned memory, runs, and reads the
+    # output back (one stream, serial)
+    host_q = torch.empty(query.shape, dtype=query.dtype, pin_memory=True)
+    host_q.copy_(query.cpu())
+    host_qs = torch.from_numpy(q.query_start).pin_memory()
+    host_cl = st.cl.cpu().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+    def e2e_step():
+        query.copy_(host_q, non_blocking=True)
+        qstart.copy_(host_qs, non_blocking=True)
+        st.cl.copy_(host_cl, non_blocking=True)
+        launch()
+        host_out.copy_(out, non_blocking=True)
+
+    ke = max(3, min(K, 10))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    ea = torch.cuda.Event(enable_timing=True)
+    eb_ = torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(ke):
+        e2e_step()
+    eb_.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb_) / ke
+    h2d = host_q.numel() * host_q.element_size() + host_qs.numel() * 4 + host_cl.numel() * 4
+    d2h = host_out.numel() * host_out.element_size()
+
     flops, nbytes = prefill_work(case, q.query_start)
     tflops = flops / (ms * 1e-3) / 1e12
     gbs = nbytes / (ms * 1e-3) / 1e9
@@ -509,6 +581,9 @@ def run_prefill(args):
         peak_tc, tk = 1700.0, "fallback"
     tensor = args.prefill == "chunk512"
     value, unit = (tflops, "TFLOP/s") if tensor else (gbs, "GB/s")
+    e2e_value = (flops / (e2e_ms * 1e-3) / 1e12) if tensor else (nbytes / (e2e_ms * 1e-3) / 1e9)
+    cpu = None if args.no_cpu_baseline else prefill_cpu_baseline(case, q, tensor,
+                                                                   args.cpu_seconds)
     line = {
         "metric": PREFILL_METRIC[args.prefill], "value": round(value, 2), "unit": unit,
         "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
@@ -534,6 +609,10 @@ def run_prefill(args):
                    and case.cache_dtype != "e4m3"
                    else "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)"
                                                      if case.cache_dtype == "e4m3" else "")),
+        "e2e": {"value": round(e2e_value, 2), "unit": unit, "ms_per_step": round(e2e_ms, 5),
+                "steps": ke, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "form": "serial on one stream: query, starts and lengths in, output out"},
+        "cpu_baseline": cpu,
         "gpu_launches": K,
         "clocks": clocks,
     }
