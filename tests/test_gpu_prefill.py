@@ -327,3 +327,23 @@ def test_full_size_llama7b_mha_f16_sampled():
     rows = np.array(sorted(rows))
     want = p.oracle_rows(rows)
     assert_decode_close(got[rows], want, c, "llama-7b mha f16 chunk")
+
+
+def test_full_size_long_context_chunk_sampled():
+    """The long-context pool (8 sequences of 32k..131k tokens): a 512-token
+    chunk at the end of each context, about a thousand key tiles per unit;
+    sampled rows (first, last and random tokens) against the oracle."""
+    c = config_case(4)
+    p = Prefill(c, ("fixed", np.minimum(512, c.context_lens)))
+    got = to_f64(p.run())
+    assert p.dc.status_bits() == 0
+    qs = p.q.query_start
+    rng = np.random.default_rng(31)
+    rows = {int(qs[0]), int(qs[-1]) - 1}
+    L = c.context_lens
+    s = int(np.argmax(L))
+    rows.update({int(qs[s]), int(qs[s + 1]) - 1})
+    rows.update(int(r) for r in rng.integers(0, int(qs[-1]), size=6))
+    rows = np.array(sorted(rows))
+    want = p.oracle_rows(rows)
+    assert_decode_close(got[rows], want, c, "long-context chunk")
