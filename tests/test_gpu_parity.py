@@ -103,6 +103,14 @@ SWEEP = [
     # shapes outside the tensor-TMA kernel (block sizes below 8, 64-byte E4M3
     # rows, 1 KB float32 rows) run the bulk-copy kernel
     ("bf16", "bf16", 32, 8, 128, 4, [1, 100, 511, 512, 513, 1200]),
+    # block sizes that are not powers of two: a multiple of 32 (tensor TMA,
+    # a 32-token stage inside a block) and others (bulk copies); the largest
+    # block size the library accepts
+    ("bf16", "bf16", 32, 8, 128, 96, [1, 95, 96, 97, 400]),
+    ("e4m3", "bf16", 16, 4, 128, 96, [2, 96, 193]),
+    ("f16", "f16", 8, 2, 64, 24, [1, 23, 24, 25, 300]),
+    ("bf16", "bf16", 8, 8, 128, 48, [47, 48, 49, 150]),
+    ("bf16", "bf16", 16, 4, 128, 1024, [1, 1023, 1024, 1025, 2500]),
     ("f16", "f16", 8, 2, 128, 2, [3, 77, 640]),
     ("f32", "f32", 4, 2, 256, 16, [1, 40, 300]),
     ("e4m3", "bf16", 16, 2, 64, 16, [7, 300]),

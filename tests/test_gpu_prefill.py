@@ -119,6 +119,9 @@ SIMT_SWEEP = [
     (3, 8, 2, 128, 1, "bf16", "bf16", ("uniform", 5, 90), ("uniform", 1, 12)),
     (2, 8, 2, 128, 1, "bf16", "e4m3", ("uniform", 20, 150), ("uniform", 1, 9)),
     (2, 8, 2, 256, 16, "f16", "e4m3", ("uniform", 20, 150), ("uniform", 1, 9)),
+    # block sizes that are not powers of two
+    (3, 8, 2, 128, 24, "bf16", "bf16", ("uniform", 20, 200), ("uniform", 1, 12)),
+    (2, 8, 4, 64, 96, "f16", "f16", ("fixed", [95, 250]), ("uniform", 1, 9)),
 ]
 
 # E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory)
