@@ -223,6 +223,25 @@ def test_empty_context_and_empty_batch():
     pk.reshape_and_cache(d.new_key[:0], d.new_value[:0], d.k_cache, d.v_cache, d.new_slots[:0])
 
 
+def test_maximum_number_of_sequences():
+    """65,535 sequences (the most one call takes) of 1..40 tokens: the write,
+    the single pass and the partitioned form (up to two 32-token partitions),
+    all against the oracle."""
+    c = W.make_case(num_seqs=65535, num_q_heads=2, num_kv_heads=1, head_size=64, block_size=16,
+                    q_dtype="bf16", cache_dtype="bf16", lengths=("uniform", 1, 40), seed=91)
+    d = DeviceCase(c)
+    d.write_step()
+    kc, vc = oracle_pool(c)
+    want = oracle_decode(c, kc, vc)
+    d.decode("single")
+    assert d.status_bits() == 0
+    assert_decode_close(to_f64(d.out), want, c, "65535 sequences, single pass")
+    d.out.fill_(float("nan"))
+    d.decode("split", 32)
+    assert d.status_bits() == 0
+    assert_decode_close(to_f64(d.out), want, c, "65535 sequences, 32-token partitions")
+
+
 def test_shared_prefix_matches_copies():
     """Sequences that share prefix blocks by reference decode exactly like
     sequences holding private copies of those blocks."""
