@@ -95,6 +95,8 @@ SWEEP = [
     ("f16", "f16", 16, 1, 128, 256, [1, 255, 256, 257, 600]),
     ("bf16", "bf16", 12, 4, 128, 64, [10, 64, 65, 300]),              # group of 3
     ("bf16", "bf16", 32, 2, 128, 16, [1, 50, 600]),                    # group of 16
+    ("bf16", "bf16", 128, 1, 128, 16, [1, 300, 700]),                  # group of 128
+    ("e4m3", "f16", 128, 2, 64, 16, [3, 257]),                         # group of 64
     ("e4m3", "bf16", 64, 8, 128, 16, [1, 20, 512, 777]),
     ("e4m3", "f16", 8, 2, 64, 16, [5, 48, 160]),
     ("e4m3", "bf16", 8, 8, 256, 8, [9, 130]),
