@@ -110,13 +110,21 @@ struct MmaSmem {
 
 // E4M3 caches run the MMAs in binary16 (every E4M3 value is exact in it):
 // K and V fragments are widened in registers, the query is rounded to f16.
+// The widened values are the codes' values times 2^-8 (see
+// e4m3x2_to_f16x2_scaled); the score and output scales carry the 2^8.
 template <typename CT> struct MathType { using T = CT; };
 template <> struct MathType<e4m3_t> { using T = __half; };
 
-// Two E4M3 codes (low 16 bits of w) -> f16x2, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Two E4M3 codes, in bytes 0 and 2 of t (bytes 1 and 3 zero), to the binary16
+// pair of their values times 2^-8, exactly, in integer operations: the
+// exponent field (bias 7) and 3 mantissa bits moved up 7 places are a binary16
+// exponent (bias 15) and mantissa of the value times 2^-8 (a subnormal code
+// gives the binary16 subnormal of that value), and the sign, moved to bit 14,
+// is carried into bit 15 by adding it to itself. The saturating write never
+// stores the NaN codes 0x7f / 0xff.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t t) {
+    const uint32_t x = t << 7;
+    return x + (x & 0x40004000u);
 }
 
 // CTAs per SM the registers must allow: 4 at head size <= 128 (shared memory
@@ -285,7 +293,8 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};    // heads 2*t4 and 2*t4+1
     float l_run[2] = {0.f, 0.f};                // this lane's share of the sums
-    const float qk_mul = p.q_mul;               // scale * log2(e)
+    // scale * log2(e) (E4M3: k_scale too, and the 2^8 of the widened codes)
+    const float qk_mul = kFp8 ? p.q_mul * 256.f : p.q_mul;
 
     // ldmatrix row addresses: lane -> (matrix mi, row r)
     const int mi = lane >> 3, r8 = lane & 7;
@@ -326,9 +335,11 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                     ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
 #pragma unroll
                     for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint32_t a[4] = {e4m3x2_to_f16x2(x[2 * h2]), e4m3x2_to_f16x2(x[2 * h2 + 1]),
-                                               e4m3x2_to_f16x2(x[2 * h2] >> 16),
-                                               e4m3x2_to_f16x2(x[2 * h2 + 1] >> 16)};
+                        const uint32_t a[4] = {
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4342)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4342))};
                         Ops::mma(sc[mt], a, qb[2 * kp + h2][0], qb[2 * kp + h2][1]);
                     }
                 }
@@ -424,10 +435,10 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
                     const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
-                    const uint32_t a[4] = {e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0020)),
-                                           e4m3x2_to_f16x2(__byte_perm(lo, 0, 0x0031)),
-                                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0020)),
-                                           e4m3x2_to_f16x2(__byte_perm(hi, 0, 0x0031))};
+                    const uint32_t a[4] = {e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4240)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4341)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4240)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4341))};
                     Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
                 }
             }
@@ -499,7 +510,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             W = fmaf(f, cl[w * 8 + h], W);
             O = fmaf(f, co[(w * 8 + h) * D + e], O);
         }
-        const float val = __fdiv_rn(O, W) * p.v_mul;
+        const float val = __fdiv_rn(O, W) * (kFp8 ? p.v_mul * 256.f : p.v_mul);
         const int hq = hq0 + h;
         if constexpr (kSplit) {
             const size_t row = ((size_t)s * p.num_q_heads + hq) * p.max_parts + blockIdx.x;

@@ -237,10 +237,17 @@ __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Two E4M3 codes (low 16 bits) -> two binary16 values, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_bits_to_f16x2(uint32_t w) {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Two E4M3 codes, in bytes 0 and 2 of t (bytes 1 and 3 zero), to the binary16
+// pair of their values times 2^-8, exactly, in integer operations: E4M3's
+// exponent field (bias 7) and 3 mantissa bits moved up 7 places become a
+// binary16 exponent (bias 15) and mantissa of the same value times 2^-8, an
+// E4M3 subnormal becomes the binary16 subnormal of that value, and the sign
+// (moved to bit 14) is carried into bit 15 by adding it to itself. The 2^8 is
+// folded into the score and output scales. (Codes 0x7f/0xff, NaN, are never
+// stored by the saturating write.)
+__device__ __forceinline__ uint32_t e4m3x2_spread_to_f16x2_scaled(uint32_t t) {
+    const uint32_t x = t << 7;
+    return x + (x & 0x40004000u);
 }
 
 // max(a, b, c) in one instruction (three-input max.f32).
@@ -466,8 +473,8 @@ __device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const C
             uint32_t h[8];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                h[2 * e] = e4m3x2_bits_to_f16x2(ws[e] & 0xffffu);
-                h[2 * e + 1] = e4m3x2_bits_to_f16x2(ws[e] >> 16);
+                h[2 * e] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4140));
+                h[2 * e + 1] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4342));
             }
             *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
             *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
@@ -1361,6 +1368,9 @@ template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
     tp.p = p;
+    // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled)
+    tp.p.q_mul *= 256.f;
+    tp.p.v_mul *= 256.f;
     constexpr int n = TcShape<128, true>::N;
     static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
     tp.box_rows = p.block_size < n ? p.block_size : n;
