@@ -206,6 +206,33 @@ def test_length_one_returns_v_exactly(cache, mode):
             assert np.array_equal(got[s, h].view(np.uint8), c.new_value[s, h // G].view(np.uint8))
 
 
+def _e4m3_token_values(d, c):
+    """Each sequence's only stored V token: its E4M3 codes decoded by torch's
+    float8_e4m3fn, times v_scale in float32, rounded to the output type."""
+    B = c.block_size
+    slots = torch.from_numpy(c.new_slots)
+    codes = d.v_cache.cpu()[slots // B, :, slots % B, :]            # [S, Hkv, d] uint8
+    vals = codes.view(torch.float8_e4m3fn).float() * torch.tensor(c.v_scale, dtype=torch.float32)
+    return vals.to(TORCH[c.q_dtype])
+
+
+@pytest.mark.parametrize("mode", ["single", "split"])
+def test_length_one_e4m3_returns_v_exactly(mode):
+    """One key per sequence: the weight is exactly 1, so the output is the
+    stored code's value times v_scale, rounded once -- bit for bit. Pins the
+    in-register widening of the codes (sign, exponent, subnormals) and the
+    scale it folds in."""
+    c = small_case("e4m3", "bf16", 8, 2, 128, 16, [1, 1, 1, 1])
+    d = DeviceCase(c)
+    d.write_step()
+    out = d.decode(mode, 512).cpu()
+    assert d.status_bits() == 0
+    want = _e4m3_token_values(d, c)
+    G = c.group
+    for h in range(c.num_q_heads):
+        assert torch.equal(out[:, h].view(torch.int16), want[:, h // G].view(torch.int16))
+
+
 def test_empty_context_and_empty_batch():
     c = small_case("bf16", "bf16", 4, 2, 128, 16, [0, 7])
     d = DeviceCase(c)

@@ -149,6 +149,26 @@ def test_prefill_cuda_core_sweep(i):
     check(c, ql, f"simt sweep {i}")
 
 
+def test_length_one_e4m3_tensor_core_returns_v_exactly():
+    """E4M3 cache, one key and one query per sequence, on the tensor-core
+    path: the output is the stored code's value times v_scale, rounded once
+    -- pins the producer's widening of the tiles and the folded scale."""
+    c = make_case(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                  q_dtype="bf16", cache_dtype="e4m3", kv_dtype="bf16", lengths=("fixed", [1] * 4),
+                  seed=977)
+    p = Prefill(c, ("fixed", [1] * 4))
+    out = p.run().cpu()
+    assert p.dc.status_bits() == 0
+    B = c.block_size
+    slots = torch.from_numpy(c.new_slots)
+    codes = p.dc.v_cache.cpu()[slots // B, :, slots % B, :]
+    want = (codes.view(torch.float8_e4m3fn).float()
+            * torch.tensor(c.v_scale, dtype=torch.float32)).to(torch.bfloat16)
+    G = c.group
+    for h in range(c.num_q_heads):
+        assert torch.equal(out[:, h].view(torch.int16), want[:, h // G].view(torch.int16))
+
+
 def test_one_query_per_sequence_is_the_decode():
     c = make_case(num_seqs=16, num_q_heads=32, num_kv_heads=8, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="bf16", lengths=("uniform", 1, 900), seed=971)
