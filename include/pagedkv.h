@@ -328,10 +328,11 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  max_queries_per_seq  an upper bound on Q_s known on the host (sizes the
  *                 grid); 0 <= Q_s <= max_queries_per_seq and Q_s <= L_s.
  *  Other arguments as pa_decode; scale must be > 0.
- *  A 16-bit query with a cache of the same type, head_size 64/128/256, a
- *  block_size that is a power of two in [8, 256] and a group of at most 128
- *  heads runs on the tensor cores (tcgen05); other supported combinations run
- *  one query token per work unit on the CUDA cores. A sequence whose lengths
+ *  A 16-bit query with a cache of the same type (head_size 64/128/256) or an
+ *  E4M3 cache (head_size 64/128), a block_size that is a power of two in
+ *  [8, 256] and a group of at most 128 heads runs on the tensor cores
+ *  (tcgen05); other supported combinations run one query token per work unit
+ *  on the CUDA cores. A sequence whose lengths
  *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
  *  num_queries == 0 launches nothing.
  */
