@@ -68,12 +68,22 @@ constexpr int kTcThreads = 11 * 32;           // softmax, K loads, MMA, V loads
 constexpr int kTcKWarp = 8;
 constexpr int kTcMmaWarp = 9;
 constexpr int kTcVWarp = 10;
+// E4M3 caches: 16 warps, the tiles widened by two warps per operand (K: warps
+// 8 and 11, V: warps 10 and 13, one per SM sub-partition), registers moved
+// from the producer warpgroups (2 and 3) to the softmax ones (0 and 1)
+constexpr int kTcThreadsFp8 = 16 * 32;
+constexpr int kTcK2Warp = 11;
+constexpr int kTcV2Warp = 13;
+constexpr int kTcSoftmaxRegs = 168;                 // 2 x 128 x 168 + 2 x 128 x 88 = 512 x 128
+constexpr int kTcProducerRegs = 88;
+static_assert(2 * 128 * kTcSoftmaxRegs + 2 * 128 * kTcProducerRegs <= kTcThreadsFp8 * 128,
+              "register split within the launch's allocation");
 constexpr float kTcRescaleLog2 = 8.0f;        // lazy rescale threshold (base 2)
 constexpr int kTcSmemLimit = 227 * 1024;
 
 // kFp8: E4M3 caches. Their tiles land row-major (D bytes per key) in two
-// staging slots per K and V, and the producer warp widens them to binary16
-// in the 16-bit rings the MMAs read.
+// staging slots per K and V, and two producer warps per operand widen them to
+// binary16 in the 16-bit rings the MMAs read.
 template <int D, bool kFp8 = false>
 struct TcShape {
     static constexpr int N = D == 256 ? 64 : 128;            // keys per tile
@@ -91,8 +101,8 @@ struct TcShape {
     static constexpr int kV8Off = kK8Off + 2 * kStage8Bytes;
     static constexpr int kBarOff = kV8Off + 2 * kStage8Bytes;
     // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
-    // q_ready, then (E4M3) k_staged[2] v_staged[2]
-    static constexpr int kNumBars = 4 * NS + 6 + (kFp8 ? 4 : 0);
+    // q_ready, then (E4M3) k_staged[2] v_staged[2] k_sfree[2] v_sfree[2]
+    static constexpr int kNumBars = 4 * NS + 6 + (kFp8 ? 8 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
     static constexpr int kBytes = kLsumOff + kTcSoftmaxThreads * 4;
@@ -401,34 +411,37 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
 }
 
-// E4M3 K (or V) tiles, by a whole warp: each tile lands row-major in one of
-// two staging slots (one plain TMA box per block segment), then the warp
-// widens it to binary16 into the ring slot the MMAs read -- 16 codes per
-// lane and step, the 128-byte swizzled K-major layout -- orders its writes
-// for the tensor cores (fence.proxy.async) and arrives on the slot's `full`
-// barrier. A slot is refilled once `empty` says its MMAs are done; staging
-// slot j % 2 is reloaded (tile j + 2) as soon as tile j is widened, with
-// that tile's block-table entries read one tile earlier.
+// E4M3 K (or V) tiles, widened by two warps: each tile lands row-major in one
+// of two staging slots (one plain TMA box per block segment), and warp `half`
+// widens rows [half * N/2, (half + 1) * N/2) of it to binary16 into the ring
+// slot the MMAs read -- 16 codes per lane and step, the 128-byte swizzled
+// K-major layout -- then orders its writes for the tensor cores
+// (fence.proxy.async). Warp 0 also reads the block table (a tile ahead) and
+// issues the copies; both wait for a tile's copy (`staged`) and for its ring
+// slot (`empty`), and each arrives on `full` (count 2) and on `sfree`
+// (count 2) once it has read its rows, after which warp 0 refills that
+// staging slot with the tile two ahead.
 template <typename Sh>
-__device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const CUtensorMap* map,
-                                              uint8_t* staging, uint8_t* ring, uint64_t* staged,
-                                              uint64_t* full, uint64_t* empty, int s, int hk,
-                                              int ntiles, int kend, int lane,
-                                              volatile int* abort_flag) {
+__device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const CUtensorMap* map,
+                                               uint8_t* staging, uint8_t* ring, uint64_t* staged,
+                                               uint64_t* sfree, uint64_t* full, uint64_t* empty,
+                                               int s, int hk, int ntiles, int kend, int half,
+                                               int lane, volatile int* abort_flag) {
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
     constexpr int D = Sh::kKvBytes / (2 * N);                // head size
     constexpr int kRow8 = D;                                 // bytes of an E4M3 row
-    constexpr int kChunks = N * kRow8 / 16;                  // 16-code chunks per tile
+    constexpr int kHalfChunks = N * kRow8 / 16 / 2;          // 16-code chunks per warp and tile
     constexpr int64_t kNone = -1;
     const PrefillParams& p = tp.p;
     const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
     const int rows = tp.box_rows;
     const int B = p.block_size;
     const int r0 = lane * rows;
+    const bool issuer = half == 0;
     auto fetch = [&](int j) -> int64_t {
         const int key = j * N + r0;
-        if (j < ntiles && r0 < N && key < kend) return (int64_t)table[key / B];
+        if (issuer && j < ntiles && r0 < N && key < kend) return (int64_t)table[key / B];
         return kNone;
     };
     auto issue = [&](int j, int64_t blk) {
@@ -444,11 +457,15 @@ __device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const C
             tma_load_2d(staging + (j & 1) * Sh::kStage8Bytes + r0 * kRow8, map, 0, y, &staged[j & 1]);
         }
     };
-    issue(0, fetch(0));
-    int64_t next = fetch(1);
-    if (ntiles > 1) issue(1, next);
-    next = fetch(2);
-    int issued = ntiles > 1 ? 2 : 1;
+    int issued = 0;
+    int64_t next = kNone;
+    if (issuer) {
+        issue(0, fetch(0));
+        next = fetch(1);
+        if (ntiles > 1) issue(1, next);
+        next = fetch(2);
+        issued = ntiles > 1 ? 2 : 1;
+    }
     bool live = true;
     for (int j = 0; j < ntiles && live; ++j) {
         const int64_t after = fetch(j + 3);                  // in flight while tile j is widened
@@ -465,8 +482,8 @@ __device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const C
         const uint8_t* src = staging + (j & 1) * Sh::kStage8Bytes;
         uint8_t* dst = ring + (j % NS) * Sh::kKvBytes;
 #pragma unroll 4
-        for (int k = 0; k < kChunks / 32; ++k) {
-            const int q = lane + 32 * k;
+        for (int k = 0; k < kHalfChunks / 32; ++k) {
+            const int q = half * kHalfChunks + lane + 32 * k;
             const int r = q / (kRow8 / 16), c = q - r * (kRow8 / 16);
             const uint4 w = *reinterpret_cast<const uint4*>(src + r * kRow8 + c * 16);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -481,21 +498,31 @@ __device__ __forceinline__ void tc_load_widen(const TcPrefillParams& tp, const C
         }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&full[j % NS]);
-        if (j + 2 < ntiles) {
-            issue(j + 2, next);                              // staging slot j % 2 is free again
+        if (lane == 0) {
+            mbar_arrive(&full[j % NS]);
+            mbar_arrive(&sfree[j & 1]);                      // this warp is done with staging j
+        }
+        if (issuer && j + 2 < ntiles) {
+            // staging slot j % 2 is free once both warps have read tile j
+            bool ok2 = true;
+            if (lane == 0) ok2 = tc_wait(&sfree[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
+            if (!__shfl_sync(0xffffffffu, ok2, 0)) {
+                live = false;
+                break;
+            }
+            issue(j + 2, next);
             issued = j + 3;
         }
         next = after;
     }
     // copies still in flight (only after an abort) land before the CTA ends
-    if (lane == 0)
+    if (issuer && lane == 0)
         for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
             mbar_wait_bounded(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
 }
 
 template <typename QT, typename CT, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp8 : kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     using MT = typename TcMath<QT, CT>::T;                  // MMA operand type
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
@@ -518,6 +545,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* q_ready = drain + 1;
     uint64_t* k_staged = q_ready + 1;                        // E4M3: [2]
     uint64_t* v_staged = k_staged + 2;                       // E4M3: [2]
+    uint64_t* k_sfree = v_staged + 2;                        // E4M3: [2]
+    uint64_t* v_sfree = k_sfree + 2;                         // E4M3: [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -557,9 +586,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     // the softmax warps load the query tile (the MMA issuer waits for it)
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&k_full[i], 1);
+            mbar_init(&k_full[i], kFp8 ? 2 : 1);             // E4M3: two widening warps
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], 1);
+            mbar_init(&v_full[i], kFp8 ? 2 : 1);
             mbar_init(&v_empty[i], 1);
         }
         mbar_init(&s_full[0], 1);
@@ -572,6 +601,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             for (int i = 0; i < 2; ++i) {
                 mbar_init(&k_staged[i], 1);
                 mbar_init(&v_staged[i], 1);
+                mbar_init(&k_sfree[i], 2);
+                mbar_init(&v_sfree[i], 2);
             }
         }
         *abort_flag = 0;
@@ -630,19 +661,26 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     }
 
 
-    if (warp == kTcKWarp) {
+    if (warp >= kTcSoftmaxThreads / 32) {
+    // producer warpgroup(s); E4M3: they give up registers to the softmax
+    // warpgroups (every warp of a warpgroup runs the same instruction, before
+    // the warps part ways)
+    if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcProducerRegs));
+    if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
         // ------------------------------------------------------------ K loads
         if constexpr (kFp8)
-            tc_load_widen<Sh>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_full,
-                              k_empty, s, hk, ntiles, kend, lane, abort_flag);
+            tc_load_widen2<Sh>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_sfree,
+                               k_full, k_empty, s, hk, ntiles, kend, warp == kTcKWarp ? 0 : 1,
+                               lane, abort_flag);
         else
             tc_load_ring<Sh, NS>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
                                  kend, lane, first, abort_flag);
-    } else if (warp == kTcVWarp) {
+    } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
         // ------------------------------------------------------------ V loads
         if constexpr (kFp8)
-            tc_load_widen<Sh>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_full,
-                              v_empty, s, hk, ntiles, kend, lane, abort_flag);
+            tc_load_widen2<Sh>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_sfree,
+                               v_full, v_empty, s, hk, ntiles, kend, warp == kTcVWarp ? 0 : 1,
+                               lane, abort_flag);
         else
             tc_load_ring<Sh, NS>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
                                  kend, lane, first, abort_flag);
@@ -703,8 +741,10 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             tc_commit(drain);
             mbar_wait_bounded(drain, 0, p.status);
         }
+    }
     } else {
         // ------------------------------------------------------------ softmax (rows)
+        if constexpr (kFp8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcSoftmaxRegs));
         // Thread t: row r = t mod 128 (its warp's TMEM lane quarter), half
         // hf = t / 128 of the key columns. Both halves read the whole row to
         // take the same max, so they make the same rescale decision; each
@@ -1388,7 +1428,7 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
         const long long units = (long long)p.num_seqs * p.num_kv_heads * p.q_tiles;
         if (units <= 0) return cudaSuccess;
         if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
-        kern<<<(unsigned)units, kTcThreads, Sh::kAlloc, stream>>>(tp);
+        kern<<<(unsigned)units, kTcThreadsFp8, Sh::kAlloc, stream>>>(tp);
         return cudaGetLastError();
     };
     switch (head_size) {
