@@ -493,6 +493,18 @@ def prefill_cpu_baseline(case, q, tensor: bool, budget_s: float = 12.0):
                       f"in fp64, {elapsed:.1f} s"}
 
 
+def prefill_kernel_name(case, max_queries: int) -> str:
+    """The kernel pa_paged_prefill selects for this workload (the rule
+    documented with it in pagedkv.h)."""
+    e4m3 = case.cache_dtype == "e4m3"
+    if max_queries * case.group <= 16:
+        return "paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows" + (
+            ", E4M3 widened in registers)" if e4m3 else ")")
+    if case.head_size <= 128 and max_queries > 128 // case.group and not e4m3:
+        return "paged_prefill_tc2_kernel (two query tiles per CTA)"
+    return "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else "")
+
+
 def run_prefill(args):
     """Multi-query paged attention (pa_paged_prefill) on the Llama-3-8B GQA
     pool: the kernel alone, K timed launches, CUDA events, clocks sampled."""
@@ -628,11 +640,7 @@ def run_prefill(args):
                      {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                       "frac": round(gbs / peak_hbm, 4), "traffic": None,
                       "peak_kind": f"{hk} HBM copy"}),
-        "kernel": ("paged_prefill_tc2_kernel (two query tiles per CTA)"
-                   if case.head_size <= 128 and q.max_queries > 128 // case.group
-                   and case.cache_dtype != "e4m3"
-                   else "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)"
-                                                     if case.cache_dtype == "e4m3" else "")),
+        "kernel": prefill_kernel_name(case, q.max_queries),
         "e2e": {"value": round(e2e_value, 2), "unit": unit, "ms_per_step": round(e2e_ms, 5),
                 "steps": ke, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipelined": "inputs of step i+1 copied in and output of step i-1 copied "

@@ -328,10 +328,16 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  max_queries_per_seq  an upper bound on Q_s known on the host (sizes the
  *                 grid); 0 <= Q_s <= max_queries_per_seq and Q_s <= L_s.
  *  Other arguments as pa_decode; scale must be > 0.
- *  A 16-bit query with a cache of the same type (head_size 64/128/256) or an
+ *  Kernel selection, by the arguments alone: with max_queries_per_seq *
+ *  (num_q_heads / num_kv_heads) <= 16 query rows per sequence and KV head, a
+ *  16-bit query with a cache of the same type or an E4M3 cache, on the shapes
+ *  of the TMA decode (rows of 128, 256 or 512 bytes, block_size 8, 16 or a
+ *  multiple of 32), runs the warp-level MMA kernel that reads each
+ *  sequence's K/V once for all its rows (speculative verification). Else a
+ *  16-bit query with a cache of the same type (head_size 64/128/256) or an
  *  E4M3 cache (head_size 64/128), a block_size that is a power of two in
- *  [8, 256] and a group of at most 128 heads runs on the tensor cores
- *  (tcgen05); other supported combinations run one query token per work unit
+ *  [8, 256] and a group of at most 128 heads runs on the tcgen05 tensor
+ *  cores; other supported combinations run one query token per work unit
  *  on the CUDA cores. A sequence whose lengths
  *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
  *  num_queries == 0 launches nothing.

@@ -226,6 +226,18 @@ void bind_fused_write(DecodeParams& p, const void* key, const void* value,
     p.v_scale_w = v_scale;
 }
 
+// The warp-level MMA multi-query kernel (a few query rows per sequence and KV
+// head): 16-bit query and a cache of the same type or of E4M3 codes, on the
+// shapes of the TMA decode.
+constexpr long long kPrefillMmaMaxRows = 16;
+
+bool prefill_mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, int block_size,
+                          int64_t num_blocks, int num_kv_heads) {
+    if (!(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
+    if (!(cache_dtype == q_dtype || cache_dtype == PA_FP8_E4M3)) return false;
+    return tma_eligible(head_size, cache_dtype, block_size, num_blocks, num_kv_heads);
+}
+
 // The tcgen05 multi-query kernel: 16-bit query and a cache of the same type
 // or of E4M3 codes (head size 64 or 128), whole 128-byte column spans, block sizes that are powers of two in [8, 256] (every
 // TMA box then starts on a swizzle-atom boundary), groups that fit the
@@ -535,6 +547,20 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     if (!out || !query_start || max_queries_per_seq == 0) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned(query_start, 4)) return PA_ERR_INVALID_ARG;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    p.out = out;
+    p.query_start = query_start;
+    p.num_queries = num_queries;
+    p.max_queries = max_queries_per_seq;
+    if ((long long)max_queries_per_seq * p.group <= kPrefillMmaMaxRows &&
+        prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks,
+                             num_kv_heads)) {
+        // one pass over each sequence's K/V for all of its query rows
+        if (cache_dtype == PA_FP8_E4M3)
+            return from_cuda(q_dtype == PA_F16 ? launch_prefill_mma_f16_e4m3(p, head_size, s)
+                                               : launch_prefill_mma_bf16_e4m3(p, head_size, s));
+        return from_cuda(q_dtype == PA_F16 ? launch_prefill_mma_f16(p, head_size, s)
+                                           : launch_prefill_mma_bf16(p, head_size, s));
+    }
     if (prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, p.group, num_blocks,
                             num_kv_heads, out, query, k_cache, v_cache)) {
         PrefillParams pp{};
@@ -568,9 +594,6 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     }
     // CUDA cores: one query token per work unit, the decode kernel over the
     // token's causal prefix
-    p.out = out;
-    p.query_start = query_start;
-    p.num_queries = num_queries;
     return from_cuda(run_simt_decode_kernel(p, head_size, q_dtype, cache_dtype, s));
 }
 

@@ -48,6 +48,7 @@ struct DecodeParams {
     // query_start[s]) + 1 keys. Single pass only, no fused write.
     const int32_t* query_start;   // [S + 1]
     int num_queries;              // rows of query / out
+    int max_queries;              // max over s of Q_s (sizes the tensor-core multi-query grid)
 };
 
 // Generic CUDA-core decode; one launcher per (query type, cache type).
@@ -87,6 +88,15 @@ cudaError_t launch_decode_mma_f16_e4m3(const DecodeParams& p, int head_size, int
                                        bool split, cudaStream_t stream);
 cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
                                         bool split, cudaStream_t stream);
+
+// Multi-query paged attention for a few query rows per (sequence, KV head)
+// (max_queries * group <= 16) on warp-level MMA: 16-bit query with a cache of
+// the same type (head_size 64/128/256) or E4M3 (128/256), TMA-eligible shapes.
+// Uses the multi-query fields of DecodeParams; single pass.
+cudaError_t launch_prefill_mma_f16(const DecodeParams& p, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_mma_bf16(const DecodeParams& p, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_mma_f16_e4m3(const DecodeParams& p, int head_size, cudaStream_t stream);
+cudaError_t launch_prefill_mma_bf16_e4m3(const DecodeParams& p, int head_size, cudaStream_t stream);
 
 // Multi-query paged attention on the tensor cores (tcgen05): 16-bit query and
 // cache of the same type (head_size in {64, 128, 256}) or E4M3 (64, 128),

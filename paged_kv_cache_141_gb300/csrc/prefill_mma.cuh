@@ -1,0 +1,536 @@
+// prefill_mma.cuh -- multi-query paged attention for a few query tokens per
+// sequence (a speculative verification step) on warp-level tensor-core MMA.
+//
+// Work unit: a sequence s, a KV head hk and 8 NT of the sequence's R = Q_s G
+// query rows, token-major (row r is query token r / G and query head
+// hk G + r % G, as in the tcgen05 kernel), cut into NT n-tiles of 8 rows.
+// Query token i sits at position L - Q_s + i and sees keys 0..L - Q_s + i
+// ("Lecture 3: PagedAttention and vLLM", "the paged implementation of
+// attention"; the queries there carry a num_queries axis).
+//
+// The kernel is the tensor-core decode (decode_mma.cuh) with the MMA's eight
+// columns holding query rows instead of the query heads of one token. The
+// producer warp loads each 32-key stage of K and V once per CTA (tensor TMA,
+// 128-byte swizzle). Consumer warp w (of 4) owns n-tile w mod NT; the NT
+// warps of different n-tiles all read every stage, the 4 / NT warps of one
+// n-tile take alternate stages and are merged at the end as in the decode.
+// Per warp and
+// 16-key row tile: S^T (16 keys x 8 rows) = K Q^T, each column masked at its
+// row's causal limit, an online softmax per row (base 2), O^T += V^T P^T with
+// P as two 16-bit terms (one binary16 term for E4M3 caches).
+//
+// Why a second multi-query kernel: for the 16 or fewer rows of a short
+// verification step a 128-row tcgen05 tile is mostly padding, and its one CTA
+// per SM leaves the SM idle while a unit starts and drains. Here one CTA
+// streams its sequence's K/V once for all its rows at up to twice the
+// decode's MMA work per byte, with 3 (16-bit) to 4 (E4M3) CTAs per SM
+// overlapping one another's starts and ends. (Four n-tiles, 32 rows, are
+// slower than the tcgen05 kernel: four warps' MMA and softmax work per stage
+// leave the warps latency-bound below the HBM rate.)
+//
+// Keys past a stage's last needed key are masked by a select on the scores
+// (never a multiply) and their V^T fragments are zeroed in registers, so stale
+// or poisoned shared memory never reaches an output (0 x NaN). Every wait is
+// bounded (PA_DEV_TIMEOUT).
+#pragma once
+
+#include "decode_mma.cuh"
+
+namespace pagedkv {
+
+// Rows of one CTA: 8 NT, NT = 1 or 2.
+constexpr int kMqMaxTiles = 2;
+// A column's reference max moves only when a score exceeds it by more than
+// this (base 2): weights stay below 2^8.
+constexpr float kMqRescaleLog2 = 8.0f;
+
+// CTAs per SM the registers must allow (shared memory allows 3 for 16-bit
+// caches at head size <= 128, more for E4M3).
+template <int D>
+constexpr int mq_min_blocks() {
+    return D <= 128 ? 4 : 2;
+}
+
+template <typename QT, typename CT, int D, int NT>
+__global__ void __launch_bounds__(kTmaThreads, mq_min_blocks<D>())
+paged_prefill_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
+    constexpr int CW = kTmaConsumerWarps;                // consumer warps; warp CW loads
+    using S = TmaShape<CT, D>;
+    using Smem = MmaSmem<CT, D>;
+    using MT = typename MathType<CT>::T;
+    using Ops = MmaOps<MT>;
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    constexpr int NST = Smem::kNst;
+    constexpr int WPT = CW / NT;                         // warps per n-tile
+    static_assert(NT == 1 || NT == kMqMaxTiles, "n-tiles per CTA");
+    // a slot's successive stages belong to the same warps, so a warp waiting
+    // on a slot is never two phases ahead of it
+    static_assert(NST % WPT == 0, "slot ownership");
+    constexpr int KS = D / 16;                           // k-steps of the score product
+    const DecodeParams& p = tp.p;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
+    uint64_t* empty = full + NST;
+
+    const int s = blockIdx.z;
+    const int kvh = blockIdx.y;
+    const int row0 = blockIdx.x * 8 * NT;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2;                             // fragment row / B column
+    const int t4 = lane & 3;                             // fragment column pair
+
+    const int q0 = __ldg(p.query_start + s);
+    const int Q = __ldg(p.query_start + s + 1) - q0;
+    const int L = __ldg(p.context_lens + s);
+    {
+        int cap = p.max_context_len;
+        const long long tab = (long long)p.max_blocks * p.block_size;
+        if (tab < cap) cap = (int)tab;
+        if (Q < 0 || Q > p.max_queries || L < Q || L > cap) {
+            if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0 && p.status)
+                atomicOr(p.status, PA_DEV_BAD_LEN);
+            return;
+        }
+    }
+    const int G = p.group;
+    const int R = Q * G;
+    if (row0 >= R) return;
+    // keys seen by the CTA's last row; every other row sees a prefix of them
+    const int Tend = L - Q + (min(R, row0 + 8 * NT) - 1) / G + 1;
+    const int n_st = (Tend + kTmaStageTokens - 1) / kTmaStageTokens;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NT);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == CW) {
+        // ------------------------------------------------------------ producer
+        const int B = p.block_size;
+        const int rows = tp.box_rows;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+        if (lane == 0) {
+            tma_prefetch_map(&tp.k_map);
+            tma_prefetch_map(&tp.v_map);
+        }
+        int issued = 0;
+        for (int k = 0; k < n_st; ++k) {
+            const int slot = k % NST;
+            if (k >= NST) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int t_lo = k * kTmaStageTokens;
+            const int t_hi = min(t_lo + kTmaStageTokens, Tend);
+            const int j0 = t_lo / B;
+            const int nseg = (t_hi - 1) / B - j0 + 1;
+            uint32_t bytes = 0;
+            int y = 0, r0 = 0;
+            if (lane < nseg) {
+                const int j = j0 + lane;
+                const int pb = table[j];
+                if (pb < 0 || (int64_t)pb >= p.num_blocks) {
+                    if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+                } else {
+                    const int off = (B >= kTmaStageTokens) ? (t_lo - j * B) : 0;
+                    y = (pb * p.num_kv_heads + kvh) * B + off;
+                    r0 = (B >= kTmaStageTokens) ? 0 : j * B - t_lo;
+                    bytes = (uint32_t)(rows * S::kRowBytes);
+                }
+            }
+            uint32_t total = bytes;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * total);
+            __syncwarp();
+            if (bytes) {
+                uint8_t* st = ring + (size_t)slot * S::kStageBytes;
+#pragma unroll
+                for (int sp = 0; sp < S::kSpans; ++sp) {
+                    const int x = sp * (128 / S::kElem);
+                    uint8_t* kd = st + sp * S::kSpanTileBytes + r0 * 128;
+                    tma_load_2d(kd, &tp.k_map, x, y, &full[slot]);
+                    tma_load_2d(kd + S::kTileBytes, &tp.v_map, x, y, &full[slot]);
+                }
+            }
+            issued = k + 1;
+        }
+        if (lane == 0) {
+            for (int k = max(0, issued - NST); k < issued; ++k)
+                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int nt = warp % NT;                            // this warp's n-tile
+    const int rw = row0 + 8 * nt;                        // its first row
+    // Q^T fragments (B operand of S = K Q^T): column g = row rw + g, zero past
+    // the sequence's rows. For E4M3 the k index of a 16-wide step maps to d as
+    // the widened ldmatrix bytes come (decode_mma.cuh): k = 2t+j <-> d = 4t+j,
+    // k = 2t+8+j <-> d = 4t+2+j, for K and Q alike.
+    uint32_t qb[KS][2];
+    {
+        const int r = rw + g;
+        const bool valid = r < R;
+        const int i = valid ? r / G : 0;
+        const QT* qp = reinterpret_cast<const QT*>(p.query) +
+                       ((size_t)(q0 + i) * p.num_q_heads + (size_t)kvh * G + (valid ? r - i * G : 0)) * D;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (!valid) {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            } else if constexpr (kFp8) {
+                const QT* q4 = qp + 16 * ks + 4 * t4;
+                qb[ks][0] = Ops::pack(to_float(q4[0]), to_float(q4[1]));
+                qb[ks][1] = Ops::pack(to_float(q4[2]), to_float(q4[3]));
+            } else {
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t4);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 2 * t4 + 8);
+            }
+        }
+    }
+    // causal limits of this lane's two columns (rows rw + 2 t4 + j): keys
+    // < kend. Padding columns (zero queries, never written) take every key
+    // of the CTA, so that their running max is finite like the others'.
+    int kend[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int r = rw + 2 * t4 + j;
+        kend[j] = r < R ? L - Q + r / G + 1 : Tend;
+    }
+    // below this key no column of the warp is masked (rows are token-major,
+    // so the warp's first row has the smallest limit)
+    const int kfree = rw < R ? L - Q + rw / G + 1 : Tend;
+    float acc[KS][4];                                    // O^T fragments: rows d, columns rows
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    // per column: the reference max m (base 2) the weights and O are taken
+    // against, and this lane's share of the sum of weights. m moves (and O is
+    // rescaled) only when a score exceeds it by more than 2^8, so weights
+    // stay below 2^8 and most stages need no cross-lane max.
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    const float qk_mul = kFp8 ? p.q_mul * 256.f : p.q_mul;
+    const int mi = lane >> 3, r8 = lane & 7;             // ldmatrix: lane -> (matrix, row)
+
+    for (int k = warp / NT; k < n_st; k += WPT) {
+        const int slot = k % NST;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
+        if (!ok) break;
+        const uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
+        const uint8_t* Vst = Kst + S::kTileBytes;
+        const int key0 = k * kTmaStageTokens;
+        const int nvalid = min(kTmaStageTokens, Tend - key0);
+
+        // ---- S = K Q^T for both 16-key row tiles, even and odd k-steps in
+        // separate accumulators (four independent MMA chains)
+        float sc[2][4];
+        {
+            float sx[2][2][4];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sx[mt][h][j] = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const int row = 16 * mt + (mi & 1) * 8 + r8;
+                const uint8_t* rbase = Kst + row * 128;
+                if constexpr (kFp8) {
+#pragma unroll
+                    for (int kp = 0; kp < KS / 2; ++kp) {
+                        const int c = 2 * kp + (mi >> 1);
+                        uint32_t x[4];
+                        ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            const uint32_t a[4] = {
+                                e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4140)),
+                                e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4140)),
+                                e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4342)),
+                                e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4342))};
+                            Ops::mma(sx[mt][h2], a, qb[2 * kp + h2][0], qb[2 * kp + h2][1]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int c = 2 * ks + (mi >> 1);
+                        uint32_t a[4];
+                        ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+                        Ops::mma(sx[mt][ks & 1], a, qb[ks][0], qb[ks][1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) sc[mt][j] = (sx[mt][0][j] + sx[mt][1][j]) * qk_mul;
+        }
+
+        // ---- online softmax per column (this lane: columns 2 t4 + j; keys g,
+        // g + 8 of each 16-key tile); masked scores are -inf (a select, never
+        // a multiply), only in a stage that reaches a column's limit
+        if (key0 + kTmaStageTokens > kfree) {
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int key = key0 + 16 * mt + g + 8 * hr;
+                        if (key >= kend[j]) sc[mt][2 * hr + j] = -INFINITY;
+                    }
+        }
+        float lmax[2];
+        bool up = false;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            lmax[j] = fmaxf(fmaxf(sc[0][j], sc[0][2 + j]), fmaxf(sc[1][j], sc[1][2 + j]));
+            up |= m_run[j] == -INFINITY || lmax[j] > m_run[j] + kMqRescaleLog2;
+        }
+        if (__any_sync(0xffffffffu, up)) {
+            // a new reference max for each column: the column's max over
+            // its eight lanes, if it exceeds the old one by more than 2^8
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float mx = lmax[j];
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                if (m_run[j] == -INFINITY || mx > m_run[j] + kMqRescaleLog2) {
+                    const float alpha = m_run[j] == -INFINITY ? 0.f : fast_exp2(m_run[j] - mx);
+                    if (mx != -INFINITY) {
+                        l_run[j] *= alpha;
+#pragma unroll
+                        for (int i = 0; i < KS; ++i) {
+                            acc[i][j] *= alpha;
+                            acc[i][2 + j] *= alpha;
+                        }
+                        m_run[j] = mx;
+                    }
+                }
+            }
+        }
+        // weights exp2(s - m) <= 2^8; -inf scores (and a column with no key
+        // yet, m = -inf) give 0
+        float pv[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float mj = m_run[e & 1];
+                pv[mt][e] = mj == -INFINITY ? 0.f : fast_exp2(sc[mt][e] - mj);
+            }
+
+        // ---- P^T fragments: hi + residual, transposed from the S layout
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
+                const uint32_t hi = Ops::pack(w0, w1);
+                if constexpr (kFp8) {
+                    // binary16 weights as one term: the sums take the
+                    // rounded weights the products use
+                    const float2 hf = Ops::unpack(hi);
+                    l_run[0] += hf.x;
+                    l_run[1] += hf.y;
+                } else {
+                    // hi + lo is the weight to 2^-17: the sums take the weight
+                    const float2 hf = Ops::unpack(hi);
+                    l_run[0] += w0;
+                    l_run[1] += w1;
+                    bl[mt][hr] = movmatrix_trans(Ops::pack(w0 - hf.x, w1 - hf.y));
+                }
+                bh[mt][hr] = movmatrix_trans(hi);
+            }
+        }
+
+        // V^T fragment masks: a fragment's registers 0-1 hold keys 2 t4, 2 t4 + 1
+        // of its 16-key step, registers 2-3 keys 2 t4 + 8, 2 t4 + 9 (low half
+        // the even key); keys at or past nvalid are zeroed
+        uint32_t vmask[2][2];
+#pragma unroll
+        for (int kt = 0; kt < 2; ++kt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int key = 16 * kt + 2 * t4 + 8 * h;
+                vmask[kt][h] = (key < nvalid ? 0x0000ffffu : 0u) | (key + 1 < nvalid ? 0xffff0000u : 0u);
+            }
+        const bool ragged = nvalid < kTmaStageTokens;
+
+        // ---- O^T += V^T P^T
+        if constexpr (kFp8) {
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+                const int row = 8 * mi + r8;                         // key
+                uint32_t y[4];
+                ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
+                                         (((md & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
+                    uint32_t a[4] = {e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4240)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4341)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4240)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4341))};
+                    if (ragged) {
+                        a[0] &= vmask[kt][0];
+                        a[1] &= vmask[kt][0];
+                        a[2] &= vmask[kt][1];
+                        a[3] &= vmask[kt][1];
+                    }
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int row = 16 * kt + (mi >> 1) * 8 + r8;       // key
+                    const int c = 2 * md + (mi & 1);                     // 16-byte chunk of d
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
+                                             (((c & 7) ^ (row & 7)) << 4));
+                    if (ragged) {
+                        a[0] &= vmask[kt][0];
+                        a[1] &= vmask[kt][0];
+                        a[2] &= vmask[kt][1];
+                        a[3] &= vmask[kt][1];
+                    }
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+
+    // ------------------------------------------ merge the warps of each n-tile
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+    }
+    named_barrier(1, CW * 32);                           // ring is free: every stage was consumed
+    float* cm = reinterpret_cast<float*>(smem);          // [CW][8]
+    float* cl = cm + CW * 8;                             // [CW][8]
+    float* co = cl + CW * 8;                             // [CW][8][D]
+    if (g == 0) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            cm[warp * 8 + 2 * t4 + j] = m_run[j];
+            cl[warp * 8 + 2 * t4 + j] = l_run[j];
+        }
+    }
+#pragma unroll
+    for (int md = 0; md < KS; ++md) {
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
+                co[(warp * 8 + 2 * t4 + j) * D + d] = acc[md][2 * hr + j];
+            }
+    }
+    named_barrier(1, CW * 32);
+
+    // row c of n-tile t was computed by warps t, t + NT, ...; the CTA's rows
+    // are written row by row, d contiguous
+    const int nrows = min(8 * NT, R - row0);
+    const float vm = kFp8 ? p.v_mul * 256.f : p.v_mul;
+    QT* out = reinterpret_cast<QT*>(p.out);
+    for (int idx = threadIdx.x; idx < nrows * D; idx += CW * 32) {
+        const int rr = idx / D;
+        const int e = idx - rr * D;
+        const int t = rr >> 3, c = rr & 7;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) M = fmaxf(M, cm[(t + NT * w) * 8 + c]);
+        float W = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) {
+            const int src = (t + NT * w) * 8 + c;
+            const float mw = cm[src];
+            const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
+            W = fmaf(f, cl[src], W);
+            O = fmaf(f, co[src * D + e], O);
+        }
+        const int r = row0 + rr;
+        const int i = r / G;
+        const size_t orow = (size_t)(q0 + i) * p.num_q_heads + (size_t)kvh * G + (r - i * G);
+        out[orow * D + e] = from_float<QT>(__fdiv_rn(O, W) * vm);
+    }
+}
+
+template <typename QT, typename CT, int D, int NT>
+cudaError_t launch_prefill_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
+    using Smem = MmaSmem<CT, D>;
+    auto kern = paged_prefill_mma_kernel<QT, CT, D, NT>;
+    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
+    if (e != cudaSuccess) return e;
+    const DecodeParams& p = tp.p;
+    const long long rows = (long long)p.max_queries * p.group;
+    const long long groups = (rows + 8 * NT - 1) / (8 * NT);
+    if (groups > 0x7fffffffll) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)groups, p.num_kv_heads, p.num_seqs);
+    kern<<<grid, kTmaThreads, Smem::kAlloc, stream>>>(tp);
+    return cudaGetLastError();
+}
+
+// The fewest n-tiles that hold max_queries * group rows, at most kMqMaxTiles
+// (more rows would take several CTAs per sequence and KV head).
+template <typename QT, typename CT, int D>
+cudaError_t launch_prefill_mma_d(const TmaDecodeParams& tp, cudaStream_t stream) {
+    const long long rows = (long long)tp.p.max_queries * tp.p.group;
+    if (rows <= 8) return launch_prefill_mma_variant<QT, CT, D, 1>(tp, stream);
+    return launch_prefill_mma_variant<QT, CT, D, kMqMaxTiles>(tp, stream);
+}
+
+template <typename QT, typename CT>
+cudaError_t launch_prefill_mma(const DecodeParams& p, int head_size, cudaStream_t stream) {
+    constexpr int eb = TypeInfo<CT>::bytes;
+    TmaDecodeParams tp;
+    tp.p = p;
+    tp.box_rows = p.block_size < kTmaStageTokens ? p.block_size : kTmaStageTokens;
+    const unsigned long long rows =
+        (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
+    cudaError_t e = encode_cache_map(&tp.k_map, p.k_cache, eb, head_size, rows, tp.box_rows);
+    if (e == cudaSuccess) e = encode_cache_map(&tp.v_map, p.v_cache, eb, head_size, rows, tp.box_rows);
+    if (e != cudaSuccess) return e;
+    if constexpr (eb == 2) {
+        switch (head_size) {
+        case 64: return launch_prefill_mma_d<QT, CT, 64>(tp, stream);
+        case 128: return launch_prefill_mma_d<QT, CT, 128>(tp, stream);
+        case 256: return launch_prefill_mma_d<QT, CT, 256>(tp, stream);
+        }
+    } else {
+        switch (head_size) {
+        case 128: return launch_prefill_mma_d<QT, CT, 128>(tp, stream);
+        case 256: return launch_prefill_mma_d<QT, CT, 256>(tp, stream);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pagedkv

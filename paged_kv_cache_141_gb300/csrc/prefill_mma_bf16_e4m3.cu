@@ -1,0 +1,11 @@
+// prefill_mma_bf16_e4m3.cu -- instantiates the warp-level MMA multi-query kernel
+// for a query of type __nv_bfloat16 and a cache of type e4m3_t.
+#include "prefill_mma.cuh"
+
+namespace pagedkv {
+
+cudaError_t launch_prefill_mma_bf16_e4m3(const DecodeParams& p, int head_size, cudaStream_t stream) {
+    return launch_prefill_mma<__nv_bfloat16, e4m3_t>(p, head_size, stream);
+}
+
+}  // namespace pagedkv

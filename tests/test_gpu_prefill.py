@@ -1,8 +1,9 @@
 """Multi-query paged attention (chunked prefill / speculative verification)
-on the GPU against the oracle: the tcgen05 path over its shapes, the CUDA-core
-path for the other types and block sizes, the decode as its one-query case,
-block-size invariance, status flags, and a full-size chunked prefill checked
-on sampled sequences."""
+on the GPU against the oracle: the tcgen05 path over its shapes, the
+warp-level MMA path for a few query rows per sequence and KV head, the
+CUDA-core path for the other types and block sizes, the decode as its
+one-query case, block-size invariance, status flags, and full-size chunked
+prefill and verification steps checked on sampled rows."""
 import numpy as np
 import pytest
 import torch
@@ -69,9 +70,19 @@ class Prefill:
         return want
 
 
-def check(case, law, what, seed=None):
+# max_queries_per_seq * group <= 16 selects the warp-level MMA kernel; a
+# larger bound (any bound >= every Q_s is valid) selects the tcgen05 kernel
+MMA_MAX_ROWS = 16
+
+
+def tc_bound(p):
+    """A max_queries_per_seq that sends the launch to the tcgen05 kernel."""
+    return max(p.q.max_queries, MMA_MAX_ROWS // p.case.group + 1)
+
+
+def check(case, law, what, seed=None, force_tc=False):
     p = Prefill(case, law, seed)
-    got = to_f64(p.run())
+    got = to_f64(p.run(tc_bound(p) if force_tc else None))
     assert p.dc.status_bits() == 0
     rows, want = p.oracle()
     return assert_decode_close(got[rows], want, case, what)
@@ -109,7 +120,7 @@ def test_prefill_tensor_core_sweep(i):
     S, Hq, Hkv, d, B, dt, lens, ql = TC_SWEEP[i]
     c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
                   q_dtype=dt, cache_dtype=dt, lengths=lens, seed=900 + i)
-    check(c, ql, f"tc sweep {i}")
+    check(c, ql, f"tc sweep {i}", force_tc=True)
 
 
 # CUDA-core shapes: binary32, block size 1 (16-bit and E4M3), E4M3 at head
@@ -138,7 +149,40 @@ def test_prefill_e4m3_tensor_core_sweep(i):
     S, Hq, Hkv, d, B, qt, lens, ql = E4M3_TC_SWEEP[i]
     c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
                   q_dtype=qt, cache_dtype="e4m3", kv_dtype=qt, lengths=lens, seed=960 + i)
-    check(c, ql, f"e4m3 tc sweep {i}")
+    check(c, ql, f"e4m3 tc sweep {i}", force_tc=True)
+
+
+# warp-level MMA shapes (at most 16 query rows per sequence and KV head): one
+# and two 8-row n-tiles, padding rows (G = 3), one token of a 16-head group,
+# head sizes 64/128/256, block sizes 8..256, whole prefills of short
+# sequences, E4M3 caches at head size 128 and 256
+MMA_SWEEP = [
+    # S, Hq, Hkv, d, B, query dtype, cache dtype, lengths, queries
+    (6, 32, 8, 128, 16, "bf16", "bf16", ("uniform", 1, 700), ("uniform", 1, 4)),
+    (5, 8, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
+    (4, 4, 4, 256, 32, "bf16", "bf16", ("uniform", 40, 500), ("uniform", 1, 8)),
+    (4, 16, 2, 128, 64, "f16", "f16", ("fixed", [1, 2, 33, 300]), ("uniform", 1, 2)),
+    (3, 6, 2, 128, 256, "bf16", "bf16", ("fixed", [31, 32, 600]), ("uniform", 1, 5)),
+    (32, 8, 8, 128, 16, "f16", "f16", ("uniform", 1, 12), ("all",)),
+    (4, 12, 4, 64, 128, "bf16", "bf16", ("uniform", 1, 200), ("uniform", 1, 5)),
+    (3, 32, 2, 128, 16, "bf16", "bf16", ("uniform", 1, 900), ("fixed", [1, 1, 1])),
+    (4, 32, 8, 128, 16, "bf16", "e4m3", ("uniform", 1, 700), ("uniform", 1, 4)),
+    (3, 8, 2, 256, 32, "f16", "e4m3", ("uniform", 20, 400), ("uniform", 1, 4)),
+    (5, 8, 4, 128, 8, "f16", "e4m3", ("uniform", 1, 100), ("uniform", 1, 3)),
+]
+
+
+@pytest.mark.parametrize("i", range(len(MMA_SWEEP)))
+def test_prefill_warp_mma_sweep(i):
+    S, Hq, Hkv, d, B, qt, ct, lens, ql = MMA_SWEEP[i]
+    c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
+                  q_dtype=qt, cache_dtype=ct, kv_dtype=qt, lengths=lens, seed=1000 + i)
+    p = Prefill(c, ql)
+    assert p.q.max_queries * c.group <= MMA_MAX_ROWS
+    got = to_f64(p.run())
+    assert p.dc.status_bits() == 0
+    rows, want = p.oracle()
+    assert_decode_close(got[rows], want, c, f"mma sweep {i}")
 
 
 @pytest.mark.parametrize("i", range(len(SIMT_SWEEP)))
@@ -149,15 +193,17 @@ def test_prefill_cuda_core_sweep(i):
     check(c, ql, f"simt sweep {i}")
 
 
-def test_length_one_e4m3_tensor_core_returns_v_exactly():
-    """E4M3 cache, one key and one query per sequence, on the tensor-core
-    path: the output is the stored code's value times v_scale, rounded once
-    -- pins the producer's widening of the tiles and the folded scale."""
+@pytest.mark.parametrize("force_tc", [False, True], ids=["warp-mma", "tcgen05"])
+def test_length_one_e4m3_tensor_core_returns_v_exactly(force_tc):
+    """E4M3 cache, one key and one query per sequence, on both tensor-core
+    kernels: the output is the stored code's value times v_scale, rounded
+    once -- pins the widening of the tiles (in shared memory for tcgen05, in
+    registers for the warp-level MMA) and the folded scale."""
     c = make_case(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="e4m3", kv_dtype="bf16", lengths=("fixed", [1] * 4),
                   seed=977)
     p = Prefill(c, ("fixed", [1] * 4))
-    out = p.run().cpu()
+    out = p.run(tc_bound(p) if force_tc else None).cpu()
     assert p.dc.status_bits() == 0
     B = c.block_size
     slots = torch.from_numpy(c.new_slots)
@@ -191,26 +237,29 @@ def test_one_query_per_sequence_is_the_decode():
     assert_decode_close(got[rows], want, c, "one query")
 
 
-def test_block_size_invariance_on_the_tensor_cores():
+@pytest.mark.parametrize("qmax", [40, 4], ids=["tcgen05", "warp-mma"])
+def test_block_size_invariance_on_the_tensor_cores(qmax):
     """Same logical K/V, pools paged with B in {8, 16, 32, 128, 256}: the key
-    tiles hold the same keys, so the outputs are bit-identical."""
+    tiles (stages) hold the same keys, so the outputs are bit-identical; 40
+    query tokens (160 rows) run the tcgen05 kernel, 4 (16 rows) the warp-level
+    MMA kernel."""
     lens = [300, 77, 513]
     outs = []
     for B in (8, 16, 32, 128, 256):
         c = make_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=B,
                       q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", lens), seed=972)
         # re-page one logical K/V stream: gather it from the first pool layout
-        outs.append(_run_with_logical_kv(c, lens))
+        outs.append(_run_with_logical_kv(c, lens, qmax))
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
 
 
-def _run_with_logical_kv(c, lens):
+def _run_with_logical_kv(c, lens, qmax):
     """Fill the case's pool so that token t of head h of sequence s holds a
     value that depends only on (s, h, t), then run the multi-query kernel."""
     rng = np.random.default_rng(5)
     Hkv, d = c.num_kv_heads, c.head_size
-    p = Prefill(c, ("fixed", [min(40, L) for L in lens]))
+    p = Prefill(c, ("fixed", [min(qmax, L) for L in lens]))
     k = p.dc.k_cache.clone()
     v = p.dc.v_cache.clone()
     for s, L in enumerate(lens):
@@ -228,11 +277,12 @@ def _run_with_logical_kv(c, lens):
     return out.clone()
 
 
-def test_empty_sequences_and_zero_queries():
+@pytest.mark.parametrize("qs", [[0, 7, 0, 0, 9], [0, 3, 0, 0, 4]], ids=["tcgen05", "warp-mma"])
+def test_empty_sequences_and_zero_queries(qs):
     c = make_case(num_seqs=5, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", [0, 50, 0, 200, 9]),
                   seed=973)
-    p = Prefill(c, ("fixed", [0, 7, 0, 0, 9]))
+    p = Prefill(c, ("fixed", qs))
     got = to_f64(p.run())
     assert p.dc.status_bits() == 0
     rows, want = p.oracle()
@@ -243,27 +293,34 @@ def test_empty_sequences_and_zero_queries():
                      c.max_context_len, c.scale)
 
 
-def test_status_flags():
+@pytest.mark.parametrize("qmax", [3, 9], ids=["warp-mma", "tcgen05"])
+def test_status_flags(qmax):
     c = make_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", [40, 60, 80]), seed=974)
-    p = Prefill(c, ("fixed", [5, 5, 5]))
+    p = Prefill(c, ("fixed", [3, 3, 3]))
     # more queries than context tokens for sequence 0
     bad = p.dc.context_lens.clone()
-    bad[0] = 3
+    bad[0] = 2
     pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
-                     p.dc.block_tables, bad, 5, c.max_context_len, c.scale, 1.0, 1.0,
+                     p.dc.block_tables, bad, qmax, c.max_context_len, c.scale, 1.0, 1.0,
                      p.dc.status)
+    assert p.dc.status_bits() & pk.DEV_BAD_LEN
+    # more queries than the host's bound for every sequence
+    p.dc.status.zero_()
+    pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
+                     p.dc.block_tables, p.dc.context_lens, 2, c.max_context_len, c.scale, 1.0,
+                     1.0, p.dc.status)
     assert p.dc.status_bits() & pk.DEV_BAD_LEN
     # a block id outside the pool: the copy is skipped and flagged
     p.dc.status.zero_()
     tables = p.dc.block_tables.clone()
     tables[1, 0] = c.num_blocks + 5
     pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache, tables,
-                     p.dc.context_lens, 5, c.max_context_len, c.scale, 1.0, 1.0, p.dc.status)
+                     p.dc.context_lens, qmax, c.max_context_len, c.scale, 1.0, 1.0, p.dc.status)
     assert p.dc.status_bits() & pk.DEV_BAD_BLOCK_ID
     # the other sequences are still right
     p.dc.status.zero_()
-    got = to_f64(p.run())
+    got = to_f64(p.run(qmax))
     rows, want = p.oracle()
     assert_decode_close(got[rows], want, c, "after flags")
 
@@ -280,16 +337,20 @@ def test_host_argument_errors():
         pk.paged_prefill(*args[:7], 0, c.max_context_len, c.scale)
 
 
-@pytest.mark.parametrize("law", [("fixed", None), ("uniform", 1, 8)], ids=["chunk512", "spec8"])
-def test_full_size_llama3_8b_sampled(law):
+@pytest.mark.parametrize("law,force_tc", [(("fixed", None), False), (("uniform", 1, 8), False),
+                                          (("uniform", 1, 4), False), (("uniform", 1, 4), True)],
+                         ids=["chunk512", "spec8", "spec4", "spec4-tcgen05"])
+def test_full_size_llama3_8b_sampled(law, force_tc):
     """Llama-3-8B GQA shape at full size (256 sequences, contexts 512..4096):
-    a 512-token prefill chunk per sequence (capped at L_s), and an 8-draft
-    speculative verification step; the oracle checks 6 sequences."""
+    a 512-token prefill chunk per sequence (capped at L_s), an 8-draft
+    speculative verification step (tcgen05), and a 4-draft one (warp-level
+    MMA, and forced onto the tcgen05 kernel); sampled rows against the
+    oracle."""
     c = config_case(3)
     if law[0] == "fixed":
         law = ("fixed", np.minimum(512, c.context_lens))
     p = Prefill(c, law)
-    got = to_f64(p.run())
+    got = to_f64(p.run(tc_bound(p) if force_tc else None))
     assert p.dc.status_bits() == 0
     # every query tile edge of the longest and shortest sequences' first and
     # last tokens, plus random rows
@@ -305,17 +366,20 @@ def test_full_size_llama3_8b_sampled(law):
     assert_decode_close(got[rows], want, c, "full size")
 
 
-@pytest.mark.parametrize("law", [("uniform", 1, 8), ("uniform", 200, 600)], ids=["spec", "chunk"])
-def test_repeated_launches_are_bit_identical(law):
+@pytest.mark.parametrize("law,force_tc", [(("uniform", 1, 4), False), (("uniform", 1, 8), False),
+                                          (("uniform", 200, 600), False)],
+                         ids=["spec4-warp-mma", "spec8-tcgen05", "chunk"])
+def test_repeated_launches_are_bit_identical(law, force_tc):
     """The same launch three times gives the same bits (no race between the
-    warps that share a row, the producers and the MMA issuer)."""
+    warps that share a row or a stage, the producers and the MMA issuer)."""
     c = config_case(3, num_seqs=64)
     p = Prefill(c, law)
-    first = p.run().clone()
+    bound = tc_bound(p) if force_tc else None
+    first = p.run(bound).clone()
     assert p.dc.status_bits() == 0
     for _ in range(2):
         p.out.fill_(float("nan"))
-        assert torch.equal(p.run(), first)
+        assert torch.equal(p.run(bound), first)
 
 
 def test_full_size_shared_prefix_e4m3_sampled():
