@@ -427,15 +427,18 @@ def run_ours(args):
 PREFILL_METRIC = {
     "chunk512": "multi-query paged attention TFLOP/s (causal, algorithmic), 512-token prefill chunks",
     "spec8": "multi-query paged attention KV GB/s, 8-token speculative verification",
+    "spec4": "multi-query paged attention KV GB/s, 4-token speculative verification",
+    "spec2": "multi-query paged attention KV GB/s, 2-token speculative verification",
 }
 
 
 def prefill_queries(case, kind):
     """The query law of a multi-query workload: a 512-token chunk at the end
-    of every context (capped at L_s), or 8 draft tokens per sequence."""
+    of every context (capped at L_s), or 8, 4 or 2 draft tokens per
+    sequence."""
     if kind == "chunk512":
         return ("fixed", np.minimum(512, case.context_lens))
-    return ("fixed", np.minimum(8, case.context_lens))
+    return ("fixed", np.minimum(int(kind[len("spec"):]), case.context_lens))
 
 
 def prefill_work(case, qs: np.ndarray, seqs=None):
@@ -969,7 +972,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--prefill", choices=["chunk512", "spec8"], default=None,
+    ap.add_argument("--prefill", choices=["chunk512", "spec8", "spec4", "spec2"], default=None,
                     help="time multi-query paged attention on the configuration's pool instead")
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="with --prefill: fewer sequences of the same shape (small ncu captures)")
