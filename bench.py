@@ -528,10 +528,15 @@ def run_prefill(args):
         torch.bfloat16).to(device) if case.q_dtype == "bf16" else torch.from_numpy(q.query).to(device)
     qstart = torch.from_numpy(q.query_start).to(device)
     out = torch.empty_like(query)
+    # the order in which sequences start: longest context first, sorted on
+    # the host from the lengths a serving scheduler holds, passed as an input
+    host_order_np = pk.longest_first(case.context_lens)
+    order = torch.from_numpy(host_order_np).to(device)
 
     def launch():
         pk.paged_prefill(out, query, qstart, st.kc, st.vc, st.bt, st.cl, q.max_queries,
-                         case.max_context_len, case.scale, case.k_scale, case.v_scale, st.status)
+                         case.max_context_len, case.scale, case.k_scale, case.v_scale, st.status,
+                         seq_order=order)
 
     launch()
     torch.cuda.synchronize()
@@ -564,10 +569,12 @@ def run_prefill(args):
     host_q.copy_(query.cpu())
     host_qs = torch.from_numpy(q.query_start).pin_memory()
     host_cl = st.cl.cpu().pin_memory()
+    host_order = torch.from_numpy(host_order_np).pin_memory()
     host_out = [torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(2)]
     dq = [query, torch.empty_like(query)]
     dqs = [qstart, torch.empty_like(qstart)]
     dcl = [st.cl, torch.empty_like(st.cl)]
+    dord = [order, torch.empty_like(order)]
     dout = [out, torch.empty_like(out)]
     s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
     in_ready = [torch.cuda.Event() for _ in range(2)]
@@ -583,13 +590,14 @@ def run_prefill(args):
                 dq[k].copy_(host_q, non_blocking=True)
                 dqs[k].copy_(host_qs, non_blocking=True)
                 dcl[k].copy_(host_cl, non_blocking=True)
+                dord[k].copy_(host_order, non_blocking=True)
             in_ready[k].record(s_in)
             stream.wait_event(in_ready[k])
             if i >= 2:
                 stream.wait_event(out_read[k])           # step i-2's output has left
             pk.paged_prefill(dout[k], dq[k], dqs[k], st.kc, st.vc, st.bt, dcl[k], q.max_queries,
                              case.max_context_len, case.scale, case.k_scale, case.v_scale,
-                             st.status)
+                             st.status, seq_order=dord[k])
             done[k].record(stream)
             s_out.wait_event(done[k])
             with torch.cuda.stream(s_out):
@@ -606,7 +614,8 @@ def run_prefill(args):
     eb_.record(s_out)                                  # after the last output has left
     torch.cuda.synchronize()
     e2e_ms = ea.elapsed_time(eb_) / ke
-    h2d = host_q.numel() * host_q.element_size() + host_qs.numel() * 4 + host_cl.numel() * 4
+    h2d = (host_q.numel() * host_q.element_size() + host_qs.numel() * 4 + host_cl.numel() * 4
+           + host_order.numel() * 4)
     d2h = host_out[0].numel() * host_out[0].element_size()
 
     flops, nbytes = prefill_work(case, q.query_start)
@@ -633,6 +642,8 @@ def run_prefill(args):
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
                    "block_size": case.block_size, "query_tokens": int(q.query_start[-1]),
                    "max_queries_per_seq": q.max_queries, "total_context_tokens": case.total_tokens,
+                   "seq_order": "longest context first (host sort of the lengths, an input "
+                                "copied in with them end to end)",
                    "l2": "KV pool %.2f GB vs 129 MB L2; no flush" % (case.kv_bytes() / 1e9)},
         "tflops": round(tflops, 2), "kv_q_o_gbs": round(gbs, 2),
         "flops_per_step": flops, "bytes_per_step": nbytes,

@@ -102,6 +102,8 @@ typedef enum pa_dtype {
 #define PA_DEV_TIMEOUT      8u  /* a bounded wait inside a kernel ran out */
 #define PA_DEV_SLOT_MISMATCH 16u /* a fused write's slot is not the newest position of its
                                     sequence (the token is stored; the decode may miss it) */
+#define PA_DEV_BAD_ORDER    32u /* a seq_order entry is outside [0, num_seqs) (the work
+                                   it names is skipped) */
 
 /* Supported shapes: head_size in {64, 128, 256}; block_size in [1, 1024];
  * partition_size a positive multiple of 32 (512 on the pages). */
@@ -327,6 +329,17 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *                 query_start[0] = 0, query_start[num_seqs] = num_queries.
  *  max_queries_per_seq  an upper bound on Q_s known on the host (sizes the
  *                 grid); 0 <= Q_s <= max_queries_per_seq and Q_s <= L_s.
+ *  seq_order      null, or [num_seqs] int32, device, 4-byte aligned: a
+ *                 permutation of 0..num_seqs-1, the order in which the
+ *                 sequences' work is started (a scheduling hint: the
+ *                 outputs do not depend on it). The GPU starts work in launch
+ *                 order and cannot see the lengths before it starts, so a
+ *                 caller that knows them on the host (a serving scheduler
+ *                 does) passes the longest contexts first, and the last CTAs
+ *                 to start are short ones. An entry outside [0, num_seqs)
+ *                 sets PA_DEV_BAD_ORDER and its work is skipped; sequences a
+ *                 non-permutation omits have unspecified rows. The CUDA-core
+ *                 path (one query token per work unit) ignores it.
  *  Other arguments as pa_decode; scale must be > 0.
  *  Kernel selection, by the arguments alone: with max_queries_per_seq *
  *  (num_q_heads / num_kv_heads) <= 16 query rows per sequence and KV head, a
@@ -349,7 +362,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
                            int num_q_heads, int num_kv_heads, int head_size, int block_size,
                            int64_t num_blocks, int max_context_len, float scale,
                            pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
-                           uint32_t* dev_status, void* stream);
+                           const int32_t* seq_order, uint32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * Block management: the host-side allocator and the copy-on-write copy.

@@ -31,6 +31,7 @@ _lib = None
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_NO_BLOCKS = range(6)
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
 DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT, DEV_SLOT_MISMATCH = 1, 2, 4, 8, 16
+DEV_BAD_ORDER = 32
 
 DEFAULT_PARTITION_SIZE = 512
 
@@ -82,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.pa_write_decode_partitions.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64,
                                                  I, F, I, I, F, F, I, P, S, P, P]
         L.pa_paged_prefill.argtypes = [P, P, P, I, I, P, P, P, I, P, I, I, I, I, I, I64, I, F, I,
-                                       I, F, F, P, P]
+                                       I, F, F, P, P, P]
         L.pa_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I64, I, P, P]
         L.pa_selftest_wait.argtypes = [I, P, P]
         L.pa_allocator_create.argtypes = [I64, I, I]
@@ -197,10 +198,12 @@ def decode(out, query, k_cache, v_cache, block_tables, context_lens, max_context
 
 def paged_prefill(out, query, query_start, k_cache, v_cache, block_tables, context_lens,
                   max_queries_per_seq, max_context_len, scale, k_scale=1.0, v_scale=1.0,
-                  dev_status=None, stream=None) -> None:
+                  dev_status=None, stream=None, *, seq_order=None) -> None:
     """Causal multi-query paged attention into `out` ([T, Hq, D] like `query`);
     the tokens of sequence s are rows query_start[s]..query_start[s+1]-1 and
-    are the last Q_s positions of its context_lens[s] tokens."""
+    are the last Q_s positions of its context_lens[s] tokens. `seq_order`
+    (int32 [num_seqs] on the device, optional): the order in which sequences'
+    work starts, e.g. longest_first(context lengths known on the host)."""
     T, Hq, D = query.shape
     nb, Hkv, B, D2 = k_cache.shape
     if D2 != D:
@@ -212,11 +215,22 @@ def paged_prefill(out, query, query_start, k_cache, v_cache, block_tables, conte
         raise ValueError("block_tables and context_lens must be int32")
     if block_tables.dim() != 2 or block_tables.shape[0] != S:
         raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    if seq_order is not None and (seq_order.dtype != torch.int32 or seq_order.numel() != S):
+        raise ValueError("seq_order must be int32 [num_seqs]")
     _check(lib().pa_paged_prefill(
         _ptr(out), _ptr(query), _ptr(query_start), T, int(max_queries_per_seq), _ptr(k_cache),
         _ptr(v_cache), _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, Hq, Hkv,
         D, B, nb, int(max_context_len), float(scale), _dtype(query), _dtype(k_cache),
-        float(k_scale), float(v_scale), _ptr(dev_status), _stream(stream)), "pa_paged_prefill")
+        float(k_scale), float(v_scale), _ptr(seq_order), _ptr(dev_status), _stream(stream)),
+        "pa_paged_prefill")
+
+
+def longest_first(context_lens) -> "np.ndarray":
+    """The sequence order that starts the longest contexts first (stable for
+    equal lengths), from lengths known on the host: int32 [num_seqs]."""
+    import numpy as np
+    L = np.asarray(context_lens)
+    return np.argsort(-L.astype(np.int64), kind="stable").astype(np.int32)
 
 
 def workspace_bytes(num_seqs, num_q_heads, head_size, max_context_len,

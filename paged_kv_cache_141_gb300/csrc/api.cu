@@ -532,8 +532,9 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
                            int num_q_heads, int num_kv_heads, int head_size, int block_size,
                            int64_t num_blocks, int max_context_len, float scale,
                            pa_dtype q_dtype, pa_dtype cache_dtype, float k_scale, float v_scale,
-                           uint32_t* dev_status, void* stream) {
+                           const int32_t* seq_order, uint32_t* dev_status, void* stream) {
     if (num_queries < 0 || max_queries_per_seq < 0 || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+    if (!aligned(seq_order, 4)) return PA_ERR_INVALID_ARG;
     // with no query tokens the data pointers may be null: validate the shape only
     const int seqs_with_work = num_queries == 0 ? 0 : num_seqs;
     DecodeParams p;
@@ -551,6 +552,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     p.query_start = query_start;
     p.num_queries = num_queries;
     p.max_queries = max_queries_per_seq;
+    p.seq_order = seq_order;
     if ((long long)max_queries_per_seq * p.group <= kPrefillMmaMaxRows &&
         prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks,
                              num_kv_heads)) {
@@ -586,6 +588,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
         const bool fp8 = cache_dtype == PA_FP8_E4M3;
         pp.q_mul = scale * 1.4426950408889634f * (fp8 ? k_scale : 1.f);
         pp.v_mul = fp8 ? v_scale : 1.f;
+        pp.seq_order = seq_order;
         if (fp8)
             return from_cuda(q_dtype == PA_F16 ? launch_prefill_tc_f16_e4m3(pp, head_size, s)
                                                : launch_prefill_tc_bf16_e4m3(pp, head_size, s));
@@ -593,7 +596,8 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
                                            : launch_prefill_tc_bf16(pp, head_size, s));
     }
     // CUDA cores: one query token per work unit, the decode kernel over the
-    // token's causal prefix
+    // token's causal prefix (the work is per token: no sequence order)
+    p.seq_order = nullptr;
     return from_cuda(run_simt_decode_kernel(p, head_size, q_dtype, cache_dtype, s));
 }
 

@@ -49,6 +49,7 @@ struct DecodeParams {
     const int32_t* query_start;   // [S + 1]
     int num_queries;              // rows of query / out
     int max_queries;              // max over s of Q_s (sizes the tensor-core multi-query grid)
+    const int32_t* seq_order;     // null or [S]: launch position -> sequence (longest first)
 };
 
 // Generic CUDA-core decode; one launcher per (query type, cache type).
@@ -123,6 +124,7 @@ struct PrefillParams {
     int q_tiles;                  // ceil(max_queries / tokens_per_tile)
     float q_mul;                  // scale * log2(e) * (E4M3 cache ? k_scale : 1)
     float v_mul;                  // E4M3 cache ? v_scale : 1
+    const int32_t* seq_order;     // null or [S]: launch position -> sequence (longest first)
 };
 
 cudaError_t launch_prefill_tc_f16(const PrefillParams& p, int head_size, cudaStream_t stream);

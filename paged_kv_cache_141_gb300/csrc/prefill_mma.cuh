@@ -75,13 +75,19 @@ paged_prefill_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
     uint64_t* empty = full + NST;
 
-    const int s = blockIdx.z;
     const int kvh = blockIdx.y;
     const int row0 = blockIdx.x * 8 * NT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2;                             // fragment row / B column
     const int t4 = lane & 3;                             // fragment column pair
+    // the sequence: launch position z, or the caller's order (longest first)
+    const int s = p.seq_order ? __ldg(p.seq_order + blockIdx.z) : (int)blockIdx.z;
+    if (s < 0 || s >= p.num_seqs) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0 && p.status)
+            atomicOr(p.status, PA_DEV_BAD_ORDER);
+        return;
+    }
 
     const int q0 = __ldg(p.query_start + s);
     const int Q = __ldg(p.query_start + s + 1) - q0;

@@ -319,6 +319,18 @@ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c) {
 // table's latency is not paid per tile.
 constexpr int kTcAhead = 4;                   // key tiles whose table entries load together
 
+// The sequence of launch position i: i, or the caller's order (longest
+// context first); -1 (and PA_DEV_BAD_ORDER, raised by `report`) for an entry
+// outside [0, S).
+__device__ __forceinline__ int tc_sequence(const PrefillParams& p, int i, bool report) {
+    const int s = p.seq_order ? __ldg(p.seq_order + i) : i;
+    if (s < 0 || s >= p.num_seqs) {
+        if (report && p.status) atomicOr(p.status, PA_DEV_BAD_ORDER);
+        return -1;
+    }
+    return s;
+}
+
 // The block-table entries of a unit's first kTcAhead key tiles for this
 // lane's box, read before the sequence's lengths are known: every unit's keys
 // start at 0, so they depend on the sequence alone (entries past the context
@@ -558,7 +570,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int tile = blockIdx.x % p.q_tiles;
     const int rest = blockIdx.x / p.q_tiles;
     const int hk = rest % p.num_kv_heads;
-    const int s = rest / p.num_kv_heads;
+    const int s = tc_sequence(p, rest / p.num_kv_heads, tid == 0 && tile == 0 && hk == 0);
+    if (s < 0) return;
     int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
     if constexpr (!kFp8)
         if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
@@ -1004,7 +1017,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int g = blockIdx.x % groups;
     const int rest = blockIdx.x / groups;
     const int hk = rest % p.num_kv_heads;
-    const int s = rest / p.num_kv_heads;
+    const int s = tc_sequence(p, rest / p.num_kv_heads, tid == 0 && g == 0 && hk == 0);
+    if (s < 0) return;
     int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
     if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
     const int q0 = p.query_start[s];

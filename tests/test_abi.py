@@ -94,10 +94,12 @@ def test_paged_prefill_argument_errors(lib):
     L = pk.lib()
     v = ctypes.c_void_p(256)
     # (out, query, query_start, T, maxQ, k, v, tables, max_blocks, lens, S, Hq, Hkv, d, B,
-    #  num_blocks, max_len, scale, q_dtype, cache_dtype, k_scale, v_scale, status, stream)
-    def call(T=4, maxq=2, S=2, scale=0.1, d=128, q=pk.PA_BF16, c=pk.PA_BF16, out=v, qs=v):
+    #  num_blocks, max_len, scale, q_dtype, cache_dtype, k_scale, v_scale, seq_order, status,
+    #  stream)
+    def call(T=4, maxq=2, S=2, scale=0.1, d=128, q=pk.PA_BF16, c=pk.PA_BF16, out=v, qs=v,
+             order=None):
         return L.pa_paged_prefill(out, v, qs, T, maxq, v, v, v, 4, v, S, 8, 2, d, 16, 10, 64,
-                                  scale, q, c, 1.0, 1.0, None, None)
+                                  scale, q, c, 1.0, 1.0, order, None, None)
     assert call(scale=0.0) == pk.PA_ERR_INVALID_ARG          # scale must be > 0
     assert call(scale=-1.0) == pk.PA_ERR_INVALID_ARG
     assert call(T=-1) == pk.PA_ERR_INVALID_ARG
@@ -110,6 +112,7 @@ def test_paged_prefill_argument_errors(lib):
     assert call(T=0, out=None, qs=None) == pk.PA_OK
     assert call(S=0, T=0) == pk.PA_OK
     assert call(S=0, T=3) == pk.PA_ERR_INVALID_ARG           # tokens without sequences
+    assert call(order=ctypes.c_void_p(258)) == pk.PA_ERR_INVALID_ARG   # int32 order, 4 bytes
 
 
 def test_misaligned_pointers_are_rejected_before_any_launch(lib):
@@ -138,9 +141,10 @@ def test_misaligned_pointers_are_rejected_before_any_launch(lib):
                       None) == pk.PA_ERR_INVALID_ARG
     # multi-query: out 16 bytes, query_start 4 bytes
     assert L.pa_paged_prefill(odd, ok, ok, 4, 2, ok, ok, ok, 4, ok, 2, 8, 2, 128, 16, 10, 64, 0.1,
-                              pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None) == pk.PA_ERR_INVALID_ARG
+                              pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None,
+                              None) == pk.PA_ERR_INVALID_ARG
     assert L.pa_paged_prefill(ok, ok, ctypes.c_void_p(258), 4, 2, ok, ok, ok, 4, ok, 2, 8, 2, 128,
-                              16, 10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None,
+                              16, 10, 64, 0.1, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0, None, None,
                               None) == pk.PA_ERR_INVALID_ARG
 
 

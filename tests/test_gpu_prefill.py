@@ -434,3 +434,32 @@ def test_full_size_long_context_chunk_sampled():
     rows = np.array(sorted(rows))
     want = p.oracle_rows(rows)
     assert_decode_close(got[rows], want, c, "long-context chunk")
+
+
+@pytest.mark.parametrize("law", [("uniform", 1, 4), ("uniform", 1, 8), ("uniform", 200, 600)],
+                         ids=["warp-mma", "tcgen05-one-tile", "tcgen05-two-tile"])
+def test_sequence_order_does_not_change_outputs(law):
+    """seq_order only changes when each sequence's work starts: longest
+    first and a random permutation give the natural order's bits; an entry
+    outside [0, S) raises DEV_BAD_ORDER and the launch still returns."""
+    c = config_case(3, num_seqs=48)
+    p = Prefill(c, law)
+    natural = p.run().clone()
+    assert p.dc.status_bits() == 0
+    dev = p.out.device
+    orders = [pk.longest_first(c.context_lens),
+              np.random.default_rng(17).permutation(c.num_seqs).astype(np.int32)]
+    for order in orders:
+        p.out.fill_(float("nan"))
+        pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
+                         p.dc.block_tables, p.dc.context_lens, p.q.max_queries,
+                         c.max_context_len, c.scale, c.k_scale, c.v_scale, p.dc.status,
+                         seq_order=torch.from_numpy(order).to(dev))
+        assert p.dc.status_bits() == 0
+        assert torch.equal(p.out, natural)
+    bad = torch.from_numpy(orders[0].copy()).to(dev)
+    bad[5] = c.num_seqs
+    pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
+                     p.dc.block_tables, p.dc.context_lens, p.q.max_queries, c.max_context_len,
+                     c.scale, c.k_scale, c.v_scale, p.dc.status, seq_order=bad)
+    assert p.dc.status_bits() & pk.DEV_BAD_ORDER
