@@ -342,11 +342,12 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *                 path (one query token per work unit) ignores it.
  *  Other arguments as pa_decode; scale must be > 0.
  *  Kernel selection, by the arguments alone: with max_queries_per_seq *
- *  (num_q_heads / num_kv_heads) <= 16 query rows per sequence and KV head, a
- *  16-bit query with a cache of the same type or an E4M3 cache, on the shapes
- *  of the TMA decode (rows of 128, 256 or 512 bytes, block_size 8, 16 or a
- *  multiple of 32), runs the warp-level MMA kernel that reads each
- *  sequence's K/V once for all its rows (speculative verification). Else a
+ *  (num_q_heads / num_kv_heads) query rows per sequence and KV head at most
+ *  32 (a 16-bit cache of the query's type, head_size <= 128) or 16 (an E4M3
+ *  cache, or head_size 256), a 16-bit query, on the shapes of the TMA decode
+ *  (rows of 128, 256 or 512 bytes, block_size 8, 16 or a multiple of 32),
+ *  the warp-level MMA kernels run, reading each sequence's K/V once for all
+ *  its rows (speculative verification). Else a
  *  16-bit query with a cache of the same type (head_size 64/128/256) or an
  *  E4M3 cache (head_size 64/128), a block_size that is a power of two in
  *  [8, 256] and a group of at most 128 heads runs on the tcgen05 tensor

@@ -70,14 +70,18 @@ class Prefill:
         return want
 
 
-# max_queries_per_seq * group <= 16 selects the warp-level MMA kernel; a
-# larger bound (any bound >= every Q_s is valid) selects the tcgen05 kernel
-MMA_MAX_ROWS = 16
+def mma_max_rows(case):
+    """max_queries_per_seq * group up to this selects the warp-level MMA
+    kernels (32 for a 16-bit cache of the query's type at head size <= 128,
+    else 16); a larger bound (any bound >= every Q_s is valid) selects the
+    tcgen05 kernels."""
+    same = case.cache_dtype == case.q_dtype
+    return 32 if same and case.head_size <= 128 else 16
 
 
 def tc_bound(p):
     """A max_queries_per_seq that sends the launch to the tcgen05 kernel."""
-    return max(p.q.max_queries, MMA_MAX_ROWS // p.case.group + 1)
+    return max(p.q.max_queries, mma_max_rows(p.case) // p.case.group + 1)
 
 
 def check(case, law, what, seed=None, force_tc=False):
@@ -152,11 +156,17 @@ def test_prefill_e4m3_tensor_core_sweep(i):
     check(c, ql, f"e4m3 tc sweep {i}", force_tc=True)
 
 
-# warp-level MMA shapes (at most 16 query rows per sequence and KV head): one
-# and two 8-row n-tiles, padding rows (G = 3), one token of a 16-head group,
-# head sizes 64/128/256, block sizes 8..256, whole prefills of short
-# sequences, E4M3 caches at head size 128 and 256
+# warp-level MMA shapes: one and two 8-row n-tiles (up to 16 rows), four
+# n-tiles two per warp (17..32 rows, 16-bit caches at head size <= 128),
+# padding rows (G = 3), one token of a 16-head group, head sizes 64/128/256,
+# block sizes 8..256, whole prefills of short sequences, E4M3 caches at head
+# size 128 and 256
 MMA_SWEEP = [
+    (6, 32, 8, 128, 16, "bf16", "bf16", ("loguniform", 1, 900), ("uniform", 1, 8)),
+    (4, 16, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
+    (3, 6, 2, 128, 256, "bf16", "bf16", ("fixed", [31, 32, 600]), ("uniform", 6, 10)),
+    (24, 8, 8, 128, 32, "f16", "f16", ("uniform", 1, 28), ("all",)),
+    (4, 8, 2, 64, 64, "bf16", "bf16", ("uniform", 100, 400), ("fixed", [8, 5, 7, 6])),
     # S, Hq, Hkv, d, B, query dtype, cache dtype, lengths, queries
     (6, 32, 8, 128, 16, "bf16", "bf16", ("uniform", 1, 700), ("uniform", 1, 4)),
     (5, 8, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
@@ -178,7 +188,7 @@ def test_prefill_warp_mma_sweep(i):
     c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
                   q_dtype=qt, cache_dtype=ct, kv_dtype=qt, lengths=lens, seed=1000 + i)
     p = Prefill(c, ql)
-    assert p.q.max_queries * c.group <= MMA_MAX_ROWS
+    assert p.q.max_queries * c.group <= mma_max_rows(c)
     got = to_f64(p.run())
     assert p.dc.status_bits() == 0
     rows, want = p.oracle()
@@ -237,12 +247,12 @@ def test_one_query_per_sequence_is_the_decode():
     assert_decode_close(got[rows], want, c, "one query")
 
 
-@pytest.mark.parametrize("qmax", [40, 4], ids=["tcgen05", "warp-mma"])
+@pytest.mark.parametrize("qmax", [40, 4, 8], ids=["tcgen05", "warp-mma", "warp-mma2"])
 def test_block_size_invariance_on_the_tensor_cores(qmax):
     """Same logical K/V, pools paged with B in {8, 16, 32, 128, 256}: the key
     tiles (stages) hold the same keys, so the outputs are bit-identical; 40
-    query tokens (160 rows) run the tcgen05 kernel, 4 (16 rows) the warp-level
-    MMA kernel."""
+    query tokens (160 rows) run the tcgen05 kernel, 4 (16 rows) and 8 (32
+    rows) the warp-level MMA kernels."""
     lens = [300, 77, 513]
     outs = []
     for B in (8, 16, 32, 128, 256):
@@ -277,7 +287,8 @@ def _run_with_logical_kv(c, lens, qmax):
     return out.clone()
 
 
-@pytest.mark.parametrize("qs", [[0, 7, 0, 0, 9], [0, 3, 0, 0, 4]], ids=["tcgen05", "warp-mma"])
+@pytest.mark.parametrize("qs", [[0, 7, 0, 0, 9], [0, 3, 0, 0, 4], [0, 7, 0, 0, 8]],
+                         ids=["tcgen05", "warp-mma", "warp-mma2"])
 def test_empty_sequences_and_zero_queries(qs):
     c = make_case(num_seqs=5, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", [0, 50, 0, 200, 9]),
@@ -293,7 +304,7 @@ def test_empty_sequences_and_zero_queries(qs):
                      c.max_context_len, c.scale)
 
 
-@pytest.mark.parametrize("qmax", [3, 9], ids=["warp-mma", "tcgen05"])
+@pytest.mark.parametrize("qmax", [3, 7, 9], ids=["warp-mma", "warp-mma2", "tcgen05"])
 def test_status_flags(qmax):
     c = make_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype="bf16", cache_dtype="bf16", lengths=("fixed", [40, 60, 80]), seed=974)
@@ -338,14 +349,14 @@ def test_host_argument_errors():
 
 
 @pytest.mark.parametrize("law,force_tc", [(("fixed", None), False), (("uniform", 1, 8), False),
-                                          (("uniform", 1, 4), False), (("uniform", 1, 4), True)],
-                         ids=["chunk512", "spec8", "spec4", "spec4-tcgen05"])
+                                          (("uniform", 1, 8), True), (("uniform", 1, 4), False)],
+                         ids=["chunk512", "spec8", "spec8-tcgen05", "spec4"])
 def test_full_size_llama3_8b_sampled(law, force_tc):
     """Llama-3-8B GQA shape at full size (256 sequences, contexts 512..4096):
     a 512-token prefill chunk per sequence (capped at L_s), an 8-draft
-    speculative verification step (tcgen05), and a 4-draft one (warp-level
-    MMA, and forced onto the tcgen05 kernel); sampled rows against the
-    oracle."""
+    speculative verification step (warp-level MMA with two n-tiles per warp,
+    and forced onto the tcgen05 kernel), and a 4-draft one; sampled rows
+    against the oracle."""
     c = config_case(3)
     if law[0] == "fixed":
         law = ("fixed", np.minimum(512, c.context_lens))
@@ -367,8 +378,8 @@ def test_full_size_llama3_8b_sampled(law, force_tc):
 
 
 @pytest.mark.parametrize("law,force_tc", [(("uniform", 1, 4), False), (("uniform", 1, 8), False),
-                                          (("uniform", 200, 600), False)],
-                         ids=["spec4-warp-mma", "spec8-tcgen05", "chunk"])
+                                          (("uniform", 1, 8), True), (("uniform", 200, 600), False)],
+                         ids=["spec4-warp-mma", "spec8-warp-mma2", "spec8-tcgen05", "chunk"])
 def test_repeated_launches_are_bit_identical(law, force_tc):
     """The same launch three times gives the same bits (no race between the
     warps that share a row or a stage, the producers and the MMA issuer)."""
@@ -436,15 +447,17 @@ def test_full_size_long_context_chunk_sampled():
     assert_decode_close(got[rows], want, c, "long-context chunk")
 
 
-@pytest.mark.parametrize("law", [("uniform", 1, 4), ("uniform", 1, 8), ("uniform", 200, 600)],
-                         ids=["warp-mma", "tcgen05-one-tile", "tcgen05-two-tile"])
-def test_sequence_order_does_not_change_outputs(law):
+@pytest.mark.parametrize("law,force_tc", [(("uniform", 1, 4), False), (("uniform", 1, 8), False),
+                                          (("uniform", 1, 8), True), (("uniform", 200, 600), False)],
+                         ids=["warp-mma", "warp-mma2", "tcgen05-one-tile", "tcgen05-two-tile"])
+def test_sequence_order_does_not_change_outputs(law, force_tc):
     """seq_order only changes when each sequence's work starts: longest
     first and a random permutation give the natural order's bits; an entry
     outside [0, S) raises DEV_BAD_ORDER and the launch still returns."""
     c = config_case(3, num_seqs=48)
     p = Prefill(c, law)
-    natural = p.run().clone()
+    bound = tc_bound(p) if force_tc else p.q.max_queries
+    natural = p.run(bound).clone()
     assert p.dc.status_bits() == 0
     dev = p.out.device
     orders = [pk.longest_first(c.context_lens),
@@ -452,7 +465,7 @@ def test_sequence_order_does_not_change_outputs(law):
     for order in orders:
         p.out.fill_(float("nan"))
         pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
-                         p.dc.block_tables, p.dc.context_lens, p.q.max_queries,
+                         p.dc.block_tables, p.dc.context_lens, bound,
                          c.max_context_len, c.scale, c.k_scale, c.v_scale, p.dc.status,
                          seq_order=torch.from_numpy(order).to(dev))
         assert p.dc.status_bits() == 0
@@ -460,6 +473,6 @@ def test_sequence_order_does_not_change_outputs(law):
     bad = torch.from_numpy(orders[0].copy()).to(dev)
     bad[5] = c.num_seqs
     pk.paged_prefill(p.out, p.query, p.query_start, p.dc.k_cache, p.dc.v_cache,
-                     p.dc.block_tables, p.dc.context_lens, p.q.max_queries, c.max_context_len,
+                     p.dc.block_tables, p.dc.context_lens, bound, c.max_context_len,
                      c.scale, c.k_scale, c.v_scale, p.dc.status, seq_order=bad)
     assert p.dc.status_bits() & pk.DEV_BAD_ORDER
