@@ -501,9 +501,10 @@ def prefill_kernel_name(case, max_queries: int) -> str:
     documented with it in pagedkv.h)."""
     e4m3 = case.cache_dtype == "e4m3"
     rows = max_queries * case.group
-    if rows <= (16 if e4m3 or case.head_size > 128 else 32):
+    if rows <= (16 if case.head_size > 128 else 32):
         if rows > 16:
-            return "paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp)"
+            return "paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp" + (
+                ", E4M3 widened in registers)" if e4m3 else ")")
         return "paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows" + (
             ", E4M3 widened in registers)" if e4m3 else ")")
     if case.head_size <= 128 and max_queries > 128 // case.group and not e4m3:

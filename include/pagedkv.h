@@ -343,8 +343,8 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  Other arguments as pa_decode; scale must be > 0.
  *  Kernel selection, by the arguments alone: with max_queries_per_seq *
  *  (num_q_heads / num_kv_heads) query rows per sequence and KV head at most
- *  32 (a 16-bit cache of the query's type, head_size <= 128) or 16 (an E4M3
- *  cache, or head_size 256), a 16-bit query, on the shapes of the TMA decode
+ *  32 (head_size <= 128) or 16 (head_size 256), a 16-bit query with a cache
+ *  of its type or of E4M3 codes, on the shapes of the TMA decode
  *  (rows of 128, 256 or 512 bytes, block_size 8, 16 or a multiple of 32),
  *  the warp-level MMA kernels run, reading each sequence's K/V once for all
  *  its rows (speculative verification). Else a

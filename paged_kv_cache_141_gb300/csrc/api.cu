@@ -229,10 +229,10 @@ void bind_fused_write(DecodeParams& p, const void* key, const void* value,
 // The warp-level MMA multi-query kernel (a few query rows per sequence and KV
 // head): 16-bit query and a cache of the same type or of E4M3 codes, on the
 // shapes of the TMA decode.
-// Rows per (sequence, KV head) it takes: 32 for 16-bit caches at head size
-// <= 128 (two n-tiles per warp), else 16.
-long long prefill_mma_max_rows(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size) {
-    return cache_dtype == q_dtype && head_size <= 128 ? 32 : 16;
+// Rows per (sequence, KV head) it takes: 32 at head size <= 128 (two n-tiles
+// per warp), 16 at head size 256.
+long long prefill_mma_max_rows(int head_size) {
+    return head_size <= 128 ? 32 : 16;
 }
 
 bool prefill_mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, int block_size,
@@ -558,7 +558,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     p.max_queries = max_queries_per_seq;
     p.seq_order = seq_order;
     if ((long long)max_queries_per_seq * p.group <=
-            prefill_mma_max_rows(q_dtype, cache_dtype, head_size) &&
+            prefill_mma_max_rows(head_size) &&
         prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks,
                              num_kv_heads)) {
         // one pass over each sequence's K/V for all of its query rows

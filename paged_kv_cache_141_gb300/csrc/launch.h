@@ -91,8 +91,8 @@ cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, in
                                         bool split, cudaStream_t stream);
 
 // Multi-query paged attention for a few query rows per (sequence, KV head)
-// (max_queries * group <= 32 for 16-bit caches at head_size <= 128, else
-// <= 16) on warp-level MMA: 16-bit query with a cache of
+// (max_queries * group <= 32 at head_size <= 128, <= 16 at 256) on
+// warp-level MMA: 16-bit query with a cache of
 // the same type (head_size 64/128/256) or E4M3 (128/256), TMA-eligible shapes.
 // Uses the multi-query fields of DecodeParams; single pass.
 cudaError_t launch_prefill_mma_f16(const DecodeParams& p, int head_size, cudaStream_t stream);

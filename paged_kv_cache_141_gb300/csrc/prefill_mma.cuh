@@ -511,18 +511,21 @@ paged_prefill_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 
 // ---------------------------------------------------------------- 32 rows
 // Four 8-row n-tiles per CTA (up to 32 rows: 8 draft tokens at G = 4), for
-// 16-bit caches at head size <= 128. A warp takes two n-tiles (16 rows), so
+// 16-bit and E4M3 caches at head size <= 128. A warp takes two n-tiles (16 rows), so
 // each K or V fragment it loads feeds two MMAs, and a stage is read by two
 // warps instead of four; warps w and w + 2 take the same rows on alternate
 // stages and are merged at the end. The query rows sit in shared memory in
 // the swizzled layout of the K tiles and are read with ldmatrix as the B
 // operand (both n-tiles' fragments of a k-step in one load), which leaves
-// the registers to the two n-tiles' accumulators.
+// the registers to the two n-tiles' accumulators. For E4M3 caches the rows
+// are stored as binary16 in the k order of the widened K fragments (as the
+// query registers of the kernel above), and K/V fragments are widened in
+// registers.
 constexpr int kMq2Rows = 32;
 
-template <typename T, int D>
+template <typename CT, int D>
 struct Mq2Smem {
-    using Ring = MmaSmem<T, D>;
+    using Ring = MmaSmem<CT, D>;
     static constexpr int kNst = Ring::kNst;
     static constexpr int kQBytes = kMq2Rows * D * 2;             // the CTA's query rows
     static constexpr int kCombineBytes = kTmaConsumerWarps * 16 * (D + 2) * 4;
@@ -534,17 +537,19 @@ struct Mq2Smem {
     static constexpr int kAlloc = kBytes + 1024;                // room to align the ring to 1 KB
 };
 
-template <typename T, int D>
+template <typename QT, typename CT, int D>
 __global__ void __launch_bounds__(kTmaThreads, 3)
 paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
-    using S = TmaShape<T, D>;
-    using Smem = Mq2Smem<T, D>;
-    using Ops = MmaOps<T>;
+    using S = TmaShape<CT, D>;
+    using Smem = Mq2Smem<CT, D>;
+    using MT = typename MathType<CT>::T;
+    using Ops = MmaOps<MT>;
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
     constexpr int CW = kTmaConsumerWarps;                // consumer warps; warp CW loads
     constexpr int NST = Smem::kNst;
     static_assert(NST % 2 == 0, "a slot's stages belong to one warp pair");
     static_assert(D <= 128, "two n-tiles' accumulators in registers");
-    constexpr bool kOneTerm = std::is_same<T, __half>::value;   // binary16 P as one term
+    constexpr bool kOneTerm = std::is_same<MT, __half>::value;  // binary16 P as one term
     constexpr int KS = D / 16;
     constexpr int kQSpan = kMq2Rows * 128;               // bytes of one 128-byte column span
     const DecodeParams& p = tp.p;
@@ -597,12 +602,14 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
     __syncthreads();
 
     if (warp == CW) {
-        mq_load_stages<T, D, NST>(tp, s, kvh, Tend, ring, full, empty, lane);
+        mq_load_stages<CT, D, NST>(tp, s, kvh, Tend, ring, full, empty, lane);
         return;
     }
 
     // ---- the CTA's query rows -> shared memory, zero past the sequence's,
-    // row r's 16-byte chunk c of span c / 8 at chunk (c mod 8) ^ (r mod 8)
+    // row r's 16-byte chunk c of span c / 8 at chunk (c mod 8) ^ (r mod 8).
+    // E4M3: binary16, chunk c = 2 ks + h holding positions 8 h .. 8 h + 7 of
+    // k-step ks, position 2 t + j <-> d = 16 ks + 4 t + 2 h + j.
     constexpr int CPR = D / 8;
     for (int i = threadIdx.x; i < kMq2Rows * CPR; i += CW * 32) {
         const int r = i / CPR, c = i - r * CPR;
@@ -610,10 +617,18 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (rg < R) {
             const int ti = rg / G;
-            const T* src = reinterpret_cast<const T*>(p.query) +
-                           ((size_t)(q0 + ti) * p.num_q_heads + (size_t)kvh * G + (rg - ti * G)) * D +
-                           c * 8;
-            v = *reinterpret_cast<const uint4*>(src);
+            const QT* qrow_g = reinterpret_cast<const QT*>(p.query) +
+                               ((size_t)(q0 + ti) * p.num_q_heads + (size_t)kvh * G + (rg - ti * G)) * D;
+            if constexpr (kFp8) {
+                const QT* q4 = qrow_g + 16 * (c >> 1) + 2 * (c & 1);
+                uint32_t w[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                    w[t] = Ops::pack(to_float(q4[4 * t]), to_float(q4[4 * t + 1]));
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+                v = *reinterpret_cast<const uint4*>(qrow_g + c * 8);
+            }
         }
         *reinterpret_cast<uint4*>(qsm + (c >> 3) * kQSpan + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
     }
@@ -649,7 +664,7 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
             m_run[nt][j] = -INFINITY;
             l_run[nt][j] = 0.f;
         }
-    const float qk_mul = p.q_mul;
+    const float qk_mul = kFp8 ? p.q_mul * 256.f : p.q_mul;  // E4M3: the widening's 2^-8
     // B fragments of a k-step: matrix mi = (n-tile mi / 2, 8-element half mi mod 2)
     const int qrow = 16 * pi + 8 * (mi >> 1) + r8;
     const uint8_t* qbase = qsm + qrow * 128;
@@ -671,19 +686,50 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) sc[nt][mt][e] = 0.f;
+        if constexpr (kFp8) {
+            // one ldmatrix.x4 of E4M3 bytes covers two k-steps of 16 keys,
+            // widened in registers (decode_mma.cuh)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            const int cq = 2 * ks + (mi & 1);
-            uint32_t b[4];
-            ldmatrix_x4(b, qbase + (cq >> 3) * kQSpan + (((cq & 7) ^ (qrow & 7)) << 4));
+            for (int kp = 0; kp < KS / 2; ++kp) {
+                uint32_t b[2][4];
 #pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const int row = 16 * mt + (mi & 1) * 8 + r8;
-                const int c = 2 * ks + (mi >> 1);
-                uint32_t a[4];
-                ldmatrix_x4(a, Kst + (c >> 3) * S::kSpanTileBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4));
-                Ops::mma(sc[0][mt], a, b[0], b[1]);
-                Ops::mma(sc[1][mt], a, b[2], b[3]);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int cq = 2 * (2 * kp + h2) + (mi & 1);
+                    ldmatrix_x4(b[h2], qbase + (cq >> 3) * kQSpan + (((cq & 7) ^ (qrow & 7)) << 4));
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int row = 16 * mt + (mi & 1) * 8 + r8;
+                    const int c = 2 * kp + (mi >> 1);
+                    uint32_t x[4];
+                    ldmatrix_x4(x, Kst + (c >> 3) * S::kSpanTileBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t a[4] = {
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4342)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4342))};
+                        Ops::mma(sc[0][mt], a, b[h2][0], b[h2][1]);
+                        Ops::mma(sc[1][mt], a, b[h2][2], b[h2][3]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const int cq = 2 * ks + (mi & 1);
+                uint32_t b[4];
+                ldmatrix_x4(b, qbase + (cq >> 3) * kQSpan + (((cq & 7) ^ (qrow & 7)) << 4));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const int row = 16 * mt + (mi & 1) * 8 + r8;
+                    const int c = 2 * ks + (mi >> 1);
+                    uint32_t a[4];
+                    ldmatrix_x4(a, Kst + (c >> 3) * S::kSpanTileBytes + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+                    Ops::mma(sc[0][mt], a, b[0], b[1]);
+                    Ops::mma(sc[1][mt], a, b[2], b[3]);
+                }
             }
         }
 #pragma unroll
@@ -780,25 +826,54 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
                 const int key = 16 * kt + 2 * t4 + 8 * h;
                 vmask[kt][h] = (key < nvalid ? 0x0000ffffu : 0u) | (key + 1 < nvalid ? 0xffff0000u : 0u);
             }
+        if constexpr (kFp8) {
+            // one 16-byte chunk = 16 d of all 32 keys (decode_mma.cuh):
+            // fragment row g <-> d 2g, row g + 8 <-> d 2g + 1
 #pragma unroll
-        for (int md = 0; md < KS; ++md) {
+            for (int md = 0; md < KS; ++md) {
+                const int row = 8 * mi + r8;
+                uint32_t y[4];
+                ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
+                                         (((md & 7) ^ (row & 7)) << 4));
 #pragma unroll
-            for (int kt = 0; kt < 2; ++kt) {
-                const int row = 16 * kt + (mi >> 1) * 8 + r8;
-                const int c = 2 * md + (mi & 1);
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
-                                         (((c & 7) ^ (row & 7)) << 4));
-                if (ragged) {
-                    a[0] &= vmask[kt][0];
-                    a[1] &= vmask[kt][0];
-                    a[2] &= vmask[kt][1];
-                    a[3] &= vmask[kt][1];
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
+                    uint32_t a[4] = {e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4240)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4341)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4240)),
+                                     e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4341))};
+                    if (ragged) {
+                        a[0] &= vmask[kt][0];
+                        a[1] &= vmask[kt][0];
+                        a[2] &= vmask[kt][1];
+                        a[3] &= vmask[kt][1];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+                        Ops::mma(acc[nt][md], a, bh[nt][kt][0], bh[nt][kt][1]);
                 }
+            }
+        } else {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    Ops::mma(acc[nt][md], a, bh[nt][kt][0], bh[nt][kt][1]);
-                    if constexpr (!kOneTerm) Ops::mma(acc[nt][md], a, bl[nt][kt][0], bl[nt][kt][1]);
+            for (int md = 0; md < KS; ++md) {
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int row = 16 * kt + (mi >> 1) * 8 + r8;
+                    const int c = 2 * md + (mi & 1);
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
+                                             (((c & 7) ^ (row & 7)) << 4));
+                    if (ragged) {
+                        a[0] &= vmask[kt][0];
+                        a[1] &= vmask[kt][0];
+                        a[2] &= vmask[kt][1];
+                        a[3] &= vmask[kt][1];
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        Ops::mma(acc[nt][md], a, bh[nt][kt][0], bh[nt][kt][1]);
+                        if constexpr (!kOneTerm) Ops::mma(acc[nt][md], a, bl[nt][kt][0], bl[nt][kt][1]);
+                    }
                 }
             }
         }
@@ -836,13 +911,14 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
             for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                    co[(warp * 16 + 8 * nt + 2 * t4 + j) * D + 16 * md + g + 8 * hr] =
-                        acc[nt][md][2 * hr + j];
+                    co[(warp * 16 + 8 * nt + 2 * t4 + j) * D +
+                       (kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr)] = acc[nt][md][2 * hr + j];
     named_barrier(1, CW * 32);
 
     // CTA row rr = 16 pair + c was computed by warps pair and pair + 2
     const int nrows = min(kMq2Rows, R - row0);
-    T* out = reinterpret_cast<T*>(p.out);
+    const float vm = kFp8 ? p.v_mul * 256.f : p.v_mul;
+    QT* out = reinterpret_cast<QT*>(p.out);
     for (int idx = threadIdx.x; idx < nrows * D; idx += CW * 32) {
         const int rr = idx / D;
         const int e = idx - rr * D;
@@ -857,14 +933,14 @@ paged_prefill_mma2_kernel(const __grid_constant__ TmaDecodeParams tp) {
         const int r = row0 + rr;
         const int i = r / G;
         const size_t orow = (size_t)(q0 + i) * p.num_q_heads + (size_t)kvh * G + (r - i * G);
-        out[orow * D + e] = from_float<T>(__fdiv_rn(O, W) * p.v_mul);
+        out[orow * D + e] = from_float<QT>(__fdiv_rn(O, W) * vm);
     }
 }
 
-template <typename T, int D>
+template <typename QT, typename CT, int D>
 cudaError_t launch_prefill_mma2(const TmaDecodeParams& tp, cudaStream_t stream) {
-    using Smem = Mq2Smem<T, D>;
-    auto kern = paged_prefill_mma2_kernel<T, D>;
+    using Smem = Mq2Smem<CT, D>;
+    auto kern = paged_prefill_mma2_kernel<QT, CT, D>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
     if (e != cudaSuccess) return e;
     const DecodeParams& p = tp.p;
@@ -897,8 +973,8 @@ template <typename QT, typename CT, int D>
 cudaError_t launch_prefill_mma_d(const TmaDecodeParams& tp, cudaStream_t stream) {
     const long long rows = (long long)tp.p.max_queries * tp.p.group;
     if (rows <= 8) return launch_prefill_mma_variant<QT, CT, D, 1>(tp, stream);
-    if constexpr (std::is_same<QT, CT>::value && D <= 128) {
-        if (rows > 8 * kMqMaxTiles) return launch_prefill_mma2<CT, D>(tp, stream);
+    if constexpr (D <= 128) {
+        if (rows > 8 * kMqMaxTiles) return launch_prefill_mma2<QT, CT, D>(tp, stream);
     }
     return launch_prefill_mma_variant<QT, CT, D, kMqMaxTiles>(tp, stream);
 }

@@ -72,11 +72,9 @@ class Prefill:
 
 def mma_max_rows(case):
     """max_queries_per_seq * group up to this selects the warp-level MMA
-    kernels (32 for a 16-bit cache of the query's type at head size <= 128,
-    else 16); a larger bound (any bound >= every Q_s is valid) selects the
-    tcgen05 kernels."""
-    same = case.cache_dtype == case.q_dtype
-    return 32 if same and case.head_size <= 128 else 16
+    kernels (32 at head size <= 128, 16 at 256); a larger bound (any bound
+    >= every Q_s is valid) selects the tcgen05 kernels."""
+    return 32 if case.head_size <= 128 else 16
 
 
 def tc_bound(p):
@@ -157,7 +155,7 @@ def test_prefill_e4m3_tensor_core_sweep(i):
 
 
 # warp-level MMA shapes: one and two 8-row n-tiles (up to 16 rows), four
-# n-tiles two per warp (17..32 rows, 16-bit caches at head size <= 128),
+# n-tiles two per warp (17..32 rows, head size <= 128, 16-bit and E4M3),
 # padding rows (G = 3), one token of a 16-head group, head sizes 64/128/256,
 # block sizes 8..256, whole prefills of short sequences, E4M3 caches at head
 # size 128 and 256
@@ -167,6 +165,8 @@ MMA_SWEEP = [
     (3, 6, 2, 128, 256, "bf16", "bf16", ("fixed", [31, 32, 600]), ("uniform", 6, 10)),
     (24, 8, 8, 128, 32, "f16", "f16", ("uniform", 1, 28), ("all",)),
     (4, 8, 2, 64, 64, "bf16", "bf16", ("uniform", 100, 400), ("fixed", [8, 5, 7, 6])),
+    (4, 32, 8, 128, 16, "bf16", "e4m3", ("loguniform", 1, 900), ("uniform", 1, 8)),
+    (3, 16, 2, 128, 32, "f16", "e4m3", ("uniform", 20, 500), ("uniform", 3, 4)),
     # S, Hq, Hkv, d, B, query dtype, cache dtype, lengths, queries
     (6, 32, 8, 128, 16, "bf16", "bf16", ("uniform", 1, 700), ("uniform", 1, 4)),
     (5, 8, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
