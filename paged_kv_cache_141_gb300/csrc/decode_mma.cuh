@@ -210,9 +210,16 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             tma_prefetch_map(&tp.k_map);
             tma_prefetch_map(&tp.v_map);
         }
+        // the fused write of position L - 1 (in stage kw of this range): its
+        // stores go out once the ring's first stages are issued, overlapping
+        // the wait for a free slot, and the fence right before stage kw's copy
+        const bool writes = p.new_key && L - 1 >= T0 && L - 1 < Tend;
+        const int kw = writes ? (L - 1 - T0) / kTmaStageTokens : -1;
+        const int kstore = kw < NST ? kw : NST;
         int issued = 0;
         for (int k = 0; k < n_st; ++k) {
             const int slot = k % NST;
+            if (k == kstore) fused_store_token<QT, CT, D>(p, s, kvh, L, lane);
             if (k >= NST) {
                 bool ok = true;
                 if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
@@ -221,8 +228,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             }
             const int t_lo = T0 + k * kTmaStageTokens;
             const int t_hi = min(t_lo + kTmaStageTokens, Tend);
-            if (p.new_key && L - 1 >= t_lo && L - 1 < t_hi)
-                fused_write_token<QT, CT, D>(p, s, kvh, L, lane);
+            if (k == kw) fused_write_fence();
             const int j0 = t_lo / B;
             const int nseg = (t_hi - 1) / B - j0 + 1;
             uint32_t bytes = 0;

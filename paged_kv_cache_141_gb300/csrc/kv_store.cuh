@@ -66,14 +66,16 @@ __device__ __forceinline__ void store_kv_vector(void* cache, size_t dst, const u
 
 // Fused KV write, run by a decode kernel's producer warp (all 32 lanes) before
 // it loads the stage that holds position L-1 of sequence s: store the
-// sequence's newest key and value (KV head kvh) at slot_mapping[s], then fence
-// the generic-proxy stores against the bulk-copy (async-proxy) reads that
-// follow. A negative slot stores nothing; a slot outside the pool sets
+// sequence's newest key and value (KV head kvh) at slot_mapping[s]
+// (fused_store_token), then fence the generic-proxy stores against the
+// bulk-copy (async-proxy) reads that follow (fused_write_token does both; a
+// producer may issue the stores earlier and fence right before that stage's
+// copy). A negative slot stores nothing; a slot outside the pool sets
 // PA_DEV_BAD_SLOT; a slot that is not position L-1 of the sequence's table
 // sets PA_DEV_SLOT_MISMATCH (the token is still stored, the decode may not see
 // it).
 template <typename QT, typename CT, int D>
-__device__ __forceinline__ void fused_write_token(const DecodeParams& p, int s, int kvh, int L,
+__device__ __forceinline__ void fused_store_token(const DecodeParams& p, int s, int kvh, int L,
                                                   int lane) {
     constexpr bool kE4M3 = std::is_same<CT, e4m3_t>::value;
     constexpr int VEC = 16 / (int)sizeof(QT);
@@ -101,8 +103,19 @@ __device__ __forceinline__ void fused_write_token(const DecodeParams& p, int s, 
             }
         }
     }
+}
+
+// The stores' fence against the async proxy, by the lanes that stored.
+__device__ __forceinline__ void fused_write_fence() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __syncwarp();
+}
+
+template <typename QT, typename CT, int D>
+__device__ __forceinline__ void fused_write_token(const DecodeParams& p, int s, int kvh, int L,
+                                                  int lane) {
+    fused_store_token<QT, CT, D>(p, s, kvh, L, lane);
+    fused_write_fence();
 }
 
 }  // namespace pagedkv
