@@ -26,6 +26,9 @@ paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
     const int s = (int)(item / num_q_heads);
     const int h = (int)(item - (long long)s * num_q_heads);
     const size_t row = (size_t)s * num_q_heads + h;
+    // launched as a programmatic dependent of the partition kernel: nothing
+    // the previous kernels wrote is read before they have completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     int L = context_lens[s];
     const long long cap = (long long)max_parts * partition_size;
@@ -46,10 +49,22 @@ static cudaError_t launch_merge_t(OT* out, const float* tmp_out, const float* ma
                                   uint32_t* status, cudaStream_t stream) {
     const long long items = (long long)num_seqs * num_q_heads;
     const unsigned grid = (unsigned)((items + kMergeWarps - 1) / kMergeWarps);
-    paged_merge_kernel<D, OT><<<grid, kMergeWarps * 32, 0, stream>>>(
-        out, tmp_out, max_logits, exp_sums, context_lens, num_seqs, num_q_heads, partition_size,
-        max_parts, status);
-    return cudaGetLastError();
+    // programmatic dependent launch: the merge's CTAs may be scheduled while
+    // the previous kernel drains; each waits (griddepcontrol.wait) for it to
+    // complete before reading anything, so stream order is kept
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_merge_kernel<D, OT>, out, tmp_out, max_logits, exp_sums,
+                              context_lens, num_seqs, num_q_heads, partition_size, max_parts,
+                              status);
 }
 
 template <typename OT>
