@@ -155,3 +155,34 @@ def test_wait_selftest_argument_errors(lib):
     assert L.pa_selftest_wait(0, None, None) == pk.PA_ERR_INVALID_ARG       # status required
     assert L.pa_selftest_wait(2, ctypes.c_void_p(256), None) == pk.PA_ERR_INVALID_ARG
     assert L.pa_selftest_wait(1, ctypes.c_void_p(258), None) == pk.PA_ERR_INVALID_ARG
+
+
+def test_longest_first_is_a_stable_permutation():
+    """The host-side order helper for pa_paged_prefill's seq_order: a
+    permutation of the sequences, non-increasing lengths, ties in index order,
+    int32 (the ABI's type)."""
+    import numpy as np
+    from paged_kv_cache_141_gb300 import binding as pk
+    lens = np.array([5, 900, 12, 900, 0, 4096, 12], dtype=np.int32)
+    order = pk.longest_first(lens)
+    assert order.dtype == np.int32
+    assert sorted(order.tolist()) == list(range(len(lens)))
+    assert order.tolist() == [5, 1, 3, 2, 6, 0, 4]
+    assert np.all(np.diff(lens[order]) <= 0)
+    assert pk.longest_first(np.zeros(0, dtype=np.int32)).shape == (0,)
+
+
+def test_paged_prefill_rejects_a_misshaped_order():
+    """seq_order must be int32 [num_seqs]: the binding checks before the call."""
+    import pytest
+    import torch
+    from paged_kv_cache_141_gb300 import binding as pk
+    S, Hq, Hkv, D, B = 2, 8, 2, 128, 16
+    q = torch.zeros(3, Hq, D, dtype=torch.bfloat16)
+    kc = torch.zeros(4, Hkv, B, D, dtype=torch.bfloat16)
+    qs = torch.tensor([0, 1, 3], dtype=torch.int32)
+    bt = torch.zeros(S, 2, dtype=torch.int32)
+    cl = torch.tensor([5, 9], dtype=torch.int32)
+    for bad in (torch.zeros(S, dtype=torch.int64), torch.zeros(S + 1, dtype=torch.int32)):
+        with pytest.raises(ValueError):
+            pk.paged_prefill(q, q, qs, kc, kc, bt, cl, 2, 32, 0.1, seq_order=bad)
