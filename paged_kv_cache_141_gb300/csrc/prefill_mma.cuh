@@ -8,26 +8,34 @@
 // ("Lecture 3: PagedAttention and vLLM", "the paged implementation of
 // attention"; the queries there carry a num_queries axis).
 //
-// The kernel is the tensor-core decode (decode_mma.cuh) with the MMA's eight
-// columns holding query rows instead of the query heads of one token. The
-// producer warp loads each 32-key stage of K and V once per CTA (tensor TMA,
-// 128-byte swizzle). Consumer warp w (of 4) owns n-tile w mod NT; the NT
-// warps of different n-tiles all read every stage, the 4 / NT warps of one
-// n-tile take alternate stages and are merged at the end as in the decode.
-// Per warp and
-// 16-key row tile: S^T (16 keys x 8 rows) = K Q^T, each column masked at its
-// row's causal limit, an online softmax per row (base 2), O^T += V^T P^T with
-// P as two bf16 terms (bf16 caches) or one binary16 term (f16 caches, E4M3
-// caches widened to binary16: at most 2^-11 relative error per weight).
+// Two kernels, both the tensor-core decode (decode_mma.cuh) with the MMA's
+// eight columns holding query rows instead of the query heads of one token.
+// The producer warp loads each 32-key stage of K and V once per CTA (tensor
+// TMA, 128-byte swizzle), whatever the number of rows. Per warp and 16-key
+// row tile: S^T (16 keys x 8 rows) = K Q^T, each column masked at its row's
+// causal limit, an online softmax per row (base 2, against a reference max
+// that moves only past 2^8), O^T += V^T P^T with P as two bf16 terms (bf16
+// caches) or one binary16 term (f16 caches, E4M3 caches widened to binary16:
+// at most 2^-11 relative error per weight).
 //
-// Why a second multi-query kernel: for the 16 or fewer rows of a short
-// verification step a 128-row tcgen05 tile is mostly padding, and its one CTA
-// per SM leaves the SM idle while a unit starts and drains. Here one CTA
-// streams its sequence's K/V once for all its rows at up to twice the
+//  * paged_prefill_mma_kernel, up to 16 rows (NT = 1 or 2 n-tiles of 8):
+//    consumer warp w (of 4) owns n-tile w mod NT; the NT warps of different
+//    n-tiles all read every stage, the 4 / NT warps of one n-tile take
+//    alternate stages and are merged at the end as in the decode. The query
+//    fragments stay in registers.
+//  * paged_prefill_mma2_kernel, 17 to 32 rows (head size <= 128): a warp owns
+//    two n-tiles, so each K or V fragment it loads feeds two MMAs; warps w and
+//    w + 2 take alternate stages. The query rows sit in shared memory and are
+//    read with ldmatrix, leaving the registers to two n-tiles' accumulators.
+//
+// Why these next to the tcgen05 kernels: for the 32 or fewer rows of a
+// verification step a 128-row tcgen05 tile is mostly padding, and its one
+// CTA per SM leaves the SM idle while a unit starts and drains. Here one CTA
+// streams its sequence's K/V once for all its rows at a few times the
 // decode's MMA work per byte, with 3 (16-bit) to 4 (E4M3) CTAs per SM
-// overlapping one another's starts and ends. (Four n-tiles, 32 rows, are
-// slower than the tcgen05 kernel: four warps' MMA and softmax work per stage
-// leave the warps latency-bound below the HBM rate.)
+// overlapping one another's starts and ends. (One n-tile per warp at 32 rows,
+// four warps per stage, was latency-bound below the tcgen05 kernel; beyond
+// 32 rows the tcgen05 kernels are faster.)
 //
 // Keys past a stage's last needed key are masked by a select on the scores
 // (never a multiply) and their V^T fragments are zeroed in registers, so stale
