@@ -50,18 +50,21 @@ def test_decode_step_graph_replay(cfg):
         assert torch.equal(out.view(torch.uint8), eager.view(torch.uint8))
 
 
-def test_multi_query_graph_replay():
+@pytest.mark.parametrize("qn,ordered", [(100, False), (4, False), (8, True)],
+                         ids=["tcgen05", "warp-mma", "warp-mma2-ordered"])
+def test_multi_query_graph_replay(qn, ordered):
     c = W.config_case(3, num_seqs=16)
-    q = W.make_queries(c, ("fixed", np.minimum(100, c.context_lens)))
+    q = W.make_queries(c, ("fixed", np.minimum(qn, c.context_lens)))
     dc = DeviceCase(c)
     dc.write_step()
     query = host_to_torch(q.query, c.q_dtype).cuda()
     qs = torch.from_numpy(q.query_start).cuda()
+    order = torch.from_numpy(pk.longest_first(c.context_lens)).cuda() if ordered else None
 
     def run(out):
         pk.paged_prefill(out, query, qs, dc.k_cache, dc.v_cache, dc.block_tables,
                          dc.context_lens, q.max_queries, c.max_context_len, c.scale, 1.0, 1.0,
-                         dc.status, torch.cuda.current_stream())
+                         dc.status, torch.cuda.current_stream(), seq_order=order)
 
     eager = torch.empty_like(query)
     run(eager)

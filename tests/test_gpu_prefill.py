@@ -167,6 +167,7 @@ MMA_SWEEP = [
     (4, 8, 2, 64, 64, "bf16", "bf16", ("uniform", 100, 400), ("fixed", [8, 5, 7, 6])),
     (4, 32, 8, 128, 16, "bf16", "e4m3", ("loguniform", 1, 900), ("uniform", 1, 8)),
     (3, 16, 2, 128, 32, "f16", "e4m3", ("uniform", 20, 500), ("uniform", 3, 4)),
+    (4, 12, 4, 128, 16, "bf16", "e4m3", ("fixed", [9, 33, 64, 700]), ("uniform", 6, 10)),
     # S, Hq, Hkv, d, B, query dtype, cache dtype, lengths, queries
     (6, 32, 8, 128, 16, "bf16", "bf16", ("uniform", 1, 700), ("uniform", 1, 4)),
     (5, 8, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
