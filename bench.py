@@ -497,19 +497,22 @@ def prefill_cpu_baseline(case, q, tensor: bool, budget_s: float = 12.0):
 
 
 def prefill_kernel_name(case, max_queries: int) -> str:
-    """The kernel pa_paged_prefill selects for this workload (the rule
-    documented with it in pagedkv.h)."""
+    """The kernel pa_paged_prefill selects for this workload, as the library
+    reports it (pa_paged_prefill_kernel)."""
+    from paged_kv_cache_141_gb300 import binding as pk
+    code = {"f32": pk.PA_F32, "f16": pk.PA_F16, "bf16": pk.PA_BF16, "e4m3": pk.PA_FP8_E4M3}
+    kind = pk.prefill_kernel(max_queries, case.num_q_heads, case.num_kv_heads, case.head_size,
+                             case.block_size, case.num_blocks, code[case.q_dtype],
+                             code[case.cache_dtype])
     e4m3 = case.cache_dtype == "e4m3"
-    rows = max_queries * case.group
-    if rows <= (16 if case.head_size > 128 else 32):
-        if rows > 16:
-            return "paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp" + (
-                ", E4M3 widened in registers)" if e4m3 else ")")
-        return "paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows" + (
-            ", E4M3 widened in registers)" if e4m3 else ")")
-    if case.head_size <= 128 and max_queries > 128 // case.group and not e4m3:
-        return "paged_prefill_tc2_kernel (two query tiles per CTA)"
-    return "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else "")
+    widened = ", E4M3 widened in registers" if e4m3 else ""
+    return {
+        "mma": f"paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows{widened})",
+        "mma_two_tiles": f"paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp{widened})",
+        "tc_two_tiles": "paged_prefill_tc2_kernel (two query tiles per CTA)",
+        "tc": "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else ""),
+        "cuda_cores": "paged_decode_simt_kernel (one query token per work unit)",
+    }[kind]
 
 
 def run_prefill(args):

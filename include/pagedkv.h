@@ -356,6 +356,24 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
  *  num_queries == 0 launches nothing.
  */
+/* The kernel pa_paged_prefill selects for a shape (16-byte-aligned pointers
+ * assumed; the selection depends on nothing else). */
+typedef enum {
+    PA_PREFILL_CUDA_CORES = 0,     /* one query token per work unit (the decode kernel) */
+    PA_PREFILL_MMA = 1,            /* warp-level MMA, up to 16 rows per (sequence, KV head) */
+    PA_PREFILL_MMA_TWO_TILES = 2,  /* warp-level MMA, 17-32 rows, two n-tiles per warp */
+    PA_PREFILL_TC = 3,             /* tcgen05, one 128-row query tile per CTA */
+    PA_PREFILL_TC_TWO_TILES = 4    /* tcgen05, two query tiles per CTA */
+} pa_prefill_kernel;
+
+/* Host only (no launch, no GPU needed): the pa_prefill_kernel value for
+ * these arguments of pa_paged_prefill, or -1 where pa_paged_prefill would
+ * reject them (max_queries_per_seq < 1, a group that is not an integer, an
+ * unsupported type pair, head size or block size). */
+int pa_paged_prefill_kernel(int max_queries_per_seq, int num_q_heads, int num_kv_heads,
+                            int head_size, int block_size, int64_t num_blocks, pa_dtype q_dtype,
+                            pa_dtype cache_dtype);
+
 pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_start,
                            int num_queries, int max_queries_per_seq, const void* k_cache,
                            const void* v_cache, const int32_t* block_tables,

@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
                                                  I, F, I, I, F, F, I, P, S, P, P]
         L.pa_paged_prefill.argtypes = [P, P, P, I, I, P, P, P, I, P, I, I, I, I, I, I64, I, F, I,
                                        I, F, F, P, P, P]
+        L.pa_paged_prefill_kernel.argtypes = [I, I, I, I, I, I64, I, I]
+        L.pa_paged_prefill_kernel.restype = I
         L.pa_copy_blocks.argtypes = [P, P, P, I64, I, I, I, I64, I, P, P]
         L.pa_selftest_wait.argtypes = [I, P, P]
         L.pa_allocator_create.argtypes = [I64, I, I]
@@ -223,6 +225,22 @@ def paged_prefill(out, query, query_start, k_cache, v_cache, block_tables, conte
         D, B, nb, int(max_context_len), float(scale), _dtype(query), _dtype(k_cache),
         float(k_scale), float(v_scale), _ptr(seq_order), _ptr(dev_status), _stream(stream)),
         "pa_paged_prefill")
+
+
+PREFILL_KERNELS = {0: "cuda_cores", 1: "mma", 2: "mma_two_tiles", 3: "tc", 4: "tc_two_tiles"}
+
+
+def prefill_kernel(max_queries_per_seq, num_q_heads, num_kv_heads, head_size, block_size,
+                   num_blocks, q_dtype, cache_dtype) -> str:
+    """The kernel paged_prefill selects for a shape (host only): one of
+    PREFILL_KERNELS' names; dtypes as PA_* codes. Raises for a shape
+    paged_prefill rejects."""
+    k = lib().pa_paged_prefill_kernel(int(max_queries_per_seq), num_q_heads, num_kv_heads,
+                                      head_size, block_size, int(num_blocks), int(q_dtype),
+                                      int(cache_dtype))
+    if k < 0:
+        raise PagedKVError("pa_paged_prefill_kernel: unsupported arguments")
+    return PREFILL_KERNELS[k]
 
 
 def longest_first(context_lens) -> "np.ndarray":

@@ -247,8 +247,7 @@ bool prefill_mma_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size,
 // TMA box then starts on a swizzle-atom boundary), groups that fit the
 // 128-row tile, 16-byte-aligned rows, row coordinates below 2^31.
 bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, int block_size,
-                         int group, int64_t num_blocks, int num_kv_heads, const void* out,
-                         const void* query, const void* k_cache, const void* v_cache) {
+                         int group, int64_t num_blocks, int num_kv_heads) {
     if (!(q_dtype == PA_F16 || q_dtype == PA_BF16)) return false;
     if (cache_dtype == PA_FP8_E4M3) {
         if (head_size != 64 && head_size != 128) return false;      // E4M3 staging fits
@@ -257,11 +256,31 @@ bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, 
     }
     if (block_size < 8 || block_size > 256 || (block_size & (block_size - 1)) != 0) return false;
     if (group < 1 || group > 128) return false;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(out) | reinterpret_cast<uintptr_t>(query) |
-                        reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
-    if (a & 15) return false;
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
     return rows > 0 && rows < (1ll << 31);
+}
+
+// The kernel pa_paged_prefill runs: the warp-level MMA kernels for up to 32
+// rows per (sequence, KV head) (16 at head size 256), else the tcgen05 ones
+// (two query tiles per CTA for 16-bit caches at head size <= 128 with at
+// least two tiles per sequence), else one query token per work unit on the
+// CUDA cores. `aligned`: out, query and the caches are 16-byte aligned (the
+// tcgen05 rows).
+pa_prefill_kernel prefill_kernel(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size,
+                                 int block_size, int group, int64_t num_blocks, int num_kv_heads,
+                                 int max_queries, bool aligned) {
+    const long long rows = (long long)max_queries * group;
+    if (rows <= prefill_mma_max_rows(head_size) &&
+        prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks, num_kv_heads))
+        return rows <= 16 ? PA_PREFILL_MMA : PA_PREFILL_MMA_TWO_TILES;
+    if (aligned && prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, group,
+                                       num_blocks, num_kv_heads)) {
+        const int per_tile = 128 / group;
+        const int tiles = (max_queries + per_tile - 1) / per_tile;
+        const bool two = cache_dtype != PA_FP8_E4M3 && head_size <= 128 && tiles >= 2;
+        return two ? PA_PREFILL_TC_TWO_TILES : PA_PREFILL_TC;
+    }
+    return PA_PREFILL_CUDA_CORES;
 }
 
 }  // namespace
@@ -557,10 +576,10 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     p.num_queries = num_queries;
     p.max_queries = max_queries_per_seq;
     p.seq_order = seq_order;
-    if ((long long)max_queries_per_seq * p.group <=
-            prefill_mma_max_rows(head_size) &&
-        prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks,
-                             num_kv_heads)) {
+    const pa_prefill_kernel kind =
+        prefill_kernel(q_dtype, cache_dtype, head_size, block_size, p.group, num_blocks,
+                       num_kv_heads, max_queries_per_seq, aligned16(out, query, k_cache, v_cache));
+    if (kind == PA_PREFILL_MMA || kind == PA_PREFILL_MMA_TWO_TILES) {
         // one pass over each sequence's K/V for all of its query rows
         if (cache_dtype == PA_FP8_E4M3)
             return from_cuda(q_dtype == PA_F16 ? launch_prefill_mma_f16_e4m3(p, head_size, s)
@@ -568,8 +587,7 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
         return from_cuda(q_dtype == PA_F16 ? launch_prefill_mma_f16(p, head_size, s)
                                            : launch_prefill_mma_bf16(p, head_size, s));
     }
-    if (prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, p.group, num_blocks,
-                            num_kv_heads, out, query, k_cache, v_cache)) {
+    if (kind == PA_PREFILL_TC || kind == PA_PREFILL_TC_TWO_TILES) {
         PrefillParams pp{};
         pp.out = out;
         pp.query = query;
@@ -604,6 +622,21 @@ pa_status pa_paged_prefill(void* out, const void* query, const int32_t* query_st
     // token's causal prefix (the work is per token: no sequence order)
     p.seq_order = nullptr;
     return from_cuda(run_simt_decode_kernel(p, head_size, q_dtype, cache_dtype, s));
+}
+
+int pa_paged_prefill_kernel(int max_queries_per_seq, int num_q_heads, int num_kv_heads,
+                            int head_size, int block_size, int64_t num_blocks, pa_dtype q_dtype,
+                            pa_dtype cache_dtype) {
+    if (max_queries_per_seq < 1 || num_q_heads <= 0 || num_kv_heads <= 0 || block_size <= 0 ||
+        num_blocks < 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    if ((int)q_dtype < 0 || (int)q_dtype > 3 || (int)cache_dtype < 0 || (int)cache_dtype > 3)
+        return -1;
+    if (!supported_pair(q_dtype, cache_dtype) || !supported_head_size(head_size) ||
+        block_size > 1024)
+        return -1;
+    return prefill_kernel(q_dtype, cache_dtype, head_size, block_size, num_q_heads / num_kv_heads,
+                          num_blocks, num_kv_heads, max_queries_per_seq, true);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs,

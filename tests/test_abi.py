@@ -186,3 +186,44 @@ def test_paged_prefill_rejects_a_misshaped_order():
     for bad in (torch.zeros(S, dtype=torch.int64), torch.zeros(S + 1, dtype=torch.int32)):
         with pytest.raises(ValueError):
             pk.paged_prefill(q, q, qs, kc, kc, bt, cl, 2, 32, 0.1, seq_order=bad)
+
+
+def test_paged_prefill_kernel_selection(lib):
+    """The kernel choice of pa_paged_prefill, host only: warp-level MMA up to
+    32 rows per (sequence, KV head) (16 at head size 256), one or two n-tiles
+    per warp by 16 rows; tcgen05 above (two query tiles per CTA for 16-bit
+    caches at head size <= 128 with two or more tiles); CUDA cores for the
+    other types and block sizes; -1 for what the call rejects."""
+    from paged_kv_cache_141_gb300 import binding as pk
+    B16, F16, F32, E4 = pk.PA_BF16, pk.PA_F16, pk.PA_F32, pk.PA_FP8_E4M3
+    cases = [
+        # (max_queries, Hq, Hkv, d, B, q, cache) -> kernel
+        ((1, 32, 8, 128, 16, B16, B16), "mma"),
+        ((4, 32, 8, 128, 16, B16, B16), "mma"),
+        ((5, 32, 8, 128, 16, B16, B16), "mma_two_tiles"),
+        ((8, 32, 8, 128, 16, B16, B16), "mma_two_tiles"),
+        ((9, 32, 8, 128, 16, B16, B16), "tc"),
+        ((32, 32, 8, 128, 16, B16, B16), "tc"),
+        ((33, 32, 8, 128, 16, B16, B16), "tc_two_tiles"),
+        ((512, 32, 8, 128, 16, B16, B16), "tc_two_tiles"),
+        ((8, 32, 8, 128, 8, B16, B16), "mma_two_tiles"),
+        ((2, 64, 8, 128, 16, B16, E4), "mma"),
+        ((4, 64, 8, 128, 16, B16, E4), "mma_two_tiles"),
+        ((5, 64, 8, 128, 16, B16, E4), "tc"),
+        ((512, 64, 8, 128, 16, B16, E4), "tc"),
+        ((4, 16, 4, 256, 16, F16, F16), "mma"),
+        ((5, 16, 4, 256, 16, F16, F16), "tc"),
+        ((200, 16, 4, 256, 16, F16, F16), "tc"),
+        ((8, 16, 4, 256, 16, F16, E4), "cuda_cores"),
+        ((4, 16, 4, 128, 24, B16, B16), "cuda_cores"),
+        ((4, 16, 4, 128, 16, F32, F32), "cuda_cores"),
+        ((32, 32, 32, 128, 16, F16, F16), "mma_two_tiles"),
+        ((33, 32, 32, 128, 16, F16, F16), "tc"),
+    ]
+    for args, want in cases:
+        assert pk.prefill_kernel(*args[:5], 1000, *args[5:]) == want, (args, want)
+    L = pk.lib()
+    assert L.pa_paged_prefill_kernel(0, 32, 8, 128, 16, 1000, B16, B16) == -1
+    assert L.pa_paged_prefill_kernel(4, 30, 8, 128, 16, 1000, B16, B16) == -1
+    assert L.pa_paged_prefill_kernel(4, 32, 8, 96, 16, 1000, B16, B16) == -1
+    assert L.pa_paged_prefill_kernel(4, 32, 8, 128, 16, 1000, B16, F16) == -1
