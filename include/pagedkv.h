@@ -289,11 +289,17 @@ pa_status pa_write_decode_partitioned(void* out, const void* query, const void* 
  *  `workspace` / `workspace_bytes`.
  *  Size limit: a problem whose pa_decode_partitioned_workspace_bytes exceeds
  *  PA_STATIC_WORKSPACE_BYTES is rejected with PA_ERR_WORKSPACE before any
- *  launch (64 MiB holds, e.g., 256 sequences x 32 query heads x 8192-token
- *  contexts at head size 128).
- *  First call on a device: it looks up the device address of the array
- *  (cudaGetSymbolAddress, with that device current) and caches it; make that
- *  first call before any stream capture. A failed lookup returns PA_ERR_CUDA.
+ *  launch. 64 MiB holds, e.g., 256 sequences x 32 query heads at head size 128
+ *  with max_context_len up to 7,680 tokens at 512-token partitions (15
+ *  partitions: 63,897,600 bytes) or up to 15,360 at 1024-token partitions;
+ *  8,192 tokens at 512 (68,157,440 bytes) does not fit.
+ *  Address lookup: the first call on a device looks up the device address of
+ *  the array (cudaGetSymbolAddress, with that device current) and caches it
+ *  against the id of the device's current context; make that first call
+ *  before any stream capture. If the context is later replaced (a
+ *  cudaDeviceReset, or another driver context made current), the next call
+ *  sees a new context id and looks the address up again, so it is also a
+ *  first call in this sense. A failed lookup returns PA_ERR_CUDA.
  *  Sharing: every call, on every stream, uses the same array, which keeps the
  *  previous call's contents (nothing in it needs to start at zero). Calls whose
  *  kernels overlap on the GPU race on it and give unspecified results:

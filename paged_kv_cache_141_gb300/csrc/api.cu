@@ -283,6 +283,39 @@ pa_prefill_kernel prefill_kernel(pa_dtype q_dtype, pa_dtype cache_dtype, int hea
     return PA_PREFILL_CUDA_CORES;
 }
 
+// pa_merge's validation and launch; len_cap is the context-length clamp of
+// the partition kernel whose partials are merged.
+pa_status merge_checked(void* out, const float* tmp_out, const float* max_logits,
+                        const float* exp_sums, const int32_t* context_lens, int num_seqs,
+                        int num_q_heads, int head_size, int partition_size, int max_partitions,
+                        long long len_cap, pa_dtype out_dtype, uint32_t* dev_status,
+                        void* stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_partitions <= 0)
+        return PA_ERR_INVALID_ARG;
+    pa_status st = check_partition_size(partition_size);
+    if (st != PA_OK) return st;
+    if ((int)out_dtype < 0 || (int)out_dtype > 3) return PA_ERR_INVALID_ARG;
+    if (!is_compute_type(out_dtype) || !supported_head_size(head_size)) return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out, tmp_out) || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
+        !aligned(context_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    const long long parts_cap = (long long)max_partitions * partition_size;
+    return from_cuda(launch_merge(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
+                                  num_q_heads, head_size, partition_size, max_partitions,
+                                  len_cap < parts_cap ? len_cap : parts_cap, out_dtype, dev_status,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+// The context-length clamp of the decode kernels: min(max_context_len,
+// max_blocks_per_seq * block_size).
+long long decode_len_cap(int max_context_len, int max_blocks_per_seq, int block_size) {
+    const long long tab = (long long)max_blocks_per_seq * block_size;
+    return tab < max_context_len ? tab : (long long)max_context_len;
+}
+
 }  // namespace
 
 extern "C" {
@@ -404,11 +437,13 @@ pa_status pa_write_decode_partitioned(void* out, const void* query, const void* 
     if (st != PA_OK || num_seqs == 0) return st;
     const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
     const uint8_t* w = static_cast<const uint8_t*>(workspace);
-    return pa_merge(out, reinterpret_cast<const float*>(w + l.tmp_out),
-                    reinterpret_cast<const float*>(w + l.max_logits),
-                    reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
-                    num_q_heads, head_size, partition_size,
-                    max_partitions(max_context_len, partition_size), q_dtype, dev_status, stream);
+    return merge_checked(out, reinterpret_cast<const float*>(w + l.tmp_out),
+                         reinterpret_cast<const float*>(w + l.max_logits),
+                         reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
+                         num_q_heads, head_size, partition_size,
+                         max_partitions(max_context_len, partition_size),
+                         decode_len_cap(max_context_len, max_blocks_per_seq, block_size), q_dtype,
+                         dev_status, stream);
 }
 
 size_t pa_decode_partitioned_workspace_bytes(int num_seqs, int num_q_heads, int head_size,
@@ -461,21 +496,10 @@ pa_status pa_merge(void* out, const float* tmp_out, const float* max_logits, con
                    const int32_t* context_lens, int num_seqs, int num_q_heads, int head_size,
                    int partition_size, int max_partitions, pa_dtype out_dtype,
                    uint32_t* dev_status, void* stream) {
-    if (num_seqs < 0 || num_q_heads <= 0 || head_size <= 0 || max_partitions <= 0)
-        return PA_ERR_INVALID_ARG;
-    pa_status st = check_partition_size(partition_size);
-    if (st != PA_OK) return st;
-    if ((int)out_dtype < 0 || (int)out_dtype > 3) return PA_ERR_INVALID_ARG;
-    if (!is_compute_type(out_dtype) || !supported_head_size(head_size)) return PA_ERR_UNSUPPORTED;
-    if (num_seqs > 65535 || num_q_heads > 65535) return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !tmp_out || !max_logits || !exp_sums || !context_lens) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out, tmp_out) || !aligned(max_logits, 4) || !aligned(exp_sums, 4) ||
-        !aligned(context_lens, 4))
-        return PA_ERR_INVALID_ARG;
-    return from_cuda(launch_merge(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                  num_q_heads, head_size, partition_size, max_partitions,
-                                  out_dtype, dev_status, static_cast<cudaStream_t>(stream)));
+    return merge_checked(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs, num_q_heads,
+                         head_size, partition_size, max_partitions,
+                         (long long)max_partitions * partition_size, out_dtype, dev_status,
+                         stream);
 }
 
 pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cache,
@@ -495,11 +519,13 @@ pa_status pa_decode_partitioned(void* out, const void* query, const void* k_cach
     if (st != PA_OK || num_seqs == 0) return st;
     const Layout l = workspace_layout(num_seqs, num_q_heads, head_size, max_context_len, partition_size);
     const uint8_t* w = static_cast<const uint8_t*>(workspace);
-    return pa_merge(out, reinterpret_cast<const float*>(w + l.tmp_out),
-                    reinterpret_cast<const float*>(w + l.max_logits),
-                    reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
-                    num_q_heads, head_size, partition_size,
-                    max_partitions(max_context_len, partition_size), q_dtype, dev_status, stream);
+    return merge_checked(out, reinterpret_cast<const float*>(w + l.tmp_out),
+                         reinterpret_cast<const float*>(w + l.max_logits),
+                         reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
+                         num_q_heads, head_size, partition_size,
+                         max_partitions(max_context_len, partition_size),
+                         decode_len_cap(max_context_len, max_blocks_per_seq, block_size), q_dtype,
+                         dev_status, stream);
 }
 
 int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len) {

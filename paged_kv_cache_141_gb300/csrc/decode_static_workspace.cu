@@ -9,9 +9,10 @@
 // point takes its workspace from a fixed array in this library's device
 // memory instead. The array is PA_STATIC_WORKSPACE_BYTES long; every GPU that
 // loads the library holds it until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "pagedkv.h"
 
@@ -22,21 +23,69 @@ namespace {
 __device__ __align__(256) unsigned char g_static_workspace[PA_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_workspace_address[kMaxDevices];
 
-// Device address of the array on the current device, looked up once per
-// device (the first call on a device does the lookup).
+// Per device: the id of the context the address was looked up in, and the
+// address. A context id is unique for the life of the process, so a device
+// whose context was destroyed and created again (cudaDeviceReset, or the
+// caller's own driver context) gets a fresh lookup instead of a stale address.
+struct Entry {
+    unsigned long long ctx_id;    // 0: not looked up yet
+    void* address;
+};
+std::mutex g_lock;
+Entry g_entries[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The id of the calling thread's current context, 0 if there is none yet.
+// Driver calls are reached through the runtime's entry-point query, so the
+// library does not link the driver library. Called with g_lock held.
+cudaError_t current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    if (!get_current || !get_id) {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000,
+                                                         cudaEnableDefault, &qa);
+        if (e != cudaSuccess || qa != cudaDriverEntryPointSuccess || !a) return cudaErrorUnknown;
+        e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb);
+        if (e != cudaSuccess || qb != cudaDriverEntryPointSuccess || !b) return cudaErrorUnknown;
+        get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+        get_id = reinterpret_cast<CtxGetIdFn>(b);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS) return cudaErrorUnknown;
+    *id = 0;
+    if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorUnknown;
+    return cudaSuccess;
+}
+
+// Device address of the array in the current device's context, looked up
+// with that device current the first time the context is seen (the first call
+// on a device, and the first after its context was replaced).
 cudaError_t static_workspace_address(void** address) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void* p = g_workspace_address[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
-        e = cudaGetSymbolAddress(&p, g_static_workspace);
-        if (e != cudaSuccess) return e;
-        g_workspace_address[dev].store(p, std::memory_order_release);
+    std::lock_guard<std::mutex> hold(g_lock);
+    unsigned long long id = 0;
+    if ((e = current_context_id(&id)) != cudaSuccess) return e;
+    Entry& entry = g_entries[dev];
+    if (id != 0 && entry.ctx_id == id) {
+        *address = entry.address;
+        return cudaSuccess;
     }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_workspace);       // makes the context current if needed
+    if (e != cudaSuccess) return e;
+    if ((e = current_context_id(&id)) != cudaSuccess) return e;
+    if (id == 0) return cudaErrorInvalidDevice;
+    entry.ctx_id = id;
+    entry.address = p;
     *address = p;
     return cudaSuccess;
 }

@@ -134,10 +134,14 @@ cudaError_t launch_prefill_tc_bf16(const PrefillParams& p, int head_size, cudaSt
 cudaError_t launch_prefill_tc_f16_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream);
 cudaError_t launch_prefill_tc_bf16_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream);
 
+// len_cap: context lengths above it are clamped to it (and flagged
+// PA_DEV_BAD_LEN), the clamp the partition kernel applied, so that only
+// partitions it wrote are merged.
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int head_size, int partition_size, int max_parts,
-                         pa_dtype out_dtype, uint32_t* status, cudaStream_t stream);
+                         long long len_cap, pa_dtype out_dtype, uint32_t* status,
+                         cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs,
                                int64_t num_pairs, int64_t num_blocks, int64_t block_bytes,

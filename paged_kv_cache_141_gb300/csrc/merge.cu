@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
 paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
                    const float* __restrict__ max_logits, const float* __restrict__ exp_sums,
                    const int32_t* __restrict__ context_lens, int num_seqs, int num_q_heads,
-                   int partition_size, int max_parts, uint32_t* status) {
+                   int partition_size, int max_parts, long long len_cap, uint32_t* status) {
     const int lane = threadIdx.x & 31;
     const long long item = (long long)blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
     if (item >= (long long)num_seqs * num_q_heads) return;
@@ -30,8 +30,9 @@ paged_merge_kernel(OT* __restrict__ out, const float* __restrict__ tmp_out,
     // the previous kernels wrote is read before they have completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    // the partition kernel's clamp (len_cap): only partitions it wrote are read
     int L = context_lens[s];
-    const long long cap = (long long)max_parts * partition_size;
+    const long long cap = len_cap;
     if (L < 0 || L > cap) {
         if (lane == 0 && h == 0 && status) atomicOr(status, PA_DEV_BAD_LEN);
         L = L < 0 ? 0 : (int)cap;
@@ -46,7 +47,7 @@ template <int D, typename OT>
 static cudaError_t launch_merge_t(OT* out, const float* tmp_out, const float* max_logits,
                                   const float* exp_sums, const int32_t* context_lens, int num_seqs,
                                   int num_q_heads, int partition_size, int max_parts,
-                                  uint32_t* status, cudaStream_t stream) {
+                                  long long len_cap, uint32_t* status, cudaStream_t stream) {
     const long long items = (long long)num_seqs * num_q_heads;
     const unsigned grid = (unsigned)((items + kMergeWarps - 1) / kMergeWarps);
     // programmatic dependent launch: the merge's CTAs may be scheduled while
@@ -64,25 +65,25 @@ static cudaError_t launch_merge_t(OT* out, const float* tmp_out, const float* ma
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, paged_merge_kernel<D, OT>, out, tmp_out, max_logits, exp_sums,
                               context_lens, num_seqs, num_q_heads, partition_size, max_parts,
-                              status);
+                              len_cap, status);
 }
 
 template <typename OT>
 static cudaError_t launch_merge_o(void* out, const float* tmp_out, const float* max_logits,
                                   const float* exp_sums, const int32_t* context_lens, int num_seqs,
                                   int num_q_heads, int head_size, int partition_size, int max_parts,
-                                  uint32_t* status, cudaStream_t stream) {
+                                  long long len_cap, uint32_t* status, cudaStream_t stream) {
     OT* o = static_cast<OT*>(out);
     switch (head_size) {
     case 64:
         return launch_merge_t<64>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                  num_q_heads, partition_size, max_parts, status, stream);
+                                  num_q_heads, partition_size, max_parts, len_cap, status, stream);
     case 128:
         return launch_merge_t<128>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                   num_q_heads, partition_size, max_parts, status, stream);
+                                   num_q_heads, partition_size, max_parts, len_cap, status, stream);
     case 256:
         return launch_merge_t<256>(o, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                   num_q_heads, partition_size, max_parts, status, stream);
+                                   num_q_heads, partition_size, max_parts, len_cap, status, stream);
     }
     return cudaErrorInvalidValue;
 }
@@ -90,20 +91,21 @@ static cudaError_t launch_merge_o(void* out, const float* tmp_out, const float* 
 cudaError_t launch_merge(void* out, const float* tmp_out, const float* max_logits,
                          const float* exp_sums, const int32_t* context_lens, int num_seqs,
                          int num_q_heads, int head_size, int partition_size, int max_parts,
-                         pa_dtype out_dtype, uint32_t* status, cudaStream_t stream) {
+                         long long len_cap, pa_dtype out_dtype, uint32_t* status,
+                         cudaStream_t stream) {
     switch (out_dtype) {
     case PA_F32:
         return launch_merge_o<float>(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                     num_q_heads, head_size, partition_size, max_parts, status,
-                                     stream);
+                                     num_q_heads, head_size, partition_size, max_parts, len_cap,
+                                     status, stream);
     case PA_F16:
         return launch_merge_o<__half>(out, tmp_out, max_logits, exp_sums, context_lens, num_seqs,
-                                      num_q_heads, head_size, partition_size, max_parts, status,
-                                      stream);
+                                      num_q_heads, head_size, partition_size, max_parts, len_cap,
+                                      status, stream);
     case PA_BF16:
         return launch_merge_o<__nv_bfloat16>(out, tmp_out, max_logits, exp_sums, context_lens,
                                              num_seqs, num_q_heads, head_size, partition_size,
-                                             max_parts, status, stream);
+                                             max_parts, len_cap, status, stream);
     default:
         return cudaErrorInvalidValue;
     }

@@ -227,3 +227,27 @@ def test_paged_prefill_kernel_selection(lib):
     assert L.pa_paged_prefill_kernel(4, 30, 8, 128, 16, 1000, B16, B16) == -1
     assert L.pa_paged_prefill_kernel(4, 32, 8, 96, 16, 1000, B16, B16) == -1
     assert L.pa_paged_prefill_kernel(4, 32, 8, 128, 16, 1000, B16, F16) == -1
+
+
+def test_static_workspace_capacity_examples():
+    """The capacities pa_decode_partitioned_static's declaration quotes, and
+    the exact-limit shape the GPU test runs (workspace sizing is host only)."""
+    from paged_kv_cache_141_gb300 import binding as pk
+    limit = pk.STATIC_WORKSPACE_BYTES
+    assert limit == 64 * 1024 * 1024
+    assert pk.workspace_bytes(256, 32, 128, 7680, 512) == 63_897_600 <= limit
+    assert pk.workspace_bytes(256, 32, 128, 15360, 1024) <= limit
+    assert pk.workspace_bytes(256, 32, 128, 8192, 512) == 68_157_440 > limit
+    # 775 x 8 heads x 41 partitions at head size 64: exactly the array
+    assert pk.workspace_bytes(775, 8, 64, 41 * 512, 512) == limit
+    assert pk.workspace_bytes(775, 8, 64, 41 * 512 + 1, 512) > limit
+
+
+def test_static_call_rejects_oversized_problem_without_a_device():
+    """The size check runs before any CUDA call."""
+    from paged_kv_cache_141_gb300 import binding as pk
+    L = pk.lib()
+    st = L.pa_decode_partitioned_static(None, None, None, None, None, 1, None, 775, 8, 2, 64, 16,
+                                        64, 41 * 512 + 1, 0.125, pk.PA_BF16, pk.PA_BF16, 1.0, 1.0,
+                                        512, None, None)
+    assert st == pk.PA_ERR_WORKSPACE

@@ -3,7 +3,8 @@ on the GPU against the oracle: the tcgen05 path over its shapes, the
 warp-level MMA path for a few query rows per sequence and KV head, the
 CUDA-core path for the other types and block sizes, the decode as its
 one-query case, block-size invariance, status flags, and full-size chunked
-prefill and verification steps checked on sampled rows."""
+prefill and verification steps checked on every row (verification) or on
+whole sequences plus every sequence's tile-edge rows (chunks)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +14,7 @@ from paged_kv_cache_141_gb300 import binding as pk
 from paged_kv_cache_141_gb300.workloads import config_case, make_case, make_queries
 
 from gpu_common import (TORCH, DeviceCase, assert_decode_close, host_to_torch, oracle_pool,
-                        to_f64)
+                        parallel_rows, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,18 +57,40 @@ class Prefill:
 
     def oracle_rows(self, rows):
         """The oracle on single query rows: row t of sequence s at position
-        pos sees the keys a one-query step over pos + 1 tokens sees."""
+        pos sees the keys a one-query step over pos + 1 tokens sees. Slices
+        of rows run on host threads."""
         c, q = self.case, self.q
         kc, vc = oracle_pool(c)
-        rows = np.asarray(rows)
-        seq = np.searchsorted(q.query_start, rows, side="right") - 1
-        pos = c.context_lens[seq] - q.counts[seq] + (rows - q.query_start[seq])
-        want = oracle.paged_prefill(np.ascontiguousarray(q.query[rows]), c.q_dtype,
-                                    np.arange(len(rows) + 1, dtype=np.int32), kc, vc,
-                                    c.cache_dtype, np.ascontiguousarray(c.block_tables[seq]),
-                                    (pos + 1).astype(np.int32), c.num_kv_heads, c.block_size,
-                                    c.scale, c.k_scale, c.v_scale)
-        return want
+
+        def some(rows):
+            seq = np.searchsorted(q.query_start, rows, side="right") - 1
+            pos = c.context_lens[seq] - q.counts[seq] + (rows - q.query_start[seq])
+            return oracle.paged_prefill(np.ascontiguousarray(q.query[rows]), c.q_dtype,
+                                        np.arange(len(rows) + 1, dtype=np.int32), kc, vc,
+                                        c.cache_dtype, np.ascontiguousarray(c.block_tables[seq]),
+                                        (pos + 1).astype(np.int32), c.num_kv_heads,
+                                        c.block_size, c.scale, c.k_scale, c.v_scale)
+
+        return parallel_rows(some, np.asarray(rows))
+
+    def dense_rows(self, whole=(), edges=(0, 1, 31, 32, 127, 128, -2, -1), n_random=0, seed=0):
+        """Rows to check: every row of the sequences `whole`, the rows at
+        the offsets `edges` (negative: from the end; the query-tile and
+        n-tile edges) of every sequence, and n_random seeded random rows."""
+        qs = self.q.query_start
+        rows = set()
+        for s_ in whole:
+            rows.update(range(int(qs[s_]), int(qs[s_ + 1])))
+        for s_ in range(self.case.num_seqs):
+            lo, hi = int(qs[s_]), int(qs[s_ + 1])
+            for e in edges:
+                r = lo + e if e >= 0 else hi + e
+                if lo <= r < hi:
+                    rows.add(r)
+        rng = np.random.default_rng(seed)
+        if n_random:
+            rows.update(int(r) for r in rng.integers(0, int(qs[-1]), size=n_random))
+        return np.array(sorted(rows))
 
 
 def mma_max_rows(case):
@@ -352,30 +375,31 @@ def test_host_argument_errors():
 @pytest.mark.parametrize("law,force_tc", [(("fixed", None), False), (("uniform", 1, 8), False),
                                           (("uniform", 1, 8), True), (("uniform", 1, 4), False)],
                          ids=["chunk512", "spec8", "spec8-tcgen05", "spec4"])
-def test_full_size_llama3_8b_sampled(law, force_tc):
+def test_full_size_llama3_8b(law, force_tc):
     """Llama-3-8B GQA shape at full size (256 sequences, contexts 512..4096):
     a 512-token prefill chunk per sequence (capped at L_s), an 8-draft
     speculative verification step (warp-level MMA with two n-tiles per warp,
-    and forced onto the tcgen05 kernel), and a 4-draft one; sampled rows
-    against the oracle."""
+    and forced onto the tcgen05 kernel), and a 4-draft one. Verification
+    steps: every row against the oracle. Chunks: every row of eight whole
+    sequences (the shortest, the longest and six random ones) and the
+    query-tile edge rows of every sequence."""
     c = config_case(3)
     if law[0] == "fixed":
         law = ("fixed", np.minimum(512, c.context_lens))
     p = Prefill(c, law)
     got = to_f64(p.run(tc_bound(p) if force_tc else None))
     assert p.dc.status_bits() == 0
-    # every query tile edge of the longest and shortest sequences' first and
-    # last tokens, plus random rows
-    L, qs = c.context_lens, p.q.query_start
-    rows = set()
-    for s in {int(np.argmin(L)), int(np.argmax(L)), 77}:
-        lo, hi = int(qs[s]), int(qs[s + 1])
-        rows.update(r for r in (lo, lo + 1, lo + 31, lo + 32, hi - 2, hi - 1) if lo <= r < hi)
-    rng = np.random.default_rng(11)
-    rows.update(int(r) for r in rng.integers(0, int(qs[-1]), size=40))
-    rows = np.array(sorted(rows))
+    L = c.context_lens
+    if law[0] == "fixed":
+        rng = np.random.default_rng(11)
+        whole = {int(np.argmin(L)), int(np.argmax(L))} | set(
+            int(x) for x in rng.choice(c.num_seqs, 6, replace=False))
+        rows = p.dense_rows(whole=sorted(whole))
+    else:
+        rows = np.arange(int(p.q.query_start[-1]))
     want = p.oracle_rows(rows)
-    assert_decode_close(got[rows], want, c, "full size")
+    assert_decode_close(got[rows], want, c, f"full: llama3-8b {p.q.max_queries}-query law, "
+                                            f"{len(rows)} of {int(p.q.query_start[-1])} rows")
 
 
 @pytest.mark.parametrize("law,force_tc", [(("uniform", 1, 4), False), (("uniform", 1, 8), False),
@@ -394,58 +418,54 @@ def test_repeated_launches_are_bit_identical(law, force_tc):
         assert torch.equal(p.run(bound), first)
 
 
-def test_full_size_shared_prefix_e4m3_sampled():
+def test_full_size_shared_prefix_e4m3():
     """The shared-prefix E4M3 pool (128 sequences, 64 query heads / 8 KV
     heads, a 1024-token prefix shared by 32 sequences each): a 256-token chunk
-    per sequence on the tensor cores, sampled rows against the oracle."""
+    per sequence on the tensor cores; every row of one sequence per prefix
+    group, the tile-edge rows of every sequence and random rows against the
+    oracle."""
     c = config_case(5)
     p = Prefill(c, ("fixed", np.minimum(256, c.context_lens)))
     got = to_f64(p.run())
     assert p.dc.status_bits() == 0
-    rng = np.random.default_rng(12)
-    qs = p.q.query_start
-    rows = np.array(sorted(set(int(r) for r in rng.integers(0, int(qs[-1]), size=48))))
+    # every row of one sequence per prefix group, the tile-edge rows of every
+    # sequence, random rows
+    rows = p.dense_rows(whole=[0, 32, 64, 96], n_random=64, seed=12)
     want = p.oracle_rows(rows)
-    assert_decode_close(got[rows], want, c, "shared-prefix e4m3")
+    assert_decode_close(got[rows], want, c, f"full: shared-prefix e4m3 256-token chunks, "
+                                            f"{len(rows)} of {int(p.q.query_start[-1])} rows")
 
 
-def test_full_size_llama7b_mha_f16_sampled():
+def test_full_size_llama7b_mha_f16():
     """The LLaMA-7B fp16 MHA pool (64 sequences, 32 heads, contexts up to
     2016): a 512-token chunk per sequence on the two-tile kernel with single
-    binary16 weights and its deeper V ring, sampled rows against the oracle."""
+    binary16 weights and its deeper V ring; every row of four sequences, the
+    tile-edge rows of every sequence and random rows against the oracle."""
     c = config_case(2)
     p = Prefill(c, ("fixed", np.minimum(512, c.context_lens)))
     got = to_f64(p.run())
     assert p.dc.status_bits() == 0
-    rng = np.random.default_rng(21)
-    qs = p.q.query_start
-    rows = set(int(r) for r in rng.integers(0, int(qs[-1]), size=40))
     L = c.context_lens
-    for s in {int(np.argmin(L)), int(np.argmax(L))}:
-        rows.update({int(qs[s]), int(qs[s + 1]) - 1})          # first and last token
-    rows = np.array(sorted(rows))
+    rows = p.dense_rows(whole=[int(np.argmin(L)), int(np.argmax(L)), 5, 40], n_random=64,
+                        seed=21)
     want = p.oracle_rows(rows)
-    assert_decode_close(got[rows], want, c, "llama-7b mha f16 chunk")
+    assert_decode_close(got[rows], want, c, f"full: llama-7b mha f16 512-token chunks, "
+                                            f"{len(rows)} of {int(p.q.query_start[-1])} rows")
 
 
-def test_full_size_long_context_chunk_sampled():
+def test_full_size_long_context_chunk():
     """The long-context pool (8 sequences of 32k..131k tokens): a 512-token
     chunk at the end of each context, about a thousand key tiles per unit;
-    sampled rows (first, last and random tokens) against the oracle."""
+    the tile-edge rows (first, last, tile boundaries) of every sequence and
+    random rows against the oracle."""
     c = config_case(4)
     p = Prefill(c, ("fixed", np.minimum(512, c.context_lens)))
     got = to_f64(p.run())
     assert p.dc.status_bits() == 0
-    qs = p.q.query_start
-    rng = np.random.default_rng(31)
-    rows = {int(qs[0]), int(qs[-1]) - 1}
-    L = c.context_lens
-    s = int(np.argmax(L))
-    rows.update({int(qs[s]), int(qs[s + 1]) - 1})
-    rows.update(int(r) for r in rng.integers(0, int(qs[-1]), size=6))
-    rows = np.array(sorted(rows))
+    rows = p.dense_rows(n_random=32, seed=31)
     want = p.oracle_rows(rows)
-    assert_decode_close(got[rows], want, c, "long-context chunk")
+    assert_decode_close(got[rows], want, c, f"full: long-context 512-token chunks, "
+                                            f"{len(rows)} of {int(p.q.query_start[-1])} rows")
 
 
 @pytest.mark.parametrize("law,force_tc", [(("uniform", 1, 4), False), (("uniform", 1, 8), False),
