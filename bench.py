@@ -268,23 +268,31 @@ class Step:
         for _, f in self.calls:
             f(stream)
 
+    @property
+    def main_call(self) -> str:
+        """The call that runs the decode kernel (partition kernel or single
+        pass; in the fused form it also stores the step's new tokens)."""
+        return "write+decode" if self.form == "fused" else "decode"
+
     def bytes_per_step(self) -> dict:
-        """Algorithmic bytes. The step: K/V read, Q read, out written, and the
-        new tokens' K/V read and stored with their slots. The decode kernel
-        (partition or single pass): K/V and Q read, and its output -- every
-        partition's partials, or `out` -- plus, in the fused form, the new
-        tokens' write."""
+        """Algorithmic bytes, by the method's definition (no workspace).
+        total: the step -- K/V read, Q read, out written, and the new tokens'
+        K/V read and stored with their slots. main_kernel: the decode
+        kernel's share -- K/V, Q and out, plus the new tokens in the fused
+        form. partials: what the partition kernel writes for the merge to
+        read (per-partition outputs, maxima and sums; 0 for the single
+        pass), reported beside the method bytes and not counted in them."""
         c = self.case
         write = c.write_bytes()
         decode = c.kv_bytes() + c.qo_bytes()
-        q_bytes = c.qo_bytes() // 2
         if self.split:
             parts = sum(-(-int(L) // self.P) for L in c.context_lens)
-            produced = parts * c.num_q_heads * (c.head_size + 2) * 4
+            partials = parts * c.num_q_heads * (c.head_size + 2) * 4
         else:
-            produced = q_bytes
-        main = c.kv_bytes() + q_bytes + produced + (write if self.form == "fused" else 0)
-        return {"write": write, "decode": decode, "total": write + decode, "main_kernel": main}
+            partials = 0
+        main = decode + (write if self.form == "fused" else 0)
+        return {"write": write, "decode": decode, "total": write + decode, "main_kernel": main,
+                "partials": partials}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -314,7 +322,8 @@ def run_ours(args):
         raise SystemExit(f"device status {int(st.status.item())} after the first step")
 
     # the clock sampler starts (and settles) before the warm-up, so that the
-    # GPU goes from the warm-up straight into the timed region at full clocks
+    # GPU goes from the warm-up straight into the timed region at full
+    # clocks; it runs on through the kernel leg below (a second or more)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.25 if sampler else 0)
     for _ in range(args.warmup):
@@ -348,7 +357,6 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    clocks = sampler.stop() if sampler else None
     total_ms = t_start.elapsed_time(t_end)
     call_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in sampled) / len(sampled)
                for j, (name, _) in enumerate(st.calls)}
@@ -359,29 +367,27 @@ def run_ours(args):
     value = whole_job_gbs(by["total"], world, ms_per_step)
     seqs_per_s = world * case.num_seqs / (ms_per_step * 1e-3)
     peak, peak_kind = hbm_peak()
-    main_name = "write+decode" if "write+decode" in call_ms else "decode"
-    main_avg = call_ms[main_name]
-    achieved = by["main_kernel"] / (main_avg * 1e-3) / 1e9
-    # shared blocks (read by several sequences, served from L2 after the
-    # first) counted once: the rate on the bytes that exist in the pool
-    unique_kv = case.unique_kv_bytes()
-    unique = None
-    if unique_kv < case.kv_bytes():
-        ub = by["total"] - case.kv_bytes() + unique_kv
-        ug = whole_job_gbs(ub, world, ms_per_step)
-        unique = {"kv_bytes": unique_kv, "bytes_per_step": ub, "gbs": round(ug, 2),
-                  "frac_of_hbm_peak": round(ug / peak, 4),
-                  "note": "each distinct cached token's K/V once (shared prefix blocks count once)"}
+    kernel = run_kernel_leg(st, device, args.kernel_seconds)
+    clocks = sampler.stop() if sampler else None
+    achieved = by["main_kernel"] / (kernel["ms"] * 1e-3) / 1e9
+    unique = unique_record(case, by, world, ms_per_step, peak)
 
     graph = run_graph(st, max(20, min(1000, K)), device)
     write_step = run_write_step(st, device)
     write_bulk = run_write_bulk(st, device)
     e2e = run_e2e(st, max(20, min(200, K // 10)), device)
+    form_used = st.form
+    del st
+    torch.cuda.empty_cache()
+    others = None
+    if rank == 0 and args.configs != "none":
+        others = run_other_configs(args, device, [int(x) for x in args.configs.split(",")])
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, st.P, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(case, P, budget_s=args.cpu_seconds)
     if rank != 0:
         return
+    split = "partitioned" if by["partials"] else "single-pass"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -391,8 +397,8 @@ def run_ours(args):
                    "num_kv_heads": case.num_kv_heads, "head_size": case.head_size,
                    "block_size": case.block_size, "kv_dtype": case.cache_dtype,
                    "context_lens": "log-uniform [512, 4096]" if args.config == 3 else "see workloads",
-                   "total_context_tokens": case.total_tokens, "partition_size": st.P,
-                   "decode_form": ("partitioned" if st.split else "single-pass") + ", " + st.form,
+                   "total_context_tokens": case.total_tokens, "partition_size": P,
+                   "decode_form": f"{split}, {form_used}",
                    "l2": "inputs larger than L2 (KV pool %.2f GB vs 129 MB L2); no flush"
                          % (case.kv_bytes() / 1e9),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -403,25 +409,164 @@ def run_ours(args):
         "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(args.config, st.P, st.form, st.split),
-                     "kernel": decode_kernel_label(case) + (
-                         (" (partition kernel" if st.split else " (single pass")
-                         + (", KV write fused)" if st.form == "fused" else ")")),
-                     "timed_call": main_name,
-                     "event_sample": f"CUDA events around each call on every {every}th of the "
-                                     f"{K} timed steps ({len(sampled)} steps)",
+                     "traffic": recorded_traffic(args.config, P, form_used, bool(by["partials"])),
+                     "kernel": kernel["name"], "kernel_ms": round(kernel["ms"], 6),
+                     "method_bytes_per_launch": by["main_kernel"],
+                     "partials_bytes_per_launch": by["partials"],
+                     "step_frac": round(value / peak, 4),
+                     "timing": kernel["timing"],
                      "peak_kind": f"{peak_kind} (HBM copy, MEASURED_PEAKS.json hbm_gbs)"
-                     if peak_kind == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": by["main_kernel"]},
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "graph": graph,
         "write_step": write_step,
         "write_bulk": write_bulk,
-        "gpu_launches": K * st.launches_per_step,
+        "configs": others,
+        "gpu_launches": K * ncall,
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def unique_record(case, by, world, ms_per_step, peak):
+    """Where sequences share blocks: the step's rate on each distinct cached
+    token's K/V once (shared prefix blocks are read from L2 after the first
+    reader), next to the logical-byte rate."""
+    unique_kv = case.unique_kv_bytes()
+    if unique_kv >= case.kv_bytes():
+        return None
+    ub = by["total"] - case.kv_bytes() + unique_kv
+    ug = whole_job_gbs(ub, world, ms_per_step)
+    return {"kv_bytes": unique_kv, "bytes_per_step": ub, "gbs": round(ug, 2),
+            "frac_of_hbm_peak": round(ug / peak, 4),
+            "note": "each distinct cached token's K/V once (shared prefix blocks count once)"}
+
+
+def run_kernel_leg(st: Step, device, min_seconds: float = 1.0, per_graph: int = 20) -> dict:
+    """The decode kernel alone (the step's main call: the partition kernel,
+    or the single pass, with the KV write in the fused form): `per_graph`
+    back-to-back launches captured in a CUDA graph and replayed until at
+    least `min_seconds` have passed; CUDA events on the replaying stream.
+    Every launch rewrites the same new tokens, so the pool is unchanged, and
+    the K/V read (far larger than L2) comes from HBM each time."""
+    import torch
+    fn = dict(st.calls)[st.main_call]
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per_graph):
+                fn(s)
+    cur = torch.cuda.current_stream(device)
+    cur.wait_stream(s)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    for _ in range(2):
+        g.replay()
+    a.record(cur)
+    g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    reps = max(10, int(math.ceil(min_seconds * 1e3 / max(a.elapsed_time(b), 1e-3))))
+    a.record(cur)
+    for _ in range(reps):
+        g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise SystemExit(f"device status {int(st.status.item())} after the kernel leg")
+    total = a.elapsed_time(b)
+    n = reps * per_graph
+    name = decode_kernel_label(st.case) + (
+        (" (partition kernel" if st.split else " (single pass")
+        + (", KV write fused)" if st.form == "fused" else ")"))
+    return {"name": name, "ms": total / n, "launches": n,
+            "timing": f"CUDA graph of {per_graph} launches of the kernel alone, replayed {reps} "
+                      f"times ({n} launches, {total / 1e3:.2f} s), events on the replaying stream"}
+
+
+def measure_config(index: int, device, partition_size, form="fused", step_seconds=0.3,
+                   kernel_seconds=0.5) -> dict:
+    """One workload's decode step and its kernel: the step launched eagerly
+    (about step_seconds of steps), the kernel alone (run_kernel_leg), and
+    the step's own KV write (run_write_step)."""
+    import torch
+    from paged_kv_cache_141_gb300 import binding as pk
+    from paged_kv_cache_141_gb300 import workloads as W
+    case = W.config_case(index)
+    P = (pk.partition_size(case.num_seqs, case.num_kv_heads, case.max_context_len)
+         if partition_size == "auto" else int(partition_size))
+    st = Step(case, device, P, form)
+    st.step()
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise SystemExit(f"configuration {index}: device status {int(st.status.item())}")
+    for _ in range(5):
+        st.step()
+    cur = torch.cuda.current_stream(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    st.step()
+    b.record(cur)
+    torch.cuda.synchronize()
+    n = max(20, int(step_seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
+    a.record(cur)
+    for _ in range(n):
+        st.step()
+    b.record(cur)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    by = st.bytes_per_step()
+    peak, _ = hbm_peak()
+    gbs = by["total"] / (ms * 1e-3) / 1e9
+    kern = run_kernel_leg(st, device, kernel_seconds)
+    kg = by["main_kernel"] / (kern["ms"] * 1e-3) / 1e9
+    graph = run_graph(st, max(20, n), device)
+    ws = run_write_step(st, device)
+    unique = unique_record(case, by, 1, ms, peak)
+    rec = {"workload": f"{case.name} (configuration {index})", "num_seqs": case.num_seqs,
+           "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
+           "head_size": case.head_size, "kv_dtype": case.cache_dtype,
+           "total_context_tokens": case.total_tokens, "partition_size": P,
+           "decode_form": ("partitioned" if st.split else "single-pass") + ", " + st.form,
+           "ms_per_step": round(ms, 5), "steps": n, "gbs": round(gbs, 2),
+           "frac_of_hbm_peak": round(gbs / peak, 4),
+           "seqs_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1),
+           "graph_ms_per_step": graph["ms_per_step"],
+           "kernel": {"name": kern["name"], "ms": round(kern["ms"], 6),
+                      "method_bytes_per_launch": by["main_kernel"],
+                      "partials_bytes_per_launch": by["partials"], "gbs": round(kg, 1),
+                      "frac": round(kg / peak, 4), "timing": kern["timing"]},
+           "write_step": {"tokens_per_s": ws["tokens_per_s"], "us_per_launch": ws["us_per_launch"]},
+           "bytes_per_step": by}
+    if unique:
+        rec["unique_bytes"] = unique
+    del st
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_other_configs(args, device, indices) -> dict:
+    """Records for the other workloads (run_ours times the main one), with
+    the SM clocks sampled across them. The long-context workload is also
+    measured at the configured 512-token partitions next to the library's
+    own choice."""
+    import torch
+    sampler = ClockSampler(torch.cuda.current_device())
+    time.sleep(0.25)
+    out = {}
+    for i in indices:
+        if i == args.config:
+            continue
+        out[str(i)] = measure_config(i, device, "auto", args.form)
+        if i == 4:
+            out["4@512"] = measure_config(i, device, 512, args.form)
+    clocks = sampler.stop()
+    out["clocks"] = clocks
+    return out
 
 
 PREFILL_METRIC = {
@@ -988,6 +1133,10 @@ def main(argv=None):
     ap.add_argument("--form", choices=["fused", "separate"], default="fused",
                     help="how the step is launched (see Step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kernel-seconds", type=float, default=1.2,
+                    help="length of the kernel-only leg behind the roofline")
+    ap.add_argument("--configs", default="1,2,4,5",
+                    help="other workloads to record in the line ('none' to skip)")
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", choices=["chunk512", "spec8", "spec4", "spec2"], default=None,
