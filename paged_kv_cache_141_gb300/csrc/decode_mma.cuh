@@ -13,9 +13,12 @@
 //   O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads),
 //     V^T fragments read with ldmatrix.trans, P^T fragments made from the S
 //     accumulators with movmatrix. P is split into a 16-bit high part and a
-//     16-bit residual, two MMAs, so the weights keep ~16 significant bits
-//     (E4M3 caches: binary16 weights as one term, 11 bits, far below the
-//     codes' own error).
+//     16-bit residual, two MMAs, so the weights keep ~16 significant bits.
+// E4M3 caches run both products as E4M3 MMAs (m16n8k32) on the stored codes,
+// with no widening: the K tile is the A operand as ldmatrix reads it, V^T is
+// regrouped by byte permutes, and the query and the weights enter as two E4M3
+// terms each (the value and its residual, ~8 significant bits, like a
+// bfloat16 operand), see below.
 // Heads beyond the group (up to the MMA's 8 columns) carry zero queries and
 // are never written out. Rows of V past the context are zeroed before the
 // P.V product, since 0 x NaN would otherwise poison every output component.
@@ -66,6 +69,65 @@ template <> struct MmaOps<__half> {
     }
 };
 
+// D (16 x 8, f32) += A (16 x 32 E4M3 codes, row) . B (32 x 8 E4M3 codes, col).
+// Register i of A holds four codes of one row: rows g (a0, a2) and g + 8
+// (a1, a3), columns 4 t + (0..3) (a0, a1) and 16 + 4 t + (0..3) (a2, a3),
+// lowest column in the lowest byte; B's b0 / b1 hold column g at rows
+// 4 t + (0..3) / 16 + 4 t + (0..3).
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats to E4M3 codes, round to nearest even, saturating: x in the low
+// byte, y in the high byte (the instruction's first source goes high).
+__device__ __forceinline__ uint32_t e4m3x2_of(float x, float y) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(y), "f"(x));
+    return r;
+}
+
+// The values of two E4M3 codes (low byte -> .x), exact through binary16.
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+    float lo, hi;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// Two-term E4M3 split of a pair: hi = E4M3(v), lo = E4M3(v - hi); the values
+// of both are returned so that a sum of weights uses exactly what the MMA
+// multiplies. v - hi is exact in float32.
+__device__ __forceinline__ void e4m3_split2(float x, float y, uint32_t& hi, uint32_t& lo,
+                                            float2& sum) {
+    hi = e4m3x2_of(x, y);
+    const float2 h = e4m3x2_value(hi);
+    lo = e4m3x2_of(x - h.x, y - h.y);
+    const float2 l = e4m3x2_value(lo);
+    sum = make_float2(h.x + l.x, h.y + l.y);
+}
+
+// A power of two s with max_abs * s in (224, 448] (1 if max_abs is 0 or not
+// finite), so that the E4M3 terms of values up to max_abs neither saturate nor
+// waste range.
+__device__ __forceinline__ float e4m3_range_scale(float max_abs) {
+    const uint32_t b = __float_as_uint(max_abs);
+    const int ef = (int)((b >> 23) & 0xffu);
+    if (max_abs == 0.f || ef == 0xff) return 1.f;
+    const int E = (ef == 0 ? -126 : ef - 127);
+    int e = ((b & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;     // 448 = 1.75 x 2^8
+    e = e < -126 ? -126 : (e > 127 ? 127 : e);
+    return __uint_as_float((uint32_t)(e + 127) << 23);
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -84,24 +146,33 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     return y;
 }
 
+// Consumer warps of the tensor-core decode: 4, as in the tensor-TMA kernel
+// (6 or 8 for E4M3 caches, one ring slot each, measured no faster: 8 with
+// three CTAs per SM took 152 us against 89 us on the shared-prefix pool).
+template <typename CT, int D>
+constexpr int mma_consumer_warps() {
+    return kTmaConsumerWarps;
+}
+
 // Shared memory of the tensor-core decode: the stage ring (reused for the
-// final four-warp merge) and the stage barriers.
-// Stage k belongs to warp k mod 4 and sits in slot k mod NST; NST is a
-// multiple of the four consumer warps so that every slot has one owner and its
+// final merge of the consumer warps) and the stage barriers.
+// Stage k belongs to warp k mod W (W consumer warps) and sits in slot k mod
+// NST; NST is a multiple of W so that every slot has one owner and its
 // mbarrier phases advance one stage at a time (a parity wait cannot alias an
 // older phase).
 template <typename CT, int D>
 struct MmaSmem {
     using S = TmaShape<CT, D>;
-    // E4M3 stages are half the bytes: four stages (one per consumer warp)
-    // keep the ring at 32 KB, so that the register file, not shared memory,
-    // limits the CTAs per SM (4 instead of 3) for these latency-bound tiles
-    static constexpr int kNstCap = std::is_same<CT, e4m3_t>::value ? kTmaConsumerWarps : 1 << 30;
+    static constexpr int kConsumers = mma_consumer_warps<CT, D>();
+    // E4M3 stages are half the bytes: one stage per consumer warp keeps the
+    // ring at 32 KB, so that the register file, not shared memory, limits the
+    // CTAs per SM (5) for these latency-bound tiles
+    static constexpr int kNstCap = std::is_same<CT, e4m3_t>::value ? kConsumers : 1 << 30;
     static constexpr int kNstT = S::kNst < kNstCap ? S::kNst : kNstCap;
-    static constexpr int kNst0 = kNstT / kTmaConsumerWarps * kTmaConsumerWarps;
-    static constexpr int kNst = kNst0 < kTmaConsumerWarps ? kTmaConsumerWarps : kNst0;
+    static constexpr int kNst0 = kNstT / kConsumers * kConsumers;
+    static constexpr int kNst = kNst0 < kConsumers ? kConsumers : kNst0;
     static constexpr int kRingBytes = kNst * S::kStageBytes;
-    static constexpr int kCombineBytes = kTmaConsumerWarps * 8 * (D + 2) * 4;
+    static constexpr int kCombineBytes = kConsumers * 8 * (D + 2) * 4;
     static constexpr int kBody = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
     static constexpr int kBarOffset = (kBody + 127) / 128 * 128;
     static constexpr int kBytes = kBarOffset + 2 * kNst * 8;
@@ -135,8 +206,13 @@ constexpr int mma_min_blocks() {
     return D <= 128 ? (std::is_same<CT, e4m3_t>::value ? 5 : 4) : 2;
 }
 
+template <typename CT, int D>
+constexpr int mma_threads() {
+    return (mma_consumer_warps<CT, D>() + 1) * 32;
+}
+
 template <typename QT, typename CT, int D, int GS, bool kSplit>
-__global__ void __launch_bounds__(kTmaThreads, mma_min_blocks<CT, D>())
+__global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
     using Smem = MmaSmem<CT, D>;
@@ -144,7 +220,8 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using Ops = MmaOps<MT>;
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
     constexpr int NST = Smem::kNst;
-    static_assert(NST % kTmaConsumerWarps == 0, "one owner per slot");
+    constexpr int NCW = Smem::kConsumers;
+    static_assert(NST % NCW == 0, "one owner per slot");
     constexpr int KS = D / 16;                 // k-steps of the score product
     static_assert(GS <= 8, "one MMA covers eight heads");
     const DecodeParams& p = tp.p;
@@ -201,7 +278,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
     __syncthreads();
 
-    if (warp == kTmaConsumerWarps) {
+    if (warp == NCW) {
         // ------------------------------------------------------------ producer
         const int B = p.block_size;
         const int rows = tp.box_rows;
@@ -271,24 +348,58 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
 
     // ---------------------------------------------------------------- consumers
     // Q^T fragments (B operand of S = K Q^T): column g = head g, rows = d.
-    // For E4M3 the k index of a 16-wide step maps to d as the widened ldmatrix
-    // bytes come: k = 2t+j <-> d = 4t+j and k = 2t+8+j <-> d = 4t+2+j (a
-    // permutation of the reduction, applied to K and Q alike).
-    uint32_t qb[KS][2];
+    // 16-bit caches: the query's own 16-bit pairs. E4M3 caches: E4M3 codes of
+    // q * s_q in two terms (hi = E4M3(q s_q), lo = E4M3(q s_q - hi); about 8
+    // significant bits together), s_q a power of two that puts the group's
+    // largest |q| in (224, 448]; per 32-wide k-step: hi b0, hi b1, lo b0, lo b1.
+    constexpr int KQ = kFp8 ? D / 32 : KS;
+    constexpr int QR = kFp8 ? 4 : 2;
+    uint32_t qb[KQ][QR];
+    float qk_mul;                               // score multiplier: scale * log2(e) (* k_scale / s_q)
     {
         const QT* qp = reinterpret_cast<const QT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
+        if constexpr (kFp8) {
+            // lane (g, t) holds d = 32 kp + 16 h + 4 t + (0..3) of head g;
+            // the query is read twice (maximum, then the terms) rather than
+            // held in registers
+            auto qd = [&](int kp, int j) { return 32 * kp + (j >> 2) * 16 + 4 * t4 + (j & 3); };
+            float mx = 0.f;
+            if (g < GS) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            if (g >= GS) {
-                qb[ks][0] = 0u;
-                qb[ks][1] = 0u;
-            } else if constexpr (kFp8) {
-                const QT* q4 = qp + g * D + 16 * ks + 4 * t4;
-                qb[ks][0] = Ops::pack(to_float(q4[0]), to_float(q4[1]));
-                qb[ks][1] = Ops::pack(to_float(q4[2]), to_float(q4[3]));
-            } else {
-                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
-                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
+                for (int kp = 0; kp < KQ; ++kp)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(to_float(qp[g * D + qd(kp, j)])));
+            }
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            const float sq = e4m3_range_scale(mx);
+            qk_mul = p.q_mul / sq;
+#pragma unroll
+            for (int kp = 0; kp < KQ; ++kp)
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        v[j] = g < GS ? to_float(qp[g * D + qd(kp, 4 * half + j)]) * sq : 0.f;
+                    uint32_t h01, l01, h23, l23;
+                    float2 unused;
+                    e4m3_split2(v[0], v[1], h01, l01, unused);
+                    e4m3_split2(v[2], v[3], h23, l23, unused);
+                    qb[kp][half] = h01 | (h23 << 16);
+                    qb[kp][2 + half] = l01 | (l23 << 16);
+                }
+        } else {
+            qk_mul = p.q_mul;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                if (g >= GS) {
+                    qb[ks][0] = 0u;
+                    qb[ks][1] = 0u;
+                } else {
+                    qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
+                    qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
+                }
             }
         }
     }
@@ -299,13 +410,11 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};    // heads 2*t4 and 2*t4+1
     float l_run[2] = {0.f, 0.f};                // this lane's share of the sums
-    // scale * log2(e) (E4M3: k_scale too, and the 2^8 of the widened codes)
-    const float qk_mul = kFp8 ? p.q_mul * 256.f : p.q_mul;
 
     // ldmatrix row addresses: lane -> (matrix mi, row r)
     const int mi = lane >> 3, r8 = lane & 7;
 
-    for (int k = warp; k < n_st; k += kTmaConsumerWarps) {
+    for (int k = warp; k < n_st; k += NCW) {
         const int slot = k % NST;
         const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
         if (!ok) break;
@@ -333,21 +442,15 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             const int row = 16 * mt + (mi & 1) * 8 + r8;
             const uint8_t* rbase = Kst + row * 128;
             if constexpr (kFp8) {
-                // one ldmatrix.x4 covers two 16-byte chunks (32 d) of 16 tokens
+                // one ldmatrix.x4 reads 16 tokens x 32 codes: the A operand of
+                // an E4M3 MMA as it stands (row = token, four d per register)
 #pragma unroll
-                for (int kp = 0; kp < KS / 2; ++kp) {
+                for (int kp = 0; kp < KQ; ++kp) {
                     const int c = 2 * kp + (mi >> 1);
                     uint32_t x[4];
                     ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const uint32_t a[4] = {
-                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4140)),
-                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4140)),
-                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4342)),
-                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4342))};
-                        Ops::mma(sc[mt], a, qb[2 * kp + h2][0], qb[2 * kp + h2][1]);
-                    }
+                    mma_e4m3(sc[mt], x, qb[kp][0], qb[kp][1]);
+                    mma_e4m3(sc[mt], x, qb[kp][2], qb[kp][3]);
                 }
             } else {
 #pragma unroll
@@ -402,53 +505,65 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         }
 
         // ---- P^T fragments: hi + residual, transposed from the S layout
-        uint32_t bh[2][2], bl[2][2];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
-                const uint32_t hi = Ops::pack(w0, w1);
-                const float2 hf = Ops::unpack(hi);
-                // the sums use exactly the weights the products use
-                if constexpr (kFp8) {
-                    // binary16 weights as one term: relative error at most
-                    // 2^-11, far inside the E4M3 codes' own 2^-4
-                    l_run[0] += hf.x;
-                    l_run[1] += hf.y;
-                } else {
-                    const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
-                    const float2 lf = Ops::unpack(lo);
-                    l_run[0] += hf.x + lf.x;
-                    l_run[1] += hf.y + lf.y;
-                    bl[mt][hr] = movmatrix_trans(lo);
-                }
-                bh[mt][hr] = movmatrix_trans(hi);
-            }
-        }
-
-        // ---- O^T += V^T P^T
         if constexpr (kFp8) {
-            // one 16-byte chunk = 16 d of all 32 tokens: ldmatrix.trans on byte
-            // pairs gives lane (tokens 2t, 2t+1) x (d 2g, 2g+1); a byte permute
-            // regroups them by d. Fragment row g <-> d 2g, row g+8 <-> d 2g+1.
+            // E4M3 weights of 256 p in two terms (hi + residual: about 8
+            // significant bits; 256 p <= 256 stays inside the format), one
+            // code per 16-bit element through movmatrix, then four codes per
+            // register in the k order (tokens 2t, 2t+1, 8+2t, 9+2t of each
+            // 16) that the V^T fragments below use. The sums use exactly the
+            // weights the MMAs multiply (in units of 1/256).
+            uint32_t bh[2], bl[2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                uint32_t th[2], tl[2];
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    uint32_t hc, lc;
+                    float2 w;
+                    e4m3_split2(pv[mt][2 * hr] * 256.f, pv[mt][2 * hr + 1] * 256.f, hc, lc, w);
+                    l_run[0] += w.x;
+                    l_run[1] += w.y;
+                    th[hr] = movmatrix_trans(__byte_perm(hc, 0u, 0x4140));
+                    tl[hr] = movmatrix_trans(__byte_perm(lc, 0u, 0x4140));
+                }
+                bh[mt] = __byte_perm(th[0], th[1], 0x6420);
+                bl[mt] = __byte_perm(tl[0], tl[1], 0x6420);
+            }
+            // ---- O^T += V^T P^T: one ldmatrix.trans gives, per lane, the
+            // codes of tokens (2t, 2t+1) + 8j at d (2g, 2g+1) of a 16-byte
+            // chunk for each 8-token group j; byte permutes regroup them into
+            // four tokens per register at one d. Fragment row g <-> d 2g,
+            // row g+8 <-> d 2g+1 of the chunk.
 #pragma unroll
             for (int md = 0; md < KS; ++md) {
                 const int row = 8 * mi + r8;                        // token
                 uint32_t y[4];
                 ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
                                          (((md & 7) ^ (row & 7)) << 4));
-#pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
-                    const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
-                    const uint32_t a[4] = {e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4240)),
-                                           e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4341)),
-                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4240)),
-                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4341))};
-                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
-                }
+                const uint32_t a[4] = {__byte_perm(y[0], y[1], 0x6420), __byte_perm(y[0], y[1], 0x7531),
+                                       __byte_perm(y[2], y[3], 0x6420), __byte_perm(y[2], y[3], 0x7531)};
+                mma_e4m3(acc[md], a, bh[0], bh[1]);
+                mma_e4m3(acc[md], a, bl[0], bl[1]);
             }
         } else {
+            uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
+                    const uint32_t hi = Ops::pack(w0, w1);
+                    const float2 hf = Ops::unpack(hi);
+                    // the sums use exactly the weights the products use
+                    const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
+                    const float2 lf = Ops::unpack(lo);
+                    l_run[0] += hf.x + lf.x;
+                    l_run[1] += hf.y + lf.y;
+                    bl[mt][hr] = movmatrix_trans(lo);
+                    bh[mt][hr] = movmatrix_trans(hi);
+                }
+            }
+            // ---- O^T += V^T P^T
 #pragma unroll
             for (int md = 0; md < KS; ++md) {
 #pragma unroll
@@ -478,10 +593,10 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
         l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
     }
-    named_barrier(1, kTmaConsumerWarps * 32);    // ring is free: every stage was consumed
-    float* cm = reinterpret_cast<float*>(smem);                 // [4][8]
-    float* cl = cm + kTmaConsumerWarps * 8;                     // [4][8]
-    float* co = cl + kTmaConsumerWarps * 8;                     // [4][8][D]
+    named_barrier(1, NCW * 32);    // ring is free: every stage was consumed
+    float* cm = reinterpret_cast<float*>(smem);                 // [NCW][8]
+    float* cl = cm + NCW * 8;                                   // [NCW][8]
+    float* co = cl + NCW * 8;                                   // [NCW][8][D]
     if (g == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -500,30 +615,30 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
                 if (h < GS) co[(warp * 8 + h) * D + d] = acc[md][2 * hr + j];
             }
     }
-    named_barrier(1, kTmaConsumerWarps * 32);
+    named_barrier(1, NCW * 32);
 
-    for (int i = threadIdx.x; i < GS * D; i += kTmaConsumerWarps * 32) {
+    for (int i = threadIdx.x; i < GS * D; i += NCW * 32) {
         const int h = i / D;
         const int e = i - h * D;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kTmaConsumerWarps; ++w) M = fmaxf(M, cm[w * 8 + h]);
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, cm[w * 8 + h]);
         float W = 0.f, O = 0.f;
 #pragma unroll
-        for (int w = 0; w < kTmaConsumerWarps; ++w) {
+        for (int w = 0; w < NCW; ++w) {
             const float mw = cm[w * 8 + h];
             const float f = (mw == -INFINITY) ? 0.f : fast_exp2(mw - M);
             W = fmaf(f, cl[w * 8 + h], W);
             O = fmaf(f, co[(w * 8 + h) * D + e], O);
         }
-        const float val = __fdiv_rn(O, W) * (kFp8 ? p.v_mul * 256.f : p.v_mul);
+        const float val = __fdiv_rn(O, W) * p.v_mul;
         const int hq = hq0 + h;
         if constexpr (kSplit) {
             const size_t row = ((size_t)s * p.num_q_heads + hq) * p.max_parts + blockIdx.x;
             p.tmp_out[row * D + e] = val;
             if (e == 0) {
                 p.max_logits[row] = M * kLn2;
-                p.exp_sums[row] = W;
+                p.exp_sums[row] = kFp8 ? W * (1.f / 256.f) : W;  // E4M3 weights are 256 p
             }
         } else {
             QT* out = reinterpret_cast<QT*>(p.out);
@@ -540,7 +655,7 @@ cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const DecodeParams& p = tp.p;
     dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups, p.num_seqs);
-    kern<<<grid, kTmaThreads, Smem::kAlloc, stream>>>(tp);
+    kern<<<grid, mma_threads<CT, D>(), Smem::kAlloc, stream>>>(tp);
     return cudaGetLastError();
 }
 
