@@ -487,6 +487,82 @@ def run_kernel_leg(st: Step, device, min_seconds: float = 1.0, per_graph: int = 
                       f"times ({n} launches, {total / 1e3:.2f} s), events on the replaying stream"}
 
 
+def run_shared_step(st: Step, device, seconds: float = 0.5) -> dict | None:
+    """Where sequences share their leading partitions' blocks: the step as
+    pa_write_decode_shared_prefix runs it (the shared-prefix kernel reading
+    each unit's shared partitions once, the partition kernel with the KV
+    write over the rest, the merge), planned on the host from the block
+    tables (pa_shared_prefix_plan, outside the timed region); launched
+    eagerly and replayed as a CUDA graph."""
+    import torch
+    c, pk = st.case, st.pk
+    plan = pk.shared_prefix_plan(c.block_tables, c.context_lens, c.block_size, st.P)
+    if plan.num_units == 0:
+        return None
+    sp, us, up = plan.to(device)
+    kw = (dict(key=st.nk, value=st.nv, slot_mapping=st.ns) if c.kv_dtype == c.q_dtype else {})
+
+    def step(stream=None):
+        if not kw:
+            pk.reshape_and_cache(st.nk, st.nv, st.kc, st.vc, st.ns, c.k_scale, c.v_scale,
+                                 st.status, stream)
+        pk.write_decode_shared_prefix(st.out, st.q, st.kc, st.vc, st.bt, st.cl, c.max_context_len,
+                                      c.scale, st.ws, sp, us, up, plan.max_unit_parts, st.P,
+                                      k_scale=c.k_scale, v_scale=c.v_scale, dev_status=st.status,
+                                      stream=stream, **kw)
+
+    step()
+    torch.cuda.synchronize()
+    if int(st.status.item()) != 0:
+        raise SystemExit(f"device status {int(st.status.item())} after the shared-prefix step")
+    cur = torch.cuda.current_stream(device)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        step()
+    a.record(cur)
+    step()
+    b.record(cur)
+    torch.cuda.synchronize()
+    n = max(20, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
+    a.record(cur)
+    for _ in range(n):
+        step()
+    b.record(cur)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / n
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(cur)
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    cur.wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    a.record(cur)
+    for _ in range(n):
+        g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    gms = a.elapsed_time(b) / n
+    by = st.bytes_per_step()
+    peak, _ = hbm_peak()
+    gbs = by["total"] / (ms * 1e-3) / 1e9
+    unique = unique_record(c, by, 1, ms, peak)
+    members = int((plan.unit_seqs >= 0).sum())
+    return {"ms_per_step": round(ms, 5), "steps": n, "graph_ms_per_step": round(gms, 5),
+            "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
+            "seqs_per_s_per_layer": round(c.num_seqs / (ms * 1e-3), 1),
+            **({"unique_bytes": unique} if unique else {}),
+            "units": plan.num_units, "unit_members": members,
+            "shared_partitions": int(plan.max_unit_parts),
+            "launches": "shared-prefix kernel, partition kernel" + (
+                " (KV write fused)" if kw else " after reshape_and_cache") + ", merge",
+            "note": "logical bytes as in the plain step; the shared partitions' K/V is read "
+                    "once per unit of up to 4 sequences"}
+
+
 def measure_config(index: int, device, partition_size, form="fused", step_seconds=0.3,
                    kernel_seconds=0.5) -> dict:
     """One workload's decode step and its kernel: the step launched eagerly
@@ -527,6 +603,7 @@ def measure_config(index: int, device, partition_size, form="fused", step_second
     graph = run_graph(st, max(20, n), device)
     ws = run_write_step(st, device)
     unique = unique_record(case, by, 1, ms, peak)
+    shared = run_shared_step(st, device) if st.split else None
     rec = {"workload": f"{case.name} (configuration {index})", "num_seqs": case.num_seqs,
            "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
            "head_size": case.head_size, "kv_dtype": case.cache_dtype,
@@ -544,6 +621,8 @@ def measure_config(index: int, device, partition_size, form="fused", step_second
            "bytes_per_step": by}
     if unique:
         rec["unique_bytes"] = unique
+    if shared:
+        rec["shared_prefix_step"] = shared
     del st
     torch.cuda.empty_cache()
     return rec

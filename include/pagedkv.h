@@ -104,6 +104,10 @@ typedef enum pa_dtype {
                                     sequence (the token is stored; the decode may miss it) */
 #define PA_DEV_BAD_ORDER    32u /* a seq_order entry is outside [0, num_seqs) (the work
                                    it names is skipped) */
+#define PA_DEV_BAD_PREFIX   64u /* a shared-prefix unit member whose context does not extend
+                                   past the unit's shared partitions, whose skip count differs
+                                   from the unit's, or whose block table differs from the
+                                   unit's first member's over a shared partition */
 
 /* Supported shapes: head_size in {64, 128, 256}; block_size in [1, 1024];
  * partition_size a positive multiple of 32 (512 on the pages). */
@@ -274,6 +278,73 @@ pa_status pa_write_decode_partitioned(void* out, const void* query, const void* 
                                       pa_dtype cache_dtype, float k_scale, float v_scale,
                                       int partition_size, void* workspace, size_t workspace_bytes,
                                       uint32_t* dev_status, void* stream);
+
+/*
+ * Shared-prefix decode. Requests with a common prompt prefix share its cached
+ * KV blocks ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 5, prefix reuse;
+ * "Lecture 3: PagedAttention and vLLM", "shared prefix": several block tables
+ * point at the same physical blocks). The partitioned decode then reads those
+ * blocks once per sequence. Here sequences whose tables agree over their
+ * first partitions are put in units of up to PA_SHARED_UNIT_MEMBERS, and a
+ * unit reads each shared partition's K/V once for all its members; the
+ * result is the partitioned decode's, up to floating-point rounding order.
+ *
+ * pa_shared_prefix_plan -- host only: the units for a batch, from the host
+ * copies of block_tables [num_seqs, max_blocks_per_seq] and context_lens
+ * [num_seqs]. A sequence can share partition j (tokens [j P, (j+1) P), P =
+ * partition_size, a multiple of 32 and of block_size) only if its table
+ * names the same blocks there as its unit's other members, and only
+ * partitions wholly before its newest token (at most (L - 1) / P).
+ * Outputs (host memory, caller-owned):
+ *   seq_shared_parts [num_seqs]   leading partitions each sequence shares (0: none)
+ *   unit_seqs [max_units * PA_SHARED_UNIT_MEMBERS]  each unit's sequences, -1 padded
+ *   unit_parts [max_units]        partitions each unit's members share (>= 1)
+ *   *num_units, *max_unit_parts   units formed, and the largest unit_parts
+ * Units stop at max_units (the remaining sequences share nothing). Argument
+ * errors -> PA_ERR_INVALID_ARG.
+ */
+#define PA_SHARED_UNIT_MEMBERS 4
+pa_status pa_shared_prefix_plan(const int32_t* block_tables, const int32_t* context_lens,
+                                int num_seqs, int max_blocks_per_seq, int block_size,
+                                int partition_size, int32_t* seq_shared_parts,
+                                int32_t* unit_seqs, int32_t* unit_parts, int max_units,
+                                int* num_units, int* max_unit_parts);
+
+/*
+ * pa_write_decode_shared_prefix -- one decode step with shared-prefix units:
+ * the shared-prefix kernel (each unit's shared partitions, every stage read
+ * once for all members), the partition kernel over every other partition
+ * (with the step's KV write folded in when key/value/slot_mapping are given,
+ * as in pa_write_decode_partitions), then pa_merge into out. Three launches
+ * on `stream`. Arguments are pa_write_decode_partitioned's plus the plan of
+ * pa_shared_prefix_plan, copied to the device by the caller:
+ *   seq_shared_parts [num_seqs], unit_seqs [num_units, PA_SHARED_UNIT_MEMBERS],
+ *   unit_parts [num_units] int32 (device); max_unit_parts <= the partitions of
+ *   max_context_len. num_units == 0: the plain partitioned step.
+ * key, value and slot_mapping are all null (decode only) or all given.
+ * The workspace is pa_decode_partitioned_workspace_bytes(num_seqs,
+ * num_q_heads, head_size, max_context_len, partition_size), as for the
+ * partitioned decode. Shapes: those of the tensor-core decode (a 16-bit
+ * query with a cache of its type or E4M3, an even group or none, rows of
+ * 128/256/512 bytes, block size 8, 16 or a multiple of 32) and
+ * partition_size a multiple of block_size; otherwise PA_ERR_UNSUPPORTED.
+ * Device checks: a member whose context does not extend past its unit's
+ * partitions (or exceeds the bounds) is computed by the partition kernel
+ * instead, and PA_DEV_BAD_PREFIX is set; so is it for a member whose skip
+ * count or block table over a shared partition differs from the unit's (its
+ * output is then unspecified). A sequence with a skip count that belongs to
+ * no unit is not detected: the plan must come from pa_shared_prefix_plan or
+ * hold the same rules.
+ */
+pa_status pa_write_decode_shared_prefix(
+    void* out, const void* query, const void* key, const void* value, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, int max_context_len, float scale, pa_dtype q_dtype,
+    pa_dtype cache_dtype, float k_scale, float v_scale, const int32_t* seq_shared_parts,
+    const int32_t* unit_seqs, const int32_t* unit_parts, int num_units, int max_unit_parts,
+    int partition_size, void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+    void* stream);
 
 /*
  * pa_decode_partitioned_static -- pa_decode_partitioned for callers that

@@ -32,6 +32,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA, PA
 PA_F32, PA_F16, PA_BF16, PA_FP8_E4M3 = range(4)
 DEV_BAD_BLOCK_ID, DEV_BAD_SLOT, DEV_BAD_LEN, DEV_TIMEOUT, DEV_SLOT_MISMATCH = 1, 2, 4, 8, 16
 DEV_BAD_ORDER = 32
+DEV_BAD_PREFIX = 64
 
 DEFAULT_PARTITION_SIZE = 512
 
@@ -78,6 +79,10 @@ def lib() -> ctypes.CDLL:
                                                    F, I, I, F, F, I, P, P]
         L.pa_write_decode.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64, I, F, I, I,
                                       F, F, P, P]
+        L.pa_shared_prefix_plan.argtypes = [P, P, I, I, I, I, P, P, P, I, P, P]
+        L.pa_write_decode_shared_prefix.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I,
+                                                    I64, I, F, I, I, F, F, P, P, P, I, I, I, P, S,
+                                                    P, P]
         L.pa_write_decode_partitioned.argtypes = [P, P, P, P, P, P, P, P, I, P, I, I, I, I, I,
                                                   I64, I, F, I, I, F, F, I, P, S, P, P]
         L.pa_write_decode_partitions.argtypes = [P, P, P, P, P, P, P, I, P, I, I, I, I, I, I64,
@@ -118,6 +123,7 @@ def lib() -> ctypes.CDLL:
                      "pa_decode_partitioned_static", "pa_write_decode",
                      "pa_write_decode_partitioned", "pa_write_decode_partitions",
                      "pa_decode_choose", "pa_decode_partition_size", "pa_version",
+                     "pa_shared_prefix_plan", "pa_write_decode_shared_prefix",
                      "pa_copy_blocks", "pa_selftest_wait", "pa_allocator_allocate", "pa_allocator_fork",
                      "pa_allocator_free", "pa_allocator_append_slot"):
             getattr(L, name).restype = ctypes.c_int
@@ -375,6 +381,75 @@ def write_decode_partitioned(out, query, key, value, k_cache, v_cache, slot_mapp
         float(v_scale), partition_size, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
         "pa_write_decode_partitioned")
+
+
+SHARED_UNIT_MEMBERS = 4
+
+
+class SharedPrefixPlan:
+    """pa_shared_prefix_plan's units for a batch (host arrays): which
+    sequences share their leading partitions' KV blocks."""
+
+    def __init__(self, seq_shared_parts, unit_seqs, unit_parts, max_unit_parts):
+        self.seq_shared_parts = seq_shared_parts      # [S] int32
+        self.unit_seqs = unit_seqs                    # [units, SHARED_UNIT_MEMBERS] int32
+        self.unit_parts = unit_parts                  # [units] int32
+        self.max_unit_parts = max_unit_parts
+
+    @property
+    def num_units(self) -> int:
+        return int(self.unit_parts.shape[0])
+
+    def to(self, device):
+        """The plan's arrays as device tensors (seq_shared_parts, unit_seqs, unit_parts)."""
+        t = lambda a: torch.from_numpy(a).to(device)
+        return t(self.seq_shared_parts), t(self.unit_seqs), t(self.unit_parts)
+
+
+def shared_prefix_plan(block_tables, context_lens, block_size,
+                       partition_size=DEFAULT_PARTITION_SIZE) -> SharedPrefixPlan:
+    """Units of sequences sharing their leading partitions, from host copies
+    of block_tables [S, max_blocks] and context_lens [S] (numpy int32)."""
+    import numpy as np
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    S, mb = bt.shape
+    cap = max(1, S // 2)
+    parts = np.zeros(S, np.int32)
+    useqs = np.full((cap, SHARED_UNIT_MEMBERS), -1, np.int32)
+    uparts = np.zeros(cap, np.int32)
+    n, mx = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().pa_shared_prefix_plan(bt.ctypes.data, cl.ctypes.data, S, mb, int(block_size),
+                                        int(partition_size), parts.ctypes.data, useqs.ctypes.data,
+                                        uparts.ctypes.data, cap, ctypes.byref(n), ctypes.byref(mx)),
+           "pa_shared_prefix_plan")
+    return SharedPrefixPlan(parts, useqs[:n.value].copy(), uparts[:n.value].copy(), mx.value)
+
+
+def write_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens,
+                               max_context_len, scale, workspace, seq_shared_parts, unit_seqs,
+                               unit_parts, max_unit_parts, partition_size=DEFAULT_PARTITION_SIZE,
+                               key=None, value=None, slot_mapping=None, k_scale=1.0,
+                               v_scale=1.0, dev_status=None, stream=None) -> None:
+    """Decode step with shared-prefix units (device tensors of a
+    SharedPrefixPlan): shared-prefix kernel, partition kernel (with the KV
+    write when key/value/slot_mapping are given), merge."""
+    S, Hq, D, nb, Hkv, B, mb = _decode_dims(query, k_cache, block_tables, context_lens)
+    if key is not None:
+        _new_tokens(key, value, slot_mapping, query, k_cache)
+    for t in (seq_shared_parts, unit_seqs, unit_parts):
+        if t.dtype != torch.int32:
+            raise ValueError("the plan's arrays must be int32")
+    if seq_shared_parts.numel() != S or unit_seqs.numel() != SHARED_UNIT_MEMBERS * unit_parts.numel():
+        raise ValueError("plan arrays do not match the batch")
+    _check(lib().pa_write_decode_shared_prefix(
+        _ptr(out), _ptr(query), _ptr(key), _ptr(value), _ptr(slot_mapping), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), mb, _ptr(context_lens), S, Hq, Hkv, D, B, nb,
+        int(max_context_len), float(scale), _dtype(query), _dtype(k_cache), float(k_scale),
+        float(v_scale), _ptr(seq_shared_parts), _ptr(unit_seqs), _ptr(unit_parts),
+        int(unit_parts.numel()), int(max_unit_parts), partition_size, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
+        "pa_write_decode_shared_prefix")
 
 
 STATIC_WORKSPACE_BYTES = 64 * 1024 * 1024

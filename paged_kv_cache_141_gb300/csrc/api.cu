@@ -194,6 +194,18 @@ cudaError_t run_simt_decode_kernel(DecodeParams p, int head_size, pa_dtype q_dty
     }
 }
 
+// The shared-prefix kernel for a tensor-core decode shape.
+cudaError_t run_shared_kernel(const DecodeParams& p, int head_size, pa_dtype q_dtype,
+                              pa_dtype cache_dtype, int max_unit_parts, cudaStream_t stream) {
+    const int gs = p.group / p.sub_groups;
+    if (cache_dtype == PA_FP8_E4M3) {
+        if (q_dtype == PA_F16) return launch_decode_shared_f16_e4m3(p, head_size, gs, max_unit_parts, stream);
+        return launch_decode_shared_bf16_e4m3(p, head_size, gs, max_unit_parts, stream);
+    }
+    if (q_dtype == PA_F16) return launch_decode_shared_f16(p, head_size, gs, max_unit_parts, stream);
+    return launch_decode_shared_bf16(p, head_size, gs, max_unit_parts, stream);
+}
+
 pa_status check_partition_size(int partition_size) {
     if (partition_size <= 0 || partition_size % 32 != 0) return PA_ERR_INVALID_ARG;
     return PA_OK;
@@ -442,6 +454,62 @@ pa_status pa_write_decode_partitioned(void* out, const void* query, const void* 
                          reinterpret_cast<const float*>(w + l.exp_sums), context_lens, num_seqs,
                          num_q_heads, head_size, partition_size,
                          max_partitions(max_context_len, partition_size),
+                         decode_len_cap(max_context_len, max_blocks_per_seq, block_size), q_dtype,
+                         dev_status, stream);
+}
+
+pa_status pa_write_decode_shared_prefix(
+    void* out, const void* query, const void* key, const void* value, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+    const int32_t* context_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_size,
+    int block_size, int64_t num_blocks, int max_context_len, float scale, pa_dtype q_dtype,
+    pa_dtype cache_dtype, float k_scale, float v_scale, const int32_t* seq_shared_parts,
+    const int32_t* unit_seqs, const int32_t* unit_parts, int num_units, int max_unit_parts,
+    int partition_size, void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+    void* stream) {
+    DecodeParams p;
+    pa_status st = check_decode(query, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_size,
+                                block_size, num_blocks, max_context_len, scale, q_dtype,
+                                cache_dtype, k_scale, v_scale, dev_status, p);
+    if (st != PA_OK) return st;
+    if ((st = check_partition_size(partition_size)) != PA_OK) return st;
+    if (num_units < 0 || max_unit_parts < 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !aligned16(out)) return PA_ERR_INVALID_ARG;
+    const bool write = key || value || slot_mapping;
+    if (write && (!key || !value || !slot_mapping || !aligned16(key, value) || !aligned(slot_mapping, 8)))
+        return PA_ERR_INVALID_ARG;
+    const bool shared = num_units > 0 && max_unit_parts > 0;
+    if (shared) {
+        if (!seq_shared_parts || !unit_seqs || !unit_parts || !aligned(seq_shared_parts, 4) ||
+            !aligned(unit_seqs, 4) || !aligned(unit_parts, 4))
+            return PA_ERR_INVALID_ARG;
+        if (max_unit_parts > max_partitions(max_context_len, partition_size)) return PA_ERR_INVALID_ARG;
+        // the tensor-core decode's shapes; whole blocks per partition, so that
+        // a sequence's newest token never lies in a shared block
+        if (!tma_eligible(head_size, cache_dtype, block_size, num_blocks, num_kv_heads) ||
+            !mma_eligible(q_dtype, cache_dtype, p.group) || partition_size % block_size != 0 ||
+            num_units > 65535)
+            return PA_ERR_UNSUPPORTED;
+    }
+    if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
+                             workspace, workspace_bytes)) != PA_OK)
+        return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (shared) {
+        p.skip_parts = seq_shared_parts;
+        p.unit_seqs = unit_seqs;
+        p.unit_parts = unit_parts;
+        p.num_units = num_units;
+        cudaError_t e = run_shared_kernel(p, head_size, q_dtype, cache_dtype, max_unit_parts, s);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (write) bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
+    cudaError_t e = run_decode_kernel(p, head_size, q_dtype, cache_dtype, true, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    return merge_checked(out, p.tmp_out, p.max_logits, p.exp_sums, context_lens, num_seqs,
+                         num_q_heads, head_size, partition_size, p.max_parts,
                          decode_len_cap(max_context_len, max_blocks_per_seq, block_size), q_dtype,
                          dev_status, stream);
 }

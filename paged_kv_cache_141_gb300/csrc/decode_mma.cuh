@@ -13,12 +13,13 @@
 //   O^T (d x 8 heads) += V^T (d x 16 tokens) . P^T (16 tokens x 8 heads),
 //     V^T fragments read with ldmatrix.trans, P^T fragments made from the S
 //     accumulators with movmatrix. P is split into a 16-bit high part and a
-//     16-bit residual, two MMAs, so the weights keep ~16 significant bits.
-// E4M3 caches run both products as E4M3 MMAs (m16n8k32) on the stored codes,
-// with no widening: the K tile is the A operand as ldmatrix reads it, V^T is
-// regrouped by byte permutes, and the query and the weights enter as two E4M3
-// terms each (the value and its residual, ~8 significant bits, like a
-// bfloat16 operand), see below.
+//     16-bit residual, two MMAs, so the weights keep ~16 significant bits
+//     (E4M3 caches: binary16 weights as one term, 11 bits, far below the
+//     codes' own error).
+// E4M3 caches are widened to binary16 in registers by integer operations
+// (e4m3x2_to_f16x2_scaled) and multiplied on binary16 MMAs. (Warp-level MMAs
+// with E4M3 operands were measured to cost as many instructions as this
+// widening on this GPU, with the query and weights cut to two E4M3 terms.)
 // Heads beyond the group (up to the MMA's 8 columns) carry zero queries and
 // are never written out. Rows of V past the context are zeroed before the
 // P.V product, since 0 x NaN would otherwise poison every output component.
@@ -68,65 +69,6 @@ template <> struct MmaOps<__half> {
         return __half22float2(*reinterpret_cast<const __half2*>(&w));
     }
 };
-
-// D (16 x 8, f32) += A (16 x 32 E4M3 codes, row) . B (32 x 8 E4M3 codes, col).
-// Register i of A holds four codes of one row: rows g (a0, a2) and g + 8
-// (a1, a3), columns 4 t + (0..3) (a0, a1) and 16 + 4 t + (0..3) (a2, a3),
-// lowest column in the lowest byte; B's b0 / b1 hold column g at rows
-// 4 t + (0..3) / 16 + 4 t + (0..3).
-__device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Two floats to E4M3 codes, round to nearest even, saturating: x in the low
-// byte, y in the high byte (the instruction's first source goes high).
-__device__ __forceinline__ uint32_t e4m3x2_of(float x, float y) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(y), "f"(x));
-    return r;
-}
-
-// The values of two E4M3 codes (low byte -> .x), exact through binary16.
-__device__ __forceinline__ float2 e4m3x2_value(uint32_t two) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
-    float lo, hi;
-    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
-        "cvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-    return make_float2(lo, hi);
-}
-
-// Two-term E4M3 split of a pair: hi = E4M3(v), lo = E4M3(v - hi); the values
-// of both are returned so that a sum of weights uses exactly what the MMA
-// multiplies. v - hi is exact in float32.
-__device__ __forceinline__ void e4m3_split2(float x, float y, uint32_t& hi, uint32_t& lo,
-                                            float2& sum) {
-    hi = e4m3x2_of(x, y);
-    const float2 h = e4m3x2_value(hi);
-    lo = e4m3x2_of(x - h.x, y - h.y);
-    const float2 l = e4m3x2_value(lo);
-    sum = make_float2(h.x + l.x, h.y + l.y);
-}
-
-// A power of two s with max_abs * s in (224, 448] (1 if max_abs is 0 or not
-// finite), so that the E4M3 terms of values up to max_abs neither saturate nor
-// waste range.
-__device__ __forceinline__ float e4m3_range_scale(float max_abs) {
-    const uint32_t b = __float_as_uint(max_abs);
-    const int ef = (int)((b >> 23) & 0xffu);
-    if (max_abs == 0.f || ef == 0xff) return 1.f;
-    const int E = (ef == 0 ? -126 : ef - 127);
-    int e = ((b & 0x7fffffu) <= 0x600000u ? 8 : 7) - E;     // 448 = 1.75 x 2^8
-    e = e < -126 ? -126 : (e > 127 ? 127 : e);
-    return __uint_as_float((uint32_t)(e + 127) << 23);
-}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem_row) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -211,6 +153,204 @@ constexpr int mma_threads() {
     return (mma_consumer_warps<CT, D>() + 1) * 32;
 }
 
+// One consumer warp's share of the decode: the query's B fragments, the
+// O^T accumulators and the online-softmax state of the heads this lane holds
+// (2 t4 and 2 t4 + 1), and the work on one 32-token stage of K and V.
+template <typename QT, typename CT, int D, int GS>
+struct MmaWarp {
+    using S = TmaShape<CT, D>;
+    using MT = typename MathType<CT>::T;
+    using Ops = MmaOps<MT>;
+    static constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    static constexpr int KS = D / 16;          // k-steps of the score product
+    // Q^T fragments (B operand of S = K Q^T): column g = head g, rows = d.
+    // For E4M3 the k index of a 16-wide step maps to d as the widened ldmatrix
+    // bytes come: k = 2t+j <-> d = 4t+j and k = 2t+8+j <-> d = 4t+2+j (a
+    // permutation of the reduction, applied to K and Q alike).
+    uint32_t qb[KS][2];
+    float qk_mul;                               // scale * log2(e) (E4M3: k_scale and 2^8 too)
+    float acc[KS][4];                           // O^T fragments: rows d, columns heads
+    float m_run[2];                             // heads 2*t4 and 2*t4+1
+    float l_run[2];                             // this lane's share of the sums
+
+    // qp: the query row of the unit's first head; q_mul: scale * log2(e)
+    // (E4M3: * k_scale).
+    __device__ __forceinline__ void load_query(const QT* __restrict__ qp, float q_mul, int lane) {
+        const int g = lane >> 2;
+        const int t4 = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (g >= GS) {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            } else if constexpr (kFp8) {
+                const QT* q4 = qp + g * D + 16 * ks + 4 * t4;
+                qb[ks][0] = Ops::pack(to_float(q4[0]), to_float(q4[1]));
+                qb[ks][1] = Ops::pack(to_float(q4[2]), to_float(q4[3]));
+            } else {
+                qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
+                qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
+            }
+        }
+        // the widened E4M3 codes are their values times 2^-8
+        qk_mul = kFp8 ? q_mul * 256.f : q_mul;
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+    }
+
+    // One stage: K and V tiles of 32 tokens in the 128-byte swizzled layout,
+    // the first nvalid of them in the context (V rows past it already zero).
+    __device__ __forceinline__ void consume(const uint8_t* Kst, const uint8_t* Vst, int nvalid,
+                                            int lane) {
+        const int g = lane >> 2;
+        const int t4 = lane & 3;
+        const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix row addresses: lane -> (matrix, row)
+        // ---- S = K Q^T for both 16-token row tiles
+        float sc[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sc[mt][j] = 0.f;
+            const int row = 16 * mt + (mi & 1) * 8 + r8;
+            const uint8_t* rbase = Kst + row * 128;
+            if constexpr (kFp8) {
+                // one ldmatrix.x4 covers two 16-byte chunks (32 d) of 16 tokens
+#pragma unroll
+                for (int kp = 0; kp < KS / 2; ++kp) {
+                    const int c = 2 * kp + (mi >> 1);
+                    uint32_t x[4];
+                    ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const uint32_t a[4] = {
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4140)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2], 0u, 0x4342)),
+                            e4m3x2_to_f16x2_scaled(__byte_perm(x[2 * h2 + 1], 0u, 0x4342))};
+                        Ops::mma(sc[mt], a, qb[2 * kp + h2][0], qb[2 * kp + h2][1]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int c = 2 * ks + (mi >> 1);
+                    uint32_t a[4];
+                    ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
+                    Ops::mma(sc[mt], a, qb[ks][0], qb[ks][1]);
+                }
+            }
+        }
+
+        // ---- online softmax per head (this lane: heads 2*t4, 2*t4+1; tokens g, g+8 of each tile)
+        float pv[2][4];
+        float alpha[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int tok = 16 * mt + g + 8 * hr;
+                    float v = sc[mt][2 * hr + j] * qk_mul;
+                    v = tok < nvalid ? v : -INFINITY;          // select, never multiply
+                    sc[mt][2 * hr + j] = v;
+                    mx = fmaxf(mx, v);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float m_new = fmaxf(m_run[j], mx);
+            alpha[j] = (m_new == -INFINITY) ? 1.f
+                     : ((m_run[j] == -INFINITY) ? 0.f : fast_exp2(m_run[j] - m_new));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int hr = 0; hr < 2; ++hr) {
+                    const float v = sc[mt][2 * hr + j];
+                    const float w = (v == -INFINITY) ? 0.f : fast_exp2(v - m_new);
+                    pv[mt][2 * hr + j] = w;
+                }
+            m_run[j] = m_new;
+            l_run[j] = l_run[j] * alpha[j];
+        }
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            acc[i][0] *= alpha[0];
+            acc[i][1] *= alpha[1];
+            acc[i][2] *= alpha[0];
+            acc[i][3] *= alpha[1];
+        }
+
+        // ---- P^T fragments: hi + residual, transposed from the S layout
+        uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
+                const uint32_t hi = Ops::pack(w0, w1);
+                const float2 hf = Ops::unpack(hi);
+                // the sums use exactly the weights the products use
+                if constexpr (kFp8) {
+                    // binary16 weights as one term: relative error at most
+                    // 2^-11, far inside the E4M3 codes' own 2^-4
+                    l_run[0] += hf.x;
+                    l_run[1] += hf.y;
+                } else {
+                    const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
+                    const float2 lf = Ops::unpack(lo);
+                    l_run[0] += hf.x + lf.x;
+                    l_run[1] += hf.y + lf.y;
+                    bl[mt][hr] = movmatrix_trans(lo);
+                }
+                bh[mt][hr] = movmatrix_trans(hi);
+            }
+        }
+
+        // ---- O^T += V^T P^T
+        if constexpr (kFp8) {
+            // one 16-byte chunk = 16 d of all 32 tokens: ldmatrix.trans on byte
+            // pairs gives lane (tokens 2t, 2t+1) x (d 2g, 2g+1); a byte permute
+            // regroups them by d. Fragment row g <-> d 2g, row g+8 <-> d 2g+1.
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+                const int row = 8 * mi + r8;                        // token
+                uint32_t y[4];
+                ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
+                                         (((md & 7) ^ (row & 7)) << 4));
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const uint32_t lo = y[2 * kt], hi = y[2 * kt + 1];
+                    const uint32_t a[4] = {e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4240)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(lo, 0u, 0x4341)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4240)),
+                                           e4m3x2_to_f16x2_scaled(__byte_perm(hi, 0u, 0x4341))};
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+#pragma unroll
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int row = 16 * kt + (mi >> 1) * 8 + r8;      // token
+                    const int c = 2 * md + (mi & 1);                    // 16-byte chunk of d
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
+                                             (((c & 7) ^ (row & 7)) << 4));
+                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
+                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                }
+            }
+        }
+    }
+};
+
 template <typename QT, typename CT, int D, int GS, bool kSplit>
 __global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
@@ -254,6 +394,15 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
     int T0, Tend;
     if constexpr (kSplit) {
+        if (p.skip_parts) {
+            // partitions the shared-prefix kernel computes for this sequence
+            // (its rule: the context extends past them and is within the bound)
+            const int sk = p.skip_parts[s];
+            const int Lr = p.context_lens[s];
+            if (sk > 0 && (int)blockIdx.x < sk && Lr > (long long)sk * p.partition_size &&
+                Lr <= p.max_context_len && Lr <= (long long)p.max_blocks * p.block_size)
+                return;
+        }
         T0 = blockIdx.x * p.partition_size;
         if (T0 >= L) return;
         Tend = min(T0 + p.partition_size, L);
@@ -347,72 +496,9 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
 
     // ---------------------------------------------------------------- consumers
-    // Q^T fragments (B operand of S = K Q^T): column g = head g, rows = d.
-    // 16-bit caches: the query's own 16-bit pairs. E4M3 caches: E4M3 codes of
-    // q * s_q in two terms (hi = E4M3(q s_q), lo = E4M3(q s_q - hi); about 8
-    // significant bits together), s_q a power of two that puts the group's
-    // largest |q| in (224, 448]; per 32-wide k-step: hi b0, hi b1, lo b0, lo b1.
-    constexpr int KQ = kFp8 ? D / 32 : KS;
-    constexpr int QR = kFp8 ? 4 : 2;
-    uint32_t qb[KQ][QR];
-    float qk_mul;                               // score multiplier: scale * log2(e) (* k_scale / s_q)
-    {
-        const QT* qp = reinterpret_cast<const QT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D;
-        if constexpr (kFp8) {
-            // lane (g, t) holds d = 32 kp + 16 h + 4 t + (0..3) of head g;
-            // the query is read twice (maximum, then the terms) rather than
-            // held in registers
-            auto qd = [&](int kp, int j) { return 32 * kp + (j >> 2) * 16 + 4 * t4 + (j & 3); };
-            float mx = 0.f;
-            if (g < GS) {
-#pragma unroll
-                for (int kp = 0; kp < KQ; ++kp)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(to_float(qp[g * D + qd(kp, j)])));
-            }
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-            const float sq = e4m3_range_scale(mx);
-            qk_mul = p.q_mul / sq;
-#pragma unroll
-            for (int kp = 0; kp < KQ; ++kp)
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    float v[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        v[j] = g < GS ? to_float(qp[g * D + qd(kp, 4 * half + j)]) * sq : 0.f;
-                    uint32_t h01, l01, h23, l23;
-                    float2 unused;
-                    e4m3_split2(v[0], v[1], h01, l01, unused);
-                    e4m3_split2(v[2], v[3], h23, l23, unused);
-                    qb[kp][half] = h01 | (h23 << 16);
-                    qb[kp][2 + half] = l01 | (l23 << 16);
-                }
-        } else {
-            qk_mul = p.q_mul;
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks) {
-                if (g >= GS) {
-                    qb[ks][0] = 0u;
-                    qb[ks][1] = 0u;
-                } else {
-                    qb[ks][0] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4);
-                    qb[ks][1] = *reinterpret_cast<const uint32_t*>(qp + g * D + 16 * ks + 2 * t4 + 8);
-                }
-            }
-        }
-    }
-    float acc[KS][4];                           // O^T fragments: rows d, columns heads
-#pragma unroll
-    for (int i = 0; i < KS; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    float m_run[2] = {-INFINITY, -INFINITY};    // heads 2*t4 and 2*t4+1
-    float l_run[2] = {0.f, 0.f};                // this lane's share of the sums
-
-    // ldmatrix row addresses: lane -> (matrix mi, row r)
-    const int mi = lane >> 3, r8 = lane & 7;
+    MmaWarp<QT, CT, D, GS> cw;
+    cw.load_query(reinterpret_cast<const QT*>(p.query) + ((size_t)s * p.num_q_heads + hq0) * D,
+                  p.q_mul, lane);
 
     for (int k = warp; k < n_st; k += NCW) {
         const int slot = k % NST;
@@ -433,151 +519,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             __syncwarp();
         }
 
-        // ---- S = K Q^T for both 16-token row tiles
-        float sc[2][4];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) sc[mt][j] = 0.f;
-            const int row = 16 * mt + (mi & 1) * 8 + r8;
-            const uint8_t* rbase = Kst + row * 128;
-            if constexpr (kFp8) {
-                // one ldmatrix.x4 reads 16 tokens x 32 codes: the A operand of
-                // an E4M3 MMA as it stands (row = token, four d per register)
-#pragma unroll
-                for (int kp = 0; kp < KQ; ++kp) {
-                    const int c = 2 * kp + (mi >> 1);
-                    uint32_t x[4];
-                    ldmatrix_x4(x, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
-                    mma_e4m3(sc[mt], x, qb[kp][0], qb[kp][1]);
-                    mma_e4m3(sc[mt], x, qb[kp][2], qb[kp][3]);
-                }
-            } else {
-#pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int c = 2 * ks + (mi >> 1);
-                    uint32_t a[4];
-                    ldmatrix_x4(a, rbase + (c >> 3) * S::kSpanTileBytes + (((c & 7) ^ (row & 7)) << 4));
-                    Ops::mma(sc[mt], a, qb[ks][0], qb[ks][1]);
-                }
-            }
-        }
-
-        // ---- online softmax per head (this lane: heads 2*t4, 2*t4+1; tokens g, g+8 of each tile)
-        float pv[2][4];
-        float alpha[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const int tok = 16 * mt + g + 8 * hr;
-                    float v = sc[mt][2 * hr + j] * qk_mul;
-                    v = tok < nvalid ? v : -INFINITY;          // select, never multiply
-                    sc[mt][2 * hr + j] = v;
-                    mx = fmaxf(mx, v);
-                }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-            const float m_new = fmaxf(m_run[j], mx);
-            alpha[j] = (m_new == -INFINITY) ? 1.f
-                     : ((m_run[j] == -INFINITY) ? 0.f : fast_exp2(m_run[j] - m_new));
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const float v = sc[mt][2 * hr + j];
-                    const float w = (v == -INFINITY) ? 0.f : fast_exp2(v - m_new);
-                    pv[mt][2 * hr + j] = w;
-                }
-            m_run[j] = m_new;
-            l_run[j] = l_run[j] * alpha[j];
-        }
-#pragma unroll
-        for (int i = 0; i < KS; ++i) {
-            acc[i][0] *= alpha[0];
-            acc[i][1] *= alpha[1];
-            acc[i][2] *= alpha[0];
-            acc[i][3] *= alpha[1];
-        }
-
-        // ---- P^T fragments: hi + residual, transposed from the S layout
-        if constexpr (kFp8) {
-            // E4M3 weights of 256 p in two terms (hi + residual: about 8
-            // significant bits; 256 p <= 256 stays inside the format), one
-            // code per 16-bit element through movmatrix, then four codes per
-            // register in the k order (tokens 2t, 2t+1, 8+2t, 9+2t of each
-            // 16) that the V^T fragments below use. The sums use exactly the
-            // weights the MMAs multiply (in units of 1/256).
-            uint32_t bh[2], bl[2];
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                uint32_t th[2], tl[2];
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    uint32_t hc, lc;
-                    float2 w;
-                    e4m3_split2(pv[mt][2 * hr] * 256.f, pv[mt][2 * hr + 1] * 256.f, hc, lc, w);
-                    l_run[0] += w.x;
-                    l_run[1] += w.y;
-                    th[hr] = movmatrix_trans(__byte_perm(hc, 0u, 0x4140));
-                    tl[hr] = movmatrix_trans(__byte_perm(lc, 0u, 0x4140));
-                }
-                bh[mt] = __byte_perm(th[0], th[1], 0x6420);
-                bl[mt] = __byte_perm(tl[0], tl[1], 0x6420);
-            }
-            // ---- O^T += V^T P^T: one ldmatrix.trans gives, per lane, the
-            // codes of tokens (2t, 2t+1) + 8j at d (2g, 2g+1) of a 16-byte
-            // chunk for each 8-token group j; byte permutes regroup them into
-            // four tokens per register at one d. Fragment row g <-> d 2g,
-            // row g+8 <-> d 2g+1 of the chunk.
-#pragma unroll
-            for (int md = 0; md < KS; ++md) {
-                const int row = 8 * mi + r8;                        // token
-                uint32_t y[4];
-                ldmatrix_x4_trans(y, Vst + (md >> 3) * S::kSpanTileBytes + row * 128 +
-                                         (((md & 7) ^ (row & 7)) << 4));
-                const uint32_t a[4] = {__byte_perm(y[0], y[1], 0x6420), __byte_perm(y[0], y[1], 0x7531),
-                                       __byte_perm(y[2], y[3], 0x6420), __byte_perm(y[2], y[3], 0x7531)};
-                mma_e4m3(acc[md], a, bh[0], bh[1]);
-                mma_e4m3(acc[md], a, bl[0], bl[1]);
-            }
-        } else {
-            uint32_t bh[2][2], bl[2][2];
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-                for (int hr = 0; hr < 2; ++hr) {
-                    const float w0 = pv[mt][2 * hr], w1 = pv[mt][2 * hr + 1];
-                    const uint32_t hi = Ops::pack(w0, w1);
-                    const float2 hf = Ops::unpack(hi);
-                    // the sums use exactly the weights the products use
-                    const uint32_t lo = Ops::pack(w0 - hf.x, w1 - hf.y);
-                    const float2 lf = Ops::unpack(lo);
-                    l_run[0] += hf.x + lf.x;
-                    l_run[1] += hf.y + lf.y;
-                    bl[mt][hr] = movmatrix_trans(lo);
-                    bh[mt][hr] = movmatrix_trans(hi);
-                }
-            }
-            // ---- O^T += V^T P^T
-#pragma unroll
-            for (int md = 0; md < KS; ++md) {
-#pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
-                    const int row = 16 * kt + (mi >> 1) * 8 + r8;      // token
-                    const int c = 2 * md + (mi & 1);                    // 16-byte chunk of d
-                    uint32_t a[4];
-                    ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
-                                             (((c & 7) ^ (row & 7)) << 4));
-                    Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
-                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
-                }
-            }
-        }
+        cw.consume(Kst, Vst, nvalid, lane);
         if (nvalid < kTmaStageTokens) {
             // the generic-proxy zeroing must be ordered before the next bulk copy into this slot
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -589,9 +531,9 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     // ------------------------------------------------- merge the four warps
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
-        l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 4);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 8);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 16);
     }
     named_barrier(1, NCW * 32);    // ring is free: every stage was consumed
     float* cm = reinterpret_cast<float*>(smem);                 // [NCW][8]
@@ -600,8 +542,8 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     if (g == 0) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            cm[warp * 8 + 2 * t4 + j] = m_run[j];
-            cl[warp * 8 + 2 * t4 + j] = l_run[j];
+            cm[warp * 8 + 2 * t4 + j] = cw.m_run[j];
+            cl[warp * 8 + 2 * t4 + j] = cw.l_run[j];
         }
     }
 #pragma unroll
@@ -612,7 +554,7 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             for (int j = 0; j < 2; ++j) {
                 const int h = 2 * t4 + j;
                 const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
-                if (h < GS) co[(warp * 8 + h) * D + d] = acc[md][2 * hr + j];
+                if (h < GS) co[(warp * 8 + h) * D + d] = cw.acc[md][2 * hr + j];
             }
     }
     named_barrier(1, NCW * 32);
@@ -631,20 +573,227 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
             W = fmaf(f, cl[w * 8 + h], W);
             O = fmaf(f, co[(w * 8 + h) * D + e], O);
         }
-        const float val = __fdiv_rn(O, W) * p.v_mul;
+        const float val = __fdiv_rn(O, W) * (kFp8 ? p.v_mul * 256.f : p.v_mul);
         const int hq = hq0 + h;
         if constexpr (kSplit) {
             const size_t row = ((size_t)s * p.num_q_heads + hq) * p.max_parts + blockIdx.x;
             p.tmp_out[row * D + e] = val;
             if (e == 0) {
                 p.max_logits[row] = M * kLn2;
-                p.exp_sums[row] = kFp8 ? W * (1.f / 256.f) : W;  // E4M3 weights are 256 p
+                p.exp_sums[row] = W;
             }
         } else {
             QT* out = reinterpret_cast<QT*>(p.out);
             out[((size_t)s * p.num_q_heads + hq) * D + e] = from_float<QT>(val);
         }
     }
+}
+
+// Shared-prefix partitions ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 5:
+// requests that share a prompt prefix share its KV blocks). A unit is up to
+// NCW sequences whose block tables agree over their first `parts` partitions;
+// CTA (partition, KV head group, unit) reads each stage of that partition
+// once, from the first valid member's table, and every consumer warp consumes every
+// stage for its own member's query, so the shared blocks are read once per
+// unit instead of once per sequence. Each warp writes its member's partials
+// (maximum, sum, normalised output) for the partition itself; the partition
+// kernel skips those partitions (skip_parts) and the merge is unchanged.
+// A member is computed here only if its context holds the shared partitions
+// and at least one more token, its skip_parts entry equals the unit's parts
+// and its table agrees with the first member's over the partition; otherwise
+// PA_DEV_BAD_PREFIX is set (the partition kernel computes a sequence whose
+// length fails the first rule itself).
+template <typename QT, typename CT, int D, int GS>
+__global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
+paged_decode_shared_kernel(const __grid_constant__ TmaDecodeParams tp) {
+    using S = TmaShape<CT, D>;
+    using Smem = MmaSmem<CT, D>;
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    constexpr int NST = Smem::kNst;
+    constexpr int NCW = Smem::kConsumers;
+    constexpr int KS = D / 16;
+    static_assert(GS <= 8, "one MMA covers eight heads");
+    const DecodeParams& p = tp.p;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
+    uint64_t* empty = full + NST;
+
+    const int u = blockIdx.z;
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / p.sub_groups;
+    const int sub = blockIdx.y - kvh * p.sub_groups;
+    const int hq0 = kvh * p.group + sub * GS;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int parts = p.unit_parts[u];
+    if (part >= parts) return;
+    const int P = p.partition_size;
+    int cap = p.max_context_len;
+    {
+        const long long tab = (long long)p.max_blocks * p.block_size;
+        if (tab < cap) cap = (int)tab;
+    }
+    // a member: in range, its context holds the shared partitions and one more
+    // token, and its own skip count names this unit's partitions
+    auto member_ok = [&](int m) {
+        if (m < 0 || m >= p.num_seqs) return false;
+        const int L = p.context_lens[m];
+        return L > (long long)parts * P && L <= cap && p.skip_parts[m] == parts;
+    };
+    // the first valid member's table names the blocks the unit reads
+    int leader = -1;
+    for (int w = 0; w < NCW && leader < 0; ++w) {
+        const int cand = p.unit_seqs[(size_t)u * NCW + w];
+        if (member_ok(cand)) leader = cand;
+    }
+    if (leader < 0) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
+        return;
+    }
+    const int T0 = part * P;
+    const int n_st = P / kTmaStageTokens;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NCW);           // every consumer reads every stage
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int32_t* lead_table = p.block_tables + (size_t)leader * p.max_blocks;
+    if (warp == NCW) {
+        // ------------------------------------------------------------ producer
+        const int B = p.block_size;
+        const int rows = tp.box_rows;
+        if (lane == 0) {
+            tma_prefetch_map(&tp.k_map);
+            tma_prefetch_map(&tp.v_map);
+        }
+        int issued = 0;
+        for (int k = 0; k < n_st; ++k) {
+            const int slot = k % NST;
+            if (k >= NST) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int t_lo = T0 + k * kTmaStageTokens;
+            const int t_hi = t_lo + kTmaStageTokens;
+            const int j0 = t_lo / B;
+            const int nseg = (t_hi - 1) / B - j0 + 1;
+            uint32_t bytes = 0;
+            int y = 0, row0 = 0;
+            if (lane < nseg) {
+                const int j = j0 + lane;
+                const int pb = lead_table[j];
+                if (pb < 0 || (int64_t)pb >= p.num_blocks) {
+                    if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+                } else {
+                    const int off = (B >= kTmaStageTokens) ? (t_lo - j * B) : 0;
+                    y = (pb * p.num_kv_heads + kvh) * B + off;
+                    row0 = (B >= kTmaStageTokens) ? 0 : j * B - t_lo;
+                    bytes = (uint32_t)(rows * S::kRowBytes);
+                }
+            }
+            uint32_t total = bytes;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * total);
+            __syncwarp();
+            if (bytes) {
+                uint8_t* st = ring + (size_t)slot * S::kStageBytes;
+#pragma unroll
+                for (int sp = 0; sp < S::kSpans; ++sp) {
+                    const int x = sp * (128 / S::kElem);
+                    uint8_t* kd = st + sp * S::kSpanTileBytes + row0 * 128;
+                    tma_load_2d(kd, &tp.k_map, x, y, &full[slot]);
+                    tma_load_2d(kd + S::kTileBytes, &tp.v_map, x, y, &full[slot]);
+                }
+            }
+            issued = k + 1;
+        }
+        if (lane == 0) {
+            for (int k = max(0, issued - NST); k < issued; ++k)
+                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int m = p.unit_seqs[(size_t)u * NCW + warp];
+    bool active = member_ok(m);
+    if (active && m != leader) {
+        // the member's table must name the leader's blocks over the partition
+        const int B = p.block_size;
+        const int32_t* t = p.block_tables + (size_t)m * p.max_blocks;
+        bool same = true;
+        for (int j = T0 / B + lane; j < (T0 + P + B - 1) / B; j += 32) same &= t[j] == lead_table[j];
+        active = __all_sync(0xffffffffu, same);
+    }
+    if (!active && m >= 0 && lane == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
+    MmaWarp<QT, CT, D, GS> cw;
+    if (active)
+        cw.load_query(reinterpret_cast<const QT*>(p.query) + ((size_t)m * p.num_q_heads + hq0) * D,
+                      p.q_mul, lane);
+    bool ok = true;
+    for (int k = 0; k < n_st; ++k) {
+        const int slot = k % NST;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
+        if (!ok) break;
+        if (active) {
+            uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
+            cw.consume(Kst, Kst + S::kTileBytes, kTmaStageTokens, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (!active || !ok) return;
+
+    // ---------------------------------------------- this member's partials
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 4);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 8);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 16);
+    }
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int h = 2 * t4 + j;
+        if (h >= GS) continue;
+        const size_t row = ((size_t)m * p.num_q_heads + hq0 + h) * p.max_parts + part;
+        const float inv = (kFp8 ? p.v_mul * 256.f : p.v_mul) / cw.l_run[j];
+#pragma unroll
+        for (int md = 0; md < KS; ++md)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
+                p.tmp_out[row * D + d] = cw.acc[md][2 * hr + j] * inv;
+            }
+        if (g == 0) {
+            p.max_logits[row] = cw.m_run[j] * kLn2;
+            p.exp_sums[row] = cw.l_run[j];
+        }
+    }
+}
+
+template <typename QT, typename CT, int D, int GS>
+cudaError_t launch_shared_variant(const TmaDecodeParams& tp, int max_unit_parts, cudaStream_t stream) {
+    using Smem = MmaSmem<CT, D>;
+    auto kern = paged_decode_shared_kernel<QT, CT, D, GS>;
+    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
+    if (e != cudaSuccess) return e;
+    const DecodeParams& p = tp.p;
+    dim3 grid(max_unit_parts, p.num_kv_heads * p.sub_groups, p.num_units);
+    kern<<<grid, mma_threads<CT, D>(), Smem::kAlloc, stream>>>(tp);
+    return cudaGetLastError();
 }
 
 template <typename QT, typename CT, int D, int GS, bool kSplit>
@@ -659,10 +808,14 @@ cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// shared_parts > 0: the shared-prefix kernel over that many leading
+// partitions of each unit (split launches only)
 template <typename QT, typename CT, int D>
-cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStream_t stream) {
+cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, int shared_parts,
+                         cudaStream_t stream) {
 #define PA_MMA_CASE(G)                                                        \
     case G:                                                                   \
+        if (shared_parts > 0) return launch_shared_variant<QT, CT, D, G>(tp, shared_parts, stream); \
         return split ? launch_mma_variant<QT, CT, D, G, true>(tp, stream)     \
                      : launch_mma_variant<QT, CT, D, G, false>(tp, stream);
     switch (gs) {
@@ -679,7 +832,7 @@ cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStre
 // 128, 256 or 512 bytes; heads_per_unit 1, 2, 4 or 8.
 template <typename QT, typename CT>
 cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, int shared_parts = 0) {
     constexpr int eb = TypeInfo<CT>::bytes;
     TmaDecodeParams tp;
     tp.p = p;
@@ -691,14 +844,14 @@ cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
     if (e != cudaSuccess) return e;
     if constexpr (eb == 2) {
         switch (head_size) {
-        case 64: return launch_mma_d<QT, CT, 64>(tp, gs, split, stream);
-        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
-        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
+        case 64: return launch_mma_d<QT, CT, 64>(tp, gs, split, shared_parts, stream);
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, shared_parts, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, shared_parts, stream);
         }
     } else {
         switch (head_size) {
-        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
-        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, shared_parts, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, shared_parts, stream);
         }
     }
     return cudaErrorInvalidValue;
