@@ -312,15 +312,16 @@ pa_status pa_shared_prefix_plan(const int32_t* block_tables, const int32_t* cont
 
 /*
  * pa_write_decode_shared_prefix -- one decode step with shared-prefix units:
- * the shared-prefix kernel (each unit's shared partitions, every stage read
- * once for all members), the partition kernel over every other partition
- * (with the step's KV write folded in when key/value/slot_mapping are given,
- * as in pa_write_decode_partitions), then pa_merge into out. Three launches
- * on `stream`. Arguments are pa_write_decode_partitioned's plus the plan of
+ * one launch of the partition kernel whose first CTAs compute each unit's
+ * shared partitions (every stage read once for all members) and whose other
+ * CTAs compute every other partition (with the step's KV write folded in when
+ * key/value/slot_mapping are given, as in pa_write_decode_partitions), then
+ * pa_merge into out. Two launches on `stream`. Arguments are pa_write_decode_partitioned's plus the plan of
  * pa_shared_prefix_plan, copied to the device by the caller:
  *   seq_shared_parts [num_seqs], unit_seqs [num_units, PA_SHARED_UNIT_MEMBERS],
- *   unit_parts [num_units] int32 (device); max_unit_parts <= the partitions of
- *   max_context_len. num_units == 0: the plain partitioned step.
+ *   unit_parts [num_units] int32 (device); max_unit_parts (the plan's largest
+ *   unit_parts) <= the partitions of max_context_len; num_seqs + num_units <=
+ *   65535. num_units == 0: the plain partitioned step.
  * key, value and slot_mapping are all null (decode only) or all given.
  * The workspace is pa_decode_partitioned_workspace_bytes(num_seqs,
  * num_q_heads, head_size, max_context_len, partition_size), as for the

@@ -194,18 +194,6 @@ cudaError_t run_simt_decode_kernel(DecodeParams p, int head_size, pa_dtype q_dty
     }
 }
 
-// The shared-prefix kernel for a tensor-core decode shape.
-cudaError_t run_shared_kernel(const DecodeParams& p, int head_size, pa_dtype q_dtype,
-                              pa_dtype cache_dtype, int max_unit_parts, cudaStream_t stream) {
-    const int gs = p.group / p.sub_groups;
-    if (cache_dtype == PA_FP8_E4M3) {
-        if (q_dtype == PA_F16) return launch_decode_shared_f16_e4m3(p, head_size, gs, max_unit_parts, stream);
-        return launch_decode_shared_bf16_e4m3(p, head_size, gs, max_unit_parts, stream);
-    }
-    if (q_dtype == PA_F16) return launch_decode_shared_f16(p, head_size, gs, max_unit_parts, stream);
-    return launch_decode_shared_bf16(p, head_size, gs, max_unit_parts, stream);
-}
-
 pa_status check_partition_size(int partition_size) {
     if (partition_size <= 0 || partition_size % 32 != 0) return PA_ERR_INVALID_ARG;
     return PA_OK;
@@ -490,7 +478,7 @@ pa_status pa_write_decode_shared_prefix(
         // a sequence's newest token never lies in a shared block
         if (!tma_eligible(head_size, cache_dtype, block_size, num_blocks, num_kv_heads) ||
             !mma_eligible(q_dtype, cache_dtype, p.group) || partition_size % block_size != 0 ||
-            num_units > 65535)
+            num_seqs + num_units > 65535)
             return PA_ERR_UNSUPPORTED;
     }
     if ((st = bind_workspace(p, num_seqs, num_q_heads, head_size, max_context_len, partition_size,
@@ -502,8 +490,6 @@ pa_status pa_write_decode_shared_prefix(
         p.unit_seqs = unit_seqs;
         p.unit_parts = unit_parts;
         p.num_units = num_units;
-        cudaError_t e = run_shared_kernel(p, head_size, q_dtype, cache_dtype, max_unit_parts, s);
-        if (e != cudaSuccess) return PA_ERR_CUDA;
     }
     if (write) bind_fused_write(p, key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale);
     cudaError_t e = run_decode_kernel(p, head_size, q_dtype, cache_dtype, true, s);

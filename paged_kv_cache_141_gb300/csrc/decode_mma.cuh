@@ -351,6 +351,199 @@ struct MmaWarp {
     }
 };
 
+// Shared-prefix partitions ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 5:
+// requests that share a prompt prefix share its KV blocks). A unit is up to
+// NCW sequences whose block tables agree over their first `parts` partitions;
+// CTA (partition, KV head group, unit) reads each stage of that partition
+// once, from the first valid member's table, and every consumer warp consumes
+// every stage for its own member's query, so the shared blocks are read once
+// per unit instead of once per sequence. These CTAs run in the partition
+// kernel's own launch, ahead of the per-sequence ones (grid z = units, then
+// sequences), so that the two kinds of latency-bound work overlap. Each warp writes its member's partials
+// (maximum, sum, normalised output) for the partition itself; the partition
+// kernel skips those partitions (skip_parts) and the merge is unchanged.
+// A member is computed here only if its context holds the shared partitions
+// and at least one more token, its skip_parts entry equals the unit's parts
+// and its table agrees with the first member's over the partition; otherwise
+// PA_DEV_BAD_PREFIX is set (the partition kernel computes a sequence whose
+// length fails the first rule itself).
+template <typename QT, typename CT, int D, int GS>
+__device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8_t* smem, int u) {
+    using S = TmaShape<CT, D>;
+    using Smem = MmaSmem<CT, D>;
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    constexpr int NST = Smem::kNst;
+    constexpr int NCW = Smem::kConsumers;
+    constexpr int KS = D / 16;
+    static_assert(GS <= 8, "one MMA covers eight heads");
+    const DecodeParams& p = tp.p;
+
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
+    uint64_t* empty = full + NST;
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / p.sub_groups;
+    const int sub = blockIdx.y - kvh * p.sub_groups;
+    const int hq0 = kvh * p.group + sub * GS;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int parts = p.unit_parts[u];
+    if (part >= parts) return;
+    const int P = p.partition_size;
+    int cap = p.max_context_len;
+    {
+        const long long tab = (long long)p.max_blocks * p.block_size;
+        if (tab < cap) cap = (int)tab;
+    }
+    // a member: in range, its context holds the shared partitions and one more
+    // token, and its own skip count names this unit's partitions
+    auto member_ok = [&](int m) {
+        if (m < 0 || m >= p.num_seqs) return false;
+        const int L = p.context_lens[m];
+        return L > (long long)parts * P && L <= cap && p.skip_parts[m] == parts;
+    };
+    // the first valid member's table names the blocks the unit reads
+    int leader = -1;
+    for (int w = 0; w < NCW && leader < 0; ++w) {
+        const int cand = p.unit_seqs[(size_t)u * NCW + w];
+        if (member_ok(cand)) leader = cand;
+    }
+    if (leader < 0) {
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
+        return;
+    }
+    const int T0 = part * P;
+    const int n_st = P / kTmaStageTokens;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NCW);           // every consumer reads every stage
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int32_t* lead_table = p.block_tables + (size_t)leader * p.max_blocks;
+    if (warp == NCW) {
+        // ------------------------------------------------------------ producer
+        const int B = p.block_size;
+        const int rows = tp.box_rows;
+        if (lane == 0) {
+            tma_prefetch_map(&tp.k_map);
+            tma_prefetch_map(&tp.v_map);
+        }
+        int issued = 0;
+        for (int k = 0; k < n_st; ++k) {
+            const int slot = k % NST;
+            if (k >= NST) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+            }
+            const int t_lo = T0 + k * kTmaStageTokens;
+            const int t_hi = t_lo + kTmaStageTokens;
+            const int j0 = t_lo / B;
+            const int nseg = (t_hi - 1) / B - j0 + 1;
+            uint32_t bytes = 0;
+            int y = 0, row0 = 0;
+            if (lane < nseg) {
+                const int j = j0 + lane;
+                const int pb = lead_table[j];
+                if (pb < 0 || (int64_t)pb >= p.num_blocks) {
+                    if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+                } else {
+                    const int off = (B >= kTmaStageTokens) ? (t_lo - j * B) : 0;
+                    y = (pb * p.num_kv_heads + kvh) * B + off;
+                    row0 = (B >= kTmaStageTokens) ? 0 : j * B - t_lo;
+                    bytes = (uint32_t)(rows * S::kRowBytes);
+                }
+            }
+            uint32_t total = bytes;
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * total);
+            __syncwarp();
+            if (bytes) {
+                uint8_t* st = ring + (size_t)slot * S::kStageBytes;
+#pragma unroll
+                for (int sp = 0; sp < S::kSpans; ++sp) {
+                    const int x = sp * (128 / S::kElem);
+                    uint8_t* kd = st + sp * S::kSpanTileBytes + row0 * 128;
+                    tma_load_2d(kd, &tp.k_map, x, y, &full[slot]);
+                    tma_load_2d(kd + S::kTileBytes, &tp.v_map, x, y, &full[slot]);
+                }
+            }
+            issued = k + 1;
+        }
+        if (lane == 0) {
+            for (int k = max(0, issued - NST); k < issued; ++k)
+                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int m = p.unit_seqs[(size_t)u * NCW + warp];
+    bool active = member_ok(m);
+    if (active && m != leader) {
+        // the member's table must name the leader's blocks over the partition
+        const int B = p.block_size;
+        const int32_t* t = p.block_tables + (size_t)m * p.max_blocks;
+        bool same = true;
+        for (int j = T0 / B + lane; j < (T0 + P + B - 1) / B; j += 32) same &= t[j] == lead_table[j];
+        active = __all_sync(0xffffffffu, same);
+    }
+    if (!active && m >= 0 && lane == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
+    MmaWarp<QT, CT, D, GS> cw;
+    if (active)
+        cw.load_query(reinterpret_cast<const QT*>(p.query) + ((size_t)m * p.num_q_heads + hq0) * D,
+                      p.q_mul, lane);
+    bool ok = true;
+    for (int k = 0; k < n_st; ++k) {
+        const int slot = k % NST;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
+        if (!ok) break;
+        if (active) {
+            uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
+            cw.consume(Kst, Kst + S::kTileBytes, kTmaStageTokens, lane);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    if (!active || !ok) return;
+
+    // ---------------------------------------------- this member's partials
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 4);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 8);
+        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 16);
+    }
+    const int g = lane >> 2;
+    const int t4 = lane & 3;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int h = 2 * t4 + j;
+        if (h >= GS) continue;
+        const size_t row = ((size_t)m * p.num_q_heads + hq0 + h) * p.max_parts + part;
+        const float inv = (kFp8 ? p.v_mul * 256.f : p.v_mul) / cw.l_run[j];
+#pragma unroll
+        for (int md = 0; md < KS; ++md)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {
+                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
+                p.tmp_out[row * D + d] = cw.acc[md][2 * hr + j] * inv;
+            }
+        if (g == 0) {
+            p.max_logits[row] = cw.m_run[j] * kLn2;
+            p.exp_sums[row] = cw.l_run[j];
+        }
+    }
+}
+
 template <typename QT, typename CT, int D, int GS, bool kSplit>
 __global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
@@ -372,7 +565,15 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
     uint64_t* empty = full + NST;
 
-    const int s = blockIdx.z;
+    int zs = blockIdx.z;
+    if constexpr (kSplit) {
+        if (zs < p.num_units) {                 // a shared-prefix unit (grid z: units first)
+            shared_unit_cta<QT, CT, D, GS>(tp, smem, zs);
+            return;
+        }
+        zs -= p.num_units;
+    }
+    const int s = zs;
     const int kvh = blockIdx.y / p.sub_groups;
     const int sub = blockIdx.y - kvh * p.sub_groups;
     const int hq0 = kvh * p.group + sub * GS;
@@ -589,213 +790,6 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
 }
 
-// Shared-prefix partitions ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 5:
-// requests that share a prompt prefix share its KV blocks). A unit is up to
-// NCW sequences whose block tables agree over their first `parts` partitions;
-// CTA (partition, KV head group, unit) reads each stage of that partition
-// once, from the first valid member's table, and every consumer warp consumes every
-// stage for its own member's query, so the shared blocks are read once per
-// unit instead of once per sequence. Each warp writes its member's partials
-// (maximum, sum, normalised output) for the partition itself; the partition
-// kernel skips those partitions (skip_parts) and the merge is unchanged.
-// A member is computed here only if its context holds the shared partitions
-// and at least one more token, its skip_parts entry equals the unit's parts
-// and its table agrees with the first member's over the partition; otherwise
-// PA_DEV_BAD_PREFIX is set (the partition kernel computes a sequence whose
-// length fails the first rule itself).
-template <typename QT, typename CT, int D, int GS>
-__global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
-paged_decode_shared_kernel(const __grid_constant__ TmaDecodeParams tp) {
-    using S = TmaShape<CT, D>;
-    using Smem = MmaSmem<CT, D>;
-    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
-    constexpr int NST = Smem::kNst;
-    constexpr int NCW = Smem::kConsumers;
-    constexpr int KS = D / 16;
-    static_assert(GS <= 8, "one MMA covers eight heads");
-    const DecodeParams& p = tp.p;
-
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    uint8_t* ring = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
-    uint64_t* empty = full + NST;
-
-    const int u = blockIdx.z;
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y / p.sub_groups;
-    const int sub = blockIdx.y - kvh * p.sub_groups;
-    const int hq0 = kvh * p.group + sub * GS;
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int parts = p.unit_parts[u];
-    if (part >= parts) return;
-    const int P = p.partition_size;
-    int cap = p.max_context_len;
-    {
-        const long long tab = (long long)p.max_blocks * p.block_size;
-        if (tab < cap) cap = (int)tab;
-    }
-    // a member: in range, its context holds the shared partitions and one more
-    // token, and its own skip count names this unit's partitions
-    auto member_ok = [&](int m) {
-        if (m < 0 || m >= p.num_seqs) return false;
-        const int L = p.context_lens[m];
-        return L > (long long)parts * P && L <= cap && p.skip_parts[m] == parts;
-    };
-    // the first valid member's table names the blocks the unit reads
-    int leader = -1;
-    for (int w = 0; w < NCW && leader < 0; ++w) {
-        const int cand = p.unit_seqs[(size_t)u * NCW + w];
-        if (member_ok(cand)) leader = cand;
-    }
-    if (leader < 0) {
-        if (threadIdx.x == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
-        return;
-    }
-    const int T0 = part * P;
-    const int n_st = P / kTmaStageTokens;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], NCW);           // every consumer reads every stage
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    const int32_t* lead_table = p.block_tables + (size_t)leader * p.max_blocks;
-    if (warp == NCW) {
-        // ------------------------------------------------------------ producer
-        const int B = p.block_size;
-        const int rows = tp.box_rows;
-        if (lane == 0) {
-            tma_prefetch_map(&tp.k_map);
-            tma_prefetch_map(&tp.v_map);
-        }
-        int issued = 0;
-        for (int k = 0; k < n_st; ++k) {
-            const int slot = k % NST;
-            if (k >= NST) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-            }
-            const int t_lo = T0 + k * kTmaStageTokens;
-            const int t_hi = t_lo + kTmaStageTokens;
-            const int j0 = t_lo / B;
-            const int nseg = (t_hi - 1) / B - j0 + 1;
-            uint32_t bytes = 0;
-            int y = 0, row0 = 0;
-            if (lane < nseg) {
-                const int j = j0 + lane;
-                const int pb = lead_table[j];
-                if (pb < 0 || (int64_t)pb >= p.num_blocks) {
-                    if (p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
-                } else {
-                    const int off = (B >= kTmaStageTokens) ? (t_lo - j * B) : 0;
-                    y = (pb * p.num_kv_heads + kvh) * B + off;
-                    row0 = (B >= kTmaStageTokens) ? 0 : j * B - t_lo;
-                    bytes = (uint32_t)(rows * S::kRowBytes);
-                }
-            }
-            uint32_t total = bytes;
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) total += __shfl_xor_sync(0xffffffffu, total, m);
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * total);
-            __syncwarp();
-            if (bytes) {
-                uint8_t* st = ring + (size_t)slot * S::kStageBytes;
-#pragma unroll
-                for (int sp = 0; sp < S::kSpans; ++sp) {
-                    const int x = sp * (128 / S::kElem);
-                    uint8_t* kd = st + sp * S::kSpanTileBytes + row0 * 128;
-                    tma_load_2d(kd, &tp.k_map, x, y, &full[slot]);
-                    tma_load_2d(kd + S::kTileBytes, &tp.v_map, x, y, &full[slot]);
-                }
-            }
-            issued = k + 1;
-        }
-        if (lane == 0) {
-            for (int k = max(0, issued - NST); k < issued; ++k)
-                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int m = p.unit_seqs[(size_t)u * NCW + warp];
-    bool active = member_ok(m);
-    if (active && m != leader) {
-        // the member's table must name the leader's blocks over the partition
-        const int B = p.block_size;
-        const int32_t* t = p.block_tables + (size_t)m * p.max_blocks;
-        bool same = true;
-        for (int j = T0 / B + lane; j < (T0 + P + B - 1) / B; j += 32) same &= t[j] == lead_table[j];
-        active = __all_sync(0xffffffffu, same);
-    }
-    if (!active && m >= 0 && lane == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
-    MmaWarp<QT, CT, D, GS> cw;
-    if (active)
-        cw.load_query(reinterpret_cast<const QT*>(p.query) + ((size_t)m * p.num_q_heads + hq0) * D,
-                      p.q_mul, lane);
-    bool ok = true;
-    for (int k = 0; k < n_st; ++k) {
-        const int slot = k % NST;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
-        if (!ok) break;
-        if (active) {
-            uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
-            cw.consume(Kst, Kst + S::kTileBytes, kTmaStageTokens, lane);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    if (!active || !ok) return;
-
-    // ---------------------------------------------- this member's partials
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 4);
-        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 8);
-        cw.l_run[j] += __shfl_xor_sync(0xffffffffu, cw.l_run[j], 16);
-    }
-    const int g = lane >> 2;
-    const int t4 = lane & 3;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int h = 2 * t4 + j;
-        if (h >= GS) continue;
-        const size_t row = ((size_t)m * p.num_q_heads + hq0 + h) * p.max_parts + part;
-        const float inv = (kFp8 ? p.v_mul * 256.f : p.v_mul) / cw.l_run[j];
-#pragma unroll
-        for (int md = 0; md < KS; ++md)
-#pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
-                p.tmp_out[row * D + d] = cw.acc[md][2 * hr + j] * inv;
-            }
-        if (g == 0) {
-            p.max_logits[row] = cw.m_run[j] * kLn2;
-            p.exp_sums[row] = cw.l_run[j];
-        }
-    }
-}
-
-template <typename QT, typename CT, int D, int GS>
-cudaError_t launch_shared_variant(const TmaDecodeParams& tp, int max_unit_parts, cudaStream_t stream) {
-    using Smem = MmaSmem<CT, D>;
-    auto kern = paged_decode_shared_kernel<QT, CT, D, GS>;
-    cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
-    if (e != cudaSuccess) return e;
-    const DecodeParams& p = tp.p;
-    dim3 grid(max_unit_parts, p.num_kv_heads * p.sub_groups, p.num_units);
-    kern<<<grid, mma_threads<CT, D>(), Smem::kAlloc, stream>>>(tp);
-    return cudaGetLastError();
-}
-
 template <typename QT, typename CT, int D, int GS, bool kSplit>
 cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     using Smem = MmaSmem<CT, D>;
@@ -803,19 +797,16 @@ cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
     if (e != cudaSuccess) return e;
     const DecodeParams& p = tp.p;
-    dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups, p.num_seqs);
+    dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups,
+              p.num_seqs + (kSplit ? p.num_units : 0));
     kern<<<grid, mma_threads<CT, D>(), Smem::kAlloc, stream>>>(tp);
     return cudaGetLastError();
 }
 
-// shared_parts > 0: the shared-prefix kernel over that many leading
-// partitions of each unit (split launches only)
 template <typename QT, typename CT, int D>
-cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, int shared_parts,
-                         cudaStream_t stream) {
+cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStream_t stream) {
 #define PA_MMA_CASE(G)                                                        \
     case G:                                                                   \
-        if (shared_parts > 0) return launch_shared_variant<QT, CT, D, G>(tp, shared_parts, stream); \
         return split ? launch_mma_variant<QT, CT, D, G, true>(tp, stream)     \
                      : launch_mma_variant<QT, CT, D, G, false>(tp, stream);
     switch (gs) {
@@ -832,7 +823,7 @@ cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, int shar
 // 128, 256 or 512 bytes; heads_per_unit 1, 2, 4 or 8.
 template <typename QT, typename CT>
 cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
-                       cudaStream_t stream, int shared_parts = 0) {
+                       cudaStream_t stream) {
     constexpr int eb = TypeInfo<CT>::bytes;
     TmaDecodeParams tp;
     tp.p = p;
@@ -844,14 +835,14 @@ cudaError_t launch_mma(const DecodeParams& p, int head_size, int gs, bool split,
     if (e != cudaSuccess) return e;
     if constexpr (eb == 2) {
         switch (head_size) {
-        case 64: return launch_mma_d<QT, CT, 64>(tp, gs, split, shared_parts, stream);
-        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, shared_parts, stream);
-        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, shared_parts, stream);
+        case 64: return launch_mma_d<QT, CT, 64>(tp, gs, split, stream);
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
         }
     } else {
         switch (head_size) {
-        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, shared_parts, stream);
-        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, shared_parts, stream);
+        case 128: return launch_mma_d<QT, CT, 128>(tp, gs, split, stream);
+        case 256: return launch_mma_d<QT, CT, 256>(tp, gs, split, stream);
         }
     }
     return cudaErrorInvalidValue;

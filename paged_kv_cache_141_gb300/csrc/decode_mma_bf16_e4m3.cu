@@ -9,9 +9,4 @@ cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, in
     return launch_mma<__nv_bfloat16, e4m3_t>(p, head_size, heads_per_unit, split, stream);
 }
 
-cudaError_t launch_decode_shared_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
-                                     int max_unit_parts, cudaStream_t stream) {
-    return launch_mma<__nv_bfloat16, e4m3_t>(p, head_size, heads_per_unit, true, stream, max_unit_parts);
-}
-
 }  // namespace pagedkv

@@ -52,8 +52,9 @@ struct DecodeParams {
     const int32_t* seq_order;     // null or [S]: launch position -> sequence (longest first)
     // shared-prefix partitions (tensor-core decode, split only; all null / 0
     // otherwise): skip_parts[s] leading partitions of sequence s are computed
-    // by the shared-prefix kernel for the unit holding s, whose members are
-    // unit_seqs[u * 4 .. u * 4 + 3] (-1 = none) sharing unit_parts[u] partitions
+    // by the CTAs of the unit holding s (grid z < num_units, in the same
+    // launch), whose members are unit_seqs[u * 4 .. u * 4 + 3] (-1 = none)
+    // sharing unit_parts[u] partitions
     const int32_t* skip_parts;    // [S]
     const int32_t* unit_seqs;     // [num_units, 4]
     const int32_t* unit_parts;    // [num_units]
@@ -97,19 +98,6 @@ cudaError_t launch_decode_mma_f16_e4m3(const DecodeParams& p, int head_size, int
                                        bool split, cudaStream_t stream);
 cudaError_t launch_decode_mma_bf16_e4m3(const DecodeParams& p, int head_size, int heads_per_unit,
                                         bool split, cudaStream_t stream);
-// The shared-prefix kernel (same shapes as the tensor-core decode): grid over
-// max_unit_parts partitions x KV head groups x units.
-cudaError_t launch_decode_shared_f16(const DecodeParams& p, int head_size, int heads_per_unit,
-                                     int max_unit_parts, cudaStream_t stream);
-cudaError_t launch_decode_shared_bf16(const DecodeParams& p, int head_size, int heads_per_unit,
-                                      int max_unit_parts, cudaStream_t stream);
-cudaError_t launch_decode_shared_f16_e4m3(const DecodeParams& p, int head_size,
-                                          int heads_per_unit, int max_unit_parts,
-                                          cudaStream_t stream);
-cudaError_t launch_decode_shared_bf16_e4m3(const DecodeParams& p, int head_size,
-                                           int heads_per_unit, int max_unit_parts,
-                                           cudaStream_t stream);
-
 // Multi-query paged attention for a few query rows per (sequence, KV head)
 // (max_queries * group <= 32 at head_size <= 128, <= 16 at 256) on
 // warp-level MMA: 16-bit query with a cache of
