@@ -181,6 +181,9 @@ class Step:
                      partition kernel) then pa_merge; or pa_write_decode.
     form "separate": pa_reshape_and_cache, pa_decode_partitions, pa_merge; or
                      pa_reshape_and_cache, pa_decode.
+    form "shared":   pa_write_decode_shared_prefix with the units of
+                     pa_shared_prefix_plan (partition kernel with shared-prefix
+                     units and the KV write, then the merge: one call).
     """
 
     def __init__(self, case, device, partition_size=512, form="fused"):
@@ -215,6 +218,14 @@ class Step:
                                partition_size) == 1
         if form == "fused" and c.kv_dtype != c.q_dtype:
             self.form = form = "separate"     # the fused write takes tokens of the query type
+        self.plan = None
+        if form == "shared":
+            # units of sequences sharing their leading partitions, planned on
+            # the host from the block tables (outside any timed region)
+            self.plan = pk.shared_prefix_plan(c.block_tables, c.context_lens, c.block_size,
+                                              partition_size)
+            self.plan_dev = self.plan.to(device)
+            self.split = True
         self.ws = pk.alloc_workspace(c.num_seqs, c.num_q_heads, c.head_size, c.max_context_len,
                                      partition_size, device)
         self.views = pk.workspace_views(self.ws, c.num_seqs, c.num_q_heads, c.head_size,
@@ -252,6 +263,19 @@ class Step:
             tmp, ml, es = self.views
             pk.merge(self.out, tmp, ml, es, self.cl, self.P, self.status, stream)
 
+        def shared_step(stream=None):
+            sp, us, up = self.plan_dev
+            kw = (dict(key=self.nk, value=self.nv, slot_mapping=self.ns)
+                  if c.kv_dtype == c.q_dtype else {})
+            if not kw:
+                write(stream)
+            pk.write_decode_shared_prefix(self.out, self.q, self.kc, self.vc, *common(), self.ws,
+                                          sp, us, up, self.plan.max_unit_parts, self.P,
+                                          k_scale=c.k_scale, v_scale=c.v_scale,
+                                          dev_status=self.status, stream=stream, **kw)
+
+        if self.form == "shared":
+            return [("write+decode+merge", shared_step)]
         if self.form == "fused":
             if self.split:
                 return [("write+decode", write_partitions), ("merge", merge)]
@@ -271,8 +295,9 @@ class Step:
     @property
     def main_call(self) -> str:
         """The call that runs the decode kernel (partition kernel or single
-        pass; in the fused form it also stores the step's new tokens)."""
-        return "write+decode" if self.form == "fused" else "decode"
+        pass; in the fused form it also stores the step's new tokens; in the
+        shared form the whole step, partition kernel and merge)."""
+        return {"fused": "write+decode", "shared": "write+decode+merge"}.get(self.form, "decode")
 
     def bytes_per_step(self) -> dict:
         """Algorithmic bytes, by the method's definition (no workspace).
@@ -290,7 +315,7 @@ class Step:
             partials = parts * c.num_q_heads * (c.head_size + 2) * 4
         else:
             partials = 0
-        main = decode + (write if self.form == "fused" else 0)
+        main = decode + (write if self.form in ("fused", "shared") else 0)
         return {"write": write, "decode": decode, "total": write + decode, "main_kernel": main,
                 "partials": partials}
 
@@ -332,35 +357,22 @@ def run_ours(args):
 
     K = args.steps
     ncall = st.launches_per_step
-    # per-call events on every 8th step (events between launches cost a few
-    # microseconds of stream time; the sample still spans the whole region)
-    every = 8
-    sampled = list(range(0, K, every))
-    ev = {i: [torch.cuda.Event(enable_timing=True) for _ in range(ncall + 1)] for i in sampled}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for i in range(K):
-        e = ev.get(i)
-        if e is None:
-            for _, f in st.calls:
-                f()
-            continue
-        e[0].record(stream)
-        for j, (_, f) in enumerate(st.calls):
+    for _ in range(K):
+        for _, f in st.calls:
             f()
-            e[j + 1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    call_ms = {name: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in sampled) / len(sampled)
-               for j, (name, _) in enumerate(st.calls)}
     total_ms = max_over_ranks(total_ms, world, device)
+    call_ms = run_call_leg(st, stream, max(8, min(64, K)))
 
     by = st.bytes_per_step()
     ms_per_step = total_ms / K
@@ -407,6 +419,7 @@ def run_ours(args):
         "seqs_per_s_per_layer": round(seqs_per_s, 1),
         "bytes_per_step": by,
         "call_ms": {k: round(v, 5) for k, v in call_ms.items()},
+        "call_ms_timing": "CUDA events around each call, a separate leg after the timed steps",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": recorded_traffic(args.config, P, form_used, bool(by["partials"])),
@@ -427,6 +440,23 @@ def run_ours(args):
         "clocks": clocks,
     }
     print(json.dumps(line))
+
+
+def run_call_leg(st: Step, stream, steps: int) -> dict:
+    """Each call of the step on its own: CUDA events around every call of
+    `steps` steps after the timed region (events between launches add a few
+    microseconds of stream time, so they stay out of the timed loop)."""
+    import torch
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(st.calls) + 1)]
+          for _ in range(steps)]
+    for e in ev:
+        e[0].record(stream)
+        for j, (_, f) in enumerate(st.calls):
+            f()
+            e[j + 1].record(stream)
+    torch.cuda.synchronize()
+    return {name: sum(e[j].elapsed_time(e[j + 1]) for e in ev) / steps
+            for j, (name, _) in enumerate(st.calls)}
 
 
 def unique_record(case, by, world, ms_per_step, peak):
@@ -479,39 +509,29 @@ def run_kernel_leg(st: Step, device, min_seconds: float = 1.0, per_graph: int = 
         raise SystemExit(f"device status {int(st.status.item())} after the kernel leg")
     total = a.elapsed_time(b)
     n = reps * per_graph
-    name = decode_kernel_label(st.case) + (
-        (" (partition kernel" if st.split else " (single pass")
-        + (", KV write fused)" if st.form == "fused" else ")"))
+    if st.form == "shared":
+        name = (decode_kernel_label(st.case) + " (partition kernel with shared-prefix units, KV "
+                "write fused) + paged_merge_kernel")
+    else:
+        name = decode_kernel_label(st.case) + (
+            (" (partition kernel" if st.split else " (single pass")
+            + (", KV write fused)" if st.form == "fused" else ")"))
     return {"name": name, "ms": total / n, "launches": n,
             "timing": f"CUDA graph of {per_graph} launches of the kernel alone, replayed {reps} "
                       f"times ({n} launches, {total / 1e3:.2f} s), events on the replaying stream"}
 
 
-def run_shared_step(st: Step, device, seconds: float = 0.5) -> dict | None:
-    """Where sequences share their leading partitions' blocks: the step as
-    pa_write_decode_shared_prefix runs it (the shared-prefix kernel reading
-    each unit's shared partitions once, the partition kernel with the KV
-    write over the rest, the merge), planned on the host from the block
-    tables (pa_shared_prefix_plan, outside the timed region); launched
-    eagerly and replayed as a CUDA graph."""
+def run_shared_step(case, device, partition_size, seconds: float = 0.5) -> dict | None:
+    """Where sequences share their leading partitions' blocks: the step in
+    the shared form (Step form "shared": pa_write_decode_shared_prefix, the
+    partition kernel whose first CTAs read each unit's shared partitions once
+    for its members, then the merge), launched eagerly and replayed as a CUDA
+    graph. None when the plan finds no units."""
     import torch
-    c, pk = st.case, st.pk
-    plan = pk.shared_prefix_plan(c.block_tables, c.context_lens, c.block_size, st.P)
-    if plan.num_units == 0:
+    st = Step(case, device, partition_size, "shared")
+    if st.plan.num_units == 0:
         return None
-    sp, us, up = plan.to(device)
-    kw = (dict(key=st.nk, value=st.nv, slot_mapping=st.ns) if c.kv_dtype == c.q_dtype else {})
-
-    def step(stream=None):
-        if not kw:
-            pk.reshape_and_cache(st.nk, st.nv, st.kc, st.vc, st.ns, c.k_scale, c.v_scale,
-                                 st.status, stream)
-        pk.write_decode_shared_prefix(st.out, st.q, st.kc, st.vc, st.bt, st.cl, c.max_context_len,
-                                      c.scale, st.ws, sp, us, up, plan.max_unit_parts, st.P,
-                                      k_scale=c.k_scale, v_scale=c.v_scale, dev_status=st.status,
-                                      stream=stream, **kw)
-
-    step()
+    st.step()
     torch.cuda.synchronize()
     if int(st.status.item()) != 0:
         raise SystemExit(f"device status {int(st.status.item())} after the shared-prefix step")
@@ -519,48 +539,36 @@ def run_shared_step(st: Step, device, seconds: float = 0.5) -> dict | None:
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     for _ in range(3):
-        step()
+        st.step()
     a.record(cur)
-    step()
+    st.step()
     b.record(cur)
     torch.cuda.synchronize()
     n = max(20, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
     a.record(cur)
     for _ in range(n):
-        step()
+        st.step()
     b.record(cur)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
-    g = torch.cuda.CUDAGraph()
-    s = torch.cuda.Stream(device)
-    s.wait_stream(cur)
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(g, stream=s):
-            step(s)
-    cur.wait_stream(s)
-    for _ in range(3):
-        g.replay()
-    a.record(cur)
-    for _ in range(n):
-        g.replay()
-    b.record(cur)
-    torch.cuda.synchronize()
-    gms = a.elapsed_time(b) / n
+    graph = run_graph(st, n, device)
     by = st.bytes_per_step()
     peak, _ = hbm_peak()
     gbs = by["total"] / (ms * 1e-3) / 1e9
-    unique = unique_record(c, by, 1, ms, peak)
-    members = int((plan.unit_seqs >= 0).sum())
-    return {"ms_per_step": round(ms, 5), "steps": n, "graph_ms_per_step": round(gms, 5),
-            "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
-            "seqs_per_s_per_layer": round(c.num_seqs / (ms * 1e-3), 1),
-            **({"unique_bytes": unique} if unique else {}),
-            "units": plan.num_units, "unit_members": members,
-            "shared_partitions": int(plan.max_unit_parts),
-            "launches": "shared-prefix kernel, partition kernel" + (
-                " (KV write fused)" if kw else " after reshape_and_cache") + ", merge",
-            "note": "logical bytes as in the plain step; the shared partitions' K/V is read "
-                    "once per unit of up to 4 sequences"}
+    unique = unique_record(case, by, 1, ms, peak)
+    plan = st.plan
+    rec = {"ms_per_step": round(ms, 5), "steps": n, "graph_ms_per_step": graph["ms_per_step"],
+           "gbs": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
+           "seqs_per_s_per_layer": round(case.num_seqs / (ms * 1e-3), 1),
+           **({"unique_bytes": unique} if unique else {}),
+           "units": plan.num_units, "unit_members": int((plan.unit_seqs >= 0).sum()),
+           "shared_partitions": int(plan.max_unit_parts),
+           "launches": "partition kernel with shared-prefix units (KV write fused), merge",
+           "note": "logical bytes as in the plain step; the shared partitions' K/V is read "
+                   "once per unit of up to 4 sequences"}
+    del st
+    torch.cuda.empty_cache()
+    return rec
 
 
 def measure_config(index: int, device, partition_size, form="fused", step_seconds=0.3,
@@ -603,7 +611,7 @@ def measure_config(index: int, device, partition_size, form="fused", step_second
     graph = run_graph(st, max(20, n), device)
     ws = run_write_step(st, device)
     unique = unique_record(case, by, 1, ms, peak)
-    shared = run_shared_step(st, device) if st.split else None
+    shared = run_shared_step(case, device, P) if st.split else None
     rec = {"workload": f"{case.name} (configuration {index})", "num_seqs": case.num_seqs,
            "num_q_heads": case.num_q_heads, "num_kv_heads": case.num_kv_heads,
            "head_size": case.head_size, "kv_dtype": case.cache_dtype,
@@ -1209,8 +1217,9 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--partition-size", default="auto",
                     help="tokens per partition, or 'auto' (the library's choice)")
-    ap.add_argument("--form", choices=["fused", "separate"], default="fused",
-                    help="how the step is launched (see Step)")
+    ap.add_argument("--form", choices=["fused", "separate", "shared"], default="fused",
+                    help="how the step is launched (see Step); shared: shared-prefix units "
+                         "(pa_write_decode_shared_prefix)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kernel-seconds", type=float, default=1.2,
                     help="length of the kernel-only leg behind the roofline")
