@@ -117,7 +117,8 @@ struct MmaSmem {
     static constexpr int kCombineBytes = kConsumers * 8 * (D + 2) * 4;
     static constexpr int kBody = kRingBytes > kCombineBytes ? kRingBytes : kCombineBytes;
     static constexpr int kBarOffset = (kBody + 127) / 128 * 128;
-    static constexpr int kBytes = kBarOffset + 2 * kNst * 8;
+    // full[kNst], empty[kNst], and two rendezvous barriers of shared-prefix units
+    static constexpr int kBytes = kBarOffset + (2 * kNst + 2) * 8;
     static constexpr int kAlloc = kBytes + 1024;                // room to align the ring to 1 KB
 };
 
@@ -156,7 +157,10 @@ constexpr int mma_threads() {
 // One consumer warp's share of the decode: the query's B fragments, the
 // O^T accumulators and the online-softmax state of the heads this lane holds
 // (2 t4 and 2 t4 + 1), and the work on one 32-token stage of K and V.
-template <typename QT, typename CT, int D, int GS>
+// kOneTermP: the weights as one 16-bit term (E4M3 values, widened in
+// registers or staged as binary16 tiles); otherwise high part + residual.
+template <typename QT, typename CT, int D, int GS,
+          bool kOneTermP = std::is_same<CT, e4m3_t>::value>
 struct MmaWarp {
     using S = TmaShape<CT, D>;
     using MT = typename MathType<CT>::T;
@@ -194,6 +198,33 @@ struct MmaWarp {
         }
         // the widened E4M3 codes are their values times 2^-8
         qk_mul = kFp8 ? q_mul * 256.f : q_mul;
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+    }
+
+    // 16-bit math on tiles of another source (widened E4M3): the query rows
+    // of type Q2 rounded to this warp's 16-bit type, natural d order.
+    template <typename Q2>
+    __device__ __forceinline__ void load_query_as(const Q2* __restrict__ qp, float q_mul, int lane) {
+        static_assert(!kFp8, "16-bit math only");
+        const int g = lane >> 2;
+        const int t4 = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            if (g >= GS) {
+                qb[ks][0] = 0u;
+                qb[ks][1] = 0u;
+            } else {
+                const Q2* q2 = qp + g * D + 16 * ks + 2 * t4;
+                qb[ks][0] = Ops::pack(to_float(q2[0]), to_float(q2[1]));
+                qb[ks][1] = Ops::pack(to_float(q2[8]), to_float(q2[9]));
+            }
+        }
+        qk_mul = q_mul;
 #pragma unroll
         for (int i = 0; i < KS; ++i)
 #pragma unroll
@@ -296,7 +327,7 @@ struct MmaWarp {
                 const uint32_t hi = Ops::pack(w0, w1);
                 const float2 hf = Ops::unpack(hi);
                 // the sums use exactly the weights the products use
-                if constexpr (kFp8) {
+                if constexpr (kOneTermP) {
                     // binary16 weights as one term: relative error at most
                     // 2^-11, far inside the E4M3 codes' own 2^-4
                     l_run[0] += hf.x;
@@ -344,12 +375,49 @@ struct MmaWarp {
                     ldmatrix_x4_trans(a, Vst + (c >> 3) * S::kSpanTileBytes + row * 128 +
                                              (((c & 7) ^ (row & 7)) << 4));
                     Ops::mma(acc[md], a, bh[kt][0], bh[kt][1]);
-                    Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
+                    if constexpr (!kOneTermP) Ops::mma(acc[md], a, bl[kt][0], bl[kt][1]);
                 }
             }
         }
     }
 };
+
+// The threads [tid, nthreads) share the widening of one E4M3 stage (K and V
+// tiles of 32 rows, 128-byte swizzled) into binary16 tiles of the same
+// swizzled layout (rows of 2 D bytes), values times 2^-8 as
+// e4m3x2_to_f16x2_scaled gives them: 16 codes in, two 16-byte chunks out.
+template <int D>
+__device__ __forceinline__ void widen_stage_f16(const uint8_t* codes_k, const uint8_t* codes_v,
+                                                uint8_t* f16_k, uint8_t* f16_v, int tid,
+                                                int nthreads) {
+    using S8 = TmaShape<e4m3_t, D>;
+    using SF = TmaShape<__half, D>;
+    constexpr int C = S8::kChunks;               // 16-code chunks per row
+    constexpr int kItems = 2 * kTmaStageTokens * C;
+    for (int i = tid; i < kItems; i += nthreads) {
+        const int t = i / (kTmaStageTokens * C);
+        const int r = (i / C) % kTmaStageTokens;
+        const int c = i % C;
+        const uint8_t* src = (t ? codes_v : codes_k) + (c >> 3) * S8::kSpanTileBytes + r * 128 +
+                             (((c & 7) ^ (r & 7)) << 4);
+        const uint4 w = *reinterpret_cast<const uint4*>(src);
+        const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+        uint32_t out[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            out[2 * q] = e4m3x2_to_f16x2_scaled(__byte_perm(in[q], 0u, 0x4140));
+            out[2 * q + 1] = e4m3x2_to_f16x2_scaled(__byte_perm(in[q], 0u, 0x4342));
+        }
+        uint8_t* dst = t ? f16_v : f16_k;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int cc = 2 * c + h;
+            *reinterpret_cast<uint4*>(dst + (cc >> 3) * SF::kSpanTileBytes + r * 128 +
+                                      (((cc & 7) ^ (r & 7)) << 4)) =
+                make_uint4(out[4 * h], out[4 * h + 1], out[4 * h + 2], out[4 * h + 3]);
+        }
+    }
+}
 
 // Shared-prefix partitions ("TGI PagedAttention deep-dive" (lpnh.cn) sec. 5:
 // requests that share a prompt prefix share its KV blocks). A unit is up to
@@ -378,9 +446,19 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
     static_assert(GS <= 8, "one MMA covers eight heads");
     const DecodeParams& p = tp.p;
 
+    // E4M3: the codes use two ring slots; the other two hold one binary16 K/V
+    // tile pair that the four warps widen each stage into once, so that the
+    // unit's members do not each widen it (16-bit math from there)
+    using SF = TmaShape<__half, D>;
+    constexpr int NSTU = kFp8 ? 2 : NST;
+    static_assert(!kFp8 || 2 * SF::kTileBytes <= (NST - NSTU) * S::kStageBytes, "staging fits");
     uint8_t* ring = smem;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Smem::kBarOffset);
     uint64_t* empty = full + NST;
+    uint64_t* conv = empty + NST;                // the stage's binary16 tiles are complete
+    uint64_t* done = conv + 1;                   // every warp has finished reading them
+    uint8_t* stg_k = ring + NSTU * S::kStageBytes;
+    uint8_t* stg_v = stg_k + SF::kTileBytes;
 
     const int part = blockIdx.x;
     const int kvh = blockIdx.y / p.sub_groups;
@@ -417,10 +495,12 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
     const int n_st = P / kTmaStageTokens;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < NST; ++i) {
+        for (int i = 0; i < NSTU; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], NCW);           // every consumer reads every stage
         }
+        mbar_init(conv, NCW);
+        mbar_init(done, NCW);
         fence_barrier_init();
     }
     __syncthreads();
@@ -436,10 +516,10 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
         }
         int issued = 0;
         for (int k = 0; k < n_st; ++k) {
-            const int slot = k % NST;
-            if (k >= NST) {
+            const int slot = k % NSTU;
+            if (k >= NSTU) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NST) - 1) & 1, p.status);
+                if (lane == 0) ok = mbar_wait_bounded(&empty[slot], ((k / NSTU) - 1) & 1, p.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
             }
@@ -479,8 +559,8 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
             issued = k + 1;
         }
         if (lane == 0) {
-            for (int k = max(0, issued - NST); k < issued; ++k)
-                mbar_wait_bounded(&full[k % NST], (k / NST) & 1, p.status);
+            for (int k = max(0, issued - NSTU); k < issued; ++k)
+                mbar_wait_bounded(&full[k % NSTU], (k / NSTU) & 1, p.status);
         }
         return;
     }
@@ -497,21 +577,41 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
         active = __all_sync(0xffffffffu, same);
     }
     if (!active && m >= 0 && lane == 0 && p.status) atomicOr(p.status, PA_DEV_BAD_PREFIX);
-    MmaWarp<QT, CT, D, GS> cw;
-    if (active)
-        cw.load_query(reinterpret_cast<const QT*>(p.query) + ((size_t)m * p.num_q_heads + hq0) * D,
-                      p.q_mul, lane);
+    using Warp = std::conditional_t<kFp8, MmaWarp<__half, __half, D, GS, true>,
+                                    MmaWarp<QT, CT, D, GS>>;
+    Warp cw;
+    if (active) {
+        const QT* qp = reinterpret_cast<const QT*>(p.query) + ((size_t)m * p.num_q_heads + hq0) * D;
+        if constexpr (kFp8) cw.load_query_as(qp, p.q_mul * 256.f, lane);   // widened values are 2^-8 x
+        else cw.load_query(qp, p.q_mul, lane);
+    }
     bool ok = true;
     for (int k = 0; k < n_st; ++k) {
-        const int slot = k % NST;
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NST) & 1, p.status));
+        const int slot = k % NSTU;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (k / NSTU) & 1, p.status));
         if (!ok) break;
-        if (active) {
-            uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
-            cw.consume(Kst, Kst + S::kTileBytes, kTmaStageTokens, lane);
+        uint8_t* Kst = ring + (size_t)slot * S::kStageBytes;
+        if constexpr (kFp8) {
+            if (k > 0) {                         // the previous stage's tiles have been read
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(done, (k - 1) & 1, p.status));
+                if (!ok) break;
+            }
+            widen_stage_f16<D>(Kst, Kst + S::kTileBytes, stg_k, stg_v, threadIdx.x, NCW * 32);
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(conv);
+                mbar_arrive(&empty[slot]);       // the codes' slot may be refilled
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait_bounded(conv, k & 1, p.status));
+            if (!ok) break;
+            if (active) cw.consume(stg_k, stg_v, kTmaStageTokens, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(done);
+        } else {
+            if (active) cw.consume(Kst, Kst + S::kTileBytes, kTmaStageTokens, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
     }
     if (!active || !ok) return;
 
@@ -534,7 +634,7 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
         for (int md = 0; md < KS; ++md)
 #pragma unroll
             for (int hr = 0; hr < 2; ++hr) {
-                const int d = kFp8 ? 16 * md + 2 * g + hr : 16 * md + g + 8 * hr;
+                const int d = 16 * md + g + 8 * hr;          // 16-bit math: natural order
                 p.tmp_out[row * D + d] = cw.acc[md][2 * hr + j] * inv;
             }
         if (g == 0) {
