@@ -59,6 +59,8 @@ SHAPES = [
     ("bf16", "bf16", 16, 2, 64, 32, 128, 6, (1, 12), ("uniform", 1, 300)),
     ("e4m3", "bf16", 8, 1, 128, 16, 64, 8, (2, 16), ("uniform", 1, 200)),
     ("e4m3", "f16", 64, 8, 128, 16, 512, 16, (4, 64), ("uniform", 16, 512)),
+    ("bf16", "bf16", 16, 2, 256, 16, 64, 9, (3, 8), ("uniform", 1, 100)),
+    ("e4m3", "bf16", 16, 2, 256, 16, 64, 9, (3, 8), ("uniform", 1, 100)),
 ]
 
 
@@ -154,3 +156,41 @@ def test_host_argument_errors():
     with pytest.raises(pk.PagedKVError) as e:           # partition size not a multiple of 32
         pk.write_decode_shared_prefix(*args, plan.max_unit_parts, 72)
     assert e.value.status == pk.PA_ERR_INVALID_ARG
+
+
+def test_shared_prefix_step_replays_in_a_cuda_graph():
+    """The step (partition kernel with units, merge) captured once and
+    replayed gives the eager launch's bits."""
+    c = W.make_case(num_seqs=16, num_q_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+                    q_dtype="bf16", cache_dtype="e4m3", lengths=("uniform", 16, 300),
+                    shared_prefix=(4, 16), seed=91)
+    d = DeviceCase(c)
+    d.write_step()
+    P = 128
+    plan = pk.shared_prefix_plan(c.block_tables, c.context_lens, c.block_size, P)
+    sp, us, up = plan.to(d.query.device)
+    ws = pk.alloc_workspace(c.num_seqs, c.num_q_heads, c.head_size, c.max_context_len, P)
+
+    def step(stream=None):
+        pk.write_decode_shared_prefix(d.out, d.query, d.k_cache, d.v_cache, d.block_tables,
+                                      d.context_lens, c.max_context_len, c.scale, ws, sp, us, up,
+                                      plan.max_unit_parts, P, k_scale=c.k_scale, v_scale=c.v_scale,
+                                      dev_status=d.status, stream=stream)
+
+    step()
+    torch.cuda.synchronize()
+    eager = d.out.clone()
+    assert d.status_bits() == 0
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        d.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(d.out, eager)
+    assert d.status_bits() == 0
