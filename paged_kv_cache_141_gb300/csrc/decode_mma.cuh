@@ -644,7 +644,10 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
     }
 }
 
-template <typename QT, typename CT, int D, int GS, bool kSplit>
+// kShared: a split launch with shared-prefix units (grid z: units, then
+// sequences); a separate instantiation, so that the plain kernels carry
+// neither the unit path nor the skip test.
+template <typename QT, typename CT, int D, int GS, bool kSplit, bool kShared = false>
 __global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
@@ -666,7 +669,8 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     uint64_t* empty = full + NST;
 
     int zs = blockIdx.z;
-    if constexpr (kSplit) {
+    if constexpr (kShared) {
+        static_assert(kSplit, "units are partitions");
         if (zs < p.num_units) {                 // a shared-prefix unit (grid z: units first)
             shared_unit_cta<QT, CT, D, GS>(tp, smem, zs);
             return;
@@ -695,9 +699,9 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
     int T0, Tend;
     if constexpr (kSplit) {
-        if (p.skip_parts) {
-            // partitions the shared-prefix kernel computes for this sequence
-            // (its rule: the context extends past them and is within the bound)
+        if (kShared && p.skip_parts) {
+            // partitions this launch's unit CTAs compute for this sequence
+            // (their rule: the context extends past them and is within the bound)
             const int sk = p.skip_parts[s];
             const int Lr = p.context_lens[s];
             if (sk > 0 && (int)blockIdx.x < sk && Lr > (long long)sk * p.partition_size &&
@@ -890,15 +894,15 @@ paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     }
 }
 
-template <typename QT, typename CT, int D, int GS, bool kSplit>
+template <typename QT, typename CT, int D, int GS, bool kSplit, bool kShared = false>
 cudaError_t launch_mma_variant(const TmaDecodeParams& tp, cudaStream_t stream) {
     using Smem = MmaSmem<CT, D>;
-    auto kern = paged_decode_mma_kernel<QT, CT, D, GS, kSplit>;
+    auto kern = paged_decode_mma_kernel<QT, CT, D, GS, kSplit, kShared>;
     cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Smem::kAlloc);
     if (e != cudaSuccess) return e;
     const DecodeParams& p = tp.p;
     dim3 grid(kSplit ? p.max_parts : 1, p.num_kv_heads * p.sub_groups,
-              p.num_seqs + (kSplit ? p.num_units : 0));
+              p.num_seqs + (kShared ? p.num_units : 0));
     kern<<<grid, mma_threads<CT, D>(), Smem::kAlloc, stream>>>(tp);
     return cudaGetLastError();
 }
@@ -907,6 +911,8 @@ template <typename QT, typename CT, int D>
 cudaError_t launch_mma_d(const TmaDecodeParams& tp, int gs, bool split, cudaStream_t stream) {
 #define PA_MMA_CASE(G)                                                        \
     case G:                                                                   \
+        if (split && tp.p.num_units > 0)                                      \
+            return launch_mma_variant<QT, CT, D, G, true, true>(tp, stream);  \
         return split ? launch_mma_variant<QT, CT, D, G, true>(tp, stream)     \
                      : launch_mma_variant<QT, CT, D, G, false>(tp, stream);
     switch (gs) {
