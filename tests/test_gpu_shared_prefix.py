@@ -194,3 +194,34 @@ def test_shared_prefix_step_replays_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(d.out, eager)
     assert d.status_bits() == 0
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_shared_prefix_random_cases(seed):
+    """Seeded random shapes: batch size, prefix groups and lengths, suffix
+    lengths, cache type (bf16, f16, E4M3), GQA group, head size, block and
+    partition sizes; the step with its KV write against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    cache = ["bf16", "f16", "e4m3"][seed % 3]
+    q = "f16" if cache == "f16" else ("bf16" if seed % 2 else "f16")
+    if cache == "bf16":
+        q = "bf16"
+    G = int(rng.choice([1, 2, 4, 8]))
+    Hkv = int(rng.choice([1, 2, 4]))
+    D = int(rng.choice([64, 128])) if cache != "e4m3" else 128
+    B = int(rng.choice([16, 32]))
+    P = int(rng.choice([32, 64, 128])) * (B // 16)
+    groups = int(rng.integers(1, 4))
+    per = int(rng.integers(1, 7))
+    prefix_blocks = int(rng.integers(1, 5)) * (P // B)
+    c = W.make_case(num_seqs=groups * per, num_q_heads=G * Hkv, num_kv_heads=Hkv, head_size=D,
+                    block_size=B, q_dtype=q, cache_dtype=cache,
+                    lengths=("uniform", 1, int(rng.integers(2, 3 * P))),
+                    shared_prefix=(groups, prefix_blocks), seed=2000 + seed)
+    d = DeviceCase(c)
+    plan = pk.shared_prefix_plan(c.block_tables, c.context_lens, B, P)
+    got = to_f64(run_shared(d, c, P, plan))
+    assert d.status_bits() == 0
+    kc, vc = oracle_pool(c)
+    assert_decode_close(got, oracle_decode(c, kc, vc), c,
+                        f"shared-prefix random case {seed} ({plan.num_units} units)")
