@@ -569,8 +569,8 @@ int pa_decode_choose(int num_seqs, int num_q_heads, int num_kv_heads, int max_co
 
 /*
  * pa_decode_partition_size -- a partition size for this device: 512 (the
- * pages' _PARTITION_SIZE) doubled (up to 2048) while the longest context
- * still spans three or more partitions and the launch keeps about four waves of
+ * pages' _PARTITION_SIZE) doubled (up to 4096) while the longest context
+ * still spans three or more partitions and the launch keeps about two waves of
  * work units. Longer partitions mean fewer CTA start-ups and fewer partials to
  * merge. Never fails.
  */

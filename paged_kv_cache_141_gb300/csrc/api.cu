@@ -592,11 +592,13 @@ int pa_decode_partition_size(int num_seqs, int num_kv_heads, int max_context_len
     }
     // Longer partitions mean fewer CTA start-ups and fewer partials, while the
     // longest context still spans three or more of them (balance) and the launch
-    // keeps about four waves of work units (3 CTAs per SM), estimating a
-    // context's length at half the maximum.
-    const long long want = 4ll * 3 * sms;
+    // keeps about two waves of work units (3 CTAs per SM), estimating a
+    // context's length at half the maximum. Measured on 8 contexts of 32k-131k
+    // tokens (32/8 heads): steps of 0.399, 0.392 and 0.477 ms at 2048, 4096 and
+    // 8192 tokens (the last 1.4 waves); shorter pools stop at the three-partition rule.
+    const long long want = 2ll * 3 * sms;
     int P = 512;
-    while (P < 2048) {
+    while (P < 4096) {
         const int next = 2 * P;
         const long long units = (long long)num_seqs * num_kv_heads *
                                 ((max_context_len / 2 + next - 1) / next);

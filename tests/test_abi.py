@@ -52,6 +52,7 @@ def test_host_only_calls(lib):
     parts = 256 * 32 * 8
     assert n == parts * 128 * 4 + 2 * parts * 4
     assert pk.partition_size(256, 8, 4096) in (512, 1024, 2048)
+    assert pk.partition_size(8, 8, 131072) in (2048, 4096)   # long contexts: at most 4096
     assert pk.partition_size(4, 4, 64) == 512
     assert pk.workspace_bytes(3, 5, 64, 1, 512) % 256 == 0
     assert pk.max_partitions(0) == 1 and pk.max_partitions(513) == 2
