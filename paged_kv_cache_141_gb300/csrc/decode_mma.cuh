@@ -238,7 +238,6 @@ struct MmaWarp {
     __device__ __forceinline__ void consume(const uint8_t* Kst, const uint8_t* Vst, int nvalid,
                                             int lane) {
         const int g = lane >> 2;
-        const int t4 = lane & 3;
         const int mi = lane >> 3, r8 = lane & 7;   // ldmatrix row addresses: lane -> (matrix, row)
         // ---- S = K Q^T for both 16-token row tiles
         float sc[2][4];
@@ -427,9 +426,10 @@ __device__ __forceinline__ void widen_stage_f16(const uint8_t* codes_k, const ui
 // every stage for its own member's query, so the shared blocks are read once
 // per unit instead of once per sequence. These CTAs run in the partition
 // kernel's own launch, ahead of the per-sequence ones (grid z = units, then
-// sequences), so that the two kinds of latency-bound work overlap. Each warp writes its member's partials
-// (maximum, sum, normalised output) for the partition itself; the partition
-// kernel skips those partitions (skip_parts) and the merge is unchanged.
+// sequences), so that the two kinds of latency-bound work overlap. Each warp
+// writes its member's partials (maximum, sum, normalised output) for the
+// partition itself; the partition kernel skips those partitions (skip_parts)
+// and the merge is unchanged.
 // A member is computed here only if its context holds the shared partitions
 // and at least one more token, its skip_parts entry equals the unit's parts
 // and its table agrees with the first member's over the partition; otherwise
@@ -444,6 +444,7 @@ __device__ __forceinline__ void shared_unit_cta(const TmaDecodeParams& tp, uint8
     constexpr int NCW = Smem::kConsumers;
     constexpr int KS = D / 16;
     static_assert(GS <= 8, "one MMA covers eight heads");
+    static_assert(NCW == PA_SHARED_UNIT_MEMBERS, "one consumer warp per unit member");
     const DecodeParams& p = tp.p;
 
     // E4M3: the codes use two ring slots; the other two hold one binary16 K/V
@@ -652,8 +653,6 @@ __global__ void __launch_bounds__(mma_threads<CT, D>(), mma_min_blocks<CT, D>())
 paged_decode_mma_kernel(const __grid_constant__ TmaDecodeParams tp) {
     using S = TmaShape<CT, D>;
     using Smem = MmaSmem<CT, D>;
-    using MT = typename MathType<CT>::T;
-    using Ops = MmaOps<MT>;
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
     constexpr int NST = Smem::kNst;
     constexpr int NCW = Smem::kConsumers;
