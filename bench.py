@@ -12,11 +12,15 @@ log-uniform in [512, 4096], random block placement, seed 0x5EED0003).
 Metric: KV GB/s = (logical K/V bytes read + Q + out + KV-write bytes) / step
 time, on the device with inputs resident in HBM (1.8 GB of KV, far larger than
 the 129 MB L2, so no flush is needed between steps). Also reported: decode
-sequences per second per layer, the dominant kernel's roofline, an end-to-end
-figure through host buffers, the oracle timed on the host cores, and the SM
-clocks sampled during the timed region.
+sequences per second per layer, the dominant kernel's roofline (the kernel
+timed alone, graph-replayed for over a second, on method bytes), an
+end-to-end figure through host buffers, the oracle timed on the host cores,
+the SM clocks sampled during the timed region, and records of the other
+four workloads (each step, its kernel alone, its own KV write; the
+shared-prefix pool also with shared-prefix units).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config 1-5] [--form fused|separate|shared] [--configs LIST|none]
 """
 from __future__ import annotations
 
@@ -528,9 +532,11 @@ def run_shared_step(case, device, partition_size, seconds: float = 0.5) -> dict 
     for its members, then the merge), launched eagerly and replayed as a CUDA
     graph. None when the plan finds no units."""
     import torch
+    from paged_kv_cache_141_gb300 import binding as pk
+    if pk.shared_prefix_plan(case.block_tables, case.context_lens, case.block_size,
+                             partition_size).num_units == 0:
+        return None                               # no sharing: nothing to build
     st = Step(case, device, partition_size, "shared")
-    if st.plan.num_units == 0:
-        return None
     st.step()
     torch.cuda.synchronize()
     if int(st.status.item()) != 0:
