@@ -747,7 +747,8 @@ def prefill_kernel_name(case, max_queries: int) -> str:
     return {
         "mma": f"paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows{widened})",
         "mma_two_tiles": f"paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp{widened})",
-        "tc_two_tiles": "paged_prefill_tc2_kernel (two query tiles per CTA)",
+        "tc_two_tiles": "paged_prefill_tc2_kernel (two query tiles per CTA"
+                        + (", E4M3 tiles widened to binary16)" if e4m3 else ")"),
         "tc": "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else ""),
         "cuda_cores": "paged_decode_simt_kernel (one query token per work unit)",
     }[kind]

@@ -262,9 +262,8 @@ bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, 
 
 // The kernel pa_paged_prefill runs: the warp-level MMA kernels for up to 32
 // rows per (sequence, KV head) (16 at head size 256), else the tcgen05 ones
-// (two query tiles per CTA for 16-bit caches at head size <= 128 with at
-// least two tiles per sequence), else one query token per work unit on the
-// CUDA cores. `aligned`: out, query and the caches are 16-byte aligned (the
+// (two query tiles per CTA at head size <= 128 with at least two tiles per
+// sequence), else one query token per work unit on the CUDA cores. `aligned`: out, query and the caches are 16-byte aligned (the
 // tcgen05 rows).
 pa_prefill_kernel prefill_kernel(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size,
                                  int block_size, int group, int64_t num_blocks, int num_kv_heads,
@@ -277,7 +276,7 @@ pa_prefill_kernel prefill_kernel(pa_dtype q_dtype, pa_dtype cache_dtype, int hea
                                        num_blocks, num_kv_heads)) {
         const int per_tile = 128 / group;
         const int tiles = (max_queries + per_tile - 1) / per_tile;
-        const bool two = cache_dtype != PA_FP8_E4M3 && head_size <= 128 && tiles >= 2;
+        const bool two = head_size <= 128 && tiles >= 2;
         return two ? PA_PREFILL_TC_TWO_TILES : PA_PREFILL_TC;
     }
     return PA_PREFILL_CUDA_CORES;

@@ -433,15 +433,14 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
 // slot (`empty`), and each arrives on `full` (count 2) and on `sfree`
 // (count 2) once it has read its rows, after which warp 0 refills that
 // staging slot with the tile two ahead.
-template <typename Sh>
+template <int N, int D, int NS>
 __device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const CUtensorMap* map,
                                                uint8_t* staging, uint8_t* ring, uint64_t* staged,
                                                uint64_t* sfree, uint64_t* full, uint64_t* empty,
                                                int s, int hk, int ntiles, int kend, int half,
                                                int lane, volatile int* abort_flag) {
-    constexpr int N = Sh::N;
-    constexpr int NS = Sh::NS;
-    constexpr int D = Sh::kKvBytes / (2 * N);                // head size
+    constexpr int kKvBytes = N * D * 2;                      // one binary16 ring slot
+    constexpr int kStage8Bytes = N * D;                      // one E4M3 staging slot
     constexpr int kRow8 = D;                                 // bytes of an E4M3 row
     constexpr int kHalfChunks = N * kRow8 / 16 / 2;          // 16-code chunks per warp and tile
     constexpr int64_t kNone = -1;
@@ -466,7 +465,7 @@ __device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const 
         if (valid) {
             const int key = j * N + r0;
             const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
-            tma_load_2d(staging + (j & 1) * Sh::kStage8Bytes + r0 * kRow8, map, 0, y, &staged[j & 1]);
+            tma_load_2d(staging + (j & 1) * kStage8Bytes + r0 * kRow8, map, 0, y, &staged[j & 1]);
         }
     };
     int issued = 0;
@@ -491,8 +490,8 @@ __device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const 
             live = false;
             break;
         }
-        const uint8_t* src = staging + (j & 1) * Sh::kStage8Bytes;
-        uint8_t* dst = ring + (j % NS) * Sh::kKvBytes;
+        const uint8_t* src = staging + (j & 1) * kStage8Bytes;
+        uint8_t* dst = ring + (j % NS) * kKvBytes;
 #pragma unroll 4
         for (int k = 0; k < kHalfChunks / 32; ++k) {
             const int q = half * kHalfChunks + lane + 32 * k;
@@ -531,6 +530,105 @@ __device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const 
     if (issuer && lane == 0)
         for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
             mbar_wait_bounded(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
+}
+
+// E4M3 K (or V) tiles for the two-tile kernel, in halves: warp `half` owns
+// rows [half * N/2, (half + 1) * N/2) of every tile -- it reads their
+// block-table entries (a tile ahead), copies them into its half of one of
+// two staging slots (plain boxes of at most N/2 rows, so no box spans both
+// halves; a barrier per half and slot), widens them to binary16 into the
+// ring slot the MMAs read once that slot is free (`empty`), orders its
+// writes for the tensor cores (fence.proxy.async, which also orders its
+// reads of the staging rows before the next copy into them), arrives on
+// `full` (count 2), and refills its half of the staging slot with the tile
+// two ahead. The two warps never wait for each other. Measured on GB300: a
+// warp whose proxy fence follows tensor copies it issued itself passes it in
+// ~200 cycles, one that issued none waited ~2,800, so both warps issue.
+template <int N, int D, int NS>
+__device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
+                                                     const CUtensorMap* map, uint8_t* staging,
+                                                     uint8_t* ring, uint64_t* staged,
+                                                     uint64_t* full, uint64_t* empty, int s,
+                                                     int hk, int ntiles, int kend, int half,
+                                                     int lane, volatile int* abort_flag) {
+    constexpr int kKvBytes = N * D * 2;                      // one binary16 ring slot
+    constexpr int kStage8Bytes = N * D;                      // one E4M3 staging slot
+    constexpr int kRow8 = D;                                 // bytes of an E4M3 row
+    constexpr int kHalfChunks = N * kRow8 / 16 / 2;          // 16-code chunks per warp and tile
+    constexpr int64_t kNone = -1;
+    const PrefillParams& p = tp.p;
+    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
+    const int rows = tp.box_rows;                            // divides N/2
+    const int B = p.block_size;
+    const int r0 = half * (N / 2) + lane * rows;             // this lane's box
+    const bool owner = lane * rows < N / 2;
+    uint64_t* my_staged = staged + 2 * half;                 // [slot] of this half
+    auto fetch = [&](int j) -> int64_t {
+        const int key = j * N + r0;
+        if (owner && j < ntiles && key < kend) return (int64_t)table[key / B];
+        return kNone;
+    };
+    auto issue = [&](int j, int64_t blk) {
+        const bool has = blk != kNone;
+        const bool valid = has && blk >= 0 && blk < p.num_blocks;
+        if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
+        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
+        if (lane == 0) mbar_arrive_expect_tx(&my_staged[j & 1], boxes * (uint32_t)rows * kRow8);
+        __syncwarp();
+        if (valid) {
+            const int key = j * N + r0;
+            const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
+            tma_load_2d(staging + (j & 1) * kStage8Bytes + r0 * kRow8, map, 0, y,
+                        &my_staged[j & 1]);
+        }
+    };
+    issue(0, fetch(0));
+    if (ntiles > 1) issue(1, fetch(1));
+    int issued = ntiles > 1 ? 2 : 1;
+    int64_t next = fetch(2);
+    bool live = true;
+    for (int j = 0; j < ntiles && live; ++j) {
+        const int64_t after = fetch(j + 3);                  // in flight while tile j is widened
+        bool ok = true;
+        if (lane == 0) {
+            ok = tc_wait(&my_staged[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
+            if (ok && j >= NS)
+                ok = tc_wait(&empty[j % NS], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+            live = false;
+            break;
+        }
+        const uint8_t* src = staging + (j & 1) * kStage8Bytes;
+        uint8_t* dst = ring + (j % NS) * kKvBytes;
+#pragma unroll 4
+        for (int k = 0; k < kHalfChunks / 32; ++k) {
+            const int q = half * kHalfChunks + lane + 32 * k;
+            const int r = q / (kRow8 / 16), c = q - r * (kRow8 / 16);
+            const uint4 w = *reinterpret_cast<const uint4*>(src + r * kRow8 + c * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                h[2 * e] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4140));
+                h[2 * e + 1] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4342));
+            }
+            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[j % NS]);
+        if (j + 2 < ntiles) {
+            issue(j + 2, next);                              // this half of staging slot j % 2
+            issued = j + 3;
+        }
+        next = after;
+    }
+    // copies still in flight (only after an abort) land before the CTA ends
+    if (lane == 0)
+        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
+            mbar_wait_bounded(&my_staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
 }
 
 template <typename QT, typename CT, int D>
@@ -682,7 +780,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
         // ------------------------------------------------------------ K loads
         if constexpr (kFp8)
-            tc_load_widen2<Sh>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_sfree,
+            tc_load_widen2<N, D, NS>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_sfree,
                                k_full, k_empty, s, hk, ntiles, kend, warp == kTcKWarp ? 0 : 1,
                                lane, abort_flag);
         else
@@ -691,7 +789,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
         // ------------------------------------------------------------ V loads
         if constexpr (kFp8)
-            tc_load_widen2<Sh>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_sfree,
+            tc_load_widen2<N, D, NS>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_sfree,
                                v_full, v_empty, s, hk, ntiles, kend, warp == kTcVWarp ? 0 : 1,
                                lane, abort_flag);
         else
@@ -939,13 +1037,20 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 
 // Shapes of the two-tile kernel (head size 64 or 128): two 128-row query
 // tiles share every K/V tile, so each loaded tile feeds twice the rows.
-template <int D, bool kPLo>
+// kFp8: E4M3 caches, whose tiles land row-major in two staging slots per
+// operand and are widened to binary16 into the rings (for every 256 rows,
+// not 128 as in the one-tile kernel). At head size 128 that leaves one K
+// stage: a K tile is widened while tile 0's softmax runs, after both tiles'
+// S products of the previous key tile, which finish early in each key tile.
+template <int D, bool kPLo, bool kFp8 = false>
 struct TcShape2 {
     static constexpr int N = 128;                            // keys per tile
     static constexpr int kSpans = D / 64;
     static constexpr int kQBytes = kTcRows * D * 2;          // one query tile
     static constexpr int kKvBytes = N * D * 2;
-    static constexpr int kFixed = 2 * kQBytes + 1024 + 256;  // Q0, Q1, slack, barriers
+    static constexpr int kStage8Bytes = kFp8 ? N * D : 0;    // one E4M3 staging slot
+    // Q0, Q1, slack, barriers, staging (K[2], V[2])
+    static constexpr int kFixed = 2 * kQBytes + 1024 + 256 + 4 * kStage8Bytes;
     static constexpr int kStages0 = (kTcSmemLimit - kFixed) / (2 * kKvBytes);
     // K and V rings of their own depths: a K slot is free once both tiles'
     // S products have read it, a V slot only after both P.V products, so V
@@ -959,9 +1064,12 @@ struct TcShape2 {
     static constexpr int kQOff = 0;                          // Q0, then Q1
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + NSK * kKvBytes;
-    static constexpr int kBarOff = kVOff + NSV * kKvBytes;
-    // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
-    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6;
+    static constexpr int kK8Off = kVOff + NSV * kKvBytes;    // E4M3 staging: K[2], V[2]
+    static constexpr int kV8Off = kK8Off + 2 * kStage8Bytes;
+    static constexpr int kBarOff = kV8Off + 2 * kStage8Bytes;
+    // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready,
+    // then (E4M3) k_staged[2][2] v_staged[2][2] (per half and staging slot)
+    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6 + (kFp8 ? 8 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -970,7 +1078,7 @@ struct TcShape2 {
     static constexpr int kTmemCols = 512;
     static constexpr int kTileCols = N + D;
     static_assert(D == 64 || D == 128, "head size");
-    static_assert(NSK >= 2 && NSV >= 2, "stages");
+    static_assert(NSK >= (kFp8 ? 1 : 2) && NSV >= 2, "stages");
     static_assert(2 * kTileCols <= kTmemCols, "TMEM columns");
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
@@ -984,11 +1092,15 @@ struct TcShape2 {
 // earlier key tiles and can rescale it at once. A K slot is freed after the
 // second tile's S, a V slot after its P.V. Without a second tile (the last
 // group of a sequence with an odd tile count) warps 4-7 idle and the tile-1
-// MMAs are skipped.
-template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// MMAs are skipped. E4M3 caches: warps 8/11 and 10/13 load and widen the K
+// and V tiles by halves (tc_load_widen_halves), and the registers move from the producer
+// warpgroups to the softmax ones as in the one-tile kernel.
+template <typename QT, typename CT, int D>
+__global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp8 : kTcThreads, 1)
 paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
-    using Sh = TcShape2<D, kTcPLo<T>>;
+    using T = typename TcMath<QT, CT>::T;                    // MMA operand type
+    constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
+    using Sh = TcShape2<D, kTcPLo<T>, kFp8>;
     constexpr int N = Sh::N;
     constexpr int NSK = Sh::NSK;                             // K ring stages
     constexpr int NSV = Sh::NSV;                             // V ring stages
@@ -1005,6 +1117,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* p_full = s_full + 2;                           // [2]
     uint64_t* drain = p_full + 2;
     uint64_t* q_ready = drain + 1;
+    uint64_t* k_staged = q_ready + 1;                        // E4M3 only: [half][slot]
+    uint64_t* v_staged = k_staged + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -1020,7 +1134,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int s = tc_sequence(p, rest / p.num_kv_heads, tid == 0 && g == 0 && hk == 0);
     if (s < 0) return;
     int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
-    if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
+    if constexpr (!kFp8)
+        if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
     const int L = p.context_lens[s];
@@ -1044,11 +1159,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NSK; ++i) {
-            mbar_init(&k_full[i], 1);
+            mbar_init(&k_full[i], kFp8 ? 2 : 1);             // E4M3: two widening warps
             mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < NSV; ++i) {
-            mbar_init(&v_full[i], 1);
+            mbar_init(&v_full[i], kFp8 ? 2 : 1);
             mbar_init(&v_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -1057,6 +1172,12 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
+        if constexpr (kFp8) {
+            for (int i = 0; i < 4; ++i) {
+                mbar_init(&k_staged[i], 1);
+                mbar_init(&v_staged[i], 1);
+            }
+        }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_map(&tp.k_map);
@@ -1077,7 +1198,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         // tile qt's rows (token, head); padding rows are zero
         const int r = tid & (kTcRows - 1);
         (void)r;
-        const T* qbase = reinterpret_cast<const T*>(p.query);
+        const QT* qbase = reinterpret_cast<const QT*>(p.query);
         const int tt0 = tok0 + qt * Tq;
         const int nt = qt == 0 ? ntok0 : ntok1;
         constexpr int CPR = D / 8;
@@ -1099,18 +1220,44 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         for (int k = 0; k < PER; ++k) {
             const int idx = (tid & (kTcRows - 1)) + k * kTcRows;
             const int rr = idx / CPR, c = idx - rr * CPR;
-            *reinterpret_cast<uint4*>(qd + sw128_chunk<kTcRows>(rr, c)) = v[k];
+            uint4 w = v[k];
+            if constexpr (!std::is_same<QT, T>::value) {
+                // E4M3 caches: the query in the MMAs' binary16
+                const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+                uint32_t o4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack2<QT>(in[e]);
+                    o4[e] = pack2<T>(f.x, f.y);
+                }
+                w = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+            }
+            *reinterpret_cast<uint4*>(qd + sw128_chunk<kTcRows>(rr, c)) = w;
         }
         fence_async_smem();
         mbar_arrive(q_ready);
     }
 
-    if (warp == kTcKWarp) {
-        tc_load_ring<Sh, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles, kend,
-                              lane, first, abort_flag);
-    } else if (warp == kTcVWarp) {
-        tc_load_ring<Sh, NSV>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles, kend,
-                              lane, first, abort_flag);
+    if (warp >= kTcSoftmaxThreads / 32) {
+    // producer warpgroup(s); E4M3: they give up registers to the softmax
+    // warpgroups (every warp of a warpgroup runs the same instruction)
+    if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcProducerRegs));
+    if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
+        if constexpr (kFp8)
+            tc_load_widen_halves<N, D, NSK>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff,
+                                            k_staged, k_full, k_empty, s, hk, ntiles, kend,
+                                            warp == kTcKWarp ? 0 : 1, lane, abort_flag);
+        else
+            tc_load_ring<Sh, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
+                                  kend, lane, first, abort_flag);
+    } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
+        if constexpr (kFp8)
+            tc_load_widen_halves<N, D, NSV>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
+                                            v_staged, v_full, v_empty, s, hk, ntiles, kend,
+                                            warp == kTcVWarp ? 0 : 1, lane, abort_flag);
+        else
+            tc_load_ring<Sh, NSV>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
+                                  kend, lane, first, abort_flag);
     } else if (warp == kTcMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -1180,8 +1327,10 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             tc_commit(drain);
             mbar_wait_bounded(drain, 0, p.status);
         }
+    }
     } else if (qt == 0 || two) {
         // ------------------------------------------------------------ softmax (tile qt)
+        if constexpr (kFp8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcSoftmaxRegs));
         const int r = tid & (kTcRows - 1);
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const uint32_t sbuf = lane_base + qt * Sh::kTileCols;
@@ -1298,10 +1447,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
         if (ok) {
             tc_fence_after();
-            const float inv = 1.f / l;
-            T* orow = reinterpret_cast<T*>(p.out) +
-                      ((size_t)(q0 + tok0 + qt * Tq + (row_valid ? i : 0)) * p.num_q_heads +
-                       (size_t)hk * G + (r - i * G)) * D;
+            // E4M3: the values were widened without their scale; it comes in here
+            const float inv = kFp8 ? p.v_mul / l : 1.f / l;
+            QT* orow = reinterpret_cast<QT*>(p.out) +
+                       ((size_t)(q0 + tok0 + qt * Tq + (row_valid ? i : 0)) * p.num_q_heads +
+                        (size_t)hk * G + (r - i * G)) * D;
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
                 uint32_t o[32];
@@ -1311,10 +1461,10 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
                         uint4 v;
-                        v.x = pack2<T>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
-                        v.y = pack2<T>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
-                        v.z = pack2<T>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
-                        v.w = pack2<T>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                        v.x = pack2<QT>(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                        v.y = pack2<QT>(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                        v.z = pack2<QT>(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                        v.w = pack2<QT>(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
                         *reinterpret_cast<uint4*>(orow + c + e) = v;
                     }
                 }
@@ -1376,7 +1526,7 @@ cudaError_t launch_prefill_tc_d(const TcPrefillParams& tp, cudaStream_t stream) 
     if constexpr (D <= 128) {
         if (p.q_tiles >= 2) {
             using Sh = TcShape2<D, kTcPLo<T>>;
-            auto kern = paged_prefill_tc2_kernel<T, D>;
+            auto kern = paged_prefill_tc2_kernel<T, T, D>;
             cudaError_t e = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
             if (e != cudaSuccess) return e;
             const long long units = (long long)p.num_seqs * p.num_kv_heads * ((p.q_tiles + 1) / 2);
@@ -1415,9 +1565,10 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
     return cudaErrorInvalidValue;
 }
 
-// E4M3 caches: the one-tile kernel with widened K/V (head size 64 or 128).
-// The tensor maps view each cache as [num_blocks*Hkv*B rows][D bytes] with
-// plain (unswizzled) boxes of one block segment.
+// E4M3 caches: widened K/V (head size 64 or 128), two query tiles per CTA
+// when sequences have at least two, else the one-tile kernel. The tensor
+// maps view each cache as [num_blocks*Hkv*B rows][D bytes] with plain
+// (unswizzled) boxes of one block segment.
 template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
@@ -1427,14 +1578,28 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     tp.p.v_mul *= 256.f;
     constexpr int n = TcShape<128, true>::N;
     static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
-    tp.box_rows = p.block_size < n ? p.block_size : n;
+    // the two-tile kernel loads each tile by halves: boxes of at most n/2 rows
+    const int box_cap = p.q_tiles >= 2 ? n / 2 : n;
+    tp.box_rows = p.block_size < box_cap ? p.block_size : box_cap;
     const unsigned long long rows =
         (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
     cudaError_t e = encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
     if (e == cudaSuccess) e = encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
     if (e != cudaSuccess) return e;
+    static_assert(TcShape2<128, false, true>::N == n && TcShape2<64, false, true>::N == n,
+                  "the two-tile kernel's box height");
     auto go = [&](auto dtag) -> cudaError_t {
         constexpr int D = decltype(dtag)::value;
+        if (p.q_tiles >= 2) {
+            using Sh2 = TcShape2<D, false, true>;
+            auto kern2 = paged_prefill_tc2_kernel<QT, e4m3_t, D>;
+            cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern2), Sh2::kAlloc);
+            if (e2 != cudaSuccess) return e2;
+            const long long units = (long long)p.num_seqs * p.num_kv_heads * ((p.q_tiles + 1) / 2);
+            if (units > 0x7fffffffLL) return cudaErrorInvalidValue;
+            kern2<<<(unsigned)units, kTcThreadsFp8, Sh2::kAlloc, stream>>>(tp);
+            return cudaGetLastError();
+        }
         using Sh = TcShape<D, true>;
         auto kern = paged_prefill_tc_kernel<QT, e4m3_t, D>;
         cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);

@@ -192,8 +192,8 @@ def test_paged_prefill_rejects_a_misshaped_order():
 def test_paged_prefill_kernel_selection(lib):
     """The kernel choice of pa_paged_prefill, host only: warp-level MMA up to
     32 rows per (sequence, KV head) (16 at head size 256), one or two n-tiles
-    per warp by 16 rows; tcgen05 above (two query tiles per CTA for 16-bit
-    caches at head size <= 128 with two or more tiles); CUDA cores for the
+    per warp by 16 rows; tcgen05 above (two query tiles per CTA at head
+    size <= 128 with two or more tiles); CUDA cores for the
     other types and block sizes; -1 for what the call rejects."""
     from paged_kv_cache_141_gb300 import binding as pk
     B16, F16, F32, E4 = pk.PA_BF16, pk.PA_F16, pk.PA_F32, pk.PA_FP8_E4M3
@@ -211,7 +211,10 @@ def test_paged_prefill_kernel_selection(lib):
         ((2, 64, 8, 128, 16, B16, E4), "mma"),
         ((4, 64, 8, 128, 16, B16, E4), "mma_two_tiles"),
         ((5, 64, 8, 128, 16, B16, E4), "tc"),
-        ((512, 64, 8, 128, 16, B16, E4), "tc"),
+        ((16, 64, 8, 128, 16, B16, E4), "tc"),
+        ((17, 64, 8, 128, 16, B16, E4), "tc_two_tiles"),
+        ((512, 64, 8, 128, 16, B16, E4), "tc_two_tiles"),
+        ((512, 32, 8, 64, 16, F16, E4), "tc_two_tiles"),
         ((4, 16, 4, 256, 16, F16, F16), "mma"),
         ((5, 16, 4, 256, 16, F16, F16), "tc"),
         ((200, 16, 4, 256, 16, F16, F16), "tc"),

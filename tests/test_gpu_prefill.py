@@ -160,12 +160,18 @@ SIMT_SWEEP = [
     (2, 8, 4, 64, 96, "f16", "f16", ("fixed", [95, 250]), ("uniform", 1, 9)),
 ]
 
-# E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory)
+# E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory):
+# one query tile per sequence (the one-tile kernel) and two or more (the
+# two-tile kernel, odd tile counts leaving a single last tile), block sizes
+# 8..256, groups that do not divide the 128-row tile
 E4M3_TC_SWEEP = [
     (3, 8, 1, 128, 16, "bf16", ("uniform", 20, 300), ("uniform", 1, 40)),
     (2, 6, 2, 64, 32, "f16", ("uniform", 40, 200), ("all",)),
     (4, 32, 8, 128, 16, "bf16", ("uniform", 100, 700), ("uniform", 100, 300)),
     (3, 16, 2, 128, 256, "f16", ("uniform", 200, 600), ("uniform", 1, 12)),
+    (3, 16, 2, 128, 256, "f16", ("uniform", 200, 600), ("uniform", 20, 60)),
+    (4, 12, 4, 64, 8, "bf16", ("fixed", [1, 2, 129, 400]), ("all",)),
+    (3, 24, 8, 128, 64, "bf16", ("fixed", [300, 511, 1000]), ("fixed", [300, 170, 257])),
 ]
 
 
