@@ -101,7 +101,7 @@ struct TcShape {
     static constexpr int kV8Off = kK8Off + 2 * kStage8Bytes;
     static constexpr int kBarOff = kV8Off + 2 * kStage8Bytes;
     // barriers: k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
-    // q_ready, then (E4M3) k_staged[2] v_staged[2] k_sfree[2] v_sfree[2]
+    // q_ready, then (E4M3) k_staged[2][2] v_staged[2][2] (per half and staging slot)
     static constexpr int kNumBars = 4 * NS + 6 + (kFp8 ? 8 : 0);
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
     static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
@@ -423,116 +423,8 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
             mbar_wait_bounded(&full[j % NS], (uint32_t)((j / NS) & 1), p.status);
 }
 
-// E4M3 K (or V) tiles, widened by two warps: each tile lands row-major in one
-// of two staging slots (one plain TMA box per block segment), and warp `half`
-// widens rows [half * N/2, (half + 1) * N/2) of it to binary16 into the ring
-// slot the MMAs read -- 16 codes per lane and step, the 128-byte swizzled
-// K-major layout -- then orders its writes for the tensor cores
-// (fence.proxy.async). Warp 0 also reads the block table (a tile ahead) and
-// issues the copies; both wait for a tile's copy (`staged`) and for its ring
-// slot (`empty`), and each arrives on `full` (count 2) and on `sfree`
-// (count 2) once it has read its rows, after which warp 0 refills that
-// staging slot with the tile two ahead.
-template <int N, int D, int NS>
-__device__ __forceinline__ void tc_load_widen2(const TcPrefillParams& tp, const CUtensorMap* map,
-                                               uint8_t* staging, uint8_t* ring, uint64_t* staged,
-                                               uint64_t* sfree, uint64_t* full, uint64_t* empty,
-                                               int s, int hk, int ntiles, int kend, int half,
-                                               int lane, volatile int* abort_flag) {
-    constexpr int kKvBytes = N * D * 2;                      // one binary16 ring slot
-    constexpr int kStage8Bytes = N * D;                      // one E4M3 staging slot
-    constexpr int kRow8 = D;                                 // bytes of an E4M3 row
-    constexpr int kHalfChunks = N * kRow8 / 16 / 2;          // 16-code chunks per warp and tile
-    constexpr int64_t kNone = -1;
-    const PrefillParams& p = tp.p;
-    const int32_t* table = p.block_tables + (size_t)s * p.max_blocks;
-    const int rows = tp.box_rows;
-    const int B = p.block_size;
-    const int r0 = lane * rows;
-    const bool issuer = half == 0;
-    auto fetch = [&](int j) -> int64_t {
-        const int key = j * N + r0;
-        if (issuer && j < ntiles && r0 < N && key < kend) return (int64_t)table[key / B];
-        return kNone;
-    };
-    auto issue = [&](int j, int64_t blk) {
-        const bool has = blk != kNone;
-        const bool valid = has && blk >= 0 && blk < p.num_blocks;
-        if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
-        const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(&staged[j & 1], boxes * (uint32_t)rows * kRow8);
-        __syncwarp();
-        if (valid) {
-            const int key = j * N + r0;
-            const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
-            tma_load_2d(staging + (j & 1) * kStage8Bytes + r0 * kRow8, map, 0, y, &staged[j & 1]);
-        }
-    };
-    int issued = 0;
-    int64_t next = kNone;
-    if (issuer) {
-        issue(0, fetch(0));
-        next = fetch(1);
-        if (ntiles > 1) issue(1, next);
-        next = fetch(2);
-        issued = ntiles > 1 ? 2 : 1;
-    }
-    bool live = true;
-    for (int j = 0; j < ntiles && live; ++j) {
-        const int64_t after = fetch(j + 3);                  // in flight while tile j is widened
-        bool ok = true;
-        if (lane == 0) {
-            ok = tc_wait(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
-            if (ok && j >= NS)
-                ok = tc_wait(&empty[j % NS], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) {
-            live = false;
-            break;
-        }
-        const uint8_t* src = staging + (j & 1) * kStage8Bytes;
-        uint8_t* dst = ring + (j % NS) * kKvBytes;
-#pragma unroll 4
-        for (int k = 0; k < kHalfChunks / 32; ++k) {
-            const int q = half * kHalfChunks + lane + 32 * k;
-            const int r = q / (kRow8 / 16), c = q - r * (kRow8 / 16);
-            const uint4 w = *reinterpret_cast<const uint4*>(src + r * kRow8 + c * 16);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            uint32_t h[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                h[2 * e] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4140));
-                h[2 * e + 1] = e4m3x2_spread_to_f16x2_scaled(__byte_perm(ws[e], 0u, 0x4342));
-            }
-            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(dst + sw128_chunk<N>(r, 2 * c + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            mbar_arrive(&full[j % NS]);
-            mbar_arrive(&sfree[j & 1]);                      // this warp is done with staging j
-        }
-        if (issuer && j + 2 < ntiles) {
-            // staging slot j % 2 is free once both warps have read tile j
-            bool ok2 = true;
-            if (lane == 0) ok2 = tc_wait(&sfree[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
-            if (!__shfl_sync(0xffffffffu, ok2, 0)) {
-                live = false;
-                break;
-            }
-            issue(j + 2, next);
-            issued = j + 3;
-        }
-        next = after;
-    }
-    // copies still in flight (only after an abort) land before the CTA ends
-    if (issuer && lane == 0)
-        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
-            mbar_wait_bounded(&staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
-}
-
-// E4M3 K (or V) tiles for the two-tile kernel, in halves: warp `half` owns
+// E4M3 K (or V) tiles, loaded and widened in halves by two warps (both
+// tcgen05 kernels): warp `half` owns
 // rows [half * N/2, (half + 1) * N/2) of every tile -- it reads their
 // block-table entries (a tile ahead), copies them into its half of one of
 // two staging slots (plain boxes of at most N/2 rows, so no box spans both
@@ -653,10 +545,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* pv_done = p_full + 1;
     uint64_t* drain = pv_done + 1;
     uint64_t* q_ready = drain + 1;
-    uint64_t* k_staged = q_ready + 1;                        // E4M3: [2]
-    uint64_t* v_staged = k_staged + 2;                       // E4M3: [2]
-    uint64_t* k_sfree = v_staged + 2;                        // E4M3: [2]
-    uint64_t* v_sfree = k_sfree + 2;                         // E4M3: [2]
+    uint64_t* k_staged = q_ready + 1;                        // E4M3: [half][slot]
+    uint64_t* v_staged = k_staged + 4;                       // E4M3: [half][slot]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -709,11 +599,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
         if constexpr (kFp8) {
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < 4; ++i) {
                 mbar_init(&k_staged[i], 1);
                 mbar_init(&v_staged[i], 1);
-                mbar_init(&k_sfree[i], 2);
-                mbar_init(&v_sfree[i], 2);
             }
         }
         *abort_flag = 0;
@@ -780,18 +668,18 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
         // ------------------------------------------------------------ K loads
         if constexpr (kFp8)
-            tc_load_widen2<N, D, NS>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff, k_staged, k_sfree,
-                               k_full, k_empty, s, hk, ntiles, kend, warp == kTcKWarp ? 0 : 1,
-                               lane, abort_flag);
+            tc_load_widen_halves<N, D, NS>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff,
+                                           k_staged, k_full, k_empty, s, hk, ntiles, kend,
+                                           warp == kTcKWarp ? 0 : 1, lane, abort_flag);
         else
             tc_load_ring<Sh, NS>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
                                  kend, lane, first, abort_flag);
     } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
         // ------------------------------------------------------------ V loads
         if constexpr (kFp8)
-            tc_load_widen2<N, D, NS>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff, v_staged, v_sfree,
-                               v_full, v_empty, s, hk, ntiles, kend, warp == kTcVWarp ? 0 : 1,
-                               lane, abort_flag);
+            tc_load_widen_halves<N, D, NS>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
+                                           v_staged, v_full, v_empty, s, hk, ntiles, kend,
+                                           warp == kTcVWarp ? 0 : 1, lane, abort_flag);
         else
             tc_load_ring<Sh, NS>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk, ntiles,
                                  kend, lane, first, abort_flag);
@@ -1568,7 +1456,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
 // E4M3 caches: widened K/V (head size 64 or 128), two query tiles per CTA
 // when sequences have at least two, else the one-tile kernel. The tensor
 // maps view each cache as [num_blocks*Hkv*B rows][D bytes] with plain
-// (unswizzled) boxes of one block segment.
+// (unswizzled) boxes of min(B, 64) rows within one block segment.
 template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
@@ -1578,9 +1466,8 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     tp.p.v_mul *= 256.f;
     constexpr int n = TcShape<128, true>::N;
     static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
-    // the two-tile kernel loads each tile by halves: boxes of at most n/2 rows
-    const int box_cap = p.q_tiles >= 2 ? n / 2 : n;
-    tp.box_rows = p.block_size < box_cap ? p.block_size : box_cap;
+    // the tiles load by halves: boxes of at most n/2 rows
+    tp.box_rows = p.block_size < n / 2 ? p.block_size : n / 2;
     const unsigned long long rows =
         (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
     cudaError_t e = encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
