@@ -172,6 +172,20 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// Instruction descriptor of kind::f8f6f4 with A and B both E4M3 (format 0)
+// and K-major, F32 accumulator, shape M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D (+)= A.B^T on E4M3 operands from shared memory: K = 32 codes per step.
+__device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -424,19 +438,19 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
 }
 
 // E4M3 K (or V) tiles, loaded and widened in halves by two warps (both
-// tcgen05 kernels): warp `half` owns
-// rows [half * N/2, (half + 1) * N/2) of every tile -- it reads their
-// block-table entries (a tile ahead), copies them into its half of one of
-// two staging slots (plain boxes of at most N/2 rows, so no box spans both
-// halves; a barrier per half and slot), widens them to binary16 into the
-// ring slot the MMAs read once that slot is free (`empty`), orders its
-// writes for the tensor cores (fence.proxy.async, which also orders its
-// reads of the staging rows before the next copy into them), arrives on
-// `full` (count 2), and refills its half of the staging slot with the tile
-// two ahead. The two warps never wait for each other. Measured on GB300: a
-// warp whose proxy fence follows tensor copies it issued itself passes it in
-// ~200 cycles, one that issued none waited ~2,800, so both warps issue.
-template <int N, int D, int NS>
+// tcgen05 kernels): warp `half` owns rows [half * N/2, (half + 1) * N/2) of
+// every tile -- it reads their block-table entries (a tile ahead), copies
+// them into its half of one of kSlots staging slots (plain boxes of at most
+// N/2 rows, so no box spans both halves; a barrier per half and slot),
+// widens them to binary16 into the ring slot the MMAs read once that slot is
+// free (`empty`), orders its writes for the tensor cores (fence.proxy.async,
+// which also orders its reads of the staging rows before the next copy into
+// them), arrives on `full` (count 2), and refills its half of the staging
+// slot with the tile kSlots ahead. The two warps never wait for each other.
+// Measured on GB300: a warp whose proxy fence follows tensor copies it issued
+// itself passes it in ~200 cycles, one that issued none waited ~2,800, so
+// both warps issue.
+template <int N, int D, int NS, int kSlots = 2>
 __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
                                                      const CUtensorMap* map, uint8_t* staging,
                                                      uint8_t* ring, uint64_t* staged,
@@ -454,7 +468,7 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
     const int B = p.block_size;
     const int r0 = half * (N / 2) + lane * rows;             // this lane's box
     const bool owner = lane * rows < N / 2;
-    uint64_t* my_staged = staged + 2 * half;                 // [slot] of this half
+    uint64_t* my_staged = staged + kSlots * half;            // [slot] of this half
     auto fetch = [&](int j) -> int64_t {
         const int key = j * N + r0;
         if (owner && j < ntiles && key < kend) return (int64_t)table[key / B];
@@ -465,25 +479,24 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
         const bool valid = has && blk >= 0 && blk < p.num_blocks;
         if (has && !valid && p.status) atomicOr(p.status, PA_DEV_BAD_BLOCK_ID);
         const uint32_t boxes = __popc(__ballot_sync(0xffffffffu, valid));
-        if (lane == 0) mbar_arrive_expect_tx(&my_staged[j & 1], boxes * (uint32_t)rows * kRow8);
+        if (lane == 0) mbar_arrive_expect_tx(&my_staged[j % kSlots], boxes * (uint32_t)rows * kRow8);
         __syncwarp();
         if (valid) {
             const int key = j * N + r0;
             const int y = (int)((blk * p.num_kv_heads + hk) * B + key % B);
-            tma_load_2d(staging + (j & 1) * kStage8Bytes + r0 * kRow8, map, 0, y,
-                        &my_staged[j & 1]);
+            tma_load_2d(staging + (j % kSlots) * kStage8Bytes + r0 * kRow8, map, 0, y,
+                        &my_staged[j % kSlots]);
         }
     };
-    issue(0, fetch(0));
-    if (ntiles > 1) issue(1, fetch(1));
-    int issued = ntiles > 1 ? 2 : 1;
-    int64_t next = fetch(2);
+    int issued = 0;
+    for (; issued < kSlots && issued < ntiles; ++issued) issue(issued, fetch(issued));
+    int64_t next = fetch(kSlots);
     bool live = true;
     for (int j = 0; j < ntiles && live; ++j) {
-        const int64_t after = fetch(j + 3);                  // in flight while tile j is widened
+        const int64_t after = fetch(j + kSlots + 1);         // in flight while tile j is widened
         bool ok = true;
         if (lane == 0) {
-            ok = tc_wait(&my_staged[j & 1], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
+            ok = tc_wait(&my_staged[j % kSlots], (uint32_t)((j / kSlots) & 1), p.status, abort_flag);
             if (ok && j >= NS)
                 ok = tc_wait(&empty[j % NS], (uint32_t)((j / NS - 1) & 1), p.status, abort_flag);
         }
@@ -491,7 +504,7 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
             live = false;
             break;
         }
-        const uint8_t* src = staging + (j & 1) * kStage8Bytes;
+        const uint8_t* src = staging + (j % kSlots) * kStage8Bytes;
         uint8_t* dst = ring + (j % NS) * kKvBytes;
 #pragma unroll 4
         for (int k = 0; k < kHalfChunks / 32; ++k) {
@@ -511,16 +524,16 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[j % NS]);
-        if (j + 2 < ntiles) {
-            issue(j + 2, next);                              // this half of staging slot j % 2
-            issued = j + 3;
+        if (j + kSlots < ntiles) {
+            issue(j + kSlots, next);                         // this half of staging slot j % kSlots
+            issued = j + kSlots + 1;
         }
         next = after;
     }
     // copies still in flight (only after an abort) land before the CTA ends
     if (lane == 0)
-        for (int j = issued - 1; j >= 0 && j >= issued - 2; --j)
-            mbar_wait_bounded(&my_staged[j & 1], (uint32_t)((j >> 1) & 1), p.status);
+        for (int j = issued - 1; j >= 0 && j >= issued - kSlots; --j)
+            mbar_wait_bounded(&my_staged[j % kSlots], (uint32_t)((j / kSlots) & 1), p.status);
 }
 
 template <typename QT, typename CT, int D>
@@ -949,6 +962,9 @@ struct TcShape2 {
     static constexpr int kStagesV0 = (kTcSmemLimit - kFixed - NSK * kKvBytes) / kKvBytes;
     static constexpr int kStagesV1 = kPLo ? NSK : kStagesV0;
     static constexpr int NSV = kStagesV1 > 4 ? 4 : kStagesV1;
+    static constexpr int kKBytes = kKvBytes;                 // one K stage
+    static constexpr int kVBytes = kKvBytes;                 // one V stage
+    static constexpr int kVSlots = 2;                        // E4M3 V staging slots
     static constexpr int kQOff = 0;                          // Q0, then Q1
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + NSK * kKvBytes;
@@ -972,6 +988,54 @@ struct TcShape2 {
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
 
+// The two-tile kernel on E4M3 caches at head size 128 with E4M3 scores: S =
+// Q.K^T runs on kind::f8f6f4 straight from the E4M3 K tiles (TMA, 128-byte
+// swizzle, no widening), the query as two E4M3 terms hi + lo of its row
+// scaled by a power of two (exact for a bf16 query, relative 2^-8 for f16);
+// V is still widened to binary16 for the P.V product, through three staging
+// slots. Shared memory: Q 4 x 16 KB (tile, term), K 3 x 16 KB, V 2 x 32 KB,
+// V staging 3 x 16 KB, barriers.
+struct TcShape2E4M3Scores {
+    static constexpr int D = 128;
+    static constexpr int N = 128;                            // keys per tile
+    static constexpr int kSpans = D / 64;                    // binary16 V column spans
+    static constexpr int kQTermBytes = kTcRows * D;          // one E4M3 term of one query tile
+    static constexpr int kQBytes = 2 * kQTermBytes;          // one query tile: hi, then lo
+    static constexpr int kKBytes = N * D;                    // one E4M3 K stage
+    static constexpr int kVBytes = N * D * 2;                // one binary16 V stage
+    static constexpr int kKvBytes = kVBytes;
+    static constexpr int kStage8Bytes = N * D;               // one E4M3 V staging slot
+    static constexpr int NSK = 3;
+    static constexpr int NSV = 2;
+    static constexpr int kVSlots = 3;
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = 2 * kQBytes;
+    static constexpr int kVOff = kKOff + NSK * kKBytes;
+    static constexpr int kK8Off = kVOff;                     // (no K staging)
+    static constexpr int kV8Off = kVOff + NSV * kVBytes;
+    static constexpr int kBarOff = kV8Off + kVSlots * kStage8Bytes;
+    // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
+    // v_staged[2][kVSlots]
+    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6 + 2 * kVSlots;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kTileCols = N + D;
+    static_assert(2 * kTileCols <= kTmemCols, "TMEM columns");
+    static_assert(kAlloc <= kTcSmemLimit, "shared memory");
+    static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
+};
+// The E4M3 K ring as tc_load_ring sees it: one 128-byte span per key.
+struct TcRingE4M3 {
+    static constexpr int N = 128;
+    static constexpr int kSpans = 1;
+    static constexpr int kKvBytes = N * 128;
+};
+// Whether the two-tile kernel takes E4M3 scores for this cache and head size.
+template <typename CT, int D>
+constexpr bool kTc2E4M3Scores = std::is_same<CT, e4m3_t>::value && D == 128;
+
 // Two query tiles per CTA: warps 0-3 run the softmax of tile 0, warps 4-7 of
 // tile 1, each thread a whole row of 128 keys. The MMA issuer interleaves the
 // tiles -- S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... -- so one tile's
@@ -988,7 +1052,8 @@ __global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp
 paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     using T = typename TcMath<QT, CT>::T;                    // MMA operand type
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
-    using Sh = TcShape2<D, kTcPLo<T>, kFp8>;
+    constexpr bool kF8S = kTc2E4M3Scores<CT, D>;              // E4M3 scores (kind::f8f6f4)
+    using Sh = std::conditional_t<kF8S, TcShape2E4M3Scores, TcShape2<D, kTcPLo<T>, kFp8>>;
     constexpr int N = Sh::N;
     constexpr int NSK = Sh::NSK;                             // K ring stages
     constexpr int NSV = Sh::NSV;                             // V ring stages
@@ -1005,8 +1070,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* p_full = s_full + 2;                           // [2]
     uint64_t* drain = p_full + 2;
     uint64_t* q_ready = drain + 1;
-    uint64_t* k_staged = q_ready + 1;                        // E4M3 only: [half][slot]
-    uint64_t* v_staged = k_staged + 4;
+    uint64_t* k_staged = q_ready + 1;                        // widened E4M3 K: [half][slot]
+    uint64_t* v_staged = kF8S ? q_ready + 1 : k_staged + 4;  // E4M3 V: [half][slot]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -1022,8 +1087,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int s = tc_sequence(p, rest / p.num_kv_heads, tid == 0 && g == 0 && hk == 0);
     if (s < 0) return;
     int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
-    if constexpr (!kFp8)
+    if constexpr (!kFp8) {
         if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
+    } else if constexpr (kF8S) {
+        if (warp == kTcKWarp) tc_ring_first<TcRingE4M3>(tp, s, lane, first);
+    }
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
     const int L = p.context_lens[s];
@@ -1044,10 +1112,27 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const bool two = ntok1 > 0;
     const int kend = L - Q + tok0 + ntok0 + ntok1;           // keys [0, kend)
     const int ntiles = (kend + N - 1) / N;
+    // E4M3 scores: each softmax thread loads its own query row here, before
+    // the setup, and converts it once the setup is done
+    [[maybe_unused]] uint4 qrow[kF8S ? D / 8 : 1];
+    float q_row_mul = 1.f;                                   // the row's inverse scale
+    if constexpr (kF8S) {
+        if (tid < kTcSoftmaxThreads) {
+            const int t0 = tid / kTcRows, r = tid & (kTcRows - 1);
+            const int i = r / p.group, gg = r - i * p.group;
+            const bool live_row = i < (t0 == 0 ? ntok0 : ntok1);
+            const uint4* src = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const QT*>(p.query) +
+                ((size_t)(q0 + tok0 + t0 * Tq + (live_row ? i : 0)) * p.num_q_heads +
+                 (size_t)hk * p.group + gg) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) qrow[c] = live_row ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NSK; ++i) {
-            mbar_init(&k_full[i], kFp8 ? 2 : 1);             // E4M3: two widening warps
+            mbar_init(&k_full[i], kFp8 && !kF8S ? 2 : 1);    // widened E4M3: two warps
             mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < NSV; ++i) {
@@ -1060,7 +1145,9 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
-        if constexpr (kFp8) {
+        if constexpr (kF8S) {
+            for (int i = 0; i < 2 * Sh::kVSlots; ++i) mbar_init(&v_staged[i], 1);
+        } else if constexpr (kFp8) {
             for (int i = 0; i < 4; ++i) {
                 mbar_init(&k_staged[i], 1);
                 mbar_init(&v_staged[i], 1);
@@ -1090,8 +1177,9 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         const int tt0 = tok0 + qt * Tq;
         const int nt = qt == 0 ? ntok0 : ntok1;
         constexpr int CPR = D / 8;
-        constexpr int PER = CPR;                             // 128 rows x CPR chunks / 128 threads
+        constexpr int PER = kF8S ? 1 : CPR;                  // 128 rows x CPR chunks / 128 threads
         uint4 v[PER];
+        if constexpr (!kF8S) {
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int idx = (tid & (kTcRows - 1)) + k * kTcRows;
@@ -1103,7 +1191,60 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 v[k] = __ldg(reinterpret_cast<const uint4*>(qbase + row * D + c * 8));
             }
         }
+        }
         uint8_t* qd = sm + Sh::kQOff + qt * Sh::kQBytes;
+        if constexpr (kF8S) {
+            // E4M3 scores: the thread's row times a power of two that puts its
+            // largest |element| in [128, 256), as hi = the value rounded to
+            // E4M3's four significant bits (integer operations, ties to even;
+            // exact in E4M3 there) and lo = E4M3(value - hi), stored K-major
+            // with one 128-byte swizzled span per row, hi then lo
+            const int r = tid & (kTcRows - 1);
+            uint32_t m2 = 0u;                                // 16-bit magnitudes order as integers
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                m2 = __vmaxu2(m2, qrow[c].x & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qrow[c].y & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qrow[c].z & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qrow[c].w & 0x7FFF7FFFu);
+            }
+            const float mx = unpack2<QT>(max(m2 & 0xFFFFu, m2 >> 16)).x;
+            int ex = 0;
+            (void)frexpf(mx, &ex);                           // mx = m 2^ex, m in [0.5, 1)
+            const float qs = mx > 0.f ? ldexpf(1.f, 8 - max(ex, -100)) : 1.f;
+            q_row_mul = 1.f / qs;
+            auto round4 = [](float y) -> float {
+                uint32_t b = __float_as_uint(y);
+                b += 0x7FFFFu + ((b >> 20) & 1u);
+                return __uint_as_float(b & 0xFFF00000u);
+            };
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint32_t in[4] = {qrow[c].x, qrow[c].y, qrow[c].z, qrow[c].w};
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t h4 = 0u, l4 = 0u;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 f2 = unpack2<QT>(in[2 * e + u]);
+                        const float y0 = f2.x * qs, y1 = f2.y * qs;
+                        const float h0 = round4(y0), h1 = round4(y1);
+                        const __nv_fp8x2_storage_t hc =
+                            __nv_cvt_float2_to_fp8x2(make_float2(h0, h1), __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t lc = __nv_cvt_float2_to_fp8x2(
+                            make_float2(y0 - h0, y1 - h1), __NV_SATFINITE, __NV_E4M3);
+                        h4 |= (uint32_t)hc << (16 * u);
+                        l4 |= (uint32_t)lc << (16 * u);
+                    }
+                    hw[e] = h4;
+                    lw[e] = l4;
+                }
+                const uint32_t off = (uint32_t)(r * 128 + ((((c * 8) >> 4) ^ (r & 7)) << 4) + ((c * 8) & 15));
+                *reinterpret_cast<uint2*>(qd + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(qd + Sh::kQTermBytes + off) = make_uint2(lw[0], lw[1]);
+            }
+        } else {
 #pragma unroll
         for (int k = 0; k < PER; ++k) {
             const int idx = (tid & (kTcRows - 1)) + k * kTcRows;
@@ -1122,6 +1263,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             }
             *reinterpret_cast<uint4*>(qd + sw128_chunk<kTcRows>(rr, c)) = w;
         }
+        }
         fence_async_smem();
         mbar_arrive(q_ready);
     }
@@ -1130,8 +1272,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     // producer warpgroup(s); E4M3: they give up registers to the softmax
     // warpgroups (every warp of a warpgroup runs the same instruction)
     if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcProducerRegs));
-    if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
-        if constexpr (kFp8)
+    if (warp == kTcKWarp || (kFp8 && !kF8S && warp == kTcK2Warp)) {
+        if constexpr (kF8S)
+            tc_load_ring<TcRingE4M3, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk,
+                                          ntiles, kend, lane, first, abort_flag);
+        else if constexpr (kFp8)
             tc_load_widen_halves<N, D, NSK>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff,
                                             k_staged, k_full, k_empty, s, hk, ntiles, kend,
                                             warp == kTcKWarp ? 0 : 1, lane, abort_flag);
@@ -1140,7 +1285,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                                   kend, lane, first, abort_flag);
     } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
         if constexpr (kFp8)
-            tc_load_widen_halves<N, D, NSV>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
+            tc_load_widen_halves<N, D, NSV, Sh::kVSlots>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
                                             v_staged, v_full, v_empty, s, hk, ntiles, kend,
                                             warp == kTcVWarp ? 0 : 1, lane, abort_flag);
         else
@@ -1160,14 +1305,27 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                     tc_fence_after();
                 }
                 const uint32_t qa = smem_u32(sm + Sh::kQOff + t * Sh::kQBytes);
-                const uint32_t ka = smem_u32(sm + Sh::kKOff + st * Sh::kKvBytes);
+                const uint32_t ka = smem_u32(sm + Sh::kKOff + st * Sh::kKBytes);
                 const uint32_t sc = tmem + t * Sh::kTileCols;
+                if constexpr (kF8S) {
+                    // the query's two terms against the E4M3 K tile, 32 codes a step
+                    constexpr uint32_t idS8 = tc_idesc_e4m3(kTcRows, N);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk & 3) * 32u;
-                    const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
-                    const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
-                    tc_mma(sc, a, b, idS, kk > 0);
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint64_t a = tc_desc(qa + u * Sh::kQTermBytes + kk * 32, 16, 1024);
+                            const uint64_t b = tc_desc(ka + kk * 32, 16, 1024);
+                            tc_mma_e4m3(sc, a, b, idS8, u > 0 || kk > 0);
+                        }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(kk & 3) * 32u;
+                        const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
+                        const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
+                        tc_mma(sc, a, b, idS, kk > 0);
+                    }
                 }
                 if (t == last_t) tc_commit(&k_empty[st]);
                 tc_commit(&s_full[t]);
@@ -1180,7 +1338,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                     !tc_wait(&v_full[st], (uint32_t)((j / NSV) & 1), p.status, abort_flag))
                     return false;
                 tc_fence_after();
-                const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kKvBytes);
+                const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kVBytes);
                 const uint32_t pt = tmem + t * Sh::kTileCols;          // P_hi | P_lo
                 const uint32_t oc = pt + N;
 #pragma unroll
@@ -1227,7 +1385,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         const int nt = qt == 0 ? ntok0 : ntok1;
         const bool row_valid = i < nt && r < Tq * G;
         const int pos = L - Q + tok0 + qt * Tq + (row_valid ? i : nt - 1);
-        const float qm = p.q_mul;
+        const float qm = p.q_mul * q_row_mul;                // E4M3 scores: the row's scale out
         const float2 qm2 = make_float2(qm, qm);
         float m = -INFINITY;
         float l = 0.f;
@@ -1319,7 +1477,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 if (!ok) break;
                 const int first = kend - key0;
                 constexpr int CPR = D / 8;
-                uint8_t* vd = sm + Sh::kVOff + st * Sh::kKvBytes;
+                uint8_t* vd = sm + Sh::kVOff + st * Sh::kVBytes;
                 for (int idx = r; idx < (N - first) * CPR; idx += kTcRows) {
                     const int rr = first + idx / CPR, c = idx % CPR;
                     *reinterpret_cast<uint4*>(vd + sw128_chunk<N>(rr, c)) = make_uint4(0u, 0u, 0u, 0u);
@@ -1453,16 +1611,20 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
     return cudaErrorInvalidValue;
 }
 
-// E4M3 caches: widened K/V (head size 64 or 128), two query tiles per CTA
-// when sequences have at least two, else the one-tile kernel. The tensor
-// maps view each cache as [num_blocks*Hkv*B rows][D bytes] with plain
-// (unswizzled) boxes of min(B, 64) rows within one block segment.
+// E4M3 caches (head size 64 or 128): two query tiles per CTA when sequences
+// have at least two, else the one-tile kernel. The V map (and K's, where K
+// is widened) views the cache as [num_blocks*Hkv*B rows][D bytes] with plain
+// (unswizzled) boxes of min(B, 64) rows within one block segment; with E4M3
+// scores (two tiles, head size 128) K's map has 128-byte swizzled boxes of
+// the same height, the layout the kind::f8f6f4 MMAs read.
 template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
     tp.p = p;
-    // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled)
-    tp.p.q_mul *= 256.f;
+    const bool e4m3_scores = head_size == 128 && p.q_tiles >= 2;
+    // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled);
+    // E4M3 scores read K as it is stored
+    if (!e4m3_scores) tp.p.q_mul *= 256.f;
     tp.p.v_mul *= 256.f;
     constexpr int n = TcShape<128, true>::N;
     static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
@@ -1470,15 +1632,17 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     tp.box_rows = p.block_size < n / 2 ? p.block_size : n / 2;
     const unsigned long long rows =
         (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
-    cudaError_t e = encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
+    cudaError_t e = e4m3_scores ? encode_cache_map(&tp.k_map, p.k_cache, 1, head_size, rows, tp.box_rows)
+                                : encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
     if (e == cudaSuccess) e = encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
     if (e != cudaSuccess) return e;
-    static_assert(TcShape2<128, false, true>::N == n && TcShape2<64, false, true>::N == n,
+    static_assert(TcShape2E4M3Scores::N == n && TcShape2<64, false, true>::N == n,
                   "the two-tile kernel's box height");
     auto go = [&](auto dtag) -> cudaError_t {
         constexpr int D = decltype(dtag)::value;
         if (p.q_tiles >= 2) {
-            using Sh2 = TcShape2<D, false, true>;
+            using Sh2 = std::conditional_t<kTc2E4M3Scores<e4m3_t, D>, TcShape2E4M3Scores,
+                                           TcShape2<D, false, true>>;
             auto kern2 = paged_prefill_tc2_kernel<QT, e4m3_t, D>;
             cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern2), Sh2::kAlloc);
             if (e2 != cudaSuccess) return e2;
