@@ -988,10 +988,10 @@ struct TcShape2 {
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
 
-// The two-tile kernel on E4M3 caches at head size 128 with E4M3 scores: S =
-// Q.K^T runs on kind::f8f6f4 straight from the E4M3 K tiles (TMA, 128-byte
-// swizzle, no widening), the query as two E4M3 terms hi + lo of its row
-// scaled by a power of two (exact for a bf16 query, relative 2^-8 for f16);
+// The two-tile kernel on E4M3 caches at head size 128 with a bf16 query, E4M3
+// scores: S = Q.K^T runs on kind::f8f6f4 straight from the E4M3 K tiles (TMA,
+// 128-byte swizzle, no widening), the query as two E4M3 terms hi + lo of its
+// row scaled by a power of two (exact for a bf16 value in E4M3's normal range);
 // V is still widened to binary16 for the P.V product, through three staging
 // slots. Shared memory: Q 4 x 16 KB (tile, term), K 3 x 16 KB, V 2 x 32 KB,
 // V staging 3 x 16 KB, barriers.
@@ -1032,9 +1032,13 @@ struct TcRingE4M3 {
     static constexpr int kSpans = 1;
     static constexpr int kKvBytes = N * 128;
 };
-// Whether the two-tile kernel takes E4M3 scores for this cache and head size.
-template <typename CT, int D>
-constexpr bool kTc2E4M3Scores = std::is_same<CT, e4m3_t>::value && D == 128;
+// Whether the two-tile kernel takes E4M3 scores: E4M3 cache, head size 128,
+// bf16 query (its 8 significant bits are exactly the two E4M3 terms; an f16
+// query's 11 are not, and a test with rows up to 32 times N(0,1) measured
+// errors of 7e-2 that way, so f16 queries keep the widened K).
+template <typename QT, typename CT, int D>
+constexpr bool kTc2E4M3Scores =
+    std::is_same<CT, e4m3_t>::value && D == 128 && std::is_same<QT, __nv_bfloat16>::value;
 
 // Two query tiles per CTA: warps 0-3 run the softmax of tile 0, warps 4-7 of
 // tile 1, each thread a whole row of 128 keys. The MMA issuer interleaves the
@@ -1052,7 +1056,7 @@ __global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp
 paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     using T = typename TcMath<QT, CT>::T;                    // MMA operand type
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
-    constexpr bool kF8S = kTc2E4M3Scores<CT, D>;              // E4M3 scores (kind::f8f6f4)
+    constexpr bool kF8S = kTc2E4M3Scores<QT, CT, D>;          // E4M3 scores (kind::f8f6f4)
     using Sh = std::conditional_t<kF8S, TcShape2E4M3Scores, TcShape2<D, kTcPLo<T>, kFp8>>;
     constexpr int N = Sh::N;
     constexpr int NSK = Sh::NSK;                             // K ring stages
@@ -1615,13 +1619,13 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
 // have at least two, else the one-tile kernel. The V map (and K's, where K
 // is widened) views the cache as [num_blocks*Hkv*B rows][D bytes] with plain
 // (unswizzled) boxes of min(B, 64) rows within one block segment; with E4M3
-// scores (two tiles, head size 128) K's map has 128-byte swizzled boxes of
-// the same height, the layout the kind::f8f6f4 MMAs read.
+// scores (two tiles, head size 128, bf16 query) K's map has 128-byte
+// swizzled boxes of the same height, the layout the kind::f8f6f4 MMAs read.
 template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
     tp.p = p;
-    const bool e4m3_scores = head_size == 128 && p.q_tiles >= 2;
+    const bool e4m3_scores = kTc2E4M3Scores<QT, e4m3_t, 128> && head_size == 128 && p.q_tiles >= 2;
     // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled);
     // E4M3 scores read K as it is stored
     if (!e4m3_scores) tp.p.q_mul *= 256.f;
@@ -1641,7 +1645,7 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     auto go = [&](auto dtag) -> cudaError_t {
         constexpr int D = decltype(dtag)::value;
         if (p.q_tiles >= 2) {
-            using Sh2 = std::conditional_t<kTc2E4M3Scores<e4m3_t, D>, TcShape2E4M3Scores,
+            using Sh2 = std::conditional_t<kTc2E4M3Scores<QT, e4m3_t, D>, TcShape2E4M3Scores,
                                            TcShape2<D, false, true>>;
             auto kern2 = paged_prefill_tc2_kernel<QT, e4m3_t, D>;
             cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern2), Sh2::kAlloc);

@@ -11,6 +11,7 @@ import torch
 
 import oracle
 from paged_kv_cache_141_gb300 import binding as pk
+from paged_kv_cache_141_gb300 import workloads as W
 from paged_kv_cache_141_gb300.workloads import config_case, make_case, make_queries
 
 from gpu_common import (TORCH, DeviceCase, assert_decode_close, host_to_torch, oracle_pool,
@@ -181,6 +182,39 @@ def test_prefill_e4m3_tensor_core_sweep(i):
     c = make_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_size=d, block_size=B,
                   q_dtype=qt, cache_dtype="e4m3", kv_dtype=qt, lengths=lens, seed=960 + i)
     check(c, ql, f"e4m3 tc sweep {i}", force_tc=True)
+
+
+@pytest.mark.parametrize("qt", ["bf16", "f16"])
+def test_e4m3_scores_query_magnitudes(qt):
+    """The two-tile kernel on an E4M3 cache at head size 128. A bf16 query
+    takes the E4M3 scores: each row goes to the tensor cores as two E4M3
+    terms of the row times a power of two. An f16 query (11 significant bits,
+    more than two E4M3 terms hold) keeps the widened K. Rows scaled by powers
+    of two over a wide range, all-zero rows, and rows of one large element
+    beside tiny ones (the E4M3 subnormal range) must all stay within the
+    E4M3 tolerance of the oracle."""
+    c = make_case(num_seqs=3, num_q_heads=16, num_kv_heads=2, head_size=128, block_size=16,
+                  q_dtype=qt, cache_dtype="e4m3", kv_dtype=qt, lengths=("uniform", 200, 500),
+                  seed=981)
+    p = Prefill(c, ("uniform", 40, 80))
+    rows = p.q.query.reshape(-1, 128)
+    x = oracle.decode_array(rows, qt)
+    rng = np.random.default_rng(982)
+    span = 12 if qt == "bf16" else 5                         # f16 keeps |x| 2^span within range
+    x *= np.exp2(rng.integers(-span, span + 1, size=(len(x), 1)))
+    x[rng.random(len(x)) < 0.05] = 0.0
+    spike = np.flatnonzero(rng.random(len(x)) < 0.05)
+    x[spike] *= 2.0 ** -10
+    x[spike, rng.integers(0, 128, size=len(spike))] = 64.0
+    p.q.query = W.to_storage(x.astype(np.float32), qt).reshape(p.q.query.shape)
+    p.query = host_to_torch(p.q.query, qt).to(p.query.device)
+    assert pk.prefill_kernel(tc_bound(p), c.num_q_heads, c.num_kv_heads, 128, 16, c.num_blocks,
+                             pk.PA_BF16 if qt == "bf16" else pk.PA_F16,
+                             pk.PA_FP8_E4M3) == "tc_two_tiles"
+    got = to_f64(p.run(tc_bound(p)))
+    assert p.dc.status_bits() == 0
+    idx, want = p.oracle()
+    assert_decode_close(got[idx], want, c, f"e4m3 scores, {qt} query magnitudes")
 
 
 # warp-level MMA shapes: one and two 8-row n-tiles (up to 16 rows), four
