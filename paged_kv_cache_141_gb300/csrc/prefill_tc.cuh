@@ -172,10 +172,12 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
-// Instruction descriptor of kind::f8f6f4 with A and B both E4M3 (format 0)
-// and K-major, F32 accumulator, shape M x N.
-__host__ __device__ constexpr uint32_t tc_idesc_e4m3(int M, int N) {
-    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f8f6f4 with A and B both E4M3 (format 0),
+// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), F32 accumulator,
+// shape M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_e4m3(int M, int N, int b_mn = 0) {
+    return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
 }
 // D (+)= A.B^T on E4M3 operands from shared memory: K = 32 codes per step.
 __device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -184,6 +186,15 @@ __device__ __forceinline__ void tc_mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
         ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+// The same with A from TMEM (a_tmem: lane = row, four E4M3 codes per column).
+__device__ __forceinline__ void tc_mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                               uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
         : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
@@ -238,10 +249,19 @@ __device__ __forceinline__ void tc_st16(uint32_t taddr, const uint32_t* r) {
 }
 
 // NC consecutive columns (16 or a multiple of 32) from r[0..NC).
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7])
+        : "memory");
+}
 template <int NC>
 __device__ __forceinline__ void tc_st_n(uint32_t taddr, const uint32_t* r) {
-    static_assert(NC == 16 || NC % 32 == 0, "columns");
-    if constexpr (NC == 16) {
+    static_assert(NC == 8 || NC == 16 || NC % 32 == 0, "columns");
+    if constexpr (NC == 8) {
+        tc_st8(taddr, r);
+    } else if constexpr (NC == 16) {
         tc_st16(taddr, r);
     } else {
 #pragma unroll
@@ -988,35 +1008,33 @@ struct TcShape2 {
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
 
-// The two-tile kernel on E4M3 caches at head size 128 with a bf16 query, E4M3
-// scores: S = Q.K^T runs on kind::f8f6f4 straight from the E4M3 K tiles (TMA,
-// 128-byte swizzle, no widening), the query as two E4M3 terms hi + lo of its
-// row scaled by a power of two (exact for a bf16 value in E4M3's normal range);
-// V is still widened to binary16 for the P.V product, through three staging
-// slots. Shared memory: Q 4 x 16 KB (tile, term), K 3 x 16 KB, V 2 x 32 KB,
-// V staging 3 x 16 KB, barriers.
+// The two-tile kernel on E4M3 caches at head size 128 with a bf16 query:
+// both products on kind::f8f6f4, straight from the E4M3 tiles (TMA, 128-byte
+// swizzle, no widening). S = Q.K^T with the query as two E4M3 terms hi + lo
+// of its row scaled by a power of two (exact for a bf16 value in E4M3's
+// normal range); O += P.V with the weights as two E4M3 terms of P 2^8 in TMEM
+// and V an MN-major operand. Shared memory: Q 4 x 16 KB (tile, term), K and V
+// rings of five 16 KB stages, barriers.
 struct TcShape2E4M3Scores {
     static constexpr int D = 128;
     static constexpr int N = 128;                            // keys per tile
-    static constexpr int kSpans = D / 64;                    // binary16 V column spans
+    static constexpr int kSpans = 1;                         // 128-byte rows
     static constexpr int kQTermBytes = kTcRows * D;          // one E4M3 term of one query tile
     static constexpr int kQBytes = 2 * kQTermBytes;          // one query tile: hi, then lo
     static constexpr int kKBytes = N * D;                    // one E4M3 K stage
-    static constexpr int kVBytes = N * D * 2;                // one binary16 V stage
+    static constexpr int kVBytes = N * D;                    // one E4M3 V stage
     static constexpr int kKvBytes = kVBytes;
-    static constexpr int kStage8Bytes = N * D;               // one E4M3 V staging slot
-    static constexpr int NSK = 3;
-    static constexpr int NSV = 2;
-    static constexpr int kVSlots = 3;
+    static constexpr int NSK = 5;
+    static constexpr int NSV = 5;
+    static constexpr int kVSlots = 0;                        // (no V staging)
     static constexpr int kQOff = 0;
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + NSK * kKBytes;
-    static constexpr int kK8Off = kVOff;                     // (no K staging)
-    static constexpr int kV8Off = kVOff + NSV * kVBytes;
-    static constexpr int kBarOff = kV8Off + kVSlots * kStage8Bytes;
+    static constexpr int kK8Off = kVOff;                     // (no staging)
+    static constexpr int kV8Off = kVOff;
+    static constexpr int kBarOff = kVOff + NSV * kVBytes;
     // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
-    // v_staged[2][kVSlots]
-    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6 + 2 * kVSlots;
+    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;
@@ -1026,6 +1044,9 @@ struct TcShape2E4M3Scores {
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
+// Weights of the E4M3 products are P 2^8 <= 448: the softmax rescales O
+// whenever the row's maximum has grown by more than log2(448 / 256).
+constexpr float kTcRescaleLog2E4M3 = 0.8f;
 // The E4M3 K ring as tc_load_ring sees it: one 128-byte span per key.
 struct TcRingE4M3 {
     static constexpr int N = 128;
@@ -1094,7 +1115,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     if constexpr (!kFp8) {
         if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
     } else if constexpr (kF8S) {
-        if (warp == kTcKWarp) tc_ring_first<TcRingE4M3>(tp, s, lane, first);
+        if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<TcRingE4M3>(tp, s, lane, first);
     }
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
@@ -1140,7 +1161,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             mbar_init(&k_empty[i], 1);
         }
         for (int i = 0; i < NSV; ++i) {
-            mbar_init(&v_full[i], kFp8 ? 2 : 1);
+            mbar_init(&v_full[i], kFp8 && !kF8S ? 2 : 1);    // widened E4M3: two warps
             mbar_init(&v_empty[i], 1);
         }
         for (int t = 0; t < 2; ++t) {
@@ -1149,9 +1170,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
-        if constexpr (kF8S) {
-            for (int i = 0; i < 2 * Sh::kVSlots; ++i) mbar_init(&v_staged[i], 1);
-        } else if constexpr (kFp8) {
+        if constexpr (kFp8 && !kF8S) {
             for (int i = 0; i < 4; ++i) {
                 mbar_init(&k_staged[i], 1);
                 mbar_init(&v_staged[i], 1);
@@ -1287,8 +1306,11 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         else
             tc_load_ring<Sh, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
                                   kend, lane, first, abort_flag);
-    } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
-        if constexpr (kFp8)
+    } else if (warp == kTcVWarp || (kFp8 && !kF8S && warp == kTcV2Warp)) {
+        if constexpr (kF8S)
+            tc_load_ring<TcRingE4M3, NSV>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk,
+                                          ntiles, kend, lane, first, abort_flag);
+        else if constexpr (kFp8)
             tc_load_widen_halves<N, D, NSV, Sh::kVSlots>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
                                             v_staged, v_full, v_empty, s, hk, ntiles, kend,
                                             warp == kTcVWarp ? 0 : 1, lane, abort_flag);
@@ -1345,10 +1367,24 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kVBytes);
                 const uint32_t pt = tmem + t * Sh::kTileCols;          // P_hi | P_lo
                 const uint32_t oc = pt + N;
+                if constexpr (kF8S) {
+                    // the weights' two E4M3 terms (32 columns each) against
+                    // the E4M3 V tile as an MN-major operand, 32 keys a step
+                    constexpr uint32_t idO8 = tc_idesc_e4m3(kTcRows, D, 1);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < N / 32; ++kk) {
+                            const uint64_t b = tc_desc(va + kk * 32 * 128, N * 128, 1024);
+                            tc_mma_e4m3_ts(oc, pt + u * (N / 4) + kk * 8, b, idO8,
+                                           j > 0 || u > 0 || kk > 0);
+                        }
+                } else {
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk) {
                     const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
                     tc_mma_ts(oc, pt + kk * 8, b, idO, j > 0 || kk > 0);
+                }
                 }
                 if constexpr (kTcPLo<T>) {
 #pragma unroll
@@ -1424,7 +1460,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
                 for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
             const float m_cand = fmaxf(m, mr[0] * qm);
-            const bool rescale = m_cand > m + kTcRescaleLog2;
+            const bool rescale = m_cand > m + (kF8S ? kTcRescaleLog2E4M3 : kTcRescaleLog2);
             const float m_use = rescale ? m_cand : m;
             const float alpha = fast_exp2(m - m_use);
             const float2 nm2 = make_float2(-m_use, -m_use);
@@ -1434,6 +1470,40 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             // weights in four quarters of 32 keys: each quarter's P_hi and
             // P_lo go to TMEM before the next is formed, so few packed words
             // are live next to the scores not yet used
+            if constexpr (kF8S) {
+                // E4M3 weights: y = P 2^8 (the 2^8 in the exponent) as hi =
+                // E4M3(y) and lo = E4M3(y - hi), the remainder taken in
+                // binary16; four codes per 32-bit column, hi in columns
+                // [0, N/4), lo in [N/4, N/2); each quarter of 32 keys stored
+                // before the next is formed
+                const float2 nm8 = make_float2(8.f - m_use, 8.f - m_use);
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t phi[N / 16], plo[N / 16];
+#pragma unroll
+                    for (int c = 0; c < N / 4; c += 4) {
+                        const int cc = h * (N / 4) + c;
+                        uint32_t hq = 0u, lq = 0u;
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const float2 t2 = __ffma2_rn(make_float2(x[cc + 2 * u], x[cc + 2 * u + 1]), qm2, nm8);
+                            const float2 y = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
+                            sr[(c / 2 + u) % (R / 2)] = __fadd2_rn(sr[(c / 2 + u) % (R / 2)], y);
+                            const __nv_fp8x2_storage_t hc = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3);
+                            const __half2 rem = __hsub2(__float22half2_rn(y), *reinterpret_cast<const __half2*>(&hr));
+                            const __nv_fp8x2_storage_t lc = __nv_cvt_halfraw2_to_fp8x2(
+                                *reinterpret_cast<const __half2_raw*>(&rem), __NV_SATFINITE, __NV_E4M3);
+                            hq |= (uint32_t)hc << (16 * u);
+                            lq |= (uint32_t)lc << (16 * u);
+                        }
+                        phi[c / 4] = hq;
+                        plo[c / 4] = lq;
+                    }
+                    tc_st_n<N / 16>(sbuf + h * (N / 16), phi);
+                    tc_st_n<N / 16>(sbuf + N / 4 + h * (N / 16), plo);
+                }
+            } else {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
                 uint32_t phi[N / 8], plo[N / 8];
@@ -1451,6 +1521,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 }
                 tc_st_n<N / 8>(sbuf + h * (N / 8), phi);
                 if constexpr (kTcPLo<T>) tc_st_n<N / 8>(sbuf + N / 2 + h * (N / 8), plo);
+            }
             }
 #pragma unroll
             for (int w = R / 4; w >= 1; w /= 2)
@@ -1480,7 +1551,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const int first = kend - key0;
-                constexpr int CPR = D / 8;
+                constexpr int CPR = kF8S ? 8 : D / 8;            // 16-byte chunks of a V row
                 uint8_t* vd = sm + Sh::kVOff + st * Sh::kVBytes;
                 for (int idx = r; idx < (N - first) * CPR; idx += kTcRows) {
                     const int rr = first + idx / CPR, c = idx % CPR;
@@ -1627,9 +1698,12 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     tp.p = p;
     const bool e4m3_scores = kTc2E4M3Scores<QT, e4m3_t, 128> && head_size == 128 && p.q_tiles >= 2;
     // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled);
-    // E4M3 scores read K as it is stored
-    if (!e4m3_scores) tp.p.q_mul *= 256.f;
-    tp.p.v_mul *= 256.f;
+    // the E4M3 products read K and V as they are stored (their weights carry
+    // a 2^8 that the row sums carry too)
+    if (!e4m3_scores) {
+        tp.p.q_mul *= 256.f;
+        tp.p.v_mul *= 256.f;
+    }
     constexpr int n = TcShape<128, true>::N;
     static_assert(TcShape<64, true>::N == n, "one box height for both head sizes");
     // the tiles load by halves: boxes of at most n/2 rows
@@ -1638,7 +1712,9 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
         (unsigned long long)p.num_blocks * p.num_kv_heads * p.block_size;
     cudaError_t e = e4m3_scores ? encode_cache_map(&tp.k_map, p.k_cache, 1, head_size, rows, tp.box_rows)
                                 : encode_plain_map(&tp.k_map, p.k_cache, head_size, rows, tp.box_rows);
-    if (e == cudaSuccess) e = encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
+    if (e == cudaSuccess)
+        e = e4m3_scores ? encode_cache_map(&tp.v_map, p.v_cache, 1, head_size, rows, tp.box_rows)
+                        : encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
     if (e != cudaSuccess) return e;
     static_assert(TcShape2E4M3Scores::N == n && TcShape2<64, false, true>::N == n,
                   "the two-tile kernel's box height");
