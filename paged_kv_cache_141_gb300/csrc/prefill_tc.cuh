@@ -1034,12 +1034,14 @@ struct TcShape2E4M3Scores {
     static constexpr int kV8Off = kVOff;
     static constexpr int kBarOff = kVOff + NSV * kVBytes;
     // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
-    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 6;
+    // q_land
+    static constexpr int kNumBars = 2 * NSK + 2 * NSV + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
     static constexpr int kAlloc = kBytes + 1024;
     static constexpr int kTmemCols = 512;
     static constexpr int kTileCols = N + D;
+    static_assert(kQBytes == kTcRows * D * 2, "a tile's bf16 query rows land in its E4M3 region");
     static_assert(2 * kTileCols <= kTmemCols, "TMEM columns");
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
@@ -1095,6 +1097,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* p_full = s_full + 2;                           // [2]
     uint64_t* drain = p_full + 2;
     uint64_t* q_ready = drain + 1;
+    uint64_t* q_land = q_ready + 1;                          // E4M3 scores: the query rows landed
     uint64_t* k_staged = q_ready + 1;                        // widened E4M3 K: [half][slot]
     uint64_t* v_staged = kF8S ? q_ready + 1 : k_staged + 4;  // E4M3 V: [half][slot]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
@@ -1137,24 +1140,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     const bool two = ntok1 > 0;
     const int kend = L - Q + tok0 + ntok0 + ntok1;           // keys [0, kend)
     const int ntiles = (kend + N - 1) / N;
-    // E4M3 scores: each softmax thread loads its own query row here, before
-    // the setup, and converts it once the setup is done
-    [[maybe_unused]] uint4 qrow[kF8S ? D / 8 : 1];
-    float q_row_mul = 1.f;                                   // the row's inverse scale
-    if constexpr (kF8S) {
-        if (tid < kTcSoftmaxThreads) {
-            const int t0 = tid / kTcRows, r = tid & (kTcRows - 1);
-            const int i = r / p.group, gg = r - i * p.group;
-            const bool live_row = i < (t0 == 0 ? ntok0 : ntok1);
-            const uint4* src = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const QT*>(p.query) +
-                ((size_t)(q0 + tok0 + t0 * Tq + (live_row ? i : 0)) * p.num_q_heads +
-                 (size_t)hk * p.group + gg) * D);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) qrow[c] = live_row ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-
+    float q_row_mul = 1.f;                                   // E4M3 scores: the row's inverse scale
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NSK; ++i) {
             mbar_init(&k_full[i], kFp8 && !kF8S ? 2 : 1);    // widened E4M3: two warps
@@ -1170,6 +1156,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         }
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
+        if constexpr (kF8S) mbar_init(q_land, 1);
         if constexpr (kFp8 && !kF8S) {
             for (int i = 0; i < 4; ++i) {
                 mbar_init(&k_staged[i], 1);
@@ -1180,6 +1167,24 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
         fence_barrier_init();
         tma_prefetch_map(&tp.k_map);
         tma_prefetch_map(&tp.v_map);
+    }
+    if constexpr (kF8S) {
+        // E4M3 scores: the query rows arrive by bulk copies, one per token
+        // (its G heads' rows are contiguous), each tile's rows (token-major)
+        // into that tile's query region, converted in place below
+        if (warp == kTcKWarp) {
+            const uint32_t tok_bytes = (uint32_t)(p.group * D * sizeof(QT));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(q_land, (uint32_t)(ntok0 + ntok1) * tok_bytes);
+            __syncwarp();
+            const QT* qbase = reinterpret_cast<const QT*>(p.query);
+            for (int k = lane; k < ntok0 + ntok1; k += 32) {
+                const int t = k < ntok0 ? 0 : 1, i = k - t * ntok0;
+                const QT* src = qbase + ((size_t)(q0 + tok0 + t * Tq + i) * p.num_q_heads +
+                                         (size_t)hk * p.group) * D;
+                bulk_copy_g2s(sm + Sh::kQOff + t * Sh::kQBytes + i * tok_bytes, src, tok_bytes, q_land);
+            }
+        }
     }
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -1221,15 +1226,28 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             // largest |element| in [128, 256), as hi = the value rounded to
             // E4M3's four significant bits (integer operations, ties to even;
             // exact in E4M3 there) and lo = E4M3(value - hi), stored K-major
-            // with one 128-byte swizzled span per row, hi then lo
+            // with one 128-byte swizzled span per row, hi then lo, over the
+            // landed 16-bit rows once every thread has read its own (each
+            // thread starts at chunk r mod 16 of its row: rows 256 bytes apart
+            // would otherwise all hit the same banks)
             const int r = tid & (kTcRows - 1);
+            const bool live_row = r / G < nt;
+            bool okq = tc_wait(q_land, 0u, p.status, abort_flag);
+            uint4 qv[D / 8];
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const int cc = (c + r) & (D / 8 - 1);
+                qv[c] = live_row && okq ? *reinterpret_cast<const uint4*>(qd + r * (D * 2) + cc * 16)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+            }
+            named_barrier(3, kTcSoftmaxThreads);             // every row read before any is overwritten
             uint32_t m2 = 0u;                                // 16-bit magnitudes order as integers
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                m2 = __vmaxu2(m2, qrow[c].x & 0x7FFF7FFFu);
-                m2 = __vmaxu2(m2, qrow[c].y & 0x7FFF7FFFu);
-                m2 = __vmaxu2(m2, qrow[c].z & 0x7FFF7FFFu);
-                m2 = __vmaxu2(m2, qrow[c].w & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].x & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].y & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].z & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].w & 0x7FFF7FFFu);
             }
             const float mx = unpack2<QT>(max(m2 & 0xFFFFu, m2 >> 16)).x;
             int ex = 0;
@@ -1243,7 +1261,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             };
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
-                const uint32_t in[4] = {qrow[c].x, qrow[c].y, qrow[c].z, qrow[c].w};
+                const uint32_t in[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
                 uint32_t hw[2], lw[2];
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -1263,7 +1281,8 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
                     hw[e] = h4;
                     lw[e] = l4;
                 }
-                const uint32_t off = (uint32_t)(r * 128 + ((((c * 8) >> 4) ^ (r & 7)) << 4) + ((c * 8) & 15));
+                const int cc = (c + r) & (D / 8 - 1);            // the chunk qv[c] holds
+                const uint32_t off = (uint32_t)(r * 128 + ((((cc * 8) >> 4) ^ (r & 7)) << 4) + ((cc * 8) & 15));
                 *reinterpret_cast<uint2*>(qd + off) = make_uint2(hw[0], hw[1]);
                 *reinterpret_cast<uint2*>(qd + Sh::kQTermBytes + off) = make_uint2(lw[0], lw[1]);
             }
@@ -1296,9 +1315,12 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     // warpgroups (every warp of a warpgroup runs the same instruction)
     if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcProducerRegs));
     if (warp == kTcKWarp || (kFp8 && !kF8S && warp == kTcK2Warp)) {
-        if constexpr (kF8S)
+        if constexpr (kF8S) {
             tc_load_ring<TcRingE4M3, NSK>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk,
                                           ntiles, kend, lane, first, abort_flag);
+            // the query copies this warp issued land before the CTA ends
+            if (lane == 0) mbar_wait_bounded(q_land, 0u, p.status);
+        }
         else if constexpr (kFp8)
             tc_load_widen_halves<N, D, NSK>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff,
                                             k_staged, k_full, k_empty, s, hk, ntiles, kend,
