@@ -748,7 +748,7 @@ def prefill_kernel_name(case, max_queries: int) -> str:
         "mma": f"paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows{widened})",
         "mma_two_tiles": f"paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp{widened})",
         "tc_two_tiles": "paged_prefill_tc2_kernel (two query tiles per CTA"
-                        + ((", E4M3 scores on kind::f8f6f4, V widened to binary16)"
+                        + ((", E4M3 products on kind::f8f6f4)"
                             if case.q_dtype == "bf16" and case.head_size == 128
                             else ", E4M3 tiles widened to binary16)") if e4m3 else ")"),
         "tc": "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else ""),
