@@ -429,8 +429,13 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  16-bit query with a cache of the same type (head_size 64/128/256) or an
  *  E4M3 cache (head_size 64/128), a block_size that is a power of two in
  *  [8, 256] and a group of at most 128 heads runs on the tcgen05 tensor
- *  cores; other supported combinations run one query token per work unit
- *  on the CUDA cores. A sequence whose lengths
+ *  cores (with an E4M3 cache, a bf16 query, head_size 128 and two or more
+ *  query tiles per sequence, both products take E4M3 operands: the query
+ *  as two E4M3 terms of each row times a power of two, exact for bf16
+ *  values in E4M3's normal range, and the softmax weights as two E4M3
+ *  terms, relative error at most about 2^-8; else the E4M3 tiles are widened
+ *  to binary16); other supported combinations run one query token per work
+ *  unit on the CUDA cores. A sequence whose lengths
  *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
  *  num_queries == 0 launches nothing.
  */
