@@ -173,6 +173,10 @@ E4M3_TC_SWEEP = [
     (3, 16, 2, 128, 256, "f16", ("uniform", 200, 600), ("uniform", 20, 60)),
     (4, 12, 4, 64, 8, "bf16", ("fixed", [1, 2, 129, 400]), ("all",)),
     (3, 24, 8, 128, 64, "bf16", ("fixed", [300, 511, 1000]), ("fixed", [300, 170, 257])),
+    # bf16 query, head size 128, two or more tiles: the E4M3 products, with
+    # 8-row and 64-row (block size 256, capped) boxes
+    (3, 16, 2, 128, 8, "bf16", ("uniform", 100, 400), ("uniform", 20, 60)),
+    (3, 16, 2, 128, 256, "bf16", ("uniform", 200, 700), ("uniform", 20, 90)),
 ]
 
 
