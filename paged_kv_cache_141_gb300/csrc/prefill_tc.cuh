@@ -48,6 +48,10 @@
 // MMAs per key tile instead of two. Binary16 operands (f16 caches, and E4M3
 // caches widened to binary16) keep 11 significant bits, a relative error of
 // at most 2^-11 per weight: P goes as one term and the P_lo product is skipped.
+// The two-tile kernel's E4M3 products (E4M3 cache, bf16 query, head size 128)
+// take the query and the weights as two E4M3 terms each (8 significant bits:
+// exact for a bf16 query in E4M3's normal range, ~2^-8 for a weight), within
+// the E4M3 cache's 3e-2 bound; an f16 query keeps the widened path.
 //
 // Every wait is bounded; a wait that runs out raises PA_DEV_TIMEOUT and a
 // shared abort flag that ends every role's loop, and the CTA drains its copies
@@ -460,17 +464,17 @@ __device__ __forceinline__ void tc_load_ring(const TcPrefillParams& tp, const CU
 // E4M3 K (or V) tiles, loaded and widened in halves by two warps (both
 // tcgen05 kernels): warp `half` owns rows [half * N/2, (half + 1) * N/2) of
 // every tile -- it reads their block-table entries (a tile ahead), copies
-// them into its half of one of kSlots staging slots (plain boxes of at most
+// them into its half of one of two staging slots (plain boxes of at most
 // N/2 rows, so no box spans both halves; a barrier per half and slot),
 // widens them to binary16 into the ring slot the MMAs read once that slot is
 // free (`empty`), orders its writes for the tensor cores (fence.proxy.async,
 // which also orders its reads of the staging rows before the next copy into
 // them), arrives on `full` (count 2), and refills its half of the staging
-// slot with the tile kSlots ahead. The two warps never wait for each other.
+// slot with the tile two ahead. The two warps never wait for each other.
 // Measured on GB300: a warp whose proxy fence follows tensor copies it issued
 // itself passes it in ~200 cycles, one that issued none waited ~2,800, so
 // both warps issue.
-template <int N, int D, int NS, int kSlots = 2>
+template <int N, int D, int NS>
 __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
                                                      const CUtensorMap* map, uint8_t* staging,
                                                      uint8_t* ring, uint64_t* staged,
@@ -479,6 +483,7 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
                                                      int lane, volatile int* abort_flag) {
     constexpr int kKvBytes = N * D * 2;                      // one binary16 ring slot
     constexpr int kStage8Bytes = N * D;                      // one E4M3 staging slot
+    constexpr int kSlots = 2;                                // staging slots
     constexpr int kRow8 = D;                                 // bytes of an E4M3 row
     constexpr int kHalfChunks = N * kRow8 / 16 / 2;          // 16-code chunks per warp and tile
     constexpr int64_t kNone = -1;
@@ -984,7 +989,6 @@ struct TcShape2 {
     static constexpr int NSV = kStagesV1 > 4 ? 4 : kStagesV1;
     static constexpr int kKBytes = kKvBytes;                 // one K stage
     static constexpr int kVBytes = kKvBytes;                 // one V stage
-    static constexpr int kVSlots = 2;                        // E4M3 V staging slots
     static constexpr int kQOff = 0;                          // Q0, then Q1
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + NSK * kKvBytes;
@@ -1026,12 +1030,9 @@ struct TcShape2E4M3Scores {
     static constexpr int kKvBytes = kVBytes;
     static constexpr int NSK = 5;
     static constexpr int NSV = 5;
-    static constexpr int kVSlots = 0;                        // (no V staging)
     static constexpr int kQOff = 0;
     static constexpr int kKOff = 2 * kQBytes;
     static constexpr int kVOff = kKOff + NSK * kKBytes;
-    static constexpr int kK8Off = kVOff;                     // (no staging)
-    static constexpr int kV8Off = kVOff;
     static constexpr int kBarOff = kVOff + NSV * kVBytes;
     // k_full[NSK] k_empty[NSK] v_full[NSV] v_empty[NSV] s_full[2] p_full[2] drain q_ready
     // q_land
@@ -1333,7 +1334,7 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             tc_load_ring<TcRingE4M3, NSV>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk,
                                           ntiles, kend, lane, first, abort_flag);
         else if constexpr (kFp8)
-            tc_load_widen_halves<N, D, NSV, Sh::kVSlots>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
+            tc_load_widen_halves<N, D, NSV>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
                                             v_staged, v_full, v_empty, s, hk, ntiles, kend,
                                             warp == kTcVWarp ? 0 : 1, lane, abort_flag);
         else
