@@ -50,10 +50,11 @@ def test_decode_step_graph_replay(cfg):
         assert torch.equal(out.view(torch.uint8), eager.view(torch.uint8))
 
 
-@pytest.mark.parametrize("qn,ordered", [(100, False), (4, False), (8, True)],
-                         ids=["tcgen05", "warp-mma", "warp-mma2-ordered"])
-def test_multi_query_graph_replay(qn, ordered):
-    c = W.config_case(3, num_seqs=16)
+@pytest.mark.parametrize("cfg,qn,ordered", [(3, 100, False), (3, 4, False), (3, 8, True),
+                                             (5, 100, False)],
+                         ids=["tcgen05", "warp-mma", "warp-mma2-ordered", "tcgen05-e4m3-products"])
+def test_multi_query_graph_replay(cfg, qn, ordered):
+    c = W.config_case(cfg, num_seqs=16)
     q = W.make_queries(c, ("fixed", np.minimum(qn, c.context_lens)))
     dc = DeviceCase(c)
     dc.write_step()
@@ -63,8 +64,8 @@ def test_multi_query_graph_replay(qn, ordered):
 
     def run(out):
         pk.paged_prefill(out, query, qs, dc.k_cache, dc.v_cache, dc.block_tables,
-                         dc.context_lens, q.max_queries, c.max_context_len, c.scale, 1.0, 1.0,
-                         dc.status, torch.cuda.current_stream(), seq_order=order)
+                         dc.context_lens, q.max_queries, c.max_context_len, c.scale, c.k_scale,
+                         c.v_scale, dc.status, torch.cuda.current_stream(), seq_order=order)
 
     eager = torch.empty_like(query)
     run(eager)
