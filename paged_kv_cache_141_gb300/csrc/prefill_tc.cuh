@@ -1016,7 +1016,7 @@ struct TcShape2 {
 // both products on kind::f8f6f4, straight from the E4M3 tiles (TMA, 128-byte
 // swizzle, no widening). S = Q.K^T with the query as two E4M3 terms hi + lo
 // of its row scaled by a power of two (exact for a bf16 value in E4M3's
-// normal range); O += P.V with the weights as two E4M3 terms of P 2^8 in TMEM
+// normal range); O += P.V with the weights as two E4M3 terms of P 2^6 in TMEM
 // and V an MN-major operand. Shared memory: Q 4 x 16 KB (tile, term), K and V
 // rings of five 16 KB stages, barriers.
 struct TcShape2E4M3Scores {
@@ -1047,9 +1047,12 @@ struct TcShape2E4M3Scores {
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
-// Weights of the E4M3 products are P 2^8 <= 448: the softmax rescales O
-// whenever the row's maximum has grown by more than log2(448 / 256).
-constexpr float kTcRescaleLog2E4M3 = 0.8f;
+// Weights of the E4M3 products are y = P 2^6 <= 448: the softmax rescales O
+// whenever the row's maximum has grown by more than log2(448 / 64) = 2.8,
+// and y below E4M3's normal range (P < 2^-12) keeps an absolute error under
+// 2^-16 in P.
+constexpr int kTcWeightLog2E4M3 = 6;
+constexpr float kTcRescaleLog2E4M3 = 2.8f;
 // The E4M3 K ring as tc_load_ring sees it: one 128-byte span per key.
 struct TcRingE4M3 {
     static constexpr int N = 128;
@@ -1494,12 +1497,12 @@ paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
             // P_lo go to TMEM before the next is formed, so few packed words
             // are live next to the scores not yet used
             if constexpr (kF8S) {
-                // E4M3 weights: y = P 2^8 (the 2^8 in the exponent) as hi =
+                // E4M3 weights: y = P 2^6 (the 2^6 in the exponent) as hi =
                 // E4M3(y) and lo = E4M3(y - hi), the remainder taken in
                 // binary16; four codes per 32-bit column, hi in columns
                 // [0, N/4), lo in [N/4, N/2); each quarter of 32 keys stored
                 // before the next is formed
-                const float2 nm8 = make_float2(8.f - m_use, 8.f - m_use);
+                const float2 nm8 = make_float2(kTcWeightLog2E4M3 - m_use, kTcWeightLog2E4M3 - m_use);
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     uint32_t phi[N / 16], plo[N / 16];
@@ -1722,7 +1725,7 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
     const bool e4m3_scores = kTc2E4M3Scores<QT, e4m3_t, 128> && head_size == 128 && p.q_tiles >= 2;
     // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled);
     // the E4M3 products read K and V as they are stored (their weights carry
-    // a 2^8 that the row sums carry too)
+    // a power of two that the row sums carry too)
     if (!e4m3_scores) {
         tp.p.q_mul *= 256.f;
         tp.p.v_mul *= 256.f;
