@@ -744,14 +744,14 @@ def prefill_kernel_name(case, max_queries: int) -> str:
                              code[case.cache_dtype])
     e4m3 = case.cache_dtype == "e4m3"
     widened = ", E4M3 widened in registers" if e4m3 else ""
+    products = case.q_dtype == "bf16" and case.head_size == 128
+    tc_e4m3 = ", E4M3 products on kind::f8f6f4" if products else ", E4M3 tiles widened to binary16"
     return {
         "mma": f"paged_prefill_mma_kernel (warp-level MMA, one K/V pass for all rows{widened})",
         "mma_two_tiles": f"paged_prefill_mma2_kernel (warp-level MMA, two n-tiles per warp{widened})",
         "tc_two_tiles": "paged_prefill_tc2_kernel (two query tiles per CTA"
-                        + ((", E4M3 products on kind::f8f6f4)"
-                            if case.q_dtype == "bf16" and case.head_size == 128
-                            else ", E4M3 tiles widened to binary16)") if e4m3 else ")"),
-        "tc": "paged_prefill_tc_kernel" + (" (E4M3 tiles widened to binary16)" if e4m3 else ""),
+                        + (tc_e4m3 if e4m3 else "") + ")",
+        "tc": "paged_prefill_tc_kernel" + (f" ({tc_e4m3[2:]})" if e4m3 else ""),
         "cuda_cores": "paged_decode_simt_kernel (one query token per work unit)",
     }[kind]
 

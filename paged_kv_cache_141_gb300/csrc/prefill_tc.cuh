@@ -48,10 +48,12 @@
 // MMAs per key tile instead of two. Binary16 operands (f16 caches, and E4M3
 // caches widened to binary16) keep 11 significant bits, a relative error of
 // at most 2^-11 per weight: P goes as one term and the P_lo product is skipped.
-// The two-tile kernel's E4M3 products (E4M3 cache, bf16 query, head size 128)
+// The E4M3 products (both kernels; E4M3 cache, bf16 query, head size 128)
 // take the query and the weights as two E4M3 terms each (8 significant bits:
 // exact for a bf16 query in E4M3's normal range, ~2^-8 for a weight), within
-// the E4M3 cache's 3e-2 bound; an f16 query keeps the widened path.
+// the E4M3 cache's 3e-2 bound; an f16 query keeps the widened path. The K and
+// V tiles then go to the tensor cores as they are stored, by TMA, in rings of
+// six (one-tile) or five (two-tile) 16 KB stages.
 //
 // Every wait is bounded; a wait that runs out raises PA_DEV_TIMEOUT and a
 // shared abort flag that ends every role's loop, and the CTA drains its copies
@@ -561,12 +563,63 @@ __device__ __forceinline__ void tc_load_widen_halves(const TcPrefillParams& tp,
             mbar_wait_bounded(&my_staged[j % kSlots], (uint32_t)((j / kSlots) & 1), p.status);
 }
 
+// Weights of the E4M3 products are y = P 2^6 <= 448: the softmax rescales O
+// whenever the row's maximum has grown by more than log2(448 / 64) = 2.8,
+// and y below E4M3's normal range (P < 2^-12) keeps an absolute error under
+// 2^-16 in P.
+constexpr int kTcWeightLog2E4M3 = 6;
+constexpr float kTcRescaleLog2E4M3 = 2.8f;
+// The E4M3 K ring as tc_load_ring sees it: one 128-byte span per key.
+struct TcRingE4M3 {
+    static constexpr int N = 128;
+    static constexpr int kSpans = 1;
+    static constexpr int kKvBytes = N * 128;
+};
+// Whether a tcgen05 kernel takes the E4M3 products: E4M3 cache, head size 128,
+// bf16 query (its 8 significant bits are exactly the two E4M3 terms; an f16
+// query's 11 are not, and a test with rows up to 32 times N(0,1) measured
+// errors of 7e-2 that way, so f16 queries keep the widened K).
+template <typename QT, typename CT, int D>
+constexpr bool kTcE4M3Products =
+    std::is_same<CT, e4m3_t>::value && D == 128 && std::is_same<QT, __nv_bfloat16>::value;
+
+// The one-tile kernel with the E4M3 products: the query's two E4M3 terms in
+// the 32 KB its bf16 rows land in, K and V rings of six 16 KB stages filled
+// straight from the cache (128-byte swizzled boxes), barriers, row sums.
+struct TcShapeE4M3Products {
+    static constexpr int D = 128;
+    static constexpr int N = 128;                            // keys per tile
+    static constexpr int kQTermBytes = kTcRows * D;          // one E4M3 term of the query tile
+    static constexpr int kQBytes = 2 * kQTermBytes;          // hi, then lo
+    static constexpr int kKvBytes = N * D;                   // one E4M3 K (or V) stage
+    static constexpr int NS = 6;                             // K stages = V stages
+    static constexpr int kQOff = 0;
+    static constexpr int kKOff = kQOff + kQBytes;
+    static constexpr int kVOff = kKOff + NS * kKvBytes;
+    static constexpr int kBarOff = kVOff + NS * kKvBytes;
+    // k_full[NS] k_empty[NS] v_full[NS] v_empty[NS] s_full[2] p_full pv_done drain
+    // q_ready q_land
+    static constexpr int kNumBars = 4 * NS + 7;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+    static constexpr int kLsumOff = kMiscOff + 16;           // row sums of the two halves
+    static constexpr int kBytes = kLsumOff + kTcSoftmaxThreads * 4;
+    static constexpr int kAlloc = kBytes + 1024;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSCol = 0;
+    static constexpr int kOCol = 2 * N;
+    static_assert(kQBytes == kTcRows * D * 2, "the bf16 query rows land in the E4M3 region");
+    static_assert(2 * N + D <= kTmemCols, "TMEM columns");
+    static_assert(kAlloc <= kTcSmemLimit, "shared memory");
+    static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
+};
+
 template <typename QT, typename CT, int D>
 __global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp8 : kTcThreads, 1)
 paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     using MT = typename TcMath<QT, CT>::T;                  // MMA operand type
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
-    using Sh = TcShape<D, kFp8>;
+    constexpr bool kF8S = kTcE4M3Products<QT, CT, D>;        // both products on kind::f8f6f4
+    using Sh = std::conditional_t<kF8S, TcShapeE4M3Products, TcShape<D, kFp8>>;
     constexpr int N = Sh::N;
     constexpr int NS = Sh::NS;
     const PrefillParams& p = tp.p;
@@ -583,8 +636,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     uint64_t* pv_done = p_full + 1;
     uint64_t* drain = pv_done + 1;
     uint64_t* q_ready = drain + 1;
-    uint64_t* k_staged = q_ready + 1;                        // E4M3: [half][slot]
-    uint64_t* v_staged = k_staged + 4;                       // E4M3: [half][slot]
+    uint64_t* q_land = q_ready + 1;                          // E4M3 products: the query rows landed
+    uint64_t* k_staged = q_ready + 1;                        // widened E4M3: [half][slot]
+    uint64_t* v_staged = k_staged + 4;                       // widened E4M3: [half][slot]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Sh::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Sh::kMiscOff + 4);
 
@@ -599,8 +653,11 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     const int s = tc_sequence(p, rest / p.num_kv_heads, tid == 0 && tile == 0 && hk == 0);
     if (s < 0) return;
     int64_t first[kTcAhead] = {-1, -1, -1, -1};              // producers: first table entries
-    if constexpr (!kFp8)
+    if constexpr (!kFp8) {
         if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<Sh>(tp, s, lane, first);
+    } else if constexpr (kF8S) {
+        if (warp == kTcKWarp || warp == kTcVWarp) tc_ring_first<TcRingE4M3>(tp, s, lane, first);
+    }
     const int q0 = p.query_start[s];
     const int Q = p.query_start[s + 1] - q0;
     const int L = p.context_lens[s];
@@ -625,9 +682,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     // the softmax warps load the query tile (the MMA issuer waits for it)
     if (tid == kTcKWarp * 32) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&k_full[i], kFp8 ? 2 : 1);             // E4M3: two widening warps
+            mbar_init(&k_full[i], kFp8 && !kF8S ? 2 : 1);    // widened E4M3: two warps
             mbar_init(&k_empty[i], 1);
-            mbar_init(&v_full[i], kFp8 ? 2 : 1);
+            mbar_init(&v_full[i], kFp8 && !kF8S ? 2 : 1);
             mbar_init(&v_empty[i], 1);
         }
         mbar_init(&s_full[0], 1);
@@ -636,7 +693,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         mbar_init(q_ready, kTcSoftmaxThreads);
-        if constexpr (kFp8) {
+        if constexpr (kF8S) mbar_init(q_land, 1);
+        if constexpr (kFp8 && !kF8S) {
             for (int i = 0; i < 4; ++i) {
                 mbar_init(&k_staged[i], 1);
                 mbar_init(&v_staged[i], 1);
@@ -646,6 +704,23 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         fence_barrier_init();
         tma_prefetch_map(&tp.k_map);
         tma_prefetch_map(&tp.v_map);
+    }
+    if constexpr (kF8S) {
+        // E4M3 products: the query rows arrive by bulk copies, one per token
+        // (its G heads' rows are contiguous), token-major into the query
+        // region, converted in place below
+        if (warp == kTcKWarp) {
+            const uint32_t tok_bytes = (uint32_t)(p.group * D * sizeof(QT));
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(q_land, (uint32_t)ntok * tok_bytes);
+            __syncwarp();
+            const QT* qbase = reinterpret_cast<const QT*>(p.query);
+            for (int i = lane; i < ntok; i += 32) {
+                const QT* src = qbase + ((size_t)(q0 + tok0 + i) * p.num_q_heads +
+                                         (size_t)hk * p.group) * D;
+                bulk_copy_g2s(sm + Sh::kQOff + i * tok_bytes, src, tok_bytes, q_land);
+            }
+        }
     }
     if (warp == kTcMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -657,7 +732,81 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int G = p.group;
-    if (tid < kTcSoftmaxThreads) {
+    float q_row_mul = 1.f;                                   // E4M3 products: the row's inverse scale
+    if constexpr (kF8S) {
+        if (tid < kTcSoftmaxThreads) {
+            // Each row times a power of two that puts its largest |element|
+            // in [128, 256), as hi = the value rounded to E4M3's four
+            // significant bits (integer operations, ties to even; exact in
+            // E4M3 there) and lo = E4M3(value - hi), stored K-major with one
+            // 128-byte swizzled span per row, hi then lo, over the landed
+            // 16-bit rows once every thread has read its row. Both threads of
+            // a row read all of it (the scale needs its maximum) and convert
+            // their half of its chunks; each visits its half's chunks from
+            // chunk r mod 8 on, so rows 256 bytes apart spread over the banks.
+            const int r = tid & (kTcRows - 1);
+            const int hf = tid / kTcRows;
+            const bool live_row = r / G < ntok;
+            const bool okq = tc_wait(q_land, 0u, p.status, abort_flag);
+            const uint8_t* qs8 = sm + Sh::kQOff + r * (D * 2);
+            uint4 qv[D / 8];                                 // [0, 8): this half's chunks
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const int cc = ((c >> 3) ^ hf) * 8 + ((c + r) & 7);
+                qv[c] = live_row && okq ? *reinterpret_cast<const uint4*>(qs8 + cc * 16)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+            }
+            named_barrier(3, kTcSoftmaxThreads);             // every row read before any is overwritten
+            uint32_t m2 = 0u;                                // 16-bit magnitudes order as integers
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                m2 = __vmaxu2(m2, qv[c].x & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].y & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].z & 0x7FFF7FFFu);
+                m2 = __vmaxu2(m2, qv[c].w & 0x7FFF7FFFu);
+            }
+            const float mx = unpack2<QT>(max(m2 & 0xFFFFu, m2 >> 16)).x;
+            int ex = 0;
+            (void)frexpf(mx, &ex);                           // mx = m 2^ex, m in [0.5, 1)
+            const float qsc = mx > 0.f ? ldexpf(1.f, 8 - max(ex, -100)) : 1.f;
+            q_row_mul = 1.f / qsc;
+            auto round4 = [](float y) -> float {
+                uint32_t b = __float_as_uint(y);
+                b += 0x7FFFFu + ((b >> 20) & 1u);
+                return __uint_as_float(b & 0xFFF00000u);
+            };
+            uint8_t* qd = sm + Sh::kQOff;
+#pragma unroll
+            for (int c = 0; c < D / 16; ++c) {
+                const uint32_t in[4] = {qv[c].x, qv[c].y, qv[c].z, qv[c].w};
+                uint32_t hw[2], lw[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    uint32_t h4 = 0u, l4 = 0u;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float2 f2 = unpack2<QT>(in[2 * e + u]);
+                        const float y0 = f2.x * qsc, y1 = f2.y * qsc;
+                        const float h0 = round4(y0), h1 = round4(y1);
+                        const __nv_fp8x2_storage_t hc =
+                            __nv_cvt_float2_to_fp8x2(make_float2(h0, h1), __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t lc = __nv_cvt_float2_to_fp8x2(
+                            make_float2(y0 - h0, y1 - h1), __NV_SATFINITE, __NV_E4M3);
+                        h4 |= (uint32_t)hc << (16 * u);
+                        l4 |= (uint32_t)lc << (16 * u);
+                    }
+                    hw[e] = h4;
+                    lw[e] = l4;
+                }
+                const int cc = hf * 8 + ((c + r) & 7);           // the chunk qv[c] holds
+                const uint32_t off = (uint32_t)(r * 128 + ((((cc * 8) >> 4) ^ (r & 7)) << 4) + ((cc * 8) & 15));
+                *reinterpret_cast<uint2*>(qd + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(qd + Sh::kQTermBytes + off) = make_uint2(lw[0], lw[1]);
+            }
+            fence_async_smem();
+            mbar_arrive(q_ready);
+        }
+    } else if (tid < kTcSoftmaxThreads) {
         // rows (token, head) of the tile; padding rows are zero. All of a
         // thread's loads are in flight before the first store.
         const QT* qbase = reinterpret_cast<const QT*>(p.query);
@@ -703,18 +852,26 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     // warpgroups (every warp of a warpgroup runs the same instruction, before
     // the warps part ways)
     if constexpr (kFp8) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTcProducerRegs));
-    if (warp == kTcKWarp || (kFp8 && warp == kTcK2Warp)) {
+    if (warp == kTcKWarp || (kFp8 && !kF8S && warp == kTcK2Warp)) {
         // ------------------------------------------------------------ K loads
-        if constexpr (kFp8)
+        if constexpr (kF8S) {
+            tc_load_ring<TcRingE4M3, NS>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk,
+                                         ntiles, kend, lane, first, abort_flag);
+            // the query copies this warp issued land before the CTA ends
+            if (lane == 0) mbar_wait_bounded(q_land, 0u, p.status);
+        } else if constexpr (kFp8)
             tc_load_widen_halves<N, D, NS>(tp, &tp.k_map, sm + Sh::kK8Off, sm + Sh::kKOff,
                                            k_staged, k_full, k_empty, s, hk, ntiles, kend,
                                            warp == kTcKWarp ? 0 : 1, lane, abort_flag);
         else
             tc_load_ring<Sh, NS>(tp, &tp.k_map, sm + Sh::kKOff, k_full, k_empty, s, hk, ntiles,
                                  kend, lane, first, abort_flag);
-    } else if (warp == kTcVWarp || (kFp8 && warp == kTcV2Warp)) {
+    } else if (warp == kTcVWarp || (kFp8 && !kF8S && warp == kTcV2Warp)) {
         // ------------------------------------------------------------ V loads
-        if constexpr (kFp8)
+        if constexpr (kF8S)
+            tc_load_ring<TcRingE4M3, NS>(tp, &tp.v_map, sm + Sh::kVOff, v_full, v_empty, s, hk,
+                                         ntiles, kend, lane, first, abort_flag);
+        else if constexpr (kFp8)
             tc_load_widen_halves<N, D, NS>(tp, &tp.v_map, sm + Sh::kV8Off, sm + Sh::kVOff,
                                            v_staged, v_full, v_empty, s, hk, ntiles, kend,
                                            warp == kTcVWarp ? 0 : 1, lane, abort_flag);
@@ -732,12 +889,26 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 if (!tc_wait(&k_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag)) return false;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(sm + Sh::kKOff + st * Sh::kKvBytes);
+                const uint32_t sc = tmem + Sh::kSCol + (j & 1) * N;
+                if constexpr (kF8S) {
+                    // the query's two terms against the E4M3 K tile, 32 codes a step
+                    constexpr uint32_t idS8 = tc_idesc_e4m3(kTcRows, N);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (uint32_t)(kk & 3) * 32u;
-                    const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
-                    const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
-                    tc_mma(tmem + Sh::kSCol + (j & 1) * N, a, b, idS, kk > 0);
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint64_t a = tc_desc(qa + u * Sh::kQTermBytes + kk * 32, 16, 1024);
+                            const uint64_t b = tc_desc(ka + kk * 32, 16, 1024);
+                            tc_mma_e4m3(sc, a, b, idS8, u > 0 || kk > 0);
+                        }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(kk & 3) * 32u;
+                        const uint64_t a = tc_desc(qa + (kk >> 2) * (kTcRows * 128) + off, 16, 1024);
+                        const uint64_t b = tc_desc(ka + (kk >> 2) * (N * 128) + off, 16, 1024);
+                        tc_mma(sc, a, b, idS, kk > 0);
+                    }
                 }
                 tc_commit(&k_empty[st]);
                 tc_commit(&s_full[j & 1]);
@@ -750,10 +921,24 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 tc_fence_after();
                 const uint32_t va = smem_u32(sm + Sh::kVOff + st * Sh::kKvBytes);
                 const uint32_t pt = tmem + Sh::kSCol + (j & 1) * N;   // P_hi | P_lo
+                if constexpr (kF8S) {
+                    // the weights' two E4M3 terms (32 columns each) against
+                    // the E4M3 V tile as an MN-major operand, 32 keys a step
+                    constexpr uint32_t idO8 = tc_idesc_e4m3(kTcRows, D, 1);
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                    const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
-                    tc_mma_ts(tmem + Sh::kOCol, pt + kk * 8, b, idO, j > 0 || kk > 0);
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int kk = 0; kk < N / 32; ++kk) {
+                            const uint64_t b = tc_desc(va + kk * 32 * 128, N * 128, 1024);
+                            tc_mma_e4m3_ts(tmem + Sh::kOCol, pt + u * (N / 4) + kk * 8, b, idO8,
+                                           j > 0 || u > 0 || kk > 0);
+                        }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < N / 16; ++kk) {
+                        const uint64_t b = tc_desc(va + kk * 2048, N * 128, 1024);
+                        tc_mma_ts(tmem + Sh::kOCol, pt + kk * 8, b, idO, j > 0 || kk > 0);
+                    }
                 }
                 if constexpr (kTcPLo<MT>) {
 #pragma unroll
@@ -793,7 +978,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         const int i = r / G;
         const bool row_valid = i < ntok && r < Tq * G;
         const int pos = first_pos + (row_valid ? i : ntok - 1);
-        const float qm = p.q_mul;
+        const float qm = p.q_mul * q_row_mul;                // E4M3 products: the row's scale out
         const float2 qm2 = make_float2(qm, qm);
         float m = -INFINITY;                                 // running max (base 2, scaled)
         float l = 0.f;                                       // this half's running sum
@@ -837,7 +1022,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
 #pragma unroll
                 for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
             const float m_cand = fmaxf(m, mr[0] * qm);
-            const bool rescale = m_cand > m + kTcRescaleLog2;
+            const bool rescale = m_cand > m + (kF8S ? kTcRescaleLog2E4M3 : kTcRescaleLog2);
             const float m_use = rescale ? m_cand : m;
             const float alpha = fast_exp2(m - m_use);        // 0 on the first tile, 1 if kept
             const float2 nm2 = make_float2(-m_use, -m_use);
@@ -860,8 +1045,48 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                     }
                 }
             };
-            if (hf == 0) weights(std::integral_constant<int, 0>{});
-            else weights(std::integral_constant<int, NH>{});
+            // E4M3 products: y = P 2^6 (the 2^6 in the exponent) as hi =
+            // E4M3(y) and lo = E4M3(y - hi), the remainder taken in binary16;
+            // four codes per 32-bit column, hi in columns [0, N/4) and lo in
+            // [N/4, N/2) of the buffer, this half's keys a half of each; its
+            // two quarters of 32 keys stored one after the other
+            auto weights8 = [&](auto off) {
+                constexpr int c0 = decltype(off)::value;
+                const float2 nm8 = make_float2(kTcWeightLog2E4M3 - m_use, kTcWeightLog2E4M3 - m_use);
+#pragma unroll
+                for (int h = 0; h < NH / 32; ++h) {
+                    uint32_t hq8[8], lq8[8];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const int cc = c0 + h * 32 + c;
+                        uint32_t hq = 0u, lq = 0u;
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const float2 t2 = __ffma2_rn(make_float2(x[cc + 2 * u], x[cc + 2 * u + 1]), qm2, nm8);
+                            const float2 y = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
+                            sr[(c / 2 + u) % (R / 2)] = __fadd2_rn(sr[(c / 2 + u) % (R / 2)], y);
+                            const __nv_fp8x2_storage_t hc = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
+                            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hc, __NV_E4M3);
+                            const __half2 rem = __hsub2(__float22half2_rn(y), *reinterpret_cast<const __half2*>(&hr));
+                            const __nv_fp8x2_storage_t lc = __nv_cvt_halfraw2_to_fp8x2(
+                                *reinterpret_cast<const __half2_raw*>(&rem), __NV_SATFINITE, __NV_E4M3);
+                            hq |= (uint32_t)hc << (16 * u);
+                            lq |= (uint32_t)lc << (16 * u);
+                        }
+                        hq8[c / 4] = hq;
+                        lq8[c / 4] = lq;
+                    }
+                    tc_st_n<8>(sbuf + c0 / 4 + h * 8, hq8);
+                    tc_st_n<8>(sbuf + N / 4 + c0 / 4 + h * 8, lq8);
+                }
+            };
+            if constexpr (kF8S) {
+                if (hf == 0) weights8(std::integral_constant<int, 0>{});
+                else weights8(std::integral_constant<int, NH>{});
+            } else {
+                if (hf == 0) weights(std::integral_constant<int, 0>{});
+                else weights(std::integral_constant<int, NH>{});
+            }
 #pragma unroll
             for (int w = R / 4; w >= 1; w /= 2)
 #pragma unroll
@@ -870,8 +1095,10 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             m = m_use;
             // P over S in the same buffer: P_hi pairs in columns [0, N/2), P_lo
             // in [N/2, N); this half's keys are a quarter of the buffer each
-            tc_st_n<NH / 2>(sbuf + hf * (NH / 2), phi);
-            if constexpr (kTcPLo<MT>) tc_st_n<NH / 2>(sbuf + N / 2 + hf * (NH / 2), plo);
+            if constexpr (!kF8S) {
+                tc_st_n<NH / 2>(sbuf + hf * (NH / 2), phi);
+                if constexpr (kTcPLo<MT>) tc_st_n<NH / 2>(sbuf + N / 2 + hf * (NH / 2), plo);
+            }
             if (j > 0 && __any_sync(0xffffffffu, rescale)) {
                 // O holds tiles < j once the previous P.V is done; each half
                 // rescales its half of the columns
@@ -900,7 +1127,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 const int first = kend - key0;
-                constexpr int CPR = D / 8;
+                constexpr int CPR = kF8S ? 8 : D / 8;            // 16-byte chunks of a V row
                 uint8_t* vd = sm + Sh::kVOff + st * Sh::kKvBytes;
                 for (int idx = tid; idx < (N - first) * CPR; idx += kTcSoftmaxThreads) {
                     const int rr = first + idx / CPR, c = idx % CPR;
@@ -916,7 +1143,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         float* lsum = reinterpret_cast<float*>(sm + Sh::kLsumOff);
         lsum[tid] = l;
         named_barrier(1, kTcSoftmaxThreads);
-        // E4M3: the values were widened without their scale; it comes in here
+        // E4M3: V's scale comes in here (the widened tiles also lack 2^8, the
+        // E4M3 products' weights carry 2^6 as the row sums do)
         const float inv = p.v_mul / (lsum[r] + lsum[r + kTcRows]);
         if (ok) {
             ok = tc_wait(drain, 0u, p.status, abort_flag);
@@ -1047,26 +1275,6 @@ struct TcShape2E4M3Scores {
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
     static_assert(2 * kAlloc > 228 * 1024, "one CTA per SM");
 };
-// Weights of the E4M3 products are y = P 2^6 <= 448: the softmax rescales O
-// whenever the row's maximum has grown by more than log2(448 / 64) = 2.8,
-// and y below E4M3's normal range (P < 2^-12) keeps an absolute error under
-// 2^-16 in P.
-constexpr int kTcWeightLog2E4M3 = 6;
-constexpr float kTcRescaleLog2E4M3 = 2.8f;
-// The E4M3 K ring as tc_load_ring sees it: one 128-byte span per key.
-struct TcRingE4M3 {
-    static constexpr int N = 128;
-    static constexpr int kSpans = 1;
-    static constexpr int kKvBytes = N * 128;
-};
-// Whether the two-tile kernel takes E4M3 scores: E4M3 cache, head size 128,
-// bf16 query (its 8 significant bits are exactly the two E4M3 terms; an f16
-// query's 11 are not, and a test with rows up to 32 times N(0,1) measured
-// errors of 7e-2 that way, so f16 queries keep the widened K).
-template <typename QT, typename CT, int D>
-constexpr bool kTc2E4M3Scores =
-    std::is_same<CT, e4m3_t>::value && D == 128 && std::is_same<QT, __nv_bfloat16>::value;
-
 // Two query tiles per CTA: warps 0-3 run the softmax of tile 0, warps 4-7 of
 // tile 1, each thread a whole row of 128 keys. The MMA issuer interleaves the
 // tiles -- S0_0, S1_0, PV0_0, S0_1, PV1_0, S1_1, PV0_1, ... -- so one tile's
@@ -1083,7 +1291,7 @@ __global__ void __launch_bounds__(std::is_same<CT, e4m3_t>::value ? kTcThreadsFp
 paged_prefill_tc2_kernel(const __grid_constant__ TcPrefillParams tp) {
     using T = typename TcMath<QT, CT>::T;                    // MMA operand type
     constexpr bool kFp8 = std::is_same<CT, e4m3_t>::value;
-    constexpr bool kF8S = kTc2E4M3Scores<QT, CT, D>;          // E4M3 scores (kind::f8f6f4)
+    constexpr bool kF8S = kTcE4M3Products<QT, CT, D>;          // E4M3 scores (kind::f8f6f4)
     using Sh = std::conditional_t<kF8S, TcShape2E4M3Scores, TcShape2<D, kTcPLo<T>, kFp8>>;
     constexpr int N = Sh::N;
     constexpr int NSK = Sh::NSK;                             // K ring stages
@@ -1713,16 +1921,16 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, int head_size, cudaStream_
 }
 
 // E4M3 caches (head size 64 or 128): two query tiles per CTA when sequences
-// have at least two, else the one-tile kernel. The V map (and K's, where K
-// is widened) views the cache as [num_blocks*Hkv*B rows][D bytes] with plain
-// (unswizzled) boxes of min(B, 64) rows within one block segment; with E4M3
-// scores (two tiles, head size 128, bf16 query) K's map has 128-byte
-// swizzled boxes of the same height, the layout the kind::f8f6f4 MMAs read.
+// have at least two, else the one-tile kernel. Both maps view the cache as
+// [num_blocks*Hkv*B rows][D bytes] with boxes of min(B, 64) rows within one
+// block segment: plain (unswizzled) where the tiles are widened to binary16,
+// 128-byte swizzled for the E4M3 products (head size 128, bf16 query), the
+// layout the kind::f8f6f4 MMAs read.
 template <typename QT>
 cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaStream_t stream) {
     TcPrefillParams tp;
     tp.p = p;
-    const bool e4m3_scores = kTc2E4M3Scores<QT, e4m3_t, 128> && head_size == 128 && p.q_tiles >= 2;
+    const bool e4m3_scores = kTcE4M3Products<QT, e4m3_t, 128> && head_size == 128;
     // the widened tiles hold K and V times 2^-8 (e4m3x2_spread_to_f16x2_scaled);
     // the E4M3 products read K and V as they are stored (their weights carry
     // a power of two that the row sums carry too)
@@ -1742,12 +1950,13 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
         e = e4m3_scores ? encode_cache_map(&tp.v_map, p.v_cache, 1, head_size, rows, tp.box_rows)
                         : encode_plain_map(&tp.v_map, p.v_cache, head_size, rows, tp.box_rows);
     if (e != cudaSuccess) return e;
-    static_assert(TcShape2E4M3Scores::N == n && TcShape2<64, false, true>::N == n,
-                  "the two-tile kernel's box height");
+    static_assert(TcShape2E4M3Scores::N == n && TcShape2<64, false, true>::N == n &&
+                      TcShapeE4M3Products::N == n,
+                  "the kernels' box height");
     auto go = [&](auto dtag) -> cudaError_t {
         constexpr int D = decltype(dtag)::value;
         if (p.q_tiles >= 2) {
-            using Sh2 = std::conditional_t<kTc2E4M3Scores<QT, e4m3_t, D>, TcShape2E4M3Scores,
+            using Sh2 = std::conditional_t<kTcE4M3Products<QT, e4m3_t, D>, TcShape2E4M3Scores,
                                            TcShape2<D, false, true>>;
             auto kern2 = paged_prefill_tc2_kernel<QT, e4m3_t, D>;
             cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern2), Sh2::kAlloc);
@@ -1757,7 +1966,8 @@ cudaError_t launch_prefill_tc_e4m3(const PrefillParams& p, int head_size, cudaSt
             kern2<<<(unsigned)units, kTcThreadsFp8, Sh2::kAlloc, stream>>>(tp);
             return cudaGetLastError();
         }
-        using Sh = TcShape<D, true>;
+        using Sh = std::conditional_t<kTcE4M3Products<QT, e4m3_t, D>, TcShapeE4M3Products,
+                                      TcShape<D, true>>;
         auto kern = paged_prefill_tc_kernel<QT, e4m3_t, D>;
         cudaError_t e2 = ensure_smem_attribute(reinterpret_cast<const void*>(kern), Sh::kAlloc);
         if (e2 != cudaSuccess) return e2;

@@ -77,5 +77,6 @@ def test_prefill_kernel_names_follow_the_library():
     c5 = config_case(5, num_seqs=8)
     assert "E4M3" in bench.prefill_kernel_name(c5, 2)
     assert bench.prefill_kernel_name(c5, 16).startswith("paged_prefill_tc_kernel")
+    assert "E4M3 products" in bench.prefill_kernel_name(c5, 16)
     assert bench.prefill_kernel_name(c5, 256).startswith("paged_prefill_tc2_kernel")
-    assert "E4M3" in bench.prefill_kernel_name(c5, 256)
+    assert "E4M3 products" in bench.prefill_kernel_name(c5, 256)

@@ -51,8 +51,9 @@ def test_decode_step_graph_replay(cfg):
 
 
 @pytest.mark.parametrize("cfg,qn,ordered", [(3, 100, False), (3, 4, False), (3, 8, True),
-                                             (5, 100, False)],
-                         ids=["tcgen05", "warp-mma", "warp-mma2-ordered", "tcgen05-e4m3-products"])
+                                             (5, 100, False), (5, 16, True)],
+                         ids=["tcgen05", "warp-mma", "warp-mma2-ordered", "tcgen05-e4m3-products",
+                              "tcgen05-one-tile-e4m3-products-ordered"])
 def test_multi_query_graph_replay(cfg, qn, ordered):
     c = W.config_case(cfg, num_seqs=16)
     q = W.make_queries(c, ("fixed", np.minimum(qn, c.context_lens)))

@@ -161,10 +161,11 @@ SIMT_SWEEP = [
     (2, 8, 4, 64, 96, "f16", "f16", ("fixed", [95, 250]), ("uniform", 1, 9)),
 ]
 
-# E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory):
-# one query tile per sequence (the one-tile kernel) and two or more (the
-# two-tile kernel, odd tile counts leaving a single last tile), block sizes
-# 8..256, groups that do not divide the 128-row tile
+# E4M3 caches on the tensor cores (K/V widened to binary16 in shared memory;
+# with a bf16 query at head size 128, the E4M3 products): one query tile per
+# sequence (the one-tile kernel) and two or more (the two-tile kernel, odd
+# tile counts leaving a single last tile), block sizes 8..256, groups that do
+# not divide the 128-row tile
 E4M3_TC_SWEEP = [
     (3, 8, 1, 128, 16, "bf16", ("uniform", 20, 300), ("uniform", 1, 40)),
     (2, 6, 2, 64, 32, "f16", ("uniform", 40, 200), ("all",)),
@@ -177,6 +178,13 @@ E4M3_TC_SWEEP = [
     # 8-row and 64-row (block size 256, capped) boxes
     (3, 16, 2, 128, 8, "bf16", ("uniform", 100, 400), ("uniform", 20, 60)),
     (3, 16, 2, 128, 256, "bf16", ("uniform", 200, 700), ("uniform", 20, 90)),
+    # the same on one query tile (the one-tile kernel): G = 8 with up to 16
+    # tokens (128 rows), 8-, 16- and 64-row boxes; G = 3 with up to 42 tokens
+    # (two padding rows)
+    (4, 32, 4, 128, 16, "bf16", ("uniform", 20, 700), ("uniform", 1, 16)),
+    (3, 16, 2, 128, 8, "bf16", ("uniform", 100, 400), ("uniform", 1, 16)),
+    (3, 16, 2, 128, 256, "bf16", ("uniform", 200, 700), ("uniform", 1, 16)),
+    (3, 12, 4, 128, 64, "bf16", ("fixed", [42, 129, 500]), ("uniform", 1, 42)),
 ]
 
 
@@ -188,10 +196,11 @@ def test_prefill_e4m3_tensor_core_sweep(i):
     check(c, ql, f"e4m3 tc sweep {i}", force_tc=True)
 
 
+@pytest.mark.parametrize("tiles", ["one", "two"])
 @pytest.mark.parametrize("qt", ["bf16", "f16"])
-def test_e4m3_scores_query_magnitudes(qt):
-    """The two-tile kernel on an E4M3 cache at head size 128. A bf16 query
-    takes the E4M3 scores: each row goes to the tensor cores as two E4M3
+def test_e4m3_scores_query_magnitudes(qt, tiles):
+    """Both tcgen05 kernels on an E4M3 cache at head size 128. A bf16 query
+    takes the E4M3 products: each row goes to the tensor cores as two E4M3
     terms of the row times a power of two. An f16 query (11 significant bits,
     more than two E4M3 terms hold) keeps the widened K. Rows scaled by powers
     of two over a wide range, all-zero rows, and rows of one large element
@@ -200,7 +209,7 @@ def test_e4m3_scores_query_magnitudes(qt):
     c = make_case(num_seqs=3, num_q_heads=16, num_kv_heads=2, head_size=128, block_size=16,
                   q_dtype=qt, cache_dtype="e4m3", kv_dtype=qt, lengths=("uniform", 200, 500),
                   seed=981)
-    p = Prefill(c, ("uniform", 40, 80))
+    p = Prefill(c, ("uniform", 1, 16) if tiles == "one" else ("uniform", 40, 80))
     rows = p.q.query.reshape(-1, 128)
     x = oracle.decode_array(rows, qt)
     rng = np.random.default_rng(982)
@@ -214,7 +223,7 @@ def test_e4m3_scores_query_magnitudes(qt):
     p.query = host_to_torch(p.q.query, qt).to(p.query.device)
     assert pk.prefill_kernel(tc_bound(p), c.num_q_heads, c.num_kv_heads, 128, 16, c.num_blocks,
                              pk.PA_BF16 if qt == "bf16" else pk.PA_F16,
-                             pk.PA_FP8_E4M3) == "tc_two_tiles"
+                             pk.PA_FP8_E4M3) == ("tc" if tiles == "one" else "tc_two_tiles")
     got = to_f64(p.run(tc_bound(p)))
     assert p.dc.status_bits() == 0
     idx, want = p.oracle()
@@ -478,6 +487,22 @@ def test_full_size_shared_prefix_e4m3():
     want = p.oracle_rows(rows)
     assert_decode_close(got[rows], want, c, f"full: shared-prefix e4m3 256-token chunks, "
                                             f"{len(rows)} of {int(p.q.query_start[-1])} rows")
+
+
+def test_full_size_shared_prefix_e4m3_draft_tokens():
+    """The shared-prefix E4M3 pool with 8 draft tokens per sequence forced
+    onto the one-tile tcgen05 kernel (the E4M3 products; 64 of a tile's 128
+    rows at G = 8): every row against the oracle."""
+    c = config_case(5)
+    p = Prefill(c, ("fixed", np.minimum(8, c.context_lens)))
+    assert pk.prefill_kernel(tc_bound(p), c.num_q_heads, c.num_kv_heads, c.head_size,
+                             c.block_size, c.num_blocks, pk.PA_BF16, pk.PA_FP8_E4M3) == "tc"
+    got = to_f64(p.run(tc_bound(p)))
+    assert p.dc.status_bits() == 0
+    rows = np.arange(int(p.q.query_start[-1]))
+    want = p.oracle_rows(rows)
+    assert_decode_close(got[rows], want, c, f"full: shared-prefix e4m3 8 draft tokens, "
+                                            f"{len(rows)} rows")
 
 
 def test_full_size_llama7b_mha_f16():
