@@ -31,8 +31,10 @@
 // Softmax. Warps 0-7: a TMEM lane (row) is readable by warps w and w + 4, so
 // thread t takes row t mod 128 and half t / 128 of the tile's key columns;
 // two warps per SM sub-partition hide each other's latencies. Both halves
-// load the whole row of S, apply the causal mask and take its max, so they
-// keep the same running max m (base 2) and make the same rescale decisions;
+// take the max of the whole masked row of S (each loads the whole row, or,
+// with the E4M3 products, its own columns, and the halves trade their
+// maxima through two spare TMEM columns per score buffer), so they keep the
+// same running max m (base 2) and make the same rescale decisions;
 // each exponentiates its own columns, keeps their running sum, and stores
 // their weights P over the same TMEM buffer. O is rescaled in TMEM (each half its
 // half of the columns) only when the max has grown by more than 2^8 since the
@@ -261,6 +263,17 @@ __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t* r) {
         ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
           "r"(r[6]), "r"(r[7])
         : "memory");
+}
+// One 32-bit TMEM column of this thread's lane: store, and load with its
+// wait (the register is tied to the wait, so no use moves above it).
+__device__ __forceinline__ void tc_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t tc_ld1_wait(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(v)::"memory");
+    return v;
 }
 template <int NC>
 __device__ __forceinline__ void tc_st_n(uint32_t taddr, const uint32_t* r) {
@@ -607,6 +620,8 @@ struct TcShapeE4M3Products {
     static constexpr int kTmemCols = 512;
     static constexpr int kSCol = 0;
     static constexpr int kOCol = 2 * N;
+    static constexpr int kXCol = kOCol + D;                  // row-max exchange: [tile parity][half]
+    static_assert(kXCol + 4 <= kTmemCols, "TMEM columns");
     static_assert(kQBytes == kTcRows * D * 2, "the bf16 query rows land in the E4M3 region");
     static_assert(2 * N + D <= kTmemCols, "TMEM columns");
     static_assert(kAlloc <= kTcSmemLimit, "shared memory");
@@ -735,6 +750,8 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     float q_row_mul = 1.f;                                   // E4M3 products: the row's inverse scale
     if constexpr (kF8S) {
         if (tid < kTcSoftmaxThreads) {
+            // the softmax warpgroups' registers, taken before the conversion
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcSoftmaxRegs));
             // Each row times a power of two that puts its largest |element|
             // in [128, 256), as hi = the value rounded to E4M3's four
             // significant bits (integer operations, ties to even; exact in
@@ -966,11 +983,13 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
     }
     } else {
         // ------------------------------------------------------------ softmax (rows)
-        if constexpr (kFp8) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcSoftmaxRegs));
+        if constexpr (kFp8 && !kF8S) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTcSoftmaxRegs));
         // Thread t: row r = t mod 128 (its warp's TMEM lane quarter), half
-        // hf = t / 128 of the key columns. Both halves read the whole row to
-        // take the same max, so they make the same rescale decision; each
-        // exponentiates, sums and stores only its own columns.
+        // hf = t / 128 of the key columns. Both halves take the same row max
+        // (each reads the whole row; with the E4M3 products each reads its
+        // own columns and the halves trade their maxima through TMEM), so
+        // they make the same rescale decision; each exponentiates, sums and
+        // stores only its own columns.
         constexpr int NH = N / 2;
         const int r = tid & (kTcRows - 1);
         const int hf = tid / kTcRows;
@@ -990,6 +1009,46 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
+            const int key0 = j * N;
+            constexpr int R = 8;
+            float m_row;                                     // the row's max of S over this tile
+            float x[kF8S ? NH : N];
+            if constexpr (kF8S) {
+                // this half's columns only; the halves trade their maxima
+                // through TMEM columns kXCol + 2 (j mod 2) + half (a column
+                // is rewritten two tiles on, after the partner's read of it
+                // has passed the barrier of the tile between)
+                uint32_t xr[NH];
+#pragma unroll
+                for (int c = 0; c < NH; c += 32)
+                    tc_ld32(sbuf + hf * NH + c, *reinterpret_cast<uint32_t(*)[32]>(xr + c));
+                tc_wait_ld();
+#pragma unroll
+                for (int c = 0; c < NH; ++c) x[c] = __uint_as_float(xr[c]);
+                if (key0 + N - 1 > pos) {                    // the causal edge crosses this tile
+#pragma unroll
+                    for (int c = 0; c < NH; ++c)
+                        if (key0 + hf * NH + c > pos) x[c] = -INFINITY;
+                }
+                float mr[R];
+#pragma unroll
+                for (int k = 0; k < R; ++k) mr[k] = x[k];
+#pragma unroll
+                for (int c = R; c + 1 < NH; c += 2) mr[(c / 2) % R] = fmax3(mr[(c / 2) % R], x[c], x[c + 1]);
+#pragma unroll
+                for (int w = R / 2; w >= 1; w /= 2)
+#pragma unroll
+                    for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
+                const uint32_t xcol = lane_base + Sh::kXCol + 2 * (j & 1);
+                tc_st1(xcol + hf, __float_as_uint(mr[0]));
+                tc_wait_st();
+                // the other half of this row must also have read its S before
+                // either half writes its weights over the buffer
+                tc_fence_before();
+                named_barrier(2, kTcSoftmaxThreads);
+                tc_fence_after();
+                m_row = fmaxf(mr[0], __uint_as_float(tc_ld1_wait(xcol + (hf ^ 1))));
+            } else {
             // the whole row in flight at once, one wait
             uint32_t xr[N];
 #pragma unroll
@@ -1001,17 +1060,14 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             tc_fence_before();
             named_barrier(2, kTcSoftmaxThreads);
             tc_fence_after();
-            float x[N];
 #pragma unroll
             for (int c = 0; c < N; ++c) x[c] = __uint_as_float(xr[c]);
-            const int key0 = j * N;
             if (key0 + N - 1 > pos) {                        // the causal edge crosses this tile
 #pragma unroll
                 for (int c = 0; c < N; ++c)
                     if (key0 + c > pos) x[c] = -INFINITY;
             }
             // the max as 8 independent chains
-            constexpr int R = 8;
             float mr[R];
 #pragma unroll
             for (int k = 0; k < R; ++k) mr[k] = x[k];
@@ -1021,7 +1077,9 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             for (int w = R / 2; w >= 1; w /= 2)
 #pragma unroll
                 for (int k = 0; k < w; ++k) mr[k] = fmaxf(mr[k], mr[k + w]);
-            const float m_cand = fmaxf(m, mr[0] * qm);
+            m_row = mr[0];
+            }
+            const float m_cand = fmaxf(m, m_row * qm);
             const bool rescale = m_cand > m + (kF8S ? kTcRescaleLog2E4M3 : kTcRescaleLog2);
             const float m_use = rescale ? m_cand : m;
             const float alpha = fast_exp2(m - m_use);        // 0 on the first tile, 1 if kept
@@ -1050,19 +1108,18 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
             // four codes per 32-bit column, hi in columns [0, N/4) and lo in
             // [N/4, N/2) of the buffer, this half's keys a half of each; its
             // two quarters of 32 keys stored one after the other
-            auto weights8 = [&](auto off) {
-                constexpr int c0 = decltype(off)::value;
+            auto weights8 = [&](const float (&xh)[NH]) {
                 const float2 nm8 = make_float2(kTcWeightLog2E4M3 - m_use, kTcWeightLog2E4M3 - m_use);
 #pragma unroll
                 for (int h = 0; h < NH / 32; ++h) {
                     uint32_t hq8[8], lq8[8];
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
-                        const int cc = c0 + h * 32 + c;
+                        const int cc = h * 32 + c;
                         uint32_t hq = 0u, lq = 0u;
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const float2 t2 = __ffma2_rn(make_float2(x[cc + 2 * u], x[cc + 2 * u + 1]), qm2, nm8);
+                            const float2 t2 = __ffma2_rn(make_float2(xh[cc + 2 * u], xh[cc + 2 * u + 1]), qm2, nm8);
                             const float2 y = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
                             sr[(c / 2 + u) % (R / 2)] = __fadd2_rn(sr[(c / 2 + u) % (R / 2)], y);
                             const __nv_fp8x2_storage_t hc = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
@@ -1076,13 +1133,12 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                         hq8[c / 4] = hq;
                         lq8[c / 4] = lq;
                     }
-                    tc_st_n<8>(sbuf + c0 / 4 + h * 8, hq8);
-                    tc_st_n<8>(sbuf + N / 4 + c0 / 4 + h * 8, lq8);
+                    tc_st_n<8>(sbuf + hf * (NH / 4) + h * 8, hq8);
+                    tc_st_n<8>(sbuf + N / 4 + hf * (NH / 4) + h * 8, lq8);
                 }
             };
             if constexpr (kF8S) {
-                if (hf == 0) weights8(std::integral_constant<int, 0>{});
-                else weights8(std::integral_constant<int, NH>{});
+                weights8(x);
             } else {
                 if (hf == 0) weights(std::integral_constant<int, 0>{});
                 else weights(std::integral_constant<int, NH>{});
