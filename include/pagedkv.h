@@ -421,7 +421,8 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  Other arguments as pa_decode; scale must be > 0.
  *  Kernel selection, by the arguments alone: with max_queries_per_seq *
  *  (num_q_heads / num_kv_heads) query rows per sequence and KV head at most
- *  32 (head_size <= 128) or 16 (head_size 256), a 16-bit query with a cache
+ *  32 (head_size <= 128) or 16 (head_size 256; also 16 where the tcgen05
+ *  kernels below take the E4M3 products), a 16-bit query with a cache
  *  of its type or of E4M3 codes, on the shapes of the TMA decode
  *  (rows of 128, 256 or 512 bytes, block_size 8, 16 or a multiple of 32),
  *  the warp-level MMA kernels run, reading each sequence's K/V once for all
@@ -429,13 +430,13 @@ pa_status pa_decode_partitioned_static(void* out, const void* query, const void*
  *  16-bit query with a cache of the same type (head_size 64/128/256) or an
  *  E4M3 cache (head_size 64/128), a block_size that is a power of two in
  *  [8, 256] and a group of at most 128 heads runs on the tcgen05 tensor
- *  cores (with an E4M3 cache, a bf16 query, head_size 128 and two or more
- *  query tiles per sequence, both products take E4M3 operands: the query
- *  as two E4M3 terms of each row times a power of two, exact for bf16
- *  values in E4M3's normal range, and the softmax weights as two E4M3
- *  terms, relative error at most about 2^-8; else the E4M3 tiles are widened
- *  to binary16); other supported combinations run one query token per work
- *  unit on the CUDA cores. A sequence whose lengths
+ *  cores (with an E4M3 cache, a bf16 query and head_size 128, both products
+ *  take E4M3 operands -- the E4M3 products: the query as two E4M3 terms of
+ *  each row times a power of two, exact for bf16 values in E4M3's normal
+ *  range, and the softmax weights as two E4M3 terms, relative error at most
+ *  about 2^-8; else the E4M3 tiles are widened to binary16); other
+ *  supported combinations run one query token per work unit on the CUDA
+ *  cores. A sequence whose lengths
  *  break the rules above sets PA_DEV_BAD_LEN and its rows are unspecified.
  *  num_queries == 0 launches nothing.
  */

@@ -261,19 +261,28 @@ bool prefill_tc_eligible(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size, 
 }
 
 // The kernel pa_paged_prefill runs: the warp-level MMA kernels for up to 32
-// rows per (sequence, KV head) (16 at head size 256), else the tcgen05 ones
-// (two query tiles per CTA at head size <= 128 with at least two tiles per
-// sequence), else one query token per work unit on the CUDA cores. `aligned`: out, query and the caches are 16-byte aligned (the
-// tcgen05 rows).
+// rows per (sequence, KV head) (16 at head size 256, and 16 where the tcgen05
+// kernels take the E4M3 products: E4M3 cache, bf16 query, head size 128),
+// else the tcgen05 ones (two query tiles per CTA at head size <= 128 with at
+// least two tiles per sequence), else one query token per work unit on the
+// CUDA cores. `aligned`: out, query and the caches are 16-byte aligned (the
+// tcgen05 rows). With the E4M3 products the one-tile tcgen05 kernel beats the
+// two-n-tile warp-level one from 17 rows on (shared-prefix E4M3 pool at
+// G = 8: 24 rows 2.75 against 2.47 TB/s of logical bytes, 32 rows 2.78
+// against 2.43; at 16 rows the warp-level kernel, 3.26 against 2.75).
 pa_prefill_kernel prefill_kernel(pa_dtype q_dtype, pa_dtype cache_dtype, int head_size,
                                  int block_size, int group, int64_t num_blocks, int num_kv_heads,
                                  int max_queries, bool aligned) {
     const long long rows = (long long)max_queries * group;
-    if (rows <= prefill_mma_max_rows(head_size) &&
+    const bool tc = aligned && prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size,
+                                                   group, num_blocks, num_kv_heads);
+    const bool e4m3_products = tc && cache_dtype == PA_FP8_E4M3 && q_dtype == PA_BF16 &&
+                               head_size == 128;
+    const long long mma_rows = e4m3_products ? 16 : prefill_mma_max_rows(head_size);
+    if (rows <= mma_rows &&
         prefill_mma_eligible(q_dtype, cache_dtype, head_size, block_size, num_blocks, num_kv_heads))
         return rows <= 16 ? PA_PREFILL_MMA : PA_PREFILL_MMA_TWO_TILES;
-    if (aligned && prefill_tc_eligible(q_dtype, cache_dtype, head_size, block_size, group,
-                                       num_blocks, num_kv_heads)) {
+    if (tc) {
         const int per_tile = 128 / group;
         const int tiles = (max_queries + per_tile - 1) / per_tile;
         const bool two = head_size <= 128 && tiles >= 2;

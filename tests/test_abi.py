@@ -192,8 +192,11 @@ def test_paged_prefill_rejects_a_misshaped_order():
 def test_paged_prefill_kernel_selection(lib):
     """The kernel choice of pa_paged_prefill, host only: warp-level MMA up to
     32 rows per (sequence, KV head) (16 at head size 256), one or two n-tiles
-    per warp by 16 rows; tcgen05 above (two query tiles per CTA at head
-    size <= 128 with two or more tiles); CUDA cores for the
+    per warp by 16 rows, except where the tcgen05 kernels take the E4M3
+    products (E4M3 cache, bf16 query, head size 128: tcgen05 from 17 rows,
+    the two-n-tile kernel only where tcgen05 is not eligible, e.g. block
+    size 96); tcgen05 above (two query tiles per CTA at head size <= 128
+    with two or more tiles); CUDA cores for the
     other types and block sizes; -1 for what the call rejects."""
     from paged_kv_cache_141_gb300 import binding as pk
     B16, F16, F32, E4 = pk.PA_BF16, pk.PA_F16, pk.PA_F32, pk.PA_FP8_E4M3
@@ -209,7 +212,11 @@ def test_paged_prefill_kernel_selection(lib):
         ((512, 32, 8, 128, 16, B16, B16), "tc_two_tiles"),
         ((8, 32, 8, 128, 8, B16, B16), "mma_two_tiles"),
         ((2, 64, 8, 128, 16, B16, E4), "mma"),
-        ((4, 64, 8, 128, 16, B16, E4), "mma_two_tiles"),
+        ((3, 64, 8, 128, 16, B16, E4), "tc"),
+        ((4, 64, 8, 128, 16, B16, E4), "tc"),
+        ((4, 64, 8, 128, 96, B16, E4), "mma_two_tiles"),
+        ((4, 64, 8, 128, 16, F16, E4), "mma_two_tiles"),
+        ((8, 32, 8, 64, 16, B16, E4), "tc"),
         ((5, 64, 8, 128, 16, B16, E4), "tc"),
         ((16, 64, 8, 128, 16, B16, E4), "tc"),
         ((17, 64, 8, 128, 16, B16, E4), "tc_two_tiles"),

@@ -96,9 +96,16 @@ class Prefill:
 
 def mma_max_rows(case):
     """max_queries_per_seq * group up to this selects the warp-level MMA
-    kernels (32 at head size <= 128, 16 at 256); a larger bound (any bound
-    >= every Q_s is valid) selects the tcgen05 kernels."""
-    return 32 if case.head_size <= 128 else 16
+    kernels (32 at head size <= 128, 16 at 256, and 16 where the tcgen05
+    kernels take the E4M3 products: E4M3 cache, bf16 query, head size 128,
+    a block size they take); a larger bound (any bound >= every Q_s is
+    valid) selects the tcgen05 kernels."""
+    if case.head_size > 128:
+        return 16
+    if (case.cache_dtype == "e4m3" and case.q_dtype == "bf16" and case.head_size == 128
+            and case.block_size & (case.block_size - 1) == 0):
+        return 16
+    return 32
 
 
 def tc_bound(p):
@@ -241,9 +248,11 @@ MMA_SWEEP = [
     (3, 6, 2, 128, 256, "bf16", "bf16", ("fixed", [31, 32, 600]), ("uniform", 6, 10)),
     (24, 8, 8, 128, 32, "f16", "f16", ("uniform", 1, 28), ("all",)),
     (4, 8, 2, 64, 64, "bf16", "bf16", ("uniform", 100, 400), ("fixed", [8, 5, 7, 6])),
-    (4, 32, 8, 128, 16, "bf16", "e4m3", ("loguniform", 1, 900), ("uniform", 1, 8)),
+    # (bf16 query, E4M3 cache, 17-32 rows: the two-n-tile kernel where the
+    # tcgen05 one is not eligible, block sizes that are not powers of two)
+    (4, 32, 8, 128, 96, "bf16", "e4m3", ("loguniform", 1, 900), ("uniform", 1, 8)),
     (3, 16, 2, 128, 32, "f16", "e4m3", ("uniform", 20, 500), ("uniform", 3, 4)),
-    (4, 12, 4, 128, 16, "bf16", "e4m3", ("fixed", [9, 33, 64, 700]), ("uniform", 6, 10)),
+    (4, 12, 4, 128, 160, "bf16", "e4m3", ("fixed", [9, 33, 64, 700]), ("uniform", 6, 10)),
     # S, Hq, Hkv, d, B, query dtype, cache dtype, lengths, queries
     (6, 32, 8, 128, 16, "bf16", "bf16", ("uniform", 1, 700), ("uniform", 1, 4)),
     (5, 8, 2, 64, 8, "f16", "f16", ("uniform", 1, 300), ("uniform", 1, 4)),
@@ -489,19 +498,22 @@ def test_full_size_shared_prefix_e4m3():
                                             f"{len(rows)} of {int(p.q.query_start[-1])} rows")
 
 
-def test_full_size_shared_prefix_e4m3_draft_tokens():
-    """The shared-prefix E4M3 pool with 8 draft tokens per sequence forced
-    onto the one-tile tcgen05 kernel (the E4M3 products; 64 of a tile's 128
-    rows at G = 8): every row against the oracle."""
+@pytest.mark.parametrize("draft", [4, 8])
+def test_full_size_shared_prefix_e4m3_draft_tokens(draft):
+    """The shared-prefix E4M3 pool with 4 and 8 draft tokens per sequence on
+    the one-tile tcgen05 kernel (the E4M3 products; 32 and 64 of a tile's 128
+    rows at G = 8; the library's own choice at both): every row against the
+    oracle."""
     c = config_case(5)
-    p = Prefill(c, ("fixed", np.minimum(8, c.context_lens)))
+    p = Prefill(c, ("fixed", np.minimum(draft, c.context_lens)))
+    assert tc_bound(p) == p.q.max_queries
     assert pk.prefill_kernel(tc_bound(p), c.num_q_heads, c.num_kv_heads, c.head_size,
                              c.block_size, c.num_blocks, pk.PA_BF16, pk.PA_FP8_E4M3) == "tc"
     got = to_f64(p.run(tc_bound(p)))
     assert p.dc.status_bits() == 0
     rows = np.arange(int(p.q.query_start[-1]))
     want = p.oracle_rows(rows)
-    assert_decode_close(got[rows], want, c, f"full: shared-prefix e4m3 8 draft tokens, "
+    assert_decode_close(got[rows], want, c, f"full: shared-prefix e4m3 {draft} draft tokens, "
                                             f"{len(rows)} rows")
 
 
