@@ -1005,9 +1005,18 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
         for (int j = 0; j < ntiles; ++j) {
             const int b = j & 1;
             const uint32_t sbuf = lane_base + Sh::kSCol + b * N;
-            ok = tc_wait(&s_full[b], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
+            if (ok) {
+                ok = tc_wait(&s_full[b], (uint32_t)((j >> 1) & 1), p.status, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+            }
+            if (!ok) {
+                // after an abort the thread still meets the halves' barrier
+                // once per key tile (and does nothing else), so every softmax
+                // thread passes it ntiles times and no half waits there for
+                // one that has stopped
+                named_barrier(2, kTcSoftmaxThreads);
+                continue;
+            }
             tc_fence_after();
             const int key0 = j * N;
             constexpr int R = 8;
@@ -1160,7 +1169,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 // rescales its half of the columns
                 ok = tc_wait(pv_done, (uint32_t)((j - 1) & 1), p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
+                if (!ok) continue;
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 2; c += 32) {
@@ -1181,7 +1190,7 @@ paged_prefill_tc_kernel(const __grid_constant__ TcPrefillParams tp) {
                 const int st = j % NS;
                 ok = tc_wait(&v_full[st], (uint32_t)((j / NS) & 1), p.status, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
+                if (!ok) continue;
                 const int first = kend - key0;
                 constexpr int CPR = kF8S ? 8 : D / 8;            // 16-byte chunks of a V row
                 uint8_t* vd = sm + Sh::kVOff + st * Sh::kKvBytes;
